@@ -1,0 +1,513 @@
+"""Benchmark: selected-block sparse attention on GB300.
+
+Headline (``value``): NSA selection forward TFLOP/s on the B=2, T=8192, Hq=64,
+Hkv=4, D=128, block 64 causal prefill (bf16), inputs resident in HBM, L2 flushed
+between steps (a 256 MB buffer is rewritten before each timed step, outside the
+step's events).  FLOPs are algorithmic: 4 * D * (number of admissible keys) per
+(token, query head), i.e. the work the selection defines, not padded tiles.
+
+The same JSON line carries ``roofline`` (dominant kernel vs the measured peak),
+``cpu_baseline`` (the fp64 oracle on a bounded sample, host cores), ``e2e`` (same
+metric with host buffers, copies inside the timed region), ``clocks`` (nvidia-smi
+sampled during the timed region) and ``rows``: the other workloads of the path
+(varlen NSA, SparseMask bounds, block-sparse attention, ragged decode), each timed
+the same way.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+``--impl reference`` times the fp64 CPU oracle on the same workload (bounded
+sample per step, host cores) and prints the same line with ``"impl": "reference"``.
+Under torchrun (N > 1) every rank runs its own replica (weak scaling, no
+collective on the data path); rank 0 prints.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selected_block_attention_gb300 import workloads  # noqa: E402
+
+METRIC = "selected-block sparse attn fwd TFLOP/s & HBM GB/s vs roofline; decode tok/s"
+L2_FLUSH_BYTES = 256 << 20
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def log(msg):
+    print(f"[bench {time.strftime('%H:%M:%S')}] {msg}", file=sys.stderr, flush=True)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in PEAKS_FALLBACK}, "measured"
+    except Exception:
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def nsa_work(w):
+    """(F_alg FLOPs, HBM bytes, gathered K/V bytes, token groups) from the inputs."""
+    idx = w.block_indices.cpu().numpy().astype(np.int64)
+    B, T, Hkv, S = idx.shape
+    Hq, D = w.q.shape[2], w.q.shape[3]
+    G = Hq // Hkv
+    bs = w.block_size
+    if isinstance(w.block_counts, int):
+        counts = np.full((B, T, Hkv), w.block_counts, dtype=np.int64)
+    else:
+        counts = w.block_counts.cpu().numpy().astype(np.int64)
+    if w.cu_seqlens is not None:
+        cu = w.cu_seqlens.cpu().numpy().astype(np.int64)
+        seq = np.searchsorted(cu, np.arange(T), side="right") - 1
+        t_rel = np.arange(T) - cu[seq]
+        L = (cu[seq + 1] - cu[seq])
+    else:
+        t_rel = np.arange(T)
+        L = np.full(T, T)
+    t_rel = np.broadcast_to(t_rel[None, :, None, None], idx.shape)
+    Lb = np.broadcast_to(L[None, :, None, None], idx.shape)
+    slot = np.arange(S)[None, None, None, :]
+    valid = (slot < np.minimum(counts, S)[..., None]) & (idx >= 0) & (idx * bs < Lb)
+    if w.causal:
+        valid &= idx * bs <= t_rel
+    hi = np.minimum(idx * bs + bs, Lb)
+    if w.causal:
+        hi = np.minimum(hi, t_rel + 1)
+    keys = np.where(valid, hi - idx * bs, 0).sum()
+    n_blocks = valid.sum()
+    elt = w.q.element_size()
+    flops = 4.0 * D * G * float(keys)
+    hbm = (w.q.numel() * 2 + w.k.numel() + w.v.numel()) * elt + B * T * Hq * 4 + idx.size * 4 + \
+        (0 if isinstance(w.block_counts, int) else counts.size * 4)
+    gather = float(n_blocks) * bs * D * 2 * elt
+    return flops, float(hbm), gather, int(B * T * Hkv)
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons, sampled every 50 ms in a thread."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        sel = [p for t, p in self.samples if t0 <= t <= t1]
+        if not sel:  # region shorter than one sample period: nearest samples
+            sel = [p for t, p in sorted(self.samples, key=lambda s: min(abs(s[0] - t0), abs(s[0] - t1)))[:3]]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in sel if num(p[1]) is not None]
+        mx = [num(p[2]) for p in sel if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for p in sel for n, v in zip(names, p[5:9]) if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sel)}
+
+
+def timed_steps(fn, steps, warmup, flush_buf, stream):
+    """Per-step device time (ms) with CUDA events on ``stream``; the L2 flush runs
+    before every step, outside its events."""
+    for _ in range(warmup):
+        flush_buf.add_(1)
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush_buf.add_(1)
+        starts[i].record(stream)
+        fn()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def decode_work(w):
+    ends = w.sequence_end.cpu().numpy().astype(np.int64)
+    starts = w.sequence_start.cpu().numpy().astype(np.int64)
+    num_sinks = 0 if w.sink_bias is None else w.sink_bias.shape[-1]
+    nkeys = 0
+    for s, e in zip(starts, ends):
+        if e <= s:
+            continue
+        lo = max(s, e - 1 - w.window_left) if w.window_left >= 0 else s
+        nkeys += (e - lo) + max(0, min(num_sinks, lo, e) - s)
+    B, Hq, D = w.q.shape
+    Hkv = w.k.shape[2]
+    kv_bytes = float(nkeys) * Hkv * D * 2 * 2
+    flops = 4.0 * D * (Hq // Hkv) * Hkv * nkeys
+    return kv_bytes + w.q.numel() * 2 * 2 + B * Hq * 4, flops
+
+
+def blocksparse_flops(w):
+    m = w.mask
+    pos = m.q_positions.cpu().numpy().astype(np.int64)
+    seg = m.q_segment_ids.cpu().numpy().astype(np.int64)
+    B, T = pos.shape
+    Hq, D = w.q.shape[2], w.q.shape[3]
+    total = 0
+    for b in range(B):
+        s = seg[b]
+        start = np.zeros(T, dtype=np.int64)
+        change = np.r_[True, s[1:] != s[:-1]]
+        start_idx = np.maximum.accumulate(np.where(change, np.arange(T), 0))
+        n = pos[b] - pos[b][start_idx] + 1
+        if m.window_left >= 0:
+            n = np.minimum(n, m.window_left + 1)
+        total += np.where(s != m.padding_segment_id, n, 0).sum()
+    return 4.0 * D * Hq * float(total)
+
+
+# ----------------------------------------------------------------------------- arms
+def run_cuda(args, rank, world, local_rank):
+    import selected_block_attention_gb300 as sba
+    from selected_block_attention_gb300 import _build
+
+    _build.build()
+    sba.load_library()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks, peak_src = load_peaks()
+    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    w = workloads.nsa_prefill(device=dev)
+    flops, hbm_bytes, gather_bytes, groups = nsa_work(w)
+    log(f"prefill inputs ready: {flops / 1e12:.4f} TFLOP/step")
+    out = torch.empty_like(w.q)
+    lse = torch.empty(w.q.shape[:3], dtype=torch.float32, device=dev)
+
+    def step():
+        sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts, w.block_size,
+                           causal=True, out=out, lse=lse)
+
+    sampler = ClockSampler(local_rank if world > 1 else int(os.environ.get("SBA_GPU_INDEX", "0")))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    times = timed_steps(step, args.steps, args.warmup, flush, stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sba.check_error(dev)
+    ms = sum(times) / len(times)
+    ms_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    clocks = sampler.summary(t0, t1)
+    sampler.stop()
+    log(f"timed steps done: {ms:.4f} ms/step")
+    value = flops * world / (ms_max * 1e-3) / 1e12
+
+    # e2e through the public API with host buffers (pinned), copies in the timed region
+    host = {n: getattr(w, n).cpu().pin_memory() for n in ("q", "k", "v", "block_indices", "block_counts")}
+    dev_in = {n: torch.empty_like(getattr(w, n)) for n in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        for n in host:
+            dev_in[n].copy_(host[n], non_blocking=True)
+        sba.nsa_select_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["block_indices"],
+                           dev_in["block_counts"], w.block_size, causal=True, out=out, lse=lse)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 10))
+    e2e_times = timed_steps(e2e_step, e2e_steps, 2, flush, stream)
+    e2e_ms = sum(e2e_times) / len(e2e_times)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    log(f"e2e done: {e2e_ms:.4f} ms/step")
+    rows = {} if args.no_rows else measure_rows(sba, dev, stream, flush, peaks, args)
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "nsa_select_prefill B=2 T=8192 Hq=64 Hkv=4 D=128 block_size=64 causal, "
+                        "counts U{1..16} clipped, own block + distinct uniform earlier blocks",
+            "tokens": w.q.shape[0] * w.q.shape[1], "token_groups": groups,
+            "flop_per_step": flops, "l2": "256 MB buffer rewritten before every timed step",
+            "parallelism": f"replicas x{world}"},
+        "roofline": {
+            "bound": "tensor",
+            "achieved": round(flops / (ms * 1e-3) / 1e12, 3),
+            "peak": peaks["bf16_tflops"],
+            "unit": "TFLOP/s",
+            "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            "traffic": None,
+            "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
+            "kernel": "nsa_select_kernel<bf16,128,64>",
+            "terms_us": {
+                "tensor": round(flops / (peaks["bf16_tflops"] * 1e12) * 1e6, 2),
+                "hbm": round(hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6, 2)},
+            "hbm_achieved_gbs": round(hbm_bytes / (ms * 1e-3) / 1e9, 1),
+            "hbm_frac": round(hbm_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "gathered_kv_bytes": gather_bytes,
+            "gather_achieved_gbs": round(gather_bytes / (ms * 1e-3) / 1e9, 1),
+        },
+        "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "rows": rows,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w, flops / groups, args.cpu_seconds)
+    return result
+
+
+def measure_rows(sba, dev, stream, flush, peaks, args):
+    rows = {}
+    steps, warm = max(3, min(args.steps, 20)), 3
+
+    # varlen NSA (8 packed sequences)
+    w = workloads.nsa_varlen(device=dev)
+    flops, hbm, gather, groups = nsa_work(w)
+    t = timed_steps(lambda: sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts,
+                                               w.block_size, cu_seqlens=w.cu_seqlens),
+                    steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    log(f"varlen nsa {ms:.4f} ms")
+    rows["nsa_select_varlen"] = {
+        "workload": w.name, "ms": round(ms, 4), "TFLOP/s": round(flops / ms / 1e9, 2),
+        "frac_tensor": round(flops / ms / 1e9 / peaks["bf16_tflops"], 4),
+        "hbm_GB/s": round(hbm / ms / 1e6, 1), "gather_GB/s": round(gather / ms / 1e6, 1)}
+    del w
+    torch.cuda.empty_cache()
+
+    # SparseMask bounds + block-sparse attention
+    w = workloads.blocksparse(device=dev)
+    m = w.mask
+    bnd = {}
+
+    def bounds():
+        bnd["b"] = sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions,
+                                          m.kv_segment_ids, 128, 128, causal=True,
+                                          window_left=1024, window_right=0)
+
+    t = timed_steps(bounds, steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    in_bytes = 4 * m.q_positions.numel() * 4 + 4 * bnd["b"][0].numel() * 4
+    log(f"bounds {ms * 1e3:.2f} us")
+    rows["sparse_mask_bounds"] = {
+        "workload": m.name, "us": round(ms * 1e3, 2), "GB/s": round(in_bytes / ms / 1e6, 1),
+        "frac_hbm": round(in_bytes / ms / 1e6 / peaks["hbm_gbs"], 4)}
+    lo, up, lof, upf = bnd["b"]
+    fl = blocksparse_flops(w)
+    t = timed_steps(lambda: sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids,
+                                                     m.kv_positions, m.kv_segment_ids, lo, up, lof,
+                                                     upf, 128, 128, causal=True, window_left=1024,
+                                                     window_right=0),
+                    steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    log(f"blocksparse {ms:.4f} ms")
+    rows["blocksparse_attn"] = {
+        "workload": w.name, "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 2),
+        "frac_tensor": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)}
+    del w, m, bnd
+    torch.cuda.empty_cache()
+
+    # ragged decode
+    w = workloads.decode(device=dev)
+    nbytes, dfl = decode_work(w)
+    ws = torch.empty(sba.ragged_decode_workspace_size(64, 32, 32768, 128, w.window_left),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty_like(w.q)
+    t = timed_steps(lambda: sba.ragged_decode_fwd(w.q, w.k, w.v, w.sequence_start, w.sequence_end,
+                                                  window_left=w.window_left,
+                                                  window_right=w.window_right,
+                                                  logits_soft_cap=w.logits_soft_cap,
+                                                  sink_bias=w.sink_bias, out=out, workspace=ws),
+                    steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    log(f"decode {ms * 1e3:.2f} us")
+    rows["ragged_decode"] = {
+        "workload": w.name, "us": round(ms * 1e3, 2), "tok/s": round(w.q.shape[0] / (ms * 1e-3), 1),
+        "GB/s": round(nbytes / ms / 1e6, 1), "frac_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
+        "kernels_per_call": 2}
+    del w
+    torch.cuda.empty_cache()
+    sba.check_error(dev)
+    return rows
+
+
+def cpu_baseline(w, flops_per_group, seconds):
+    """fp64 oracle on host cores over a bounded, seeded sample of token groups."""
+    import oracle
+
+    q = w.q.cpu().double().numpy()
+    k = w.k.cpu().double().numpy()
+    v = w.v.cpu().double().numpy()
+    idx = w.block_indices.cpu().numpy()
+    counts = w.block_counts.cpu().numpy()
+    B, T = q.shape[:2]
+    rng = np.random.default_rng(0)
+    done_rows = 0
+    t0 = time.perf_counter()
+    flops = 0.0
+    while time.perf_counter() - t0 < seconds:
+        rows = [(int(b), int(t)) for b, t in zip(rng.integers(0, B, 32), rng.integers(0, T, 32))]
+        oracle.nsa_select_attention(q, k, v, idx, counts, w.block_size, rows=rows)
+        for b, t in rows:
+            hi = np.minimum(idx[b, t] * w.block_size + w.block_size, t + 1)
+            valid = (np.arange(idx.shape[-1])[None, :] < counts[b, t][:, None]) & (idx[b, t] >= 0)
+            flops += 4.0 * q.shape[3] * (q.shape[2] // k.shape[2]) * np.where(valid, hi - idx[b, t] * w.block_size, 0).sum()
+        done_rows += len(rows)
+    dt = time.perf_counter() - t0
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done_rows} random tokens (all {k.shape[2]} KV heads x {q.shape[2]} query heads) "
+                      f"of the prefill workload, {dt:.1f} s, numpy float64, 1 thread"}
+
+
+def run_reference(args):
+    """The fp64 oracle on host cores, same workload, bounded sample per step."""
+    import oracle
+
+    w = workloads.nsa_prefill(device="cpu")
+    q = w.q.double().numpy()
+    k = w.k.double().numpy()
+    v = w.v.double().numpy()
+    idx = w.block_indices.numpy()
+    counts = w.block_counts.numpy()
+    rng = np.random.default_rng(0)
+    per_step = 48
+
+    def one():
+        rows = [(int(b), int(t)) for b, t in zip(rng.integers(0, 2, per_step), rng.integers(0, 8192, per_step))]
+        t0 = time.perf_counter()
+        oracle.nsa_select_attention(q, k, v, idx, counts, w.block_size, rows=rows)
+        dt = time.perf_counter() - t0
+        fl = 0.0
+        for b, t in rows:
+            hi = np.minimum(idx[b, t] * 64 + 64, t + 1)
+            valid = (np.arange(16)[None, :] < counts[b, t][:, None]) & (idx[b, t] >= 0)
+            fl += 4.0 * 128 * 16 * np.where(valid, hi - idx[b, t] * 64, 0).sum()
+        return dt, fl
+
+    for _ in range(args.warmup):
+        one()
+    tot_t, tot_f = 0.0, 0.0
+    for _ in range(args.steps):
+        dt, fl = one()
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = f"{per_step} random tokens per step (all 4 KV heads x 64 query heads), numpy float64, 1 thread"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(tot_t / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "nsa_select_prefill B=2 T=8192 Hq=64 Hkv=4 D=128 block_size=64 causal "
+                               "(bounded sample per step)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)))
+        return
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_cuda(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

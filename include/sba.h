@@ -1,0 +1,199 @@
+/*
+ * sba.h -- C ABI of libsba, selected-block sparse attention for NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every function returns an int status: SBA_OK (0) or a negative SBA_ERR_* code.
+ *    On error nothing is launched and sba_last_error() (thread-local) describes why.
+ *    No C++ exception crosses this boundary.
+ *  - Every tensor pointer is caller-owned DEVICE memory (from cudaMalloc, a caching
+ *    allocator, ...), dense row-major in the layout given per argument, 16-byte aligned.
+ *    The library keeps no pointer after a call returns and allocates no device memory.
+ *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream); nothing
+ *    synchronises.  Errors a kernel detects while running (a malformed cu_seqlens, an
+ *    internal wait that timed out) are recorded in a device-side error word and
+ *    reported by sba_check_error().
+ *  - dtype codes: SBA_BF16 = 0 (bfloat16), SBA_F32 = 1 (float32).
+ *  - softmax_scale <= 0 selects 1 / sqrt(D).
+ *  - Log-sum-exp outputs are natural-log, float32; a row with no admissible key gets
+ *    output 0 and LSE = -inf.
+ */
+#ifndef SBA_H_
+#define SBA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SBA_API __attribute__((visibility("default")))
+#else
+#define SBA_API
+#endif
+
+typedef struct CUstream_st* sba_stream_t; /* same object as cudaStream_t */
+
+enum {
+  SBA_OK = 0,
+  SBA_ERR_INVALID_ARG = -1, /* a size, pointer, alignment or flag is out of range   */
+  SBA_ERR_UNSUPPORTED = -2, /* valid arguments this build has no kernel for         */
+  SBA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed (message attached) */
+  SBA_ERR_TIMEOUT = -4,     /* a kernel gave up on an internal wait (see check)     */
+  SBA_ERR_DEVICE_INPUT = -5 /* a kernel found malformed device-side input           */
+};
+
+enum { SBA_BF16 = 0, SBA_F32 = 1 };
+
+/* Library version string, e.g. "sba 0.1.0 sm_103a". */
+SBA_API const char* sba_version(void);
+
+/* Message of the last failing call on this host thread ("" if none). */
+SBA_API const char* sba_last_error(void);
+
+/*
+ * sba_nsa_select_fwd -- native-sparse-attention forward, selection branch.
+ *
+ * Defined by: "ejkernel.modules.operations.native_sparse_attention" (operation API
+ * page), method NativeSparseAttention.run and function native_sparse_attention.
+ * Each query token attends, per KV head, only to the key blocks of `block_size`
+ * tokens named by block_indices[b, t, h_kv, :count]; Hq query heads share Hkv KV
+ * heads (query head hq reads KV head hq / (Hq / Hkv)); cu_seqlens packs
+ * variable-length sequences into one batch row; the output has the query's shape.
+ *
+ *  q             [B, T, Hq, D]  dtype        (B == 1 when cu_seqlens != NULL)
+ *  k, v          [B, T, Hkv, D] dtype
+ *  block_indices [B, T, Hkv, S] int32: block ids relative to the start of the
+ *                token's own sequence.  Entries < 0, >= ceil(L / block_size) (L = the
+ *                sequence's length) or, when causal, after the token's own block are
+ *                ignored.  Order does not matter; duplicates count once.
+ *  block_counts  [B, T, Hkv] int32, or NULL to use block_count_scalar for every
+ *                token; only the first min(count, S) entries are read.
+ *  cu_seqlens    [num_seqs + 1] int32 (0 = c[0] <= c[1] <= ... <= c[num_seqs] = T),
+ *                or NULL for fixed-length rows of T tokens.
+ *  causal        nonzero: key k of a token at sequence position t is visible iff k <= t.
+ *  out           [B, T, Hq, D] dtype (written).
+ *  lse           [B, T, Hq] float32 (written), or NULL.
+ * Supported: D in {64, 128}; block_size in {32, 64, 128}; 1 <= Hq/Hkv <= 16;
+ * 1 <= S <= 32; dtype bf16 (tensor cores, bf16 inputs, fp32 accumulation) or f32 with
+ * D == 64 (tensor cores in tf32, fp32 accumulation).
+ */
+SBA_API int sba_nsa_select_fwd(const void* q, const void* k, const void* v,
+                       const int32_t* block_indices, const int32_t* block_counts,
+                       int block_count_scalar, int S,
+                       const int32_t* cu_seqlens, int num_seqs,
+                       int B, int T, int Hq, int Hkv, int D, int block_size, int causal,
+                       float softmax_scale, int dtype,
+                       void* out, float* lse, sba_stream_t stream);
+
+/*
+ * sba_sparse_mask_bounds -- SparseMask block bounds for the forward pass.
+ *
+ * Defined by: "ejkernel.kernels._triton.blocksparse_attention._mask" (module source
+ * page): dataclass SparseMask, kernel _compute_sparse_mask with the query as the
+ * outer operand, and the padding, padding-segment remap and clip/fix-up steps of
+ * define_sparse_mask_fn.  Tq and Tkv are padded to block multiples (query positions
+ * with -1, key positions with INT32_MAX, segment ids with padding_segment_id), the
+ * padding id is remapped to padded_Tkv + 1, each (query block, key block) pair is
+ * tested for segment-range overlap, causality and the inclusive window, and the
+ * half-open bounds are min/max-accumulated then clipped.  Results are bit-exact
+ * integers.
+ *
+ *  q_pos, q_seg    [B, Tq] int32  positions / segment ids of the query tokens
+ *  kv_pos, kv_seg  [B, Tkv] int32 positions / segment ids of the key tokens
+ *  window_left/right  inclusive window in positions; -1 = unbounded
+ *  padding_segment_id  segment id that marks padding tokens
+ *  lower, upper, lower_full, upper_full  [B, 1, ceil(Tq / q_block)] int32 (written)
+ * Preconditions: real segment ids < padded_Tkv + 1; |positions| + window < 2^31.
+ */
+SBA_API int sba_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg,
+                           const int32_t* kv_pos, const int32_t* kv_seg,
+                           int B, int Tq, int Tkv, int q_block, int kv_block, int causal,
+                           int window_left, int window_right, int padding_segment_id,
+                           int32_t* lower, int32_t* upper,
+                           int32_t* lower_full, int32_t* upper_full,
+                           sba_stream_t stream);
+
+/*
+ * sba_blocksparse_attn_fwd -- attention restricted by SparseMask bounds.
+ *
+ * Defined by: "ejkernel.kernels._triton.blocksparse_attention._mask" (module source
+ * page), module docstring and SparseMask docstring: key blocks outside
+ * [lower, upper) of a query block are skipped; blocks inside
+ * [lower_full, upper_full) are processed without per-token masking.  Token-level
+ * mask (the page does not print one; plainest reading): same segment, neither
+ * padding, causal on positions, inclusive window on positions.
+ *
+ *  q [B, T, Hq, D] bf16; k, v [B, T, Hkv, D] bf16 (queries and keys share T)
+ *  q_pos, q_seg, kv_pos, kv_seg [B, T] int32
+ *  lower, upper, lower_full, upper_full [B, 1, T / q_block] int32 (as produced by
+ *  sba_sparse_mask_bounds with the same block sizes)
+ *  out [B, T, Hq, D] bf16 (written); lse [B, T, Hq] float32 (written) or NULL.
+ * Supported: q_block == 128, kv_block in {64, 128}, T % 128 == 0, D in {64, 128},
+ * 1 <= Hq / Hkv, bf16 only.
+ */
+SBA_API int sba_blocksparse_attn_fwd(const void* q, const void* k, const void* v,
+                             const int32_t* q_pos, const int32_t* q_seg,
+                             const int32_t* kv_pos, const int32_t* kv_seg,
+                             const int32_t* lower, const int32_t* upper,
+                             const int32_t* lower_full, const int32_t* upper_full,
+                             int B, int T, int Hq, int Hkv, int D, int q_block, int kv_block,
+                             int causal, int window_left, int window_right,
+                             int padding_segment_id, float softmax_scale,
+                             void* out, float* lse, sba_stream_t stream);
+
+/*
+ * sba_ragged_decode_workspace_size -- bytes of device workspace that
+ * sba_ragged_decode_fwd needs for these sizes (fp32 split partials).  window_left < 0
+ * means no left window.  Returns 0 for invalid sizes.
+ */
+SBA_API size_t sba_ragged_decode_workspace_size(int B, int Hq, int S, int D, int window_left);
+
+/*
+ * sba_ragged_decode_fwd -- ragged single-token decode attention.
+ *
+ * Defined by: "ejkernel.kernels._xla.ragged_decode_attention._xla_impl_fwd" (API
+ * page): ragged_decode_mqa_xla / inner_decode_xla (per-row key range
+ * [sequence_start, sequence_end), sliding window, logits soft cap, softmax_aux sink
+ * biases), create_attention_mask (sinks are always attendable),
+ * apply_logits_soft_cap and apply_attention_sinks_block.  The query sits at
+ * position end - 1; key k is attendable iff start <= k < end and it lies in the
+ * inclusive window or k < num_sinks.  Logit = scale * <q, k>, then
+ * cap * tanh(logit / cap) when cap > 0, then + sink_bias for sink keys.
+ *
+ *  q          [B, Hq, D] bf16
+ *  k, v       [B, S, Hkv, D] bf16 (the KV cache; rows beyond sequence_end unread)
+ *  seq_start, seq_end  [B] int32
+ *  sink_bias  float32 [Hq, num_sinks] (sink_bias_per_head != 0) or [num_sinks];
+ *             NULL with num_sinks == 0 for none.  num_sinks <= 16.
+ *  out        [B, Hq, D] bf16 (written); lse [B, Hq] float32 (written) or NULL
+ *  workspace  device scratch of at least
+ *             sba_ragged_decode_workspace_size(B, Hq, S, D, window_left) bytes,
+ *             16-byte aligned, caller-owned; contents need no initialisation.
+ * Supported: D == 128, 1 <= Hq / Hkv <= 16, num_sinks <= 16, sequence_end <= S, bf16.
+ * Internally: split-KV partial kernel + combine kernel on `stream`.
+ */
+SBA_API int sba_ragged_decode_fwd(const void* q, const void* k, const void* v,
+                          const int32_t* seq_start, const int32_t* seq_end,
+                          int B, int Hq, int Hkv, int S, int D, float softmax_scale,
+                          int window_left, int window_right, float logits_soft_cap,
+                          const float* sink_bias, int num_sinks, int sink_bias_per_head,
+                          void* out, float* lse,
+                          void* workspace, size_t workspace_bytes, sba_stream_t stream);
+
+/*
+ * sba_check_error -- synchronise `stream`, then read and clear the device-side error
+ * word of every kernel of this library.  Returns SBA_OK, SBA_ERR_TIMEOUT (a kernel
+ * gave up on a bounded internal wait and returned early), SBA_ERR_DEVICE_INPUT (a
+ * kernel found malformed device data such as a non-monotone cu_seqlens) or
+ * SBA_ERR_CUDA (an asynchronous CUDA error).
+ */
+SBA_API int sba_check_error(sba_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SBA_H_ */

@@ -1,0 +1,210 @@
+// C ABI of libsba: argument validation, error reporting, and dispatch to the kernel
+// launchers.  Nothing here computes attention; every step of the path runs in the
+// kernels of the other translation units.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+
+namespace sba {
+
+static thread_local std::string g_last_error;
+
+int set_error(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_error(cudaError_t e, const char* what) {
+  return set_error(SBA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
+                           void* gaddr, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                           const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_encode) return CUDA_ERROR_NOT_FOUND;
+  cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
+  return g_encode(map, dtype, rank, gaddr, dims, strides_bytes, box, elem_strides,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 1;
+  }
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace sba
+
+using namespace sba;
+
+#define SBA_REQUIRE(cond, msg)                                                  \
+  do {                                                                          \
+    if (!(cond)) return set_error(SBA_ERR_INVALID_ARG, std::string(__func__) + ": " + (msg)); \
+  } while (0)
+#define SBA_SUPPORT(cond, msg)                                                  \
+  do {                                                                          \
+    if (!(cond)) return set_error(SBA_ERR_UNSUPPORTED, std::string(__func__) + ": " + (msg)); \
+  } while (0)
+
+extern "C" {
+
+const char* sba_version(void) { return "sba 0.1.0 sm_103a"; }
+
+const char* sba_last_error(void) { return g_last_error.c_str(); }
+
+int sba_nsa_select_fwd(const void* q, const void* k, const void* v,
+                       const int32_t* block_indices, const int32_t* block_counts,
+                       int block_count_scalar, int S, const int32_t* cu_seqlens, int num_seqs,
+                       int B, int T, int Hq, int Hkv, int D, int block_size, int causal,
+                       float softmax_scale, int dtype, void* out, float* lse,
+                       sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q && k && v && block_indices && out, "null tensor pointer");
+  SBA_REQUIRE(B >= 1 && T >= 1 && Hq >= 1 && Hkv >= 1, "sizes must be positive");
+  SBA_REQUIRE(Hq % Hkv == 0, "Hq must be a multiple of Hkv");
+  SBA_REQUIRE(S >= 1, "S (selected-block slots) must be >= 1");
+  SBA_REQUIRE(dtype == SBA_BF16 || dtype == SBA_F32, "dtype must be SBA_BF16 or SBA_F32");
+  SBA_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out),
+              "q, k, v and out must be 16-byte aligned");
+  SBA_REQUIRE(cu_seqlens == nullptr || (num_seqs >= 1 && B == 1),
+              "cu_seqlens needs num_seqs >= 1 and B == 1");
+  SBA_REQUIRE(block_counts != nullptr || block_count_scalar >= 0,
+              "block_count_scalar must be >= 0");
+  SBA_REQUIRE(std::isfinite(softmax_scale), "softmax_scale must be finite");
+  SBA_SUPPORT(D == 64 || D == 128, "D must be 64 or 128");
+  SBA_SUPPORT(block_size == 32 || block_size == 64 || block_size == 128,
+              "block_size must be 32, 64 or 128");
+  SBA_SUPPORT(Hq / Hkv <= 16, "Hq / Hkv must be <= 16");
+  SBA_SUPPORT(S <= 32, "S must be <= 32");
+  SBA_SUPPORT((long long)B * T * Hq < (1LL << 31), "B * T * Hq must be < 2^31");
+  float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_nsa_select(q, k, v, block_indices, block_counts, block_count_scalar, S,
+                           cu_seqlens, cu_seqlens ? num_seqs : 0, B, T, Hq, Hkv, D, block_size,
+                           causal ? 1 : 0, scale, dtype, out, lse,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sba_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const int32_t* kv_pos,
+                           const int32_t* kv_seg, int B, int Tq, int Tkv, int q_block,
+                           int kv_block, int causal, int window_left, int window_right,
+                           int padding_segment_id, int32_t* lower, int32_t* upper,
+                           int32_t* lower_full, int32_t* upper_full, sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q_pos && q_seg && kv_pos && kv_seg && lower && upper && lower_full && upper_full,
+              "null pointer");
+  SBA_REQUIRE(B >= 1 && Tq >= 1 && Tkv >= 1, "sizes must be positive");
+  SBA_REQUIRE(q_block >= 1 && kv_block >= 1, "block sizes must be positive");
+  SBA_REQUIRE(window_left >= -1 && window_right >= -1, "windows must be >= -1");
+  SBA_SUPPORT(q_block <= 4096 && kv_block <= 4096, "block sizes must be <= 4096");
+  SBA_SUPPORT(B <= 65535, "B must be <= 65535");
+  SBA_SUPPORT((long long)B * ((Tq + q_block - 1) / q_block) < (1LL << 31), "too many blocks");
+  return launch_sparse_mask_bounds(q_pos, q_seg, kv_pos, kv_seg, B, Tq, Tkv, q_block, kv_block,
+                                   causal ? 1 : 0, window_left, window_right, padding_segment_id,
+                                   lower, upper, lower_full, upper_full,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sba_blocksparse_attn_fwd(const void* q, const void* k, const void* v, const int32_t* q_pos,
+                             const int32_t* q_seg, const int32_t* kv_pos, const int32_t* kv_seg,
+                             const int32_t* lower, const int32_t* upper,
+                             const int32_t* lower_full, const int32_t* upper_full, int B, int T,
+                             int Hq, int Hkv, int D, int q_block, int kv_block, int causal,
+                             int window_left, int window_right, int padding_segment_id,
+                             float softmax_scale, void* out, float* lse, sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q && k && v && q_pos && q_seg && kv_pos && kv_seg && lower && upper &&
+                  lower_full && upper_full && out,
+              "null pointer");
+  SBA_REQUIRE(B >= 1 && T >= 1 && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, "bad head/size arguments");
+  SBA_REQUIRE(window_left >= -1 && window_right >= -1, "windows must be >= -1");
+  SBA_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) &&
+                  aligned16(kv_pos) && aligned16(kv_seg),
+              "q, k, v, out, kv_pos and kv_seg must be 16-byte aligned");
+  SBA_REQUIRE(std::isfinite(softmax_scale), "softmax_scale must be finite");
+  SBA_SUPPORT(q_block == 128, "q_block must be 128");
+  SBA_SUPPORT(kv_block == 64 || kv_block == 128, "kv_block must be 64 or 128");
+  SBA_SUPPORT(T % 128 == 0, "T must be a multiple of 128");
+  SBA_SUPPORT(D == 64 || D == 128, "D must be 64 or 128");
+  SBA_SUPPORT((long long)B * T * Hq < (1LL << 31), "B * T * Hq must be < 2^31");
+  float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_blocksparse_attn(q, k, v, q_pos, q_seg, kv_pos, kv_seg, lower, upper, lower_full,
+                                 upper_full, B, T, Hq, Hkv, D, q_block, kv_block, causal ? 1 : 0,
+                                 window_left, window_right, padding_segment_id, scale, out, lse,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sba_ragged_decode_workspace_size(int B, int Hq, int S, int D, int window_left) {
+  if (B < 1 || Hq < 1 || S < 1 || D < 1) return 0;
+  return decode_workspace_bytes(B, Hq, S, D, window_left);
+}
+
+int sba_ragged_decode_fwd(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                          const int32_t* seq_end, int B, int Hq, int Hkv, int S, int D,
+                          float softmax_scale, int window_left, int window_right,
+                          float logits_soft_cap, const float* sink_bias, int num_sinks,
+                          int sink_bias_per_head, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q && k && v && seq_start && seq_end && out, "null pointer");
+  SBA_REQUIRE(B >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1 && Hq % Hkv == 0, "bad sizes");
+  SBA_REQUIRE(window_left >= -1 && window_right >= -1, "windows must be >= -1");
+  SBA_REQUIRE(num_sinks >= 0 && (num_sinks == 0 || sink_bias != nullptr),
+              "num_sinks > 0 needs sink_bias");
+  SBA_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out),
+              "q, k, v and out must be 16-byte aligned");
+  SBA_REQUIRE(std::isfinite(softmax_scale) && std::isfinite(logits_soft_cap),
+              "scale and cap must be finite");
+  SBA_SUPPORT(D == 128, "D must be 128");
+  SBA_SUPPORT(Hq / Hkv <= 16, "Hq / Hkv must be <= 16");
+  SBA_SUPPORT(num_sinks <= 16, "num_sinks must be <= 16");
+  size_t need = decode_workspace_bytes(B, Hq, S, D, window_left);
+  SBA_REQUIRE(workspace != nullptr && aligned16(workspace) && workspace_bytes >= need,
+              "workspace missing, misaligned or smaller than sba_ragged_decode_workspace_size()");
+  float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_ragged_decode(q, k, v, seq_start, seq_end, B, Hq, Hkv, S, D, scale, window_left,
+                              window_right, logits_soft_cap, sink_bias, num_sinks,
+                              sink_bias_per_head ? 1 : 0, out, lse, workspace, workspace_bytes,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sba_check_error(sba_stream_t stream) {
+  g_last_error.clear();
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_error(e, "sba_check_error: stream synchronize");
+  std::string where;
+  unsigned w = read_and_clear_error_nsa(s, &where) | read_and_clear_error_mask(s, &where) |
+               read_and_clear_error_blocksparse(s, &where) | read_and_clear_error_decode(s, &where);
+  if (w & kDevErrTimeout)
+    return set_error(SBA_ERR_TIMEOUT, "a kernel gave up on a bounded internal wait" + where);
+  if (w & kDevErrInput)
+    return set_error(SBA_ERR_DEVICE_INPUT, "a kernel found malformed device-side input" + where);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "sba_check_error");
+  return SBA_OK;
+}
+
+}  // extern "C"

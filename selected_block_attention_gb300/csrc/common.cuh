@@ -1,0 +1,68 @@
+// Shared host/device helpers of libsba: status codes, error words, bounded waits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/sba.h"
+
+namespace sba {
+
+// Bits of the per-translation-unit device error word.
+enum : unsigned {
+  kDevErrTimeout = 1u,  // a bounded wait expired; the kernel returned early
+  kDevErrInput = 2u,    // malformed device-side input (e.g. cu_seqlens)
+};
+
+// Roughly two seconds at the GB300 boost clock: every spin-wait on an mbarrier
+// gives up after this many SM cycles, flags kDevErrTimeout and unwinds.
+constexpr long long kWaitTimeoutCycles = 4000000000LL;
+
+// Host-side error reporting (defined in api.cu).
+int set_error(int code, const std::string& msg);
+int cuda_error(cudaError_t e, const char* what);
+
+// Per-translation-unit error word readers (each kernel file defines one).
+// Each returns the kDevErr* flags and appends a short location note to *where.
+unsigned read_and_clear_error_nsa(cudaStream_t s, std::string* where);
+unsigned read_and_clear_error_mask(cudaStream_t s, std::string* where);
+unsigned read_and_clear_error_blocksparse(cudaStream_t s, std::string* where);
+unsigned read_and_clear_error_decode(cudaStream_t s, std::string* where);
+
+// Launch entry points implemented by the kernel files (arguments already validated).
+int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_indices,
+                      const int32_t* block_counts, int block_count_scalar, int S,
+                      const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
+                      int D, int block_size, int causal, float scale, int dtype, void* out,
+                      float* lse, cudaStream_t stream);
+int launch_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const int32_t* kv_pos,
+                              const int32_t* kv_seg, int B, int Tq, int Tkv, int q_block,
+                              int kv_block, int causal, int window_left, int window_right,
+                              int pad_id, int32_t* lower, int32_t* upper, int32_t* lower_full,
+                              int32_t* upper_full, cudaStream_t stream);
+int launch_blocksparse_attn(const void* q, const void* k, const void* v, const int32_t* q_pos,
+                            const int32_t* q_seg, const int32_t* kv_pos, const int32_t* kv_seg,
+                            const int32_t* lower, const int32_t* upper, const int32_t* lower_full,
+                            const int32_t* upper_full, int B, int T, int Hq, int Hkv, int D,
+                            int q_block, int kv_block, int causal, int window_left,
+                            int window_right, int pad_id, float scale, void* out, float* lse,
+                            cudaStream_t stream);
+size_t decode_workspace_bytes(int B, int Hq, int S, int D, int window_left);
+int launch_ragged_decode(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                         const int32_t* seq_end, int B, int Hq, int Hkv, int S, int D,
+                         float scale, int window_left, int window_right, float cap,
+                         const float* sink_bias, int num_sinks, int sink_per_head, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+// Driver entry point for tensor-map encoding, resolved once through the runtime.
+CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
+                           void* gaddr, const cuuint64_t* dims, const cuuint64_t* strides_bytes,
+                           const cuuint32_t* box, CUtensorMapSwizzle swizzle);
+
+int num_sms();
+
+}  // namespace sba

@@ -1,0 +1,414 @@
+// Ragged single-token decode attention: split-KV partial kernel + combine kernel.
+//
+// Follows "ejkernel.kernels._xla.ragged_decode_attention._xla_impl_fwd" (API page):
+// ragged_decode_mqa_xla / inner_decode_xla (per-row [sequence_start, sequence_end),
+// sliding window, logits soft cap, softmax_aux sinks), create_attention_mask (sinks
+// always attendable), apply_logits_soft_cap, apply_attention_sinks_block, and the
+// online-softmax carry of flash_attention_block.
+//
+// The query sits at position end - 1.  Key k is attendable iff start <= k < end and
+// it is inside the inclusive window or k < num_sinks.  Logit: scale * <q, k>, then
+// cap * tanh(. / cap) when cap > 0, then + sink bias for k < num_sinks.
+//
+// Work split: CTA (split s, KV head h, row b) covers kKeysPerCta keys of the
+// window [lo_w, end); its four warps each stream kKeysPerWarp of them.  Each warp
+// holds the G query heads of KV head h as the 16 rows of an m16n8k16 tile (rows
+// >= G are zero), streams 16-key K/V tiles with 16-byte cp.async (each key row of
+// one head is 256 contiguous bytes) through a 3-stage shared-memory ring, and keeps
+// the online-softmax state in registers.  The four warps merge through shared
+// memory and write one fp32 partial (o * exp(-m), m, l) per (row, split, q head);
+// split 0 additionally folds in the sink tokens left of the window.  The combine
+// kernel merges the partials of a row with max / exp weights and writes the bf16
+// output and the natural-log LSE.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace sba {
+
+static __device__ unsigned g_err_decode = 0;
+
+namespace {
+
+constexpr int kD = 128;
+constexpr int kWarps = 4;
+constexpr int kKeysPerWarp = 128;
+constexpr int kKeysPerCta = kWarps * kKeysPerWarp;
+constexpr int kTileKeys = 16;
+constexpr int kStages = 3;
+constexpr int kRowBytes = kD * 2 + 16;  // padded shared-memory row (ldmatrix without conflicts)
+constexpr int kTileBytes = kTileKeys * kRowBytes;
+constexpr int kWarpSmem = kStages * 2 * kTileBytes;
+constexpr int kSmemBytes = kWarps * kWarpSmem;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DecodeParams {
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  const int* seq_start;
+  const int* seq_end;
+  const float* sink_bias;
+  float* o_part;   // [B][max_splits][Hq][D]
+  float* ml_part;  // [B][max_splits][Hq][2]
+  int B, Hq, Hkv, S, G, max_splits;
+  float scale, cap;
+  int window_left, num_sinks, sink_per_head;
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Issue the cp.async copies of one 16-key K/V tile of KV head h (keys clamped into
+// the cache so no copy leaves the tensor; clamped rows are masked later).
+__device__ __forceinline__ void load_tile(const DecodeParams& p, int b, int h, int key0,
+                                          uint32_t k_dst, uint32_t v_dst, int lane) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int u = lane + 32 * i;  // 256 chunks of 16 bytes per tensor
+    const int key = u >> 4, part = u & 15;
+    const int kk = min(max(key0 + key, 0), p.S - 1);
+    const long long row = ((long long)b * p.S + kk) * p.Hkv + h;
+    const uint32_t off = key * kRowBytes + part * 16;
+    cp_async16(k_dst + off, p.k + row * kD + part * 8);
+    cp_async16(v_dst + off, p.v + row * kD + part * 8);
+  }
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+decode_split_kernel(const DecodeParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+
+  const int start = p.seq_start[b], end = min(p.seq_end[b], p.S);
+  if (end <= max(start, 0)) return;  // empty row: the combine kernel writes 0 / -inf
+  const int pos = end - 1;
+  const int lo_w = p.window_left >= 0 ? max(max(start, 0), pos - p.window_left) : max(start, 0);
+  const int n_win = end - lo_w;
+  const int n_split = (n_win + kKeysPerCta - 1) / kKeysPerCta;
+  if (s >= n_split) return;
+  const int sink_hi = min(min(p.num_sinks, lo_w), end);  // sinks left of the window
+  const bool do_sinks = (s == 0) && (warp == 0) && (sink_hi > max(start, 0));
+
+  const int key_lo = lo_w + s * kKeysPerCta + warp * kKeysPerWarp;
+  const int key_hi = min(key_lo + kKeysPerWarp, end);
+  int n_tiles = key_hi > key_lo ? (key_hi - key_lo + kTileKeys - 1) / kTileKeys : 0;
+  const int first_tile = do_sinks ? -1 : 0;  // tile -1 = sink tile at keys [0, 16)
+
+  // Query fragments (A operand, 16 rows = q heads h*G + r, rows >= G zero).
+  uint32_t qa[8][4];
+  {
+    const __nv_bfloat16* qb = p.q + ((long long)b * p.Hq + (long long)h * p.G) * kD;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d0 = ks * 16 + 2 * c;
+      auto ld = [&](int r, int d) -> uint32_t {
+        return r < p.G ? *reinterpret_cast<const uint32_t*>(qb + (long long)r * kD + d) : 0u;
+      };
+      qa[ks][0] = ld(g, d0);
+      qa[ks][1] = ld(g + 8, d0);
+      qa[ks][2] = ld(g, d0 + 8);
+      qa[ks][3] = ld(g + 8, d0 + 8);
+    }
+  }
+  const float* bias_row0 = nullptr;
+  const float* bias_row1 = nullptr;
+  if (p.num_sinks > 0) {
+    const int hq0 = h * p.G + g, hq1 = h * p.G + g + 8;
+    bias_row0 = p.sink_bias + (p.sink_per_head ? (long long)min(hq0, p.Hq - 1) * p.num_sinks : 0);
+    bias_row1 = p.sink_bias + (p.sink_per_head ? (long long)min(hq1, p.Hq - 1) * p.num_sinks : 0);
+  }
+
+  const uint32_t wbase = ptx::smem_u32(smem) + warp * kWarpSmem;
+  auto k_stage = [&](int st) { return wbase + st * 2 * kTileBytes; };
+  auto v_stage = [&](int st) { return wbase + st * 2 * kTileBytes + kTileBytes; };
+  auto tile_key0 = [&](int t) { return t < 0 ? 0 : key_lo + t * kTileKeys; };
+
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  const int last_tile = n_tiles - 1;
+  // Prologue: stages for the first kStages-1 tiles.
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    const int t = first_tile + i;
+    if (t <= last_tile) load_tile(p, b, h, tile_key0(t), k_stage(i), v_stage(i), lane);
+    cp_async_commit();
+  }
+  int stage = 0;
+  for (int t = first_tile; t <= last_tile; ++t) {
+    {  // prefetch tile t + kStages - 1
+      const int tn = t + kStages - 1;
+      const int sn = (stage + kStages - 1) % kStages;
+      if (tn <= last_tile) load_tile(p, b, h, tile_key0(tn), k_stage(sn), v_stage(sn), lane);
+      cp_async_commit();
+    }
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const uint32_t ks_base = k_stage(stage), vs_base = v_stage(stage);
+    const int key0 = tile_key0(t);
+
+    // S = Q K^T for 16 keys: two n-tiles of 8 keys.
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const uint32_t row_addr = ks_base + ((mi >> 1) * 8 + ri) * kRowBytes + (mi & 1) * 16;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(row_addr + kk * 32, b00, b01, b10, b11);
+        mma_bf16(sc[0], qa[kk], b00, b01);
+        mma_bf16(sc[1], qa[kk], b10, b11);
+      }
+    }
+    // Logits, mask, online softmax (rows g and g+8 of this thread).
+    float tmax0 = -INFINITY, tmax1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = key0 + nt * 8 + 2 * c + e;
+        bool valid;
+        if (t < 0) valid = key >= max(start, 0) && key < sink_hi;
+        else valid = key >= key_lo && key < key_hi;
+        float x0 = sc[nt][e] * p.scale, x1 = sc[nt][2 + e] * p.scale;
+        if (p.cap > 0.f) {
+          x0 = p.cap * tanhf(x0 / p.cap);
+          x1 = p.cap * tanhf(x1 / p.cap);
+        }
+        if (key < p.num_sinks) {
+          x0 += bias_row0[key];
+          x1 += bias_row1[key];
+        }
+        sc[nt][e] = valid ? x0 : -INFINITY;
+        sc[nt][2 + e] = valid ? x1 : -INFINITY;
+        tmax0 = fmaxf(tmax0, sc[nt][e]);
+        tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
+      }
+    }
+    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
+    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
+    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
+    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
+    const float mn0 = fmaxf(m0, tmax0), mn1 = fmaxf(m1, tmax1);
+    const float alpha0 = mn0 == -INFINITY ? 1.f : ptx::ex2((m0 - mn0) * kLog2e);
+    const float alpha1 = mn1 == -INFINITY ? 1.f : ptx::ex2((m1 - mn1) * kLog2e);
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p0 = mn0 == -INFINITY ? 0.f : ptx::ex2((sc[nt][e] - mn0) * kLog2e);
+        const float p1 = mn1 == -INFINITY ? 0.f : ptx::ex2((sc[nt][2 + e] - mn1) * kLog2e);
+        sc[nt][e] = p0;
+        sc[nt][2 + e] = p1;
+        ps0 += p0;
+        ps1 += p1;
+      }
+    }
+    l0 = l0 * alpha0 + ps0;
+    l1 = l1 * alpha1 + ps1;
+    uint32_t pa[4];
+    pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+    pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+    pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+    pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+    // O = O * alpha + P V  (16 n-tiles of 8 d columns).
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const uint32_t row_addr = vs_base + ((mi & 1) * 8 + ri) * kRowBytes + (mi >> 1) * 16;
+#pragma unroll
+      for (int dn = 0; dn < 16; dn += 2) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4_t(row_addr + dn * 16, b00, b01, b10, b11);
+        o[dn][0] *= alpha0; o[dn][1] *= alpha0; o[dn][2] *= alpha1; o[dn][3] *= alpha1;
+        o[dn + 1][0] *= alpha0; o[dn + 1][1] *= alpha0;
+        o[dn + 1][2] *= alpha1; o[dn + 1][3] *= alpha1;
+        mma_bf16(o[dn], pa, b00, b01);
+        mma_bf16(o[dn + 1], pa, b10, b11);
+      }
+    }
+    __syncwarp();
+    stage = (stage + 1) % kStages;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // Merge the four warps of the CTA through shared memory (reusing the ring).
+  float* s_o = reinterpret_cast<float*>(smem);           // [kWarps][16][kD]
+  float* s_ml = s_o + kWarps * 16 * kD;                    // [kWarps][16][2]
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+  for (int dn = 0; dn < 16; ++dn) {
+    const int d = dn * 8 + 2 * c;
+    s_o[(warp * 16 + g) * kD + d] = o[dn][0];
+    s_o[(warp * 16 + g) * kD + d + 1] = o[dn][1];
+    s_o[(warp * 16 + g + 8) * kD + d] = o[dn][2];
+    s_o[(warp * 16 + g + 8) * kD + d + 1] = o[dn][3];
+  }
+  if (c == 0) {
+    s_ml[(warp * 16 + g) * 2 + 0] = m0;
+    s_ml[(warp * 16 + g) * 2 + 1] = l0;
+    s_ml[(warp * 16 + g + 8) * 2 + 0] = m1;
+    s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
+  }
+  __syncthreads();
+  const int d = threadIdx.x;  // kD == blockDim.x
+  for (int r = 0; r < p.G; ++r) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[(w * 16 + r) * 2]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = s_ml[(w * 16 + r) * 2];
+        const float f = mw == -INFINITY ? 0.f : ptx::ex2((mw - M) * kLog2e);
+        L += f * s_ml[(w * 16 + r) * 2 + 1];
+        O += f * s_o[(w * 16 + r) * kD + d];
+      }
+    }
+    const int hq = h * p.G + r;
+    const long long slot = ((long long)b * p.max_splits + s) * p.Hq + hq;
+    p.o_part[slot * kD + d] = O;
+    if (d == 0) {
+      p.ml_part[slot * 2 + 0] = M;
+      p.ml_part[slot * 2 + 1] = L;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kD)
+decode_combine_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ out,
+                      float* __restrict__ lse) {
+  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+  const int start = p.seq_start[b], end = min(p.seq_end[b], p.S);
+  int n_split = 0;
+  if (end > max(start, 0)) {
+    const int pos = end - 1;
+    const int lo_w = p.window_left >= 0 ? max(max(start, 0), pos - p.window_left) : max(start, 0);
+    n_split = (end - lo_w + kKeysPerCta - 1) / kKeysPerCta;
+  }
+  float M = -INFINITY;
+  for (int s = 0; s < n_split; ++s)
+    M = fmaxf(M, p.ml_part[(((long long)b * p.max_splits + s) * p.Hq + hq) * 2]);
+  float L = 0.f, O = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < n_split; ++s) {
+      const long long slot = ((long long)b * p.max_splits + s) * p.Hq + hq;
+      const float ms = p.ml_part[slot * 2];
+      const float f = ms == -INFINITY ? 0.f : ptx::ex2((ms - M) * kLog2e);
+      L += f * p.ml_part[slot * 2 + 1];
+      O += f * p.o_part[slot * kD + d];
+    }
+  }
+  const long long orow = (long long)b * p.Hq + hq;
+  out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+  if (lse != nullptr && d == 0) lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
+}  // namespace
+
+unsigned read_and_clear_error_decode(cudaStream_t, std::string*) {
+  unsigned w = 0, zero = 0;
+  cudaMemcpyFromSymbol(&w, g_err_decode, sizeof(w));
+  if (w) cudaMemcpyToSymbol(g_err_decode, &zero, sizeof(zero));
+  return w;
+}
+
+static int decode_max_splits(int S, int window_left) {
+  const long long win = window_left >= 0 ? std::min<long long>(S, (long long)window_left + 1) : S;
+  return static_cast<int>(std::max<long long>(1, (win + kKeysPerCta - 1) / kKeysPerCta));
+}
+
+size_t decode_workspace_bytes(int B, int Hq, int S, int D, int window_left) {
+  (void)D;
+  const size_t splits = decode_max_splits(S, window_left);
+  return (size_t)B * splits * Hq * (kD + 2) * sizeof(float);
+}
+
+int launch_ragged_decode(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                         const int32_t* seq_end, int B, int Hq, int Hkv, int S, int D,
+                         float scale, int window_left, int window_right, float cap,
+                         const float* sink_bias, int num_sinks, int sink_per_head, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  (void)D;
+  (void)window_right;  // the query is the last key: a right window never cuts
+  (void)workspace_bytes;
+  if (B > 65535 || Hkv > 65535) return set_error(SBA_ERR_UNSUPPORTED, "ragged_decode: B, Hkv <= 65535");
+  DecodeParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.seq_start = seq_start;
+  p.seq_end = seq_end;
+  p.sink_bias = sink_bias;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.G = Hq / Hkv;
+  p.max_splits = decode_max_splits(S, window_left);
+  p.o_part = static_cast<float*>(workspace);
+  p.ml_part = p.o_part + (size_t)B * p.max_splits * Hq * kD;
+  p.scale = scale;
+  p.cap = cap > 0.f ? cap : 0.f;
+  p.window_left = window_left;
+  p.num_sinks = num_sinks;
+  p.sink_per_head = sink_per_head;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return cuda_error(e, "ragged_decode: set smem attribute");
+    attr_done = true;
+  }
+  dim3 grid(p.max_splits, Hkv, B);
+  decode_split_kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "ragged_decode split launch");
+  decode_combine_kernel<<<dim3(Hq, B), kD, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out), lse);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "ragged_decode combine launch");
+  return SBA_OK;
+}
+
+}  // namespace sba

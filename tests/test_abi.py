@@ -1,0 +1,101 @@
+"""C ABI checks that need no GPU: the library builds for sm_103a, loads, exports
+every symbol the header declares, and rejects bad arguments before any launch."""
+
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sba.h")
+
+needs_nvcc = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                                reason="nvcc not available")
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SBA_API\s+[\w\s\*]+?\b(sba_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from selected_block_attention_gb300 import _build
+    import selected_block_attention_gb300 as sba
+
+    _build.build()
+    return sba.load_library()
+
+
+def test_header_declares_expected_entry_points():
+    import selected_block_attention_gb300 as sba
+
+    assert _declared() == sorted(sba.EXPORTED_SYMBOLS)
+
+
+@needs_nvcc
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    assert lib.sba_version().decode().startswith("sba ")
+
+
+@needs_nvcc
+def test_argument_validation_without_launch(lib):
+    c = ctypes
+    fake = c.c_void_p(0x10000)  # never dereferenced: validation fails first
+    # null pointers
+    r = lib.sba_nsa_select_fwd(None, None, None, None, None, 16, 16, None, 0, 1, 64, 4, 1, 128,
+                               64, 1, 0.0, 0, None, None, None)
+    assert r == -1 and b"null" in lib.sba_last_error()
+    # unsupported head dim
+    r = lib.sba_nsa_select_fwd(fake, fake, fake, fake, None, 16, 16, None, 0, 1, 64, 4, 1, 96,
+                               64, 1, 0.0, 0, fake, None, None)
+    assert r == -2 and b"D must be" in lib.sba_last_error()
+    # Hq not a multiple of Hkv
+    r = lib.sba_nsa_select_fwd(fake, fake, fake, fake, None, 16, 16, None, 0, 1, 64, 6, 4, 128,
+                               64, 1, 0.0, 0, fake, None, None)
+    assert r == -1
+    # misaligned pointer
+    r = lib.sba_nsa_select_fwd(c.c_void_p(0x10002), fake, fake, fake, None, 16, 16, None, 0, 1, 64,
+                               4, 1, 128, 64, 1, 0.0, 0, fake, None, None)
+    assert r == -1 and b"aligned" in lib.sba_last_error()
+    # varlen with B > 1
+    r = lib.sba_nsa_select_fwd(fake, fake, fake, fake, None, 16, 16, fake, 3, 2, 64, 4, 1, 128,
+                               64, 1, 0.0, 0, fake, None, None)
+    assert r == -1
+    # bounds: window below -1
+    r = lib.sba_sparse_mask_bounds(fake, fake, fake, fake, 1, 64, 64, 16, 16, 1, -2, 0, -1, fake,
+                                   fake, fake, fake, None)
+    assert r == -1
+    # block-sparse: q_block must be 128
+    r = lib.sba_blocksparse_attn_fwd(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+                                     fake, 1, 256, 4, 2, 128, 64, 64, 1, -1, -1, -1, 0.0, fake,
+                                     None, None)
+    assert r == -2
+    # decode: workspace too small
+    need = lib.sba_ragged_decode_workspace_size(4, 8, 1024, 128, -1)
+    assert need > 0
+    r = lib.sba_ragged_decode_fwd(fake, fake, fake, fake, fake, 4, 8, 2, 1024, 128, 0.0, -1, -1,
+                                  0.0, None, 0, 0, fake, None, fake, need - 1, None)
+    assert r == -1 and b"workspace" in lib.sba_last_error()
+    # decode: too many sinks
+    r = lib.sba_ragged_decode_fwd(fake, fake, fake, fake, fake, 4, 8, 2, 1024, 128, 0.0, -1, -1,
+                                  0.0, fake, 17, 1, fake, None, fake, need, None)
+    assert r == -2
+    assert lib.sba_ragged_decode_workspace_size(0, 8, 1024, 128, -1) == 0
+
+
+def test_workspace_size_grows_with_window():
+    """Host-only arithmetic of the workspace query (library built or not)."""
+    import selected_block_attention_gb300 as sba
+
+    try:
+        lib = sba.load_library()
+    except RuntimeError:
+        pytest.skip("library not built")
+    a = lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, 4096)
+    b = lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, -1)
+    assert 0 < a < b

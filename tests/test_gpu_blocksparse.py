@@ -1,0 +1,85 @@
+"""GPU parity: SparseMask bounds + block-sparse attention vs the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selected_block_attention_gb300 import workloads
+from tests._parity import assert_attention_close, to_np
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def sba():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import selected_block_attention_gb300 as m
+
+    return m
+
+
+def _run(sba, w, kv_block=128, rows=None, heads=None, softmax_scale=None):
+    m = w.mask
+    bounds = sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions,
+                                    m.kv_segment_ids, m.q_blocksize, kv_block, causal=m.causal,
+                                    window_left=m.window_left, window_right=m.window_right,
+                                    padding_segment_id=m.padding_segment_id)
+    out, lse = sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids,
+                                        m.kv_positions, m.kv_segment_ids, *bounds, m.q_blocksize,
+                                        kv_block, causal=m.causal, window_left=m.window_left,
+                                        window_right=m.window_right,
+                                        padding_segment_id=m.padding_segment_id,
+                                        softmax_scale=softmax_scale)
+    sba.check_error()
+    np_ = lambda t: t.cpu().numpy()
+    ref, ref_lse = oracle.blocksparse_attention(
+        to_np(w.q), to_np(w.k), to_np(w.v), np_(m.q_positions), np_(m.q_segment_ids),
+        np_(m.kv_positions), np_(m.kv_segment_ids), np_(bounds[0]), np_(bounds[1]),
+        m.q_blocksize, kv_block, causal=m.causal, window_left=m.window_left,
+        window_right=m.window_right, padding_segment_id=m.padding_segment_id, rows=rows,
+        heads=heads, softmax_scale=softmax_scale)
+    got, gl = to_np(out), to_np(lse)
+    if rows is not None:
+        idx = tuple(np.array(rows).T)
+        got, ref, gl, ref_lse = got[idx], ref[idx], gl[idx], ref_lse[idx]
+    if heads is not None:
+        got, ref, gl, ref_lse = got[..., heads, :], ref[..., heads, :], gl[..., heads], ref_lse[..., heads]
+    return got, ref, gl, ref_lse
+
+
+@pytest.mark.parametrize("kv_block,D", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_small(sba, kv_block, D):
+    w = workloads.blocksparse(device=DEV, B=2, T=1024, Hq=4, Hkv=2, D=D, mean_doc=300,
+                              pad_tail=70, window=(256, 0), seed=500 + kv_block + D)
+    assert_attention_close(*_run(sba, w, kv_block=kv_block), what=f"bsa kb={kv_block} D={D}")
+
+
+@pytest.mark.parametrize("kv_block,D", [(128, 128), (64, 64)])
+def test_large_logits_rescale(sba, kv_block, D):
+    """Scale 0.6 makes logits ~5-7x larger than 1/sqrt(D): running maxima jump by
+    more than 2^8 between blocks, exercising the lazy rescale of O in TMEM."""
+    w = workloads.blocksparse(device=DEV, B=1, T=1024, Hq=4, Hkv=1, D=D, mean_doc=500,
+                              pad_tail=10, window=(300, 0), seed=700 + kv_block + D)
+    assert_attention_close(*_run(sba, w, kv_block=kv_block, softmax_scale=0.6),
+                           what=f"bsa large logits kb={kv_block} D={D}")
+
+
+@pytest.mark.parametrize("window", [(-1, -1), (200, 50), (0, 0)])
+def test_windows_and_noncausal(sba, window):
+    w = workloads.blocksparse(device=DEV, B=1, T=768, Hq=2, Hkv=1, D=128, mean_doc=1000,
+                              pad_tail=0, window=window, seed=600)
+    w.mask.causal = window[0] != 200
+    assert_attention_close(*_run(sba, w), what=f"bsa window {window}")
+
+
+def test_full_size_sampled(sba):
+    """B=4, T=16384, Hq=32, Hkv=8, window (1024, 0): 48 sampled tokens, all heads."""
+    w = workloads.blocksparse(device=DEV)
+    rng = np.random.default_rng(3)
+    rows = [(int(b), int(t)) for b, t in zip(rng.integers(0, 4, 48), rng.integers(0, 16384, 48))]
+    rows += [(0, 0), (3, 16383), (1, 16083), (2, 16084)]
+    assert_attention_close(*_run(sba, w, rows=rows), what="bsa full sampled")

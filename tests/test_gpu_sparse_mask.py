@@ -1,0 +1,91 @@
+"""GPU parity: SparseMask bounds kernel vs the oracle, bit-exact."""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selected_block_attention_gb300 import workloads
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "sparse_mask_causal_4block.txt")
+
+
+@pytest.fixture(scope="module")
+def sba():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import selected_block_attention_gb300 as m
+
+    return m
+
+
+def _check(sba, qp, qs, kp, ks, qb, kb, **kw):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(DEV)
+    got = sba.sparse_mask_bounds(t(qp), t(qs), t(kp), t(ks), qb, kb, **kw)
+    sba.check_error()
+    ref = oracle.sparse_mask_bounds(qp, qs, kp, ks, qb, kb, **kw)
+    for name, g, r in zip(("lower", "upper", "lower_full", "upper_full"), got, ref):
+        np.testing.assert_array_equal(g.cpu().numpy(), r, err_msg=name)
+    return got
+
+
+def test_page_example(sba):
+    rows = np.loadtxt(GOLDEN, dtype=np.int64, comments="#")
+    pos = np.arange(256)[None]
+    seg = np.zeros((1, 256), np.int64)
+    lo, up, _, _ = _check(sba, pos, seg, pos, seg, 64, 64, causal=True)
+    for j, lower, upper in rows:
+        assert (int(lo[0, 0, j]), int(up[0, 0, j])) == (lower, upper)
+
+
+def test_full_size_workload(sba):
+    """B=4, T=16384, block 128, window (1024, 0), documents + 300 padding tokens."""
+    m = workloads.mask(device="cpu")
+    _check(sba, m.q_positions.numpy(), m.q_segment_ids.numpy(), m.kv_positions.numpy(),
+           m.kv_segment_ids.numpy(), 128, 128, causal=True, window_left=1024, window_right=0,
+           padding_segment_id=-1)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_ragged(sba, seed):
+    """Ragged lengths (scalar load path), odd block sizes, windows both sides,
+    non-causal, shuffled positions, several documents and padding."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 4))
+    Tq, Tkv = int(rng.integers(1, 700)), int(rng.integers(1, 700))
+    qb, kb = int(rng.choice([7, 16, 33, 64, 128])), int(rng.choice([5, 16, 32, 100, 128]))
+    qp = np.sort(rng.integers(-5, 900, size=(B, Tq)), axis=1)
+    kp = np.sort(rng.integers(-5, 900, size=(B, Tkv)), axis=1)
+    if seed % 2:
+        rng.shuffle(qp, axis=1)
+    qs = np.sort(rng.integers(0, 6, size=(B, Tq)), axis=1)
+    ks = np.sort(rng.integers(0, 6, size=(B, Tkv)), axis=1)
+    qs[:, -int(rng.integers(0, 40)) or Tq:] = -1
+    ks[:, -int(rng.integers(0, 40)) or Tkv:] = -1
+    wl = int(rng.choice([-1, 0, 37, 128]))
+    wr = int(rng.choice([-1, 0, 64]))
+    _check(sba, qp, qs, kp, ks, qb, kb, causal=bool(seed % 3), window_left=wl, window_right=wr,
+           padding_segment_id=-1)
+
+
+def test_multiple_of_four_vector_path(sba):
+    rng = np.random.default_rng(9)
+    T = 4096
+    seg = np.sort(rng.integers(0, 12, size=(2, T)), axis=1)
+    seg[:, -100:] = 77  # another padding id
+    pos = np.broadcast_to(np.arange(T), (2, T))
+    _check(sba, pos, seg, pos, seg, 64, 128, causal=True, window_left=300, window_right=-1,
+           padding_segment_id=77)
+
+
+def test_many_kv_blocks_chunked(sba):
+    """More key blocks than one shared-memory chunk holds (1024)."""
+    T = 40000
+    pos = np.arange(T)[None]
+    seg = (np.arange(T) // 5000)[None]
+    _check(sba, pos, seg, pos, seg, 512, 32, causal=True, window_left=2000, window_right=-1)
