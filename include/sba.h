@@ -184,6 +184,34 @@ SBA_API int sba_ragged_decode_fwd(const void* q, const void* k, const void* v,
                           void* workspace, size_t workspace_bytes, sba_stream_t stream);
 
 /*
+ * sba_ragged_decode_fwd_noalloc -- sba_ragged_decode_fwd without a workspace argument.
+ *
+ * The pages have no counterpart of this entry point; it exists for callers that cannot
+ * allocate device memory when they call the library (device memory owned by another
+ * allocator with a fixed budget, plugin interfaces that receive only input and output
+ * buffers, loops that must not incur the device-wide synchronisation of
+ * cudaMalloc/cudaFree).  The split partials live in a 16 MiB array inside the library:
+ * every GPU that loads the library reserves it until the process exits.  Arguments,
+ * layouts and results are those of sba_ragged_decode_fwd.
+ *  - Sizes whose sba_ragged_decode_workspace_size() exceeds 16 MiB are rejected with
+ *    SBA_ERR_INVALID_ARG (use sba_ragged_decode_fwd with a workspace instead).
+ *  - The first call on each device looks up the array's device address (with that device
+ *    current) and caches it; make that first call before any stream capture.
+ *  - All calls on a device share the array: calls that may overlap on the GPU (different
+ *    streams, no ordering between them) race and corrupt each other's results.  Calls on
+ *    one stream are ordered and safe.
+ *  - Nothing is allocated, here or in the first-call set-up.
+ */
+SBA_API int sba_ragged_decode_fwd_noalloc(const void* q, const void* k, const void* v,
+                                          const int32_t* seq_start, const int32_t* seq_end,
+                                          int B, int Hq, int Hkv, int S, int D,
+                                          float softmax_scale, int window_left,
+                                          int window_right, float logits_soft_cap,
+                                          const float* sink_bias, int num_sinks,
+                                          int sink_bias_per_head, void* out, float* lse,
+                                          sba_stream_t stream);
+
+/*
  * sba_check_error -- synchronise `stream`, then read and clear the device-side error
  * word of every kernel of this library.  Returns SBA_OK, SBA_ERR_TIMEOUT (a kernel
  * gave up on a bounded internal wait and returned early), SBA_ERR_DEVICE_INPUT (a

@@ -23,6 +23,8 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
+#include <string>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -412,3 +414,70 @@ int launch_ragged_decode(const void* q, const void* k, const void* v, const int3
 }
 
 }  // namespace sba
+
+// ---------------------------------------------------------------------------------------
+// Decode without caller-provided workspace.
+//
+// Some callers cannot allocate device memory at call time: a host application whose
+// device memory is owned by another allocator with a fixed budget, a plugin interface
+// that hands the library nothing but its input and output buffers, or a serving loop
+// that must not take the device-wide synchronisation a cudaMalloc/cudaFree can cause.
+// For them the split partials live in a fixed array inside the library.  Every GPU that
+// loads the library reserves this array until the process exits, and every call on a
+// device shares it.
+namespace sba {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB of fp32 partials
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The array's name in host
+// code is only a host-side stand-in, so the address is looked up once per device (with
+// that device current) and cached.
+int scratch_for_current_device(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "sba_ragged_decode_fwd_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(SBA_ERR_UNSUPPORTED, "sba_ragged_decode_fwd_noalloc: device ordinal >= 64");
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return cuda_error(e, "sba_ragged_decode_fwd_noalloc: cudaGetSymbolAddress(scratch)");
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return SBA_OK;
+}
+
+}  // namespace
+}  // namespace sba
+
+extern "C" SBA_API int sba_ragged_decode_fwd_noalloc(
+    const void* q, const void* k, const void* v, const int32_t* seq_start, const int32_t* seq_end,
+    int B, int Hq, int Hkv, int S, int D, float softmax_scale, int window_left, int window_right,
+    float logits_soft_cap, const float* sink_bias, int num_sinks, int sink_bias_per_head,
+    void* out, float* lse, sba_stream_t stream) {
+  using namespace sba;
+  const size_t need = sba_ragged_decode_workspace_size(B, Hq, S, D, window_left);
+  if (need > kNoAllocScratchBytes)
+    return set_error(SBA_ERR_INVALID_ARG,
+                     "sba_ragged_decode_fwd_noalloc: these sizes need " + std::to_string(need) +
+                         " bytes of split partials, more than the built-in " +
+                         std::to_string(kNoAllocScratchBytes) +
+                         " bytes; use sba_ragged_decode_fwd with a workspace");
+  void* scratch = nullptr;
+  const int rc = scratch_for_current_device(&scratch);
+  if (rc != SBA_OK) return rc;
+  // The partials need no initialisation: every slot the combine kernel reads is written
+  // by the split kernel of the same call.
+  return sba_ragged_decode_fwd(q, k, v, seq_start, seq_end, B, Hq, Hkv, S, D, softmax_scale,
+                               window_left, window_right, logits_soft_cap, sink_bias, num_sinks,
+                               sink_bias_per_head, out, lse, scratch, kNoAllocScratchBytes, stream);
+}
