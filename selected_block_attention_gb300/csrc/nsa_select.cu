@@ -5,24 +5,24 @@
 // KV head, only to the key blocks named by block_indices[b, t, h_kv, :count]; the G
 // query heads of a KV head share its keys (GQA); cu_seqlens packs sequences.
 //
-// bf16 path (tensor cores).  Work item = one (token, KV head) "token group".  A
-// persistent CTA per SM walks the items with a warp-specialised pipeline:
-//   warp 0      producer: filters/deduplicates the token's block list (one index per
-//               lane), then TMA-gathers the selected K and V blocks into a shared-memory
-//               ring (128 keys per tile = 128 / block_size blocks; a missing block is
-//               fetched from beyond the last token, which TMA fills with zeros) and the
-//               token's G query rows;
-//   warp 1      MMA issuer (one thread): S^T = K_tile * Q^T with tcgen05
-//               (M = 128 keys, N = 16 query heads, fp32 accumulator in TMEM), then
-//               O_tile^T = V_tile^T * P^T (M = 128 head-dim rows, N = 16);
-//   warps 4..7  softmax warpgroup: one thread per key lane reads its 16 head scores
-//               from TMEM, masks (causal, sequence end, padding block), finds per-head
-//               tile maxima by a warp reduce-scatter plus a shared-memory exchange,
-//               writes P^T (bf16) for the PV MMA, and folds each O_tile (one thread per
-//               head-dim lane) into a register accumulator with the online-softmax
-//               rescale; finally writes O / l and the natural-log LSE.
-// Keys sit on the MMA M dimension and the query heads of one KV head on N, so every
-// gathered block feeds a dense MMA with no padded rows.
+// bf16 path (tensor cores): "union walk".  A work item is a group of NT consecutive
+// tokens and one KV head; its NT * G query rows (token-major, head-minor; NT = 8 when
+// G = 16) fill the M = 128 rows of one tcgen05 MMA.  The item's key set is the union
+// of the blocks its tokens selected (deduplicated, sorted by first key row), walked in
+// tiles of 64 keys; every row keeps only the keys of blocks its own token selected
+// (plus the causal / sequence-end limit), so a union block is gathered once per item
+// and shared by all tokens that picked it.  A persistent CTA per SM runs:
+//   warp 2      item builder: reads the NT tokens' index lists (cu_seqlens binary
+//               search for packed sequences), filters them, and forms the union with a
+//               warp bitonic sort plus a run merge into (first key row, token bitmask);
+//   warp 0      loader: TMA loads of the item's Q rows (one 3D box per 64-wide panel,
+//               double-buffered) and of each K / V tile into a 4-stage ring;
+//   warp 1      MMA issuer (one thread): S = Q K^T (M = 128 rows, N = 64 keys, fp32 in
+//               TMEM, double-buffered), O += P V (N = head dim, O in TMEM per item);
+//   warps 4..7  softmax warpgroup, one thread per row: selection / causal mask, lazy
+//               online softmax (O rescaled only when the running max grows by > 2^8),
+//               P (bf16) written over the K tile it replaces (QK is done with it), and
+//               the epilogue O / l, LSE.
 //
 // fp32 path (CUDA cores, exact fp32 products and sums): one CTA per token group.
 // Tensor cores would round fp32 inputs to tf32, which is not accurate enough for the
@@ -44,27 +44,21 @@ namespace {
 using namespace ptx;
 
 constexpr int kThreads = 256;
-constexpr int kTileKeys = 128;  // MMA M of the S^T product (keys)
-constexpr int kNH = 16;         // MMA N (query heads of one KV head, padded)
-constexpr int kMaxSel = 32;
-constexpr int kItemSlots = 4;
+constexpr int kRows = 128;      // MMA M: NT tokens x G query heads
+constexpr int kTileKeys = 64;   // keys per pipeline tile (MMA N of S = Q K^T)
+constexpr int kNH = 16;         // largest supported G
+constexpr int kMaxNT = 16;      // tokens per item
+constexpr int kMaxSel = 32;     // largest supported S
+constexpr int kMaxUnion = kMaxNT * kMaxSel;
+constexpr int kItemSlots = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-enum Role : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
+enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleBuilder = 4 };
 enum BarId : unsigned {
   kBarItemFull = 1, kBarItemEmpty, kBarQFull, kBarQEmpty, kBarKvFull, kBarKvEmpty, kBarSFull,
-  kBarSEmpty, kBarPFull, kBarPEmpty, kBarOFull, kBarOEmpty, kBarWg
-};
-
-struct Item {
-  int tok;       // global token row b * T + t
-  int hkv;
-  int t_rel;     // position inside the token's sequence
-  int seq_len;
-  int seq_tok0;  // global token row of the sequence start
-  int n_blocks;  // selected blocks after filtering
-  int blocks[kMaxSel];
+  kBarSEmpty, kBarPFull, kBarPvDone, kBarOEmpty
 };
 
 struct Params {
@@ -75,53 +69,53 @@ struct Params {
   float* lse;
   int count_scalar, S, num_seqs;
   int B, T, Hq, Hkv, G, causal, bs;
+  int NT, rows;  // tokens per item, rows used (NT * G <= 128)
   float scale, scale_log2;
   int n_items, n_tok;
 };
 
-template <int D, int BS>
-struct Cfg {
-  static constexpr int kPanels = D * 2 / 128;            // 128-byte panels per row
-  static constexpr int kPanelBytes = kTileKeys * 128;    // 16 KB: one panel of a tile
-  static constexpr int kTileBytes = kPanels * kPanelBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;     // [V tile][K tile]
-  static constexpr int kStages = (kStageBytes <= 32 * 1024) ? 5 : 3;
-  static constexpr int kQPanelBytes = kNH * 128;         // 2 KB
-  static constexpr int kQBytes = kPanels * kQPanelBytes;
-  static constexpr int kPBytes = kTileKeys * kNH * 2;
-  static constexpr int kBlocksPerTile = kTileKeys / BS;
-  static constexpr int kQKSteps = D / 16;
-  static constexpr int kPVSteps = kTileKeys / 16;
-  static constexpr int kPLbo = 256;                      // P^T: stride of 8-key groups
-  static constexpr uint32_t kIdescQK = make_idesc(128, kNH, 1u, false, false);
-  static constexpr uint32_t kIdescPV = make_idesc(128, kNH, 1u, true, true);
-  static constexpr int kOffStages = 0;
-  static constexpr int kOffQ = kStages * kStageBytes;
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;
-  static constexpr int kOffItems = kOffP + 2 * kPBytes;
-  static constexpr int kOffRed = kOffItems + kItemSlots * (int)sizeof(Item);
-  static constexpr int kOffBars = kOffRed + 2 * 4 * kNH * 4;
-  static constexpr int kNumBars = 2 * kItemSlots + 4 + 2 * kStages + 12 + 2;
-  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  static_assert(kSmemBytes <= 232448, "shared memory budget");
+// One union-walk item as the builder hands it to the other roles.
+struct Item {
+  int g, hkv, n_union, n_tiles;
+  unsigned tok_valid;              // bit i: token g * NT + i exists
+  int limit[kMaxNT];               // last key row (absolute) token i may see; -1 if none
+  int ux[kMaxUnion];               // first key row (absolute) of each union block
+  unsigned short ubits[kMaxUnion]; // tokens of the group that selected it
 };
 
-struct Bars {
-  uint64_t* item_full;   // [kItemSlots]
-  uint64_t* item_empty;  // [kItemSlots]
-  uint64_t* q_full;      // [2]
-  uint64_t* q_empty;     // [2]
-  uint64_t* kv_full;     // [kStages]
-  uint64_t* kv_empty;    // [kStages]
-  uint64_t* s_full;      // [2]
-  uint64_t* s_empty;     // [2]
-  uint64_t* p_full;      // [2]
-  uint64_t* p_empty;     // [2]
-  uint64_t* o_full;      // [2]
-  uint64_t* o_empty;     // [2]
-  uint64_t* mma_done;    // [1]
-  uint64_t* wg;          // [1] softmax warpgroup barrier
+template <int D, int BS>
+struct Cfg {
+  static constexpr int kPanels = D / 64;                   // 64-element (128-byte) panels
+  static constexpr int kSegLen = BS < kTileKeys ? BS : kTileKeys;
+  static constexpr int kSegs = kTileKeys / kSegLen;        // union blocks per tile (BS <= 64)
+  static constexpr int kKVPanelBytes = kTileKeys * 128;    // 8 KB
+  static constexpr int kKTileBytes = kPanels * kKVPanelBytes;
+  static constexpr int kPBytes = kRows * 128;              // 128 rows x 64 keys bf16
+  static constexpr int kKPBytes = kKTileBytes > kPBytes ? kKTileBytes : kPBytes;
+  static constexpr int kStageBytes = kKPBytes + kKTileBytes;  // [K, later P][V]
+  static constexpr int kLoadBytes = 2 * kKTileBytes;
+  static constexpr int kQPanelBytes = kRows * 128;
+  static constexpr int kQBytes = kPanels * kQPanelBytes;
+  static constexpr int kItemBytes = (static_cast<int>(sizeof(Item)) + 127) & ~127;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffStages = 2 * kQBytes;
+  static constexpr int kFixed = 2 * kQBytes + kItemSlots * kItemBytes + kMaxUnion * 8 + 1024 + 1024;
+  static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kOffItems = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffSort = kOffItems + kItemSlots * kItemBytes;
+  static constexpr int kOffBars = kOffSort + kMaxUnion * 8;
+  static constexpr int kNumBars = 2 * kItemSlots + 4 + 2 * kStages + 4 + 4;
+  static constexpr int kOffMisc = ((kOffBars + kNumBars * 8) + 15) & ~15;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static constexpr int kSCol = 0;                          // S: 2 x 64 columns
+  static constexpr int kOCol = 2 * kTileKeys;              // O: D columns
+  static constexpr int kTmemCols = 256;
+  static constexpr uint32_t kIdescQK = make_idesc(128, kTileKeys, 1u, false, false);
+  static constexpr uint32_t kIdescPV = make_idesc(128, D, 1u, false, true);
+  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
 };
 
 __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, int& hkv, int& t) {
@@ -129,37 +123,6 @@ __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, i
   const int r = item / p.T;
   hkv = r % p.Hkv;
   b = r / p.Hkv;
-}
-
-// Reduce 16 per-lane values over the 32 lanes of a warp (max or sum); on return lane
-// L holds the result for head (L >> 1) & 15.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce_scatter16(const float* v, int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-  float a[8], b4[4], c2[2];
-  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float send = u16 ? v[j] : v[j + 8];
-    const float keep = u16 ? v[j + 8] : v[j];
-    a[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float send = u8 ? a[j] : a[j + 4];
-    const float keep = u8 ? a[j + 4] : a[j];
-    b4[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const float send = u4 ? b4[j] : b4[j + 2];
-    const float keep = u4 ? b4[j + 2] : b4[j];
-    c2[j] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-  const float send = u2 ? c2[0] : c2[1];
-  const float keep = u2 ? c2[1] : c2[0];
-  float d = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  return op(d, __shfl_xor_sync(0xffffffffu, d, 1));
 }
 
 // Sequence of token t (cu_seqlens may be NULL): start row, length, position inside.
@@ -210,52 +173,158 @@ __device__ __forceinline__ unsigned select_blocks(const Params& p, long long row
   return __ballot_sync(0xffffffffu, valid && !dup);
 }
 
+// ------------------------------------------------------------------ item builder
+// Forms the union of the selected blocks of tokens g*NT .. g*NT+NT-1 for KV head hkv.
+// Keys (first key row << 16 | token bit) are sorted by one warp (bitonic network in
+// shared memory); equal rows are merged by OR-ing their token bits.
+template <int BS>
+__device__ __forceinline__ void build_item(const Params& p, int g, int hkv, int lane,
+                                           int& cached_seq, Item& it, uint64_t* keys) {
+  const unsigned kFull = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int tok = g * p.NT + lane;
+  const bool tv = lane < p.NT && tok < p.n_tok;
+  int seq0 = 0, slen = 0, trel = 0, cnt = 0, limit = -1;
+  if (tv) {
+    const int b = p.cu_seqlens ? 0 : tok / p.T;
+    const int t = p.cu_seqlens ? tok : tok - b * p.T;
+    if (locate_token(p, b, t, cached_seq, seq0, slen, trel)) {
+      cnt = p.block_counts ? p.block_counts[(long long)tok * p.Hkv + hkv] : p.count_scalar;
+      cnt = min(max(cnt, 0), p.S);
+      limit = p.causal ? tok : seq0 + slen - 1;
+    }
+  }
+  // all index loads first (independent of the counts), then filter
+  const int total = p.NT * p.S;
+  constexpr int kChunks = kMaxUnion / 32;
+  int ev[kChunks];
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    const int idx = c * 32 + lane;
+    ev[c] = -1;
+    if (idx < total) {
+      const int i = idx / p.S, j = idx - i * p.S;
+      const int trow = g * p.NT + i;
+      if (trow < p.n_tok) ev[c] = p.block_indices[((long long)trow * p.Hkv + hkv) * p.S + j];
+    }
+  }
+  int n = 0;
+#pragma unroll
+  for (int c = 0; c < kChunks; ++c) {
+    if (c * 32 >= total) break;
+    const int idx = c * 32 + lane;
+    const int i = idx < total ? idx / p.S : 0;
+    const int j = idx - i * p.S;
+    const int cnt_i = __shfl_sync(kFull, cnt, i);
+    const int seq0_i = __shfl_sync(kFull, seq0, i);
+    const int slen_i = __shfl_sync(kFull, slen, i);
+    const int trel_i = __shfl_sync(kFull, trel, i);
+    const int e = ev[c];
+    const int nb = (slen_i + BS - 1) / BS;
+    const bool valid = idx < total && j < cnt_i && e >= 0 && e < nb && (!p.causal || e * BS <= trel_i);
+    const unsigned bal = __ballot_sync(kFull, valid);
+    if (valid)
+      keys[n + __popc(bal & lt_mask)] =
+          (static_cast<uint64_t>(static_cast<uint32_t>(seq0_i + e * BS)) << 16) | (1u << i);
+    n += __popc(bal);
+  }
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int idx = n + lane; idx < N; idx += 32) keys[idx] = ~0ull;
+  __syncwarp();
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int idx = lane; idx < N; idx += 32) {
+        const int ixj = idx ^ jj;
+        if (ixj > idx) {
+          const uint64_t a = keys[idx], b = keys[ixj];
+          if ((a > b) == ((idx & k) == 0)) {
+            keys[idx] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  int nu = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int idx = base + lane;
+    bool head = false;
+    uint32_t x = 0;
+    unsigned bits = 0;
+    if (idx < n) {
+      const uint64_t key = keys[idx];
+      x = static_cast<uint32_t>(key >> 16);
+      head = idx == 0 || static_cast<uint32_t>(keys[idx - 1] >> 16) != x;
+      if (head) {
+        bits = static_cast<unsigned>(key & 0xFFFFu);
+        for (int u = idx + 1; u < n; ++u) {
+          const uint64_t k2 = keys[u];
+          if (static_cast<uint32_t>(k2 >> 16) != x) break;
+          bits |= static_cast<unsigned>(k2 & 0xFFFFu);
+        }
+      }
+    }
+    const unsigned bal = __ballot_sync(kFull, head);
+    if (head) {
+      const int pos = nu + __popc(bal & lt_mask);
+      it.ux[pos] = static_cast<int>(x);
+      it.ubits[pos] = static_cast<unsigned short>(bits);
+    }
+    nu += __popc(bal);
+  }
+  if (lane < kMaxNT) it.limit[lane] = limit;
+  const unsigned tv_bits = __ballot_sync(kFull, tv);
+  if (lane == 0) {
+    it.g = g;
+    it.hkv = hkv;
+    it.n_union = nu;
+    it.n_tiles = BS <= kTileKeys ? (nu * BS + kTileKeys - 1) / kTileKeys : nu * (BS / kTileKeys);
+    it.tok_valid = tv_bits;
+  }
+  __syncwarp();
+}
+
 template <int D, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
-nsa_select_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
+nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const Params p) {
   using C = Cfg<D, BS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Item* items = reinterpret_cast<Item*>(smem + C::kOffItems);
-  float* red = reinterpret_cast<float*>(smem + C::kOffRed);  // [2][4][16]
-  uint64_t* bar_base = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem + C::kOffSort);
+  uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* item_full = bb;   bb += kItemSlots;
+  uint64_t* item_empty = bb;  bb += kItemSlots;
+  uint64_t* q_full = bb;      bb += 2;
+  uint64_t* q_empty = bb;     bb += 2;
+  uint64_t* kv_full = bb;     bb += C::kStages;
+  uint64_t* kv_empty = bb;    bb += C::kStages;
+  uint64_t* s_full = bb;      bb += 2;
+  uint64_t* s_empty = bb;     bb += 2;
+  uint64_t* p_full = bb;      bb += 1;
+  uint64_t* pv_done = bb;     bb += 1;
+  uint64_t* o_empty = bb;     bb += 1;
+  uint64_t* mma_done = bb;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Abort ab{abort_flag, &g_err_nsa, 1u};
-
-  Bars bars;
-  {
-    uint64_t* b = bar_base;
-    bars.item_full = b; b += kItemSlots;
-    bars.item_empty = b; b += kItemSlots;
-    bars.q_full = b; b += 2;
-    bars.q_empty = b; b += 2;
-    bars.kv_full = b; b += C::kStages;
-    bars.kv_empty = b; b += C::kStages;
-    bars.s_full = b; b += 2;
-    bars.s_empty = b; b += 2;
-    bars.p_full = b; b += 2;
-    bars.p_empty = b; b += 2;
-    bars.o_full = b; b += 2;
-    bars.o_empty = b; b += 2;
-    bars.mma_done = b; b += 1;
-    bars.wg = b;
-  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto item_at = [&](int slot) -> Item& {
+    return *reinterpret_cast<Item*>(smem + C::kOffItems + slot * C::kItemBytes);
+  };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&bars.item_full[i], 1); mbar_init(&bars.item_empty[i], 2); }
+    // item slots are released by the loader, the MMA thread and the 4 softmax warps
+    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 6); }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.q_full[i], 1); mbar_init(&bars.q_empty[i], 1);
-      mbar_init(&bars.s_full[i], 1); mbar_init(&bars.s_empty[i], 4);
-      mbar_init(&bars.p_full[i], 4); mbar_init(&bars.p_empty[i], 1);
-      mbar_init(&bars.o_full[i], 1); mbar_init(&bars.o_empty[i], 4);
+      mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
     }
-    for (int i = 0; i < C::kStages; ++i) { mbar_init(&bars.kv_full[i], 1); mbar_init(&bars.kv_empty[i], 1); }
-    mbar_init(bars.mma_done, 1);
-    mbar_init(bars.wg, 4);
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    mbar_init(p_full, 4); mbar_init(pv_done, 1); mbar_init(o_empty, 4); mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -263,7 +332,7 @@ nsa_select_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     tma_prefetch_desc(&tm_v);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, 64);
+    tmem_alloc(tmem_holder, C::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -272,95 +341,87 @@ nsa_select_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   const uint32_t tmem = *tmem_holder;
   const uint32_t smem_base = smem_u32(smem);
 
-  if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+  if (warp == 2) {
+    // ------------------------------------------------------------------ item builder
+    int islot = 0; uint32_t iphase = 0;
+    int cached_seq = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+      const int g = item / p.Hkv, hkv = item - g * p.Hkv;
+      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, item)) break;
+      build_item<BS>(p, g, hkv, lane, cached_seq, item_at(islot), keys);
+      if (lane == 0) mbar_arrive(&item_full[islot]);
+      if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
     int qslot = 0; uint32_t qphase = 0;
     int stage = 0; uint32_t kvphase = 0;
-    uint32_t last_kv_parity[8];
     bool kv_issued[8];
-    bool q_issued[2] = {false, false};
-    uint32_t last_q_parity[2] = {0, 0};
+    uint32_t last_kv_parity[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) { kv_issued[i] = false; last_kv_parity[i] = 0; }
-    int cached_seq = 0;
+    bool q_issued[2] = {false, false};
+    uint32_t last_q_parity[2] = {0, 0};
+    const uint32_t q_box_bytes = static_cast<uint32_t>(C::kPanels * 128 * p.G * p.NT);
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-      int b, hkv, t;
-      decode_item(p, item, b, hkv, t);
-      int seq_tok0, seq_len, t_rel;
-      const bool seq_ok = locate_token(p, b, t, cached_seq, seq_tok0, seq_len, t_rel);
-      const long long row = ((long long)b * p.T + t) * p.Hkv + hkv;
-      int count = p.block_counts ? p.block_counts[row] : p.count_scalar;
-      count = seq_ok ? min(max(count, 0), p.S) : 0;
-      int e;
-      const unsigned ballot = select_blocks(p, row, count, seq_len, t_rel, BS, lane, e);
-      const int n_blocks = __popc(ballot);
-      if (!warp_wait(&bars.item_empty[islot], iphase ^ 1, ab, kRoleProducer, kBarItemEmpty, item)) break;
-      Item& it = items[islot];
-      if ((ballot >> lane) & 1u) it.blocks[__popc(ballot & ((1u << lane) - 1u))] = e;
-      if (lane == 0) {
-        it.tok = b * p.T + t;
-        it.hkv = hkv;
-        it.t_rel = t_rel;
-        it.seq_len = seq_len;
-        it.seq_tok0 = seq_tok0;
-        it.n_blocks = n_blocks;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.item_full[islot]);
-      if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
-      if (n_blocks == 0) continue;
-
-      if (!warp_wait(&bars.q_empty[qslot], qphase ^ 1, ab, kRoleProducer, kBarQEmpty, item)) break;
-      if (lane == 0) {
-        uint64_t* fb = &bars.q_full[qslot];
-        mbar_arrive_expect_tx(fb, C::kQBytes);
-        uint8_t* dst = smem + C::kOffQ + qslot * C::kQBytes;
-        const int qrow = (b * p.T + t) * p.Hq + hkv * p.G;
-#pragma unroll
-        for (int pn = 0; pn < C::kPanels; ++pn)
-          tma_load_2d(dst + pn * C::kQPanelBytes, &tm_q, fb, pn * 64, qrow);
-      }
-      q_issued[qslot] = true;
-      last_q_parity[qslot] = qphase;
-      if (++qslot == 2) { qslot = 0; qphase ^= 1; }
-
-      const int tiles = (n_blocks + C::kBlocksPerTile - 1) / C::kBlocksPerTile;
-      for (int ti = 0; ti < tiles; ++ti) {
-        if (!warp_wait(&bars.kv_empty[stage], kvphase ^ 1, ab, kRoleProducer, kBarKvEmpty, item)) {
-          ok = false;
-          break;
-        }
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, item)) break;
+      const Item& it = item_at(islot);
+      const int nt = it.n_tiles, nu = it.n_union, hkv = it.hkv;
+      if (nt > 0) {
+        if (!warp_wait(&q_empty[qslot], qphase ^ 1, ab, kRoleLoader, kBarQEmpty, item)) break;
         if (lane == 0) {
-          uint64_t* fb = &bars.kv_full[stage];
-          mbar_arrive_expect_tx(fb, C::kStageBytes);
-          uint8_t* vdst = smem + C::kOffStages + stage * C::kStageBytes;
-          uint8_t* kdst = vdst + C::kTileBytes;
+          uint64_t* fb = &q_full[qslot];
+          mbar_arrive_expect_tx(fb, q_box_bytes);
+          uint8_t* dst = smem + C::kOffQ + qslot * C::kQBytes;
 #pragma unroll
-          for (int sub = 0; sub < C::kBlocksPerTile; ++sub) {
-            const int bi = ti * C::kBlocksPerTile + sub;
-            // a missing block is read from beyond the last token: TMA fills zeros
-            const int tok0 = bi < n_blocks ? seq_tok0 + it.blocks[bi] * BS : p.n_tok;
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_load_3d(dst + pn * C::kQPanelBytes, &tm_q, fb, pn * 64, hkv * p.G, it.g * p.NT);
+        }
+        q_issued[qslot] = true;
+        last_q_parity[qslot] = qphase;
+        if (++qslot == 2) { qslot = 0; qphase ^= 1; }
+        for (int t = 0; t < nt; ++t) {
+          if (!warp_wait(&kv_empty[stage], kvphase ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
+          if (lane == 0) {
+            uint64_t* fb = &kv_full[stage];
+            mbar_arrive_expect_tx(fb, C::kLoadBytes);
+            uint8_t* kdst = smem + C::kOffStages + stage * C::kStageBytes;
+            uint8_t* vdst = kdst + C::kKPBytes;
 #pragma unroll
-            for (int pn = 0; pn < C::kPanels; ++pn) {
-              const int off = pn * C::kPanelBytes + sub * BS * 128;
-              tma_load_3d(kdst + off, &tm_k, fb, pn * 64, hkv, tok0);
-              tma_load_3d(vdst + off, &tm_v, fb, pn * 64, hkv, tok0);
+            for (int e = 0; e < C::kSegs; ++e) {
+              int row0;
+              if constexpr (BS <= kTileKeys) {
+                const int ui = t * C::kSegs + e;
+                // a missing block is read from beyond the last token: TMA fills zeros
+                row0 = ui < nu ? it.ux[ui] : p.n_tok;
+              } else {
+                row0 = it.ux[t / (BS / kTileKeys)] + (t % (BS / kTileKeys)) * kTileKeys;
+              }
+#pragma unroll
+              for (int pn = 0; pn < C::kPanels; ++pn) {
+                const int off = pn * C::kKVPanelBytes + e * C::kSegLen * 128;
+                tma_load_3d(kdst + off, &tm_k, fb, pn * 64, hkv, row0);
+                tma_load_3d(vdst + off, &tm_v, fb, pn * 64, hkv, row0);
+              }
             }
           }
+          kv_issued[stage] = true;
+          last_kv_parity[stage] = kvphase;
+          if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
         }
-        kv_issued[stage] = true;
-        last_kv_parity[stage] = kvphase;
-        if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
+      if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
     }
     // Drain: wait (bounded) for every copy this warp issued before the CTA exits.
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s)
-        if (kv_issued[s]) drain_wait(&bars.kv_full[s], last_kv_parity[s]);
+        if (kv_issued[s]) drain_wait(&kv_full[s], last_kv_parity[s]);
       for (int s = 0; s < 2; ++s)
-        if (q_issued[s]) drain_wait(&bars.q_full[s], last_q_parity[s]);
+        if (q_issued[s]) drain_wait(&q_full[s], last_q_parity[s]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
@@ -369,218 +430,232 @@ nsa_select_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       int qslot = 0; uint32_t qphase = 0;
       int stage = 0; uint32_t kvphase = 0;
       int sbuf = 0; uint32_t sphase = 0;
-      int pbuf = 0; uint32_t pphase = 0;
-      int obuf = 0; uint32_t ophase = 0;
+      uint32_t pphase = 0, ophase = 0;
       int pending_stage = -1;
+      bool pending_first = false;
       int cur_item = -1;
       bool ok = true;
-      auto issue_pv = [&](int st) -> bool {
-        if (!bounded_wait(&bars.p_full[pbuf], pphase, ab, kRoleMma, kBarPFull, cur_item)) return false;
-        if (!bounded_wait(&bars.o_empty[obuf], ophase ^ 1, ab, kRoleMma, kBarOEmpty, cur_item)) return false;
-        tc_fence_after();
-        const uint32_t v_addr = smem_base + C::kOffStages + st * C::kStageBytes;
-        const uint32_t p_addr = smem_base + C::kOffP + pbuf * C::kPBytes;
-        const uint32_t d_tmem = tmem + 32 + obuf * 16;
-#pragma unroll
-        for (int k = 0; k < C::kPVSteps; ++k) {
-          const uint64_t a = make_sdesc(v_addr + k * 16 * 128, C::kPanelBytes, 1024, kLayoutSW128);
-          const uint64_t bd = make_sdesc(p_addr + k * 2 * C::kPLbo, C::kPLbo, 128, kLayoutNone);
-          mma_f16_ss(d_tmem, a, bd, C::kIdescPV, k > 0);
+      auto issue_pv = [&](int st, bool first) -> bool {
+        if (!bounded_wait(p_full, pphase, ab, kRoleMma, kBarPFull, cur_item)) return false;
+        pphase ^= 1;
+        if (first) {
+          if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, cur_item)) return false;
+          ophase ^= 1;
         }
-        mma_commit(&bars.kv_empty[st]);
-        mma_commit(&bars.p_empty[pbuf]);
-        mma_commit(&bars.o_full[obuf]);
-        if (++pbuf == 2) { pbuf = 0; pphase ^= 1; }
-        if (++obuf == 2) { obuf = 0; ophase ^= 1; }
+        tc_fence_after();
+        const uint32_t p_addr = smem_base + C::kOffStages + st * C::kStageBytes;
+        const uint32_t v_addr = p_addr + C::kKPBytes;
+#pragma unroll
+        for (int k = 0; k < kTileKeys / 16; ++k) {
+          const uint64_t a = make_sdesc(p_addr + k * 32, 16, 1024, kLayoutSW128);
+          const uint64_t bd = make_sdesc(v_addr + k * 16 * 128, C::kKVPanelBytes, 1024, kLayoutSW128);
+          mma_f16_ss(tmem + C::kOCol, a, bd, C::kIdescPV, (first && k == 0) ? 0u : 1u);
+        }
+        mma_commit(&kv_empty[st]);
+        mma_commit(pv_done);
         return true;
       };
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         cur_item = item;
-        if (!bounded_wait(&bars.item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
-        const int n_blocks = items[islot].n_blocks;
-        const int tiles = (n_blocks + C::kBlocksPerTile - 1) / C::kBlocksPerTile;
-        if (tiles == 0) {
+        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        const int nt = item_at(islot).n_tiles;
+        mbar_arrive(&item_empty[islot]);
+        if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+        if (nt == 0) {
           // nothing to compute: release the deferred PV now so the softmax group, which
           // waits for it before finishing the previous item, never starves
           if (pending_stage >= 0) {
-            if (!issue_pv(pending_stage)) break;
+            if (!issue_pv(pending_stage, pending_first)) break;
             pending_stage = -1;
           }
-          mbar_arrive(&bars.item_empty[islot]);
-          if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
           continue;
         }
-        if (!bounded_wait(&bars.q_full[qslot], qphase, ab, kRoleMma, kBarQFull, item)) break;
+        if (!bounded_wait(&q_full[qslot], qphase, ab, kRoleMma, kBarQFull, item)) break;
         const uint32_t q_addr = smem_base + C::kOffQ + qslot * C::kQBytes;
-        for (int ti = 0; ti < tiles; ++ti) {
-          if (!bounded_wait(&bars.kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
-              !bounded_wait(&bars.s_empty[sbuf], sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) {
-            ok = false;
-            break;
-          }
+        for (int t = 0; t < nt; ++t) {
+          if (!bounded_wait(&kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
+              !bounded_wait(&s_empty[sbuf], sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t k_addr = smem_base + C::kOffStages + stage * C::kStageBytes + C::kTileBytes;
-          const uint32_t d_tmem = tmem + sbuf * 16;
+          const uint32_t k_addr = smem_base + C::kOffStages + stage * C::kStageBytes;
 #pragma unroll
-          for (int k = 0; k < C::kQKSteps; ++k) {
+          for (int k = 0; k < D / 16; ++k) {
             const int pn = k / 4, kk = k % 4;
-            const uint64_t a = make_sdesc(k_addr + pn * C::kPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
-            const uint64_t bd = make_sdesc(q_addr + pn * C::kQPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
-            mma_f16_ss(d_tmem, a, bd, C::kIdescQK, k > 0);
+            const uint64_t a = make_sdesc(q_addr + pn * C::kQPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
+            const uint64_t bd = make_sdesc(k_addr + pn * C::kKVPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
+            mma_f16_ss(tmem + C::kSCol + sbuf * kTileKeys, a, bd, C::kIdescQK, k > 0);
           }
-          mma_commit(&bars.s_full[sbuf]);
-          if (ti == tiles - 1) mma_commit(&bars.q_empty[qslot]);
-          if (pending_stage >= 0 && !issue_pv(pending_stage)) { ok = false; break; }
+          mma_commit(&s_full[sbuf]);
+          if (t == nt - 1) mma_commit(&q_empty[qslot]);
+          if (pending_stage >= 0 && !issue_pv(pending_stage, pending_first)) { ok = false; break; }
           pending_stage = stage;
+          pending_first = (t == 0);
           if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
           if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
         }
-        if (!ok) break;
-        mbar_arrive(&bars.item_empty[islot]);
-        if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         if (++qslot == 2) { qslot = 0; qphase ^= 1; }
       }
-      if (ok && pending_stage >= 0) issue_pv(pending_stage);
+      if (ok && pending_stage >= 0) issue_pv(pending_stage, pending_first);
       // every tcgen05 op issued by this thread has finished once mma_done fires
-      mma_commit(bars.mma_done);
-      drain_wait(bars.mma_done, 0);
+      mma_commit(mma_done);
+      drain_wait(mma_done, 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
-    const int q4 = warp - 4;            // TMEM lane quadrant
-    const int r = q4 * 32 + lane;       // key lane (S^T) and head-dim lane (O^T)
+    const int q4 = warp - 4;
+    const int r = q4 * 32 + lane;  // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int ti = r < p.rows ? r / p.G : 0;  // token of this row within the item
+    const int h = r - ti * p.G;
     int islot = 0; uint32_t iphase = 0;
+    int stage = 0;
     int sbuf = 0; uint32_t sphase = 0;
-    int pbuf = 0; uint32_t pphase = 0;
-    int obuf = 0; uint32_t ophase = 0;
-    uint32_t wg_phase = 0;
-    int par = 0;
+    uint32_t pvphase = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-      if (!warp_wait(&bars.item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
-      const Item& it = items[islot];
-      const int n_blocks = it.n_blocks;
-      const int tiles = (n_blocks + C::kBlocksPerTile - 1) / C::kBlocksPerTile;
-      const int tok = it.tok, hkv = it.hkv, t_rel = it.t_rel, seq_len = it.seq_len;
-      const long long out_row0 = (long long)tok * p.Hq + (long long)hkv * p.G;
-      float m[kNH], l[kNH], o[kNH], m_acc[kNH], m_pend[kNH];
-#pragma unroll
-      for (int h = 0; h < kNH; ++h) { m[h] = -INFINITY; l[h] = 0.f; o[h] = 0.f; m_acc[h] = -INFINITY; m_pend[h] = -INFINITY; }
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
+      const Item& it = item_at(islot);
+      const int nt = it.n_tiles, nu = it.n_union;
+      const bool row_ok = r < p.rows && ((it.tok_valid >> ti) & 1u);
+      const int limit = r < p.rows ? it.limit[ti] : -1;
+      const unsigned tbit = 1u << ti;
+      float m = -INFINITY, l = 0.f;
       bool ok = true;
-      auto accumulate_o = [&]() -> bool {
-        if (!warp_wait(&bars.o_full[obuf], ophase, ab, kRoleSoftmax, kBarOFull, item)) return false;
-        tc_fence_after();
-        float ov[kNH];
-        tmem_ld_32x32b_x16(tmem + lane_off + 32 + obuf * 16, ov);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.o_empty[obuf]);
-        if (++obuf == 2) { obuf = 0; ophase ^= 1; }
+      for (int t = 0; t < nt; ++t) {
+        // valid keys of each segment of the tile for this row's token
+        int nv[C::kSegs];
+        int nvsum = 0;
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          const float f = m_acc[h] == -INFINITY ? 0.f : ex2(m_acc[h] - m_pend[h]);
-          o[h] = o[h] * f + ov[h];
-          m_acc[h] = m_pend[h];
+        for (int e = 0; e < C::kSegs; ++e) {
+          int ui, x0;
+          if constexpr (BS <= kTileKeys) {
+            ui = t * C::kSegs + e;
+            x0 = ui < nu ? it.ux[ui] : 0;
+          } else {
+            ui = t / (BS / kTileKeys);
+            x0 = it.ux[ui] + (t % (BS / kTileKeys)) * kTileKeys;
+          }
+          const bool sel = ui < nu && (it.ubits[ui] & tbit) != 0u;
+          nv[e] = sel ? min(max(limit - x0 + 1, 0), C::kSegLen) : 0;
+          nvsum += nv[e];
         }
-        return true;
-      };
-      for (int ti = 0; ti < tiles; ++ti) {
-        if (!warp_wait(&bars.s_full[sbuf], sphase, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
-        tc_fence_after();
-        float x[kNH];
-        tmem_ld_32x32b_x16(tmem + lane_off + sbuf * 16, x);
+        const bool any = __any_sync(0xffffffffu, nvsum > 0);
+        if (!warp_wait(&s_full[sbuf], sphase, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        float x[kTileKeys];
+        if (any) {
+          tc_fence_after();
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kSCol + sbuf * kTileKeys, x);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kSCol + sbuf * kTileKeys + 32, x + 32);
+        }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.s_empty[sbuf]);
+        if (lane == 0) mbar_arrive(&s_empty[sbuf]);
         if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
-        // key of this lane
-        const int bi = ti * C::kBlocksPerTile + r / BS;
-        const int blk = bi < n_blocks ? it.blocks[bi] : -1;
-        const int key = blk * BS + (r % BS);
-        const bool valid = blk >= 0 && key < seq_len && (!p.causal || key <= t_rel);
+        float tmax = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) x[h] = valid ? x[h] * p.scale_log2 : -INFINITY;
-        // per-head tile maxima over the 128 key lanes
-        const float wmax = warp_reduce_scatter16<true>(x, lane);
-        if ((lane & 1) == 0) red[(par * 4 + q4) * kNH + (lane >> 1)] = wmax;
-        if (!warps_barrier(bars.wg, wg_phase, ab, kRoleSoftmax, kBarWg, item)) { ok = false; break; }
-        float tmax[kNH];
+        for (int e = 0; e < C::kSegs; ++e) {
 #pragma unroll
-        for (int h = 0; h < kNH; h += 4) {
-          float4 a0 = *reinterpret_cast<const float4*>(&red[(par * 4 + 0) * kNH + h]);
-          float4 a1 = *reinterpret_cast<const float4*>(&red[(par * 4 + 1) * kNH + h]);
-          float4 a2 = *reinterpret_cast<const float4*>(&red[(par * 4 + 2) * kNH + h]);
-          float4 a3 = *reinterpret_cast<const float4*>(&red[(par * 4 + 3) * kNH + h]);
-          tmax[h + 0] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
-          tmax[h + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
-          tmax[h + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
-          tmax[h + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
+          for (int jj = 0; jj < C::kSegLen; ++jj) {
+            const int j = e * C::kSegLen + jj;
+            x[j] = jj < nv[e] ? x[j] * p.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, x[j]);
+          }
         }
-        par ^= 1;
-        float pv[kNH];
+        // lazy online softmax: move the reference max only when it grows by > 2^8
+        float m_new = m;
+        if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
+        const float alpha = (m == -INFINITY || m_new == m) ? (m_new == m ? 1.f : 0.f) : ex2(m - m_new);
+        float psum = 0.f;
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) {
-          const float mn = fmaxf(m[h], tmax[h]);
-          const float alpha = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
-          pv[h] = mn == -INFINITY ? 0.f : ex2(x[h] - mn);
-          l[h] = l[h] * alpha + pv[h];
-          m[h] = mn;
+        for (int e = 0; e < C::kSegs; ++e) {
+          if (nv[e] > 0) {
+#pragma unroll
+            for (int jj = 0; jj < C::kSegLen; ++jj) {
+              const int j = e * C::kSegLen + jj;
+              x[j] = ex2(x[j] - m_new);
+              psum += x[j];
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < C::kSegLen; ++jj) x[e * C::kSegLen + jj] = 0.f;
+          }
         }
-        // P^T row of this key lane -> shared memory (MN-major, 16-byte core rows)
-        if (!warp_wait(&bars.p_empty[pbuf], pphase ^ 1, ab, kRoleSoftmax, kBarPEmpty, item)) { ok = false; break; }
-        const uint32_t prow = smem_base + C::kOffP + pbuf * C::kPBytes + (r >> 3) * C::kPLbo + (r & 7) * 16;
+        l = l * alpha + psum;
+        // P row (bf16) over the K tile of this stage: 128-byte swizzled K-major rows
+        const uint32_t prow = smem_base + C::kOffStages + stage * C::kStageBytes + r * 128;
 #pragma unroll
-        for (int hg = 0; hg < 2; ++hg) {
+        for (int cchunk = 0; cchunk < 8; ++cchunk) {
           uint32_t w[4];
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(pv[8 * hg + 2 * j], pv[8 * hg + 2 * j + 1]);
-            w[j] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int u = 0; u < 4; ++u) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(x[cchunk * 8 + 2 * u], x[cchunk * 8 + 2 * u + 1]);
+            w[u] = *reinterpret_cast<uint32_t*>(&h2);
           }
-          st_shared_v4(prow + hg * 128, w[0], w[1], w[2], w[3]);
+          st_shared_v4(prow + ((cchunk ^ (r & 7)) * 16), w[0], w[1], w[2], w[3]);
         }
         fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars.p_full[pbuf]);
-        if (++pbuf == 2) { pbuf = 0; pphase ^= 1; }
-        if (ti > 0 && !accumulate_o()) { ok = false; break; }
+        if (++stage == C::kStages) stage = 0;
+        // the previous PV must be done before O is rescaled
+        if (t > 0) {
+          if (!warp_wait(pv_done, pvphase, ab, kRoleSoftmax, kBarPvDone, item)) { ok = false; break; }
+          pvphase ^= 1;
+          tc_fence_after();
+          // TMEM loads/stores are warp-collective (.sync.aligned): the whole warp rescales
+          // together when any of its rows moved its reference max; other rows use 1.
+          const bool my_rescale = m_new != m && m != -INFINITY;
+          if (__any_sync(0xffffffffu, my_rescale)) {
+            const float f = my_rescale ? alpha : 1.f;
 #pragma unroll
-        for (int h = 0; h < kNH; ++h) m_pend[h] = m[h];
+            for (int c = 0; c < D / 32; ++c) {
+              float ov[32];
+              tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) ov[j] *= f;
+              tmem_st_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+            }
+          }
+        }
+        m = m_new;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
       if (!ok) break;
-      if (tiles > 0) {
-        if (!accumulate_o()) break;
-        // l: sum of the per-lane partial sums over the 128 key lanes
-        const float wsum = warp_reduce_scatter16<false>(l, lane);
-        if ((lane & 1) == 0) red[(par * 4 + q4) * kNH + (lane >> 1)] = wsum;
-        if (!warps_barrier(bars.wg, wg_phase, ab, kRoleSoftmax, kBarWg, item)) break;
-        float lt[kNH];
+      const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+      if (nt > 0) {
+        if (!warp_wait(pv_done, pvphase, ab, kRoleSoftmax, kBarPvDone, item)) break;
+        pvphase ^= 1;
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int h = 0; h < kNH; ++h)
-          lt[h] = red[(par * 4 + 0) * kNH + h] + red[(par * 4 + 1) * kNH + h] +
-                  red[(par * 4 + 2) * kNH + h] + red[(par * 4 + 3) * kNH + h];
-        par ^= 1;
-        if (r < D) {
+        for (int c = 0; c < D / 32; ++c) {
+          float ov[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+          if (row_ok) {
 #pragma unroll
-          for (int h = 0; h < kNH; ++h)
-            if (h < p.G) out[(out_row0 + h) * D + r] = __float2bfloat16_rn(o[h] / lt[h]);
+            for (int j = 0; j < 32; j += 8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[j + 2 * u] * inv, ov[j + 2 * u + 1] * inv);
+                w[u] = *reinterpret_cast<uint32_t*>(&h2);
+              }
+              *reinterpret_cast<uint4*>(out + orow * D + c * 32 + j) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
         }
-        if (p.lse != nullptr && r < p.G) {
-          float mr = m[0], lr = lt[0];
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_empty);
+        if (row_ok && p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      } else if (row_ok) {
 #pragma unroll
-          for (int h = 1; h < kNH; ++h) if (h == r) { mr = m[h]; lr = lt[h]; }
-          p.lse[out_row0 + r] = (mr + log2f(lr)) * kLn2;
-        }
-      } else {
-        if (r < D)
-          for (int h = 0; h < p.G; ++h) out[(out_row0 + h) * D + r] = __float2bfloat16_rn(0.f);
-        if (p.lse != nullptr && r < p.G) p.lse[out_row0 + r] = -INFINITY;
+        for (int j = 0; j < D; j += 8)
+          *reinterpret_cast<uint4*>(out + orow * D + j) = make_uint4(0u, 0u, 0u, 0u);
+        if (p.lse != nullptr) p.lse[orow] = -INFINITY;
       }
-      // all four warps are done with the item descriptor before it is released
-      if (!warps_barrier(bars.wg, wg_phase, ab, kRoleSoftmax, kBarWg, item)) break;
-      if (r == 0) mbar_arrive(&bars.item_empty[islot]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
     }
   }
@@ -589,19 +664,20 @@ nsa_select_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 64);
+    tmem_dealloc(tmem, C::kTmemCols);
   }
 }
 
 // ---------------------------------------------------------------------------- fp32
 constexpr int kF32Threads = 128;
+constexpr int kF32MaxBlock = 128;  // largest block size
 
 template <int D>
 __global__ void __launch_bounds__(kF32Threads)
 nsa_select_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
                       const float* __restrict__ v, const Params p) {
   __shared__ float q_s[kNH][D];
-  __shared__ float s_s[kNH][kTileKeys + 1];
+  __shared__ float s_s[kNH][kF32MaxBlock + 1];
   __shared__ float m_s[kNH], a_s[kNH];
   __shared__ int blocks_s[kMaxSel];
   __shared__ int meta_s[4];
@@ -715,17 +791,19 @@ int launch_bf16(const void* q, const void* k, const void* v, const Params& p, cu
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
   {
-    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.B * p.T * p.Hq};
-    cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    cuuint32_t box[2] = {64, (cuuint32_t)kNH};
-    if (encode_tensor_map(&tq, dt, 2, const_cast<void*>(q), dims, strides, box,
+    // Q as (D, Hq, tokens): one box = 64 head-dim elements x G heads x NT tokens, i.e.
+    // rows (token-major, head-minor) of one item
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.n_tok};
+    cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hq * D * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)p.NT};
+    if (encode_tensor_map(&tq, dt, 3, const_cast<void*>(q), dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return set_error(SBA_ERR_CUDA, "nsa_select: tensor map (q) failed");
   }
   {
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.T};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.n_tok};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)BS};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)C::kSegLen};
     if (encode_tensor_map(&tk, dt, 3, const_cast<void*>(k), dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
         encode_tensor_map(&tv, dt, 3, const_cast<void*>(v), dims, strides, box,
@@ -734,13 +812,13 @@ int launch_bf16(const void* q, const void* k, const void* v, const Params& p, cu
   }
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(nsa_select_kernel<D, BS>,
+    cudaError_t e = cudaFuncSetAttribute(nsa_union_kernel<D, BS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return cuda_error(e, "nsa_select: set smem attribute");
     attr_done = true;
   }
   const int grid = std::min(p.n_items, num_sms());
-  nsa_select_kernel<D, BS><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  nsa_union_kernel<D, BS><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "nsa_select launch");
   return SBA_OK;
@@ -792,13 +870,17 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t
   p.bs = block_size;
   p.scale = scale;
   p.scale_log2 = scale * kLog2e;
+  p.NT = std::min(kMaxNT, kRows / p.G);
+  p.rows = p.NT * p.G;
   if ((long long)B * T * Hkv >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "nsa_select: too many items");
-  p.n_items = B * T * Hkv;
   p.n_tok = B * T;
   if (dtype == SBA_BF16) {
+    const long long groups = (p.n_tok + p.NT - 1) / p.NT;
+    p.n_items = static_cast<int>(groups * Hkv);
     if (D == 128) return dispatch_bs<128>(block_size, q, k, v, p, stream);
     return dispatch_bs<64>(block_size, q, k, v, p, stream);
   }
+  p.n_items = B * T * Hkv;
   const int grid = std::min(p.n_items, 1 << 20);
   if (D == 128)
     nsa_select_f32_kernel<128><<<grid, kF32Threads, 0, stream>>>(

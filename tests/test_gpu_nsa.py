@@ -24,16 +24,17 @@ def sba():
 DEV = "cuda"
 
 
-def _run(sba, w, rows=None):
+def _run(sba, w, rows=None, softmax_scale=None):
     out, lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts, w.block_size,
-                                  cu_seqlens=w.cu_seqlens, causal=w.causal)
+                                  cu_seqlens=w.cu_seqlens, causal=w.causal,
+                                  softmax_scale=softmax_scale)
     sba.check_error()
     counts = w.block_counts if isinstance(w.block_counts, int) else w.block_counts.cpu().numpy()
     cu = None if w.cu_seqlens is None else w.cu_seqlens.cpu().numpy()
     ref, ref_lse = oracle.nsa_select_attention(
         to_np(w.q), to_np(w.k), to_np(w.v),
         w.block_indices.cpu().numpy(), counts, w.block_size, cu_seqlens=cu, causal=w.causal,
-        rows=rows)
+        softmax_scale=softmax_scale, rows=rows)
     got, got_lse = to_np(out), to_np(lse)
     if rows is not None:
         idx = tuple(np.array(rows).T)
@@ -42,7 +43,7 @@ def _run(sba, w, rows=None):
 
 
 def test_tiny_fp32_full(sba):
-    """The 256-token fp32 workload (tf32 tensor cores), every row."""
+    """The 256-token fp32 workload (exact fp32 on CUDA cores), every row."""
     w = workloads.nsa_tiny(device=DEV)
     assert_attention_close(*_run(sba, w), what="nsa_tiny")
 
@@ -94,6 +95,59 @@ def test_varlen_small(sba):
     w = workloads.nsa_varlen(device=DEV, lengths=[100, 257, 1, 64, 190], Hq=8, Hkv=2, D=128,
                              block_size=64, S=4, count=4, seed=11)
     assert_attention_close(*_run(sba, w), what="varlen small")
+
+
+def test_union_full_sort_capacity(sba):
+    """G=8 puts 16 tokens in one item; S=32 entries each (with repeats across tokens and
+    within a token) fill the 512-entry union sort."""
+    rng = np.random.default_rng(21)
+    T, bs = 700, 32
+    w = workloads.nsa_prefill(device=DEV, B=1, T=T, Hq=16, Hkv=2, D=128, block_size=bs, S=32,
+                              max_count=32, seed=21)
+    nb = -(-T // bs)
+    own = (np.arange(T) // bs)[None, :, None, None]
+    idx = rng.integers(0, nb, size=(1, T, 2, 32))
+    idx = np.minimum(idx, own).astype(np.int32)      # mostly past blocks, many repeats
+    idx[..., 0] = own[..., 0]
+    w.block_indices = torch.from_numpy(idx).to(DEV)
+    w.block_counts = torch.full((1, T, 2), 32, dtype=torch.int32, device=DEV)
+    assert_attention_close(*_run(sba, w), what="union sort capacity")
+
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_union_dense_selection(sba, bs):
+    """Every token selects every block up to its own: equals causal dense attention,
+    and every union block is shared by all tokens of an item."""
+    T = 640
+    nb = -(-T // bs)
+    w = workloads.nsa_prefill(device=DEV, B=1, T=T, Hq=32, Hkv=2, D=128, block_size=bs, S=nb,
+                              max_count=nb, seed=30 + bs) if nb <= 32 else None
+    if w is None:
+        pytest.skip("more blocks than selection slots")
+    idx = np.tile(np.arange(nb, dtype=np.int32), (1, T, 2, 1))
+    w.block_indices = torch.from_numpy(idx).to(DEV)
+    w.block_counts = nb
+    assert_attention_close(*_run(sba, w), what=f"dense bs={bs}")
+
+
+@pytest.mark.parametrize("G", [3, 12])
+def test_union_odd_group_sizes(sba, G):
+    """G that does not divide 128: items of 128 // G tokens (at most 16), rows below 128."""
+    w = workloads.nsa_prefill(device=DEV, B=2, T=300, Hq=2 * G, Hkv=2, D=64, block_size=64,
+                              S=8, max_count=8, seed=40 + G)
+    assert_attention_close(*_run(sba, w), what=f"G={G}")
+
+
+def test_union_large_logits_rescale(sba):
+    """Scale 0.5 on N(0,1) data makes per-tile maxima jump by more than 2^8 in log2
+    units between tiles, exercising the lazy rescale of O in TMEM.  Such a peaked
+    softmax copies single V values into the output, and for |v| > 4 the bf16 rounding
+    of the output alone costs up to 2^-6; V is halved (exactly) so the absolute bound
+    measures the rescale and not the output format."""
+    w = workloads.nsa_prefill(device=DEV, B=1, T=1024, Hq=32, Hkv=2, D=128, block_size=64,
+                              S=16, max_count=16, seed=50)
+    w.v = w.v * 0.5
+    assert_attention_close(*_run(sba, w, softmax_scale=0.5), what="large logits")
 
 
 def test_prefill_full_size_sampled(sba):
