@@ -15,14 +15,23 @@
 //   warp 2      item builder: reads the NT tokens' index lists (cu_seqlens binary
 //               search for packed sequences), filters them, and forms the union with a
 //               warp bitonic sort plus a run merge into (first key row, token bitmask);
-//   warp 0      loader: TMA loads of the item's Q rows (one 3D box per 64-wide panel,
-//               double-buffered) and of each K / V tile into a 4-stage ring;
-//   warp 1      MMA issuer (one thread): S = Q K^T (M = 128 rows, N = 64 keys, fp32 in
-//               TMEM, double-buffered), O += P V (N = head dim, O in TMEM per item);
-//   warps 4..7  softmax warpgroup, one thread per row: selection / causal mask, lazy
-//               online softmax (O rescaled only when the running max grows by > 2^8),
-//               P (bf16) written over the K tile it replaces (QK is done with it), and
-//               the epilogue O / l, LSE.
+//   warp 0      loader: TMA loads of the item's Q rows (one 3D box per 64-wide panel)
+//               into a staging buffer and of each K / V tile into a shared-memory ring;
+//   warp 1      QK issuer (one thread): copies Q into tensor memory (tcgen05.cp, in
+//               order with its MMAs), then S = Q K^T (M = 128 rows, N = 64 keys, A from
+//               TMEM, fp32 in TMEM);
+//   warp 3      PV issuer (one thread): O += P V (N = head dim, A = P from TMEM).  With
+//               both A operands in TMEM the MMAs read only K and V from shared memory,
+//               and with two issuing threads one's barrier waits overlap the other's
+//               MMAs;
+//   warps 4..11 two softmax warpgroups, one thread per row each.  Tiles alternate
+//               between them (tile t -> warpgroup t & 1), each with its own S buffer,
+//               running (m, l) and O accumulator, so two tiles' softmax overlap the MMAs.
+//               Per tile: selection / causal mask, lazy online softmax (O rescaled only
+//               when the running max grows by > 2^8), P (bf16) stored to TMEM.  The
+//               epilogue merges the two partial results ((m, l) exchanged through
+//               shared memory; each warpgroup writes half of the head-dim columns) and
+//               writes O / l and the LSE.
 //
 // fp32 path (CUDA cores, exact fp32 products and sums): one CTA per token group.
 // Tensor cores would round fp32 inputs to tf32, which is not accurate enough for the
@@ -43,7 +52,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;   // warps 0-3: loader, MMA, builder, spare; 4-11: two softmax warpgroups
 constexpr int kRows = 128;      // MMA M: NT tokens x G query heads
 constexpr int kTileKeys = 64;   // keys per pipeline tile (MMA N of S = Q K^T)
 constexpr int kNH = 16;         // largest supported G
@@ -58,7 +67,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleBuilder = 4 };
 enum BarId : unsigned {
   kBarItemFull = 1, kBarItemEmpty, kBarQFull, kBarQEmpty, kBarKvFull, kBarKvEmpty, kBarSFull,
-  kBarSEmpty, kBarPFull, kBarPvDone, kBarOEmpty
+  kBarSEmpty, kBarPFull, kBarPvDone, kBarOEmpty, kBarXch
 };
 
 struct Params {
@@ -90,32 +99,35 @@ struct Cfg {
   static constexpr int kSegs = kTileKeys / kSegLen;        // union blocks per tile (BS <= 64)
   static constexpr int kKVPanelBytes = kTileKeys * 128;    // 8 KB
   static constexpr int kKTileBytes = kPanels * kKVPanelBytes;
-  static constexpr int kPBytes = kRows * 128;              // 128 rows x 64 keys bf16
-  static constexpr int kKPBytes = kKTileBytes > kPBytes ? kKTileBytes : kPBytes;
-  static constexpr int kStageBytes = kKPBytes + kKTileBytes;  // [K, later P][V]
+  static constexpr int kStageBytes = 2 * kKTileBytes;      // [K][V]
   static constexpr int kLoadBytes = 2 * kKTileBytes;
   static constexpr int kQPanelBytes = kRows * 128;
-  static constexpr int kQBytes = kPanels * kQPanelBytes;
+  static constexpr int kQBytes = kPanels * kQPanelBytes;   // Q staging (copied into TMEM)
   static constexpr int kItemBytes = (static_cast<int>(sizeof(Item)) + 127) & ~127;
+  static constexpr int kMlBytes = 2 * 2 * kRows * 8;       // (m, l) per row: [item parity][wg]
   static constexpr int kOffQ = 0;
-  static constexpr int kOffStages = 2 * kQBytes;
-  static constexpr int kFixed = 2 * kQBytes + kItemSlots * kItemBytes + kMaxUnion * 8 + 1024 + 1024;
+  static constexpr int kOffStages = kQBytes;
+  static constexpr int kFixed = kQBytes + kItemSlots * kItemBytes + kMaxUnion * 8 + kMlBytes + 1024 + 1024;
   static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
   static constexpr int kOffItems = kOffStages + kStages * kStageBytes;
   static constexpr int kOffSort = kOffItems + kItemSlots * kItemBytes;
-  static constexpr int kOffBars = kOffSort + kMaxUnion * 8;
-  static constexpr int kNumBars = 2 * kItemSlots + 4 + 2 * kStages + 4 + 4;
+  static constexpr int kOffMl = kOffSort + kMaxUnion * 8;
+  static constexpr int kOffBars = kOffMl + kMlBytes;
+  static constexpr int kNumBars = 2 * kItemSlots + 3 + 2 * kStages + 8 + 4;
   static constexpr int kOffMisc = ((kOffBars + kNumBars * 8) + 15) & ~15;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  static constexpr int kSCol = 0;                          // S: 2 x 64 columns
-  static constexpr int kOCol = 2 * kTileKeys;              // O: D columns
-  static constexpr int kTmemCols = 256;
+  // tensor memory columns (512): S and P per warpgroup, O per warpgroup, Q of the item
+  static constexpr int kSCol = 0;                          // S of wg w: 64 fp32 at w * 64
+  static constexpr int kOCol = 2 * kTileKeys;              // O of wg w: D fp32 at kOCol + w * D
+  static constexpr int kPCol = kOCol + 2 * D;              // P of wg w: 64 bf16 (32 cols) at kPCol + w * 32
+  static constexpr int kQCol = kPCol + kTileKeys;          // Q: D bf16 (D / 2 cols)
+  static constexpr int kTmemCols = 512;
   static constexpr uint32_t kIdescQK = make_idesc(128, kTileKeys, 1u, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(128, D, 1u, false, true);
   static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kOCol + D <= kTmemCols, "tensor memory budget");
+  static_assert(kQCol + D / 2 <= kTmemCols, "tensor memory budget");
 };
 
 __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, int& hkv, int& t) {
@@ -295,19 +307,22 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* keys = reinterpret_cast<uint64_t*>(smem + C::kOffSort);
+  float2* ml = reinterpret_cast<float2*>(smem + C::kOffMl);
   uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* item_full = bb;   bb += kItemSlots;
   uint64_t* item_empty = bb;  bb += kItemSlots;
-  uint64_t* q_full = bb;      bb += 2;
-  uint64_t* q_empty = bb;     bb += 2;
+  uint64_t* q_full = bb;      bb += 1;   // Q staging loaded
+  uint64_t* q_empty = bb;     bb += 1;   // Q staging copied into TMEM
+  uint64_t* q_used = bb;      bb += 1;   // last QK of an item done: TMEM Q may be replaced
   uint64_t* kv_full = bb;     bb += C::kStages;
   uint64_t* kv_empty = bb;    bb += C::kStages;
-  uint64_t* s_full = bb;      bb += 2;
+  uint64_t* s_full = bb;      bb += 2;   // per warpgroup
   uint64_t* s_empty = bb;     bb += 2;
-  uint64_t* p_full = bb;      bb += 1;
-  uint64_t* pv_done = bb;     bb += 1;
+  uint64_t* p_full = bb;      bb += 2;
+  uint64_t* pv_done = bb;     bb += 2;
   uint64_t* o_empty = bb;     bb += 1;
-  uint64_t* mma_done = bb;
+  uint64_t* mma_done = bb;    bb += 2;   // per issuing thread
+  uint64_t* xch = bb;         // (m, l) exchange between the two warpgroups
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Abort ab{abort_flag, &g_err_nsa, 1u};
@@ -317,14 +332,15 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   };
 
   if (threadIdx.x == 0) {
-    // item slots are released by the loader, the MMA thread and the 4 softmax warps
-    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 6); }
+    // item slots are released by the loader, the two MMA threads and the 8 softmax warps
+    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 11); }
+    mbar_init(q_full, 1); mbar_init(q_empty, 1); mbar_init(q_used, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&q_full[i], 1); mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1);
     }
     for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
-    mbar_init(p_full, 4); mbar_init(pv_done, 1); mbar_init(o_empty, 4); mbar_init(mma_done, 1);
+    mbar_init(o_empty, 8); mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1); mbar_init(xch, 8);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -355,14 +371,14 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   } else if (warp == 0) {
     // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
-    int qslot = 0; uint32_t qphase = 0;
+    uint32_t qphase = 0;
     int stage = 0; uint32_t kvphase = 0;
     bool kv_issued[8];
     uint32_t last_kv_parity[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) { kv_issued[i] = false; last_kv_parity[i] = 0; }
-    bool q_issued[2] = {false, false};
-    uint32_t last_q_parity[2] = {0, 0};
+    bool q_issued = false;
+    uint32_t last_q_parity = 0;
     const uint32_t q_box_bytes = static_cast<uint32_t>(C::kPanels * 128 * p.G * p.NT);
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
@@ -370,25 +386,24 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union, hkv = it.hkv;
       if (nt > 0) {
-        if (!warp_wait(&q_empty[qslot], qphase ^ 1, ab, kRoleLoader, kBarQEmpty, item)) break;
+        if (!warp_wait(q_empty, qphase ^ 1, ab, kRoleLoader, kBarQEmpty, item)) break;
         if (lane == 0) {
-          uint64_t* fb = &q_full[qslot];
-          mbar_arrive_expect_tx(fb, q_box_bytes);
-          uint8_t* dst = smem + C::kOffQ + qslot * C::kQBytes;
+          mbar_arrive_expect_tx(q_full, q_box_bytes);
+          uint8_t* dst = smem + C::kOffQ;
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(dst + pn * C::kQPanelBytes, &tm_q, fb, pn * 64, hkv * p.G, it.g * p.NT);
+            tma_load_3d(dst + pn * C::kQPanelBytes, &tm_q, q_full, pn * 64, hkv * p.G, it.g * p.NT);
         }
-        q_issued[qslot] = true;
-        last_q_parity[qslot] = qphase;
-        if (++qslot == 2) { qslot = 0; qphase ^= 1; }
+        q_issued = true;
+        last_q_parity = qphase;
+        qphase ^= 1;
         for (int t = 0; t < nt; ++t) {
           if (!warp_wait(&kv_empty[stage], kvphase ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
           if (lane == 0) {
             uint64_t* fb = &kv_full[stage];
             mbar_arrive_expect_tx(fb, C::kLoadBytes);
             uint8_t* kdst = smem + C::kOffStages + stage * C::kStageBytes;
-            uint8_t* vdst = kdst + C::kKPBytes;
+            uint8_t* vdst = kdst + C::kKTileBytes;
 #pragma unroll
             for (int e = 0; e < C::kSegs; ++e) {
               int row0;
@@ -420,97 +435,124 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s)
         if (kv_issued[s]) drain_wait(&kv_full[s], last_kv_parity[s]);
-      for (int s = 0; s < 2; ++s)
-        if (q_issued[s]) drain_wait(&q_full[s], last_q_parity[s]);
+      if (q_issued) drain_wait(q_full, last_q_parity);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ QK issuer
+    // Two threads issue the MMAs (QK here, PV in warp 3): a thread's wait on a barrier
+    // stalls only its own stream while the tensor core runs the other's MMAs.
     if (lane == 0) {
       int islot = 0; uint32_t iphase = 0;
-      int qslot = 0; uint32_t qphase = 0;
+      uint32_t qphase = 0, quphase = 0;
+      bool q_in_use = false;  // a QK of an earlier item may still read the TMEM copy of Q
       int stage = 0; uint32_t kvphase = 0;
-      int sbuf = 0; uint32_t sphase = 0;
-      uint32_t pphase = 0, ophase = 0;
-      int pending_stage = -1;
-      bool pending_first = false;
-      int cur_item = -1;
+      uint32_t sph[2] = {0u, 0u};
       bool ok = true;
-      auto issue_pv = [&](int st, bool first) -> bool {
-        if (!bounded_wait(p_full, pphase, ab, kRoleMma, kBarPFull, cur_item)) return false;
-        pphase ^= 1;
-        if (first) {
-          if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, cur_item)) return false;
-          ophase ^= 1;
-        }
-        tc_fence_after();
-        const uint32_t p_addr = smem_base + C::kOffStages + st * C::kStageBytes;
-        const uint32_t v_addr = p_addr + C::kKPBytes;
-#pragma unroll
-        for (int k = 0; k < kTileKeys / 16; ++k) {
-          const uint64_t a = make_sdesc(p_addr + k * 32, 16, 1024, kLayoutSW128);
-          const uint64_t bd = make_sdesc(v_addr + k * 16 * 128, C::kKVPanelBytes, 1024, kLayoutSW128);
-          mma_f16_ss(tmem + C::kOCol, a, bd, C::kIdescPV, (first && k == 0) ? 0u : 1u);
-        }
-        mma_commit(&kv_empty[st]);
-        mma_commit(pv_done);
-        return true;
-      };
+      // descriptors of the shared-memory operands; a byte offset x adds x >> 4
+      const uint64_t q_desc0 = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
+      const uint64_t k_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        cur_item = item;
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
         mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
-        if (nt == 0) {
-          // nothing to compute: release the deferred PV now so the softmax group, which
-          // waits for it before finishing the previous item, never starves
-          if (pending_stage >= 0) {
-            if (!issue_pv(pending_stage, pending_first)) break;
-            pending_stage = -1;
-          }
-          continue;
+        if (nt == 0) continue;
+        // Q of this item: staging buffer -> TMEM, once the previous item's QKs are done
+        if (!bounded_wait(q_full, qphase, ab, kRoleMma, kBarQFull, item)) break;
+        qphase ^= 1;
+        if (q_in_use) {
+          if (!bounded_wait(q_used, quphase, ab, kRoleMma, kBarQEmpty, item)) break;
+          quphase ^= 1;
         }
-        if (!bounded_wait(&q_full[qslot], qphase, ab, kRoleMma, kBarQFull, item)) break;
-        const uint32_t q_addr = smem_base + C::kOffQ + qslot * C::kQBytes;
-        for (int t = 0; t < nt; ++t) {
-          if (!bounded_wait(&kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
-              !bounded_wait(&s_empty[sbuf], sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_base + C::kOffStages + stage * C::kStageBytes;
+        tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const int pn = k / 4, kk = k % 4;
-            const uint64_t a = make_sdesc(q_addr + pn * C::kQPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
-            const uint64_t bd = make_sdesc(k_addr + pn * C::kKVPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
-            mma_f16_ss(tmem + C::kSCol + sbuf * kTileKeys, a, bd, C::kIdescQK, k > 0);
+        for (int kk = 0; kk < D / 16; ++kk)
+          tmem_cp_128x256b(tmem + C::kQCol + kk * 8,
+                           q_desc0 + static_cast<uint64_t>(((kk / 4) * C::kQPanelBytes + (kk % 4) * 32) >> 4));
+        mma_commit(q_empty);
+        for (int t = 0; t < nt; ++t) {
+          const int w = t & 1;
+          if (!bounded_wait(&kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
+              !bounded_wait(&s_empty[w], sph[w] ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
+          sph[w] ^= 1;
+          tc_fence_after();
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_ts(tmem + C::kSCol + w * kTileKeys, tmem + C::kQCol + kk * 8,
+                       kd + static_cast<uint64_t>(((kk / 4) * C::kKVPanelBytes + (kk % 4) * 32) >> 4),
+                       C::kIdescQK, kk > 0);
+          mma_commit(&s_full[w]);
+          if (t == nt - 1) {
+            mma_commit(q_used);
+            q_in_use = true;
           }
-          mma_commit(&s_full[sbuf]);
-          if (t == nt - 1) mma_commit(&q_empty[qslot]);
-          if (pending_stage >= 0 && !issue_pv(pending_stage, pending_first)) { ok = false; break; }
-          pending_stage = stage;
-          pending_first = (t == 0);
           if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
-          if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
         }
-        if (++qslot == 2) { qslot = 0; qphase ^= 1; }
       }
-      if (ok && pending_stage >= 0) issue_pv(pending_stage, pending_first);
       // every tcgen05 op issued by this thread has finished once mma_done fires
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
+      mma_commit(&mma_done[0]);
+      drain_wait(&mma_done[0], 0);
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      int islot = 0; uint32_t iphase = 0;
+      int stage = 0;
+      uint32_t pph[2] = {0u, 0u};
+      uint32_t ophase = 0;
+      bool ok = true;
+      const uint64_t v_desc0 =
+          make_sdesc(smem_base + C::kOffStages + C::kKTileBytes, C::kKVPanelBytes, 1024, kLayoutSW128);
+      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        const int nt = item_at(islot).n_tiles;
+        mbar_arrive(&item_empty[islot]);
+        if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+        // PV of tile t (A = P of warpgroup t & 1 in TMEM, B = V tile) goes to the O
+        // accumulator of warpgroup t & 1; each warpgroup's first tile of an item
+        // overwrites it.  A PV follows its tile's softmax, which follows the tile's QK,
+        // so the stage (K and V) is free once the PV is done.
+        for (int t = 0; t < nt; ++t) {
+          const int w = t & 1;
+          if (!bounded_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+          pph[w] ^= 1;
+          if (t == 0) {
+            if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
+            ophase ^= 1;
+          }
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < kTileKeys / 16; ++k)
+            mma_f16_ts(tmem + C::kOCol + w * D, tmem + C::kPCol + w * (kTileKeys / 2) + k * 8,
+                       vd + static_cast<uint64_t>((k * 16 * 128) >> 4), C::kIdescPV,
+                       (t < 2 && k == 0) ? 0u : 1u);
+          mma_commit(&kv_empty[stage]);
+          mma_commit(&pv_done[w]);
+          if (++stage == C::kStages) stage = 0;
+        }
+      }
+      mma_commit(&mma_done[1]);
+      drain_wait(&mma_done[1], 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
-    const int q4 = warp - 4;
-    const int r = q4 * 32 + lane;  // row of the tile = TMEM lane
+    const int w = (warp - 4) >> 2;   // warpgroup: tiles t with t & 1 == w
+    const int q4 = warp & 3;         // TMEM lane quadrant of this warp
+    const int r = q4 * 32 + lane;    // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + C::kSCol + w * kTileKeys;
+    const uint32_t o_col = tmem + lane_off + C::kOCol + w * D;
+    const uint32_t p_col = tmem + lane_off + C::kPCol + w * (kTileKeys / 2);
     const int ti = r < p.rows ? r / p.G : 0;  // token of this row within the item
     const int h = r - ti * p.G;
     int islot = 0; uint32_t iphase = 0;
     int stage = 0;
-    int sbuf = 0; uint32_t sphase = 0;
-    uint32_t pvphase = 0;
+    uint32_t sph = 0, pvph = 0, xph = 0;
+    int par = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
@@ -519,9 +561,14 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const bool row_ok = r < p.rows && ((it.tok_valid >> ti) & 1u);
       const int limit = r < p.rows ? it.limit[ti] : -1;
       const unsigned tbit = 1u << ti;
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // log2 units, lazily moved reference max
+      int mine = 0;                  // tiles of this item handled by this warpgroup so far
       bool ok = true;
       for (int t = 0; t < nt; ++t) {
+        if ((t & 1) != w) {
+          if (++stage == C::kStages) stage = 0;
+          continue;
+        }
         // valid keys of each segment of the tile for this row's token
         int nv[C::kSegs];
         int nvsum = 0;
@@ -540,66 +587,76 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           nvsum += nv[e];
         }
         const bool any = __any_sync(0xffffffffu, nvsum > 0);
-        if (!warp_wait(&s_full[sbuf], sphase, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        if (!warp_wait(&s_full[w], sph, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        sph ^= 1;
         float x[kTileKeys];
         if (any) {
           tc_fence_after();
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kSCol + sbuf * kTileKeys, x);
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kSCol + sbuf * kTileKeys + 32, x + 32);
+          tmem_ld_32x32b_x32(s_col, x);
+          tmem_ld_32x32b_x32(s_col + 32, x + 32);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[sbuf]);
-        if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
-        float tmax = -INFINITY;
+        if (lane == 0) mbar_arrive(&s_empty[w]);
+        float m_new = m, alpha = 1.f, psum = 0.f;
+        if (any) {
+          // masked raw scores; maximum with four independent chains
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int e = 0; e < C::kSegs; ++e) {
+          for (int e = 0; e < C::kSegs; ++e) {
+            if (nv[e] < C::kSegLen) {
 #pragma unroll
-          for (int jj = 0; jj < C::kSegLen; ++jj) {
-            const int j = e * C::kSegLen + jj;
-            x[j] = jj < nv[e] ? x[j] * p.scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[j]);
-          }
-        }
-        // lazy online softmax: move the reference max only when it grows by > 2^8
-        float m_new = m;
-        if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
-        const float alpha = (m == -INFINITY || m_new == m) ? (m_new == m ? 1.f : 0.f) : ex2(m - m_new);
-        float psum = 0.f;
-#pragma unroll
-        for (int e = 0; e < C::kSegs; ++e) {
-          if (nv[e] > 0) {
+              for (int jj = 0; jj < C::kSegLen; ++jj)
+                if (jj >= nv[e]) x[e * C::kSegLen + jj] = -INFINITY;
+            }
 #pragma unroll
             for (int jj = 0; jj < C::kSegLen; ++jj) {
               const int j = e * C::kSegLen + jj;
-              x[j] = ex2(x[j] - m_new);
-              psum += x[j];
+              mx[j & 3] = fmaxf(mx[j & 3], x[j]);
             }
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < C::kSegLen; ++jj) x[e * C::kSegLen + jj] = 0.f;
           }
+          const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+          // lazy online softmax: move the reference max only when it grows by > 2^8
+          if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
+          alpha = (m == -INFINITY || m_new == m) ? (m_new == m ? 1.f : 0.f) : ex2(m - m_new);
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int e = 0; e < C::kSegs; ++e) {
+            if (nv[e] > 0) {
+#pragma unroll
+              for (int jj = 0; jj < C::kSegLen; ++jj) {
+                const int j = e * C::kSegLen + jj;
+                x[j] = ex2(fmaf(x[j], p.scale_log2, -m_new));
+                ps[j & 3] += x[j];
+              }
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < C::kSegLen; ++jj) x[e * C::kSegLen + jj] = 0.f;
+            }
+          }
+          psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kTileKeys; ++j) x[j] = 0.f;
         }
         l = l * alpha + psum;
-        // P row (bf16) over the K tile of this stage: 128-byte swizzled K-major rows
-        const uint32_t prow = smem_base + C::kOffStages + stage * C::kStageBytes + r * 128;
+        uint32_t pk[kTileKeys / 2];
 #pragma unroll
-        for (int cchunk = 0; cchunk < 8; ++cchunk) {
-          uint32_t w[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(x[cchunk * 8 + 2 * u], x[cchunk * 8 + 2 * u + 1]);
-            w[u] = *reinterpret_cast<uint32_t*>(&h2);
-          }
-          st_shared_v4(prow + ((cchunk ^ (r & 7)) * 16), w[0], w[1], w[2], w[3]);
+        for (int j = 0; j < kTileKeys / 2; ++j) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+          pk[j] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        fence_proxy_async_smem();
         if (++stage == C::kStages) stage = 0;
-        // the previous PV must be done before O is rescaled
-        if (t > 0) {
-          if (!warp_wait(pv_done, pvphase, ab, kRoleSoftmax, kBarPvDone, item)) { ok = false; break; }
-          pvphase ^= 1;
+        // this warpgroup's previous PV must be done before its P is replaced and its O
+        // rescaled
+        if (mine > 0) {
+          if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) { ok = false; break; }
+          pvph ^= 1;
           tc_fence_after();
+        }
+        // P row (bf16 pairs, key order) into this warpgroup's TMEM P columns
+        tmem_st_32x32b_x32_u(p_col, pk);
+        if (mine > 0) {
           // TMEM loads/stores are warp-collective (.sync.aligned): the whole warp rescales
           // together when any of its rows moved its reference max; other rows use 1.
           const bool my_rescale = m_new != m && m != -INFINITY;
@@ -608,55 +665,81 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               float ov[32];
-              tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+              tmem_ld_32x32b_x32(o_col + c * 32, ov);
 #pragma unroll
               for (int j = 0; j < 32; ++j) ov[j] *= f;
-              tmem_st_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+              tmem_st_32x32b_x32(o_col + c * 32, ov);
             }
           }
         }
         m = m_new;
+        ++mine;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[w]);
       }
       if (!ok) break;
-      const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+      if (mine > 0) {
+        if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) break;
+        pvph ^= 1;
+      }
+      // merge the two warpgroups' partial results row by row
+      ml[(par * 2 + w) * kRows + r] = make_float2(m, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xch);
+      if (!warp_wait(xch, xph, ab, kRoleSoftmax, kBarXch, item)) break;
+      xph ^= 1;
+      const float2 oth = ml[(par * 2 + (w ^ 1)) * kRows + r];
+      const float mx = fmaxf(m, oth.x);
+      const float a_me = l > 0.f ? ex2(m - mx) : 0.f;
+      const float a_ot = oth.y > 0.f ? ex2(oth.x - mx) : 0.f;
+      const float L = l * a_me + oth.y * a_ot;
+      const float a0 = w == 0 ? a_me : a_ot, a1 = w == 0 ? a_ot : a_me;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      constexpr int kHalf = D / 2;
       if (nt > 0) {
-        if (!warp_wait(pv_done, pvphase, ab, kRoleSoftmax, kBarPvDone, item)) break;
-        pvphase ^= 1;
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+        for (int c = 0; c < kHalf / 32; ++c) {
+          const int col = w * kHalf + c * 32;
+          float o0[32], o1[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + col, o0);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + D + col, o1);
           if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
-              uint32_t w[4];
+              uint32_t wv[4];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[j + 2 * u] * inv, ov[j + 2 * u + 1] * inv);
-                w[u] = *reinterpret_cast<uint32_t*>(&h2);
+                // an accumulator that received no PV this item holds stale data: select
+                const int j0 = j + 2 * u;
+                const float v0 = ((a0 > 0.f) ? o0[j0] * a0 : 0.f) + ((a1 > 0.f) ? o1[j0] * a1 : 0.f);
+                const float v1 = ((a0 > 0.f) ? o0[j0 + 1] * a0 : 0.f) + ((a1 > 0.f) ? o1[j0 + 1] * a1 : 0.f);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(v0 * inv, v1 * inv);
+                wv[u] = *reinterpret_cast<uint32_t*>(&h2);
               }
-              *reinterpret_cast<uint4*>(out + orow * D + c * 32 + j) = make_uint4(w[0], w[1], w[2], w[3]);
+              const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+              *reinterpret_cast<uint4*>(out + orow * D + col + j) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty);
-        if (row_ok && p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       } else if (row_ok) {
+        const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
 #pragma unroll
-        for (int j = 0; j < D; j += 8)
-          *reinterpret_cast<uint4*>(out + orow * D + j) = make_uint4(0u, 0u, 0u, 0u);
-        if (p.lse != nullptr) p.lse[orow] = -INFINITY;
+        for (int j = 0; j < kHalf; j += 8)
+          *reinterpret_cast<uint4*>(out + orow * D + w * kHalf + j) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      if (w == 0 && row_ok && p.lse != nullptr) {
+        const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+        p.lse[orow] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+      par ^= 1;
     }
   }
 
