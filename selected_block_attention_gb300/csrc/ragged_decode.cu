@@ -46,6 +46,8 @@ constexpr int kTileBytes = kTileKeys * kRowBytes;
 constexpr int kWarpSmem = kStages * 2 * kTileBytes;
 constexpr int kSmemBytes = kWarps * kWarpSmem;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct DecodeParams {
   const __nv_bfloat16* q;
@@ -88,6 +90,15 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
+// cap * tanh(x / cap) from tanh(y) = 1 - 2 / (1 + e^(2y)): one ex2, one reciprocal.
+// Saturates to +-cap (e^(2y) -> inf or 0); near 0 the absolute error is a few ulp of cap.
+__device__ __forceinline__ float soft_cap(float x, float two_log2e_over_cap, float cap) {
+  const float t = ptx::ex2(x * two_log2e_over_cap);
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + t));
+  return fmaf(-2.f * cap, r, cap);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -109,6 +120,8 @@ __device__ __forceinline__ void load_tile(const DecodeParams& p, int b, int h, i
   }
 }
 
+// kHiRows: G > 8, so the rows g + 8 of the m16n8k16 tiles hold query heads too.
+template <bool kHiRows>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_split_kernel(const DecodeParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -199,7 +212,9 @@ decode_split_kernel(const DecodeParams p) {
         mma_bf16(sc[1], qa[kk], b10, b11);
       }
     }
-    // Logits, mask, online softmax (rows g and g+8 of this thread).
+    // Logits, mask, online softmax (rows g and g+8 of this thread), in log2 units with a
+    // lazily moved reference max (O is rescaled only when the max grows by > 2^8).
+    const float two_log2e_over_cap = p.cap > 0.f ? 2.f * kLog2e / p.cap : 0.f;
     float tmax0 = -INFINITY, tmax1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -209,28 +224,33 @@ decode_split_kernel(const DecodeParams p) {
         bool valid;
         if (t < 0) valid = key >= max(start, 0) && key < sink_hi;
         else valid = key >= key_lo && key < key_hi;
-        float x0 = sc[nt][e] * p.scale, x1 = sc[nt][2 + e] * p.scale;
-        if (p.cap > 0.f) {
-          x0 = p.cap * tanhf(x0 / p.cap);
-          x1 = p.cap * tanhf(x1 / p.cap);
-        }
-        if (key < p.num_sinks) {
-          x0 += bias_row0[key];
-          x1 += bias_row1[key];
-        }
-        sc[nt][e] = valid ? x0 : -INFINITY;
-        sc[nt][2 + e] = valid ? x1 : -INFINITY;
+        float x0 = sc[nt][e] * p.scale;
+        if (p.cap > 0.f) x0 = soft_cap(x0, two_log2e_over_cap, p.cap);
+        if (key < p.num_sinks) x0 += bias_row0[key];
+        sc[nt][e] = valid ? x0 * kLog2e : -INFINITY;
         tmax0 = fmaxf(tmax0, sc[nt][e]);
-        tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
+        if constexpr (kHiRows) {
+          float x1 = sc[nt][2 + e] * p.scale;
+          if (p.cap > 0.f) x1 = soft_cap(x1, two_log2e_over_cap, p.cap);
+          if (key < p.num_sinks) x1 += bias_row1[key];
+          sc[nt][2 + e] = valid ? x1 * kLog2e : -INFINITY;
+          tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
+        } else {
+          sc[nt][2 + e] = -INFINITY;
+        }
       }
     }
     tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
     tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
-    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
-    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
-    const float mn0 = fmaxf(m0, tmax0), mn1 = fmaxf(m1, tmax1);
-    const float alpha0 = mn0 == -INFINITY ? 1.f : ptx::ex2((m0 - mn0) * kLog2e);
-    const float alpha1 = mn1 == -INFINITY ? 1.f : ptx::ex2((m1 - mn1) * kLog2e);
+    if constexpr (kHiRows) {
+      tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
+      tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
+    }
+    const float mn0 = (tmax0 > m0 + kRescaleThreshold || (m0 == -INFINITY && tmax0 != -INFINITY)) ? tmax0 : m0;
+    const float mn1 = (tmax1 > m1 + kRescaleThreshold || (m1 == -INFINITY && tmax1 != -INFINITY)) ? tmax1 : m1;
+    const bool mv0 = mn0 != m0, mv1 = mn1 != m1;
+    const float alpha0 = (mv0 && m0 != -INFINITY) ? ptx::ex2(m0 - mn0) : 1.f;
+    const float alpha1 = (mv1 && m1 != -INFINITY) ? ptx::ex2(m1 - mn1) : 1.f;
     m0 = mn0;
     m1 = mn1;
     float ps0 = 0.f, ps1 = 0.f;
@@ -238,16 +258,27 @@ decode_split_kernel(const DecodeParams p) {
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float p0 = mn0 == -INFINITY ? 0.f : ptx::ex2((sc[nt][e] - mn0) * kLog2e);
-        const float p1 = mn1 == -INFINITY ? 0.f : ptx::ex2((sc[nt][2 + e] - mn1) * kLog2e);
+        const float p0 = mn0 == -INFINITY ? 0.f : ptx::ex2(sc[nt][e] - mn0);
         sc[nt][e] = p0;
-        sc[nt][2 + e] = p1;
         ps0 += p0;
-        ps1 += p1;
+        if constexpr (kHiRows) {
+          const float p1 = mn1 == -INFINITY ? 0.f : ptx::ex2(sc[nt][2 + e] - mn1);
+          sc[nt][2 + e] = p1;
+          ps1 += p1;
+        } else {
+          sc[nt][2 + e] = 0.f;
+        }
       }
     }
     l0 = l0 * alpha0 + ps0;
     l1 = l1 * alpha1 + ps1;
+    // the whole warp rescales O when any of its rows moved its reference max
+    if (__any_sync(0xffffffffu, mv0 || mv1)) {
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        o[dn][0] *= alpha0; o[dn][1] *= alpha0; o[dn][2] *= alpha1; o[dn][3] *= alpha1;
+      }
+    }
     uint32_t pa[4];
     pa[0] = pack_bf16(sc[0][0], sc[0][1]);
     pa[1] = pack_bf16(sc[0][2], sc[0][3]);
@@ -261,9 +292,6 @@ decode_split_kernel(const DecodeParams p) {
       for (int dn = 0; dn < 16; dn += 2) {
         uint32_t b00, b01, b10, b11;
         ldsm_x4_t(row_addr + dn * 16, b00, b01, b10, b11);
-        o[dn][0] *= alpha0; o[dn][1] *= alpha0; o[dn][2] *= alpha1; o[dn][3] *= alpha1;
-        o[dn + 1][0] *= alpha0; o[dn + 1][1] *= alpha0;
-        o[dn + 1][2] *= alpha1; o[dn + 1][3] *= alpha1;
         mma_bf16(o[dn], pa, b00, b01);
         mma_bf16(o[dn + 1], pa, b10, b11);
       }
@@ -274,6 +302,9 @@ decode_split_kernel(const DecodeParams p) {
   cp_async_wait<0>();
   __syncthreads();
 
+  // back to natural-log units for the merge and the combine kernel
+  m0 = m0 == -INFINITY ? m0 : m0 * kLn2;
+  m1 = m1 == -INFINITY ? m1 : m1 * kLn2;
   // Merge the four warps of the CTA through shared memory (reusing the ring).
   float* s_o = reinterpret_cast<float*>(smem);           // [kWarps][16][kD]
   float* s_ml = s_o + kWarps * 16 * kD;                    // [kWarps][16][2]
@@ -398,13 +429,19 @@ int launch_ragged_decode(const void* q, const void* k, const void* v, const int3
   p.sink_per_head = sink_per_head;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel,
+    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemBytes);
     if (e != cudaSuccess) return cuda_error(e, "ragged_decode: set smem attribute");
     attr_done = true;
   }
   dim3 grid(p.max_splits, Hkv, B);
-  decode_split_kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
+  if (p.G > 8)
+    decode_split_kernel<true><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
+  else
+    decode_split_kernel<false><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "ragged_decode split launch");
   decode_combine_kernel<<<dim3(Hq, B), kD, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out), lse);
