@@ -14,6 +14,8 @@ sampled during the timed region) and ``rows``: the other workloads of the path
 the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --case {nsa_prefill,nsa_varlen,blocksparse,decode} [--repeat R]
+                  [--decode-batch B]      # profiling: launches only, no JSON line
 
 ``--impl reference`` times the fp64 CPU oracle on the same workload (bounded
 sample per step, host cores) and prints the same line with ``"impl": "reference"``.
@@ -100,6 +102,78 @@ def nsa_work(w):
         (0 if isinstance(w.block_counts, int) else counts.size * 4)
     gather = float(n_blocks) * bs * D * 2 * elt
     return flops, float(hbm), gather, int(B * T * Hkv)
+
+
+def union_tiles(w, rows=128, tile_keys=64):
+    """Tiles the union walk executes: per (group of NT = rows // G consecutive tokens,
+    KV head), the number of distinct selected blocks (each block of <= 64 keys is one
+    64-key tile)."""
+    idx = w.block_indices.cpu().numpy().astype(np.int64)
+    B, T, Hkv, S = idx.shape
+    G = w.q.shape[2] // Hkv
+    NT = min(16, rows // G)
+    bs = w.block_size
+    counts = (np.full((B, T, Hkv), w.block_counts, dtype=np.int64) if isinstance(w.block_counts, int)
+              else w.block_counts.cpu().numpy().astype(np.int64))
+    if w.cu_seqlens is not None:
+        cu = w.cu_seqlens.cpu().numpy().astype(np.int64)
+        seq = np.searchsorted(cu, np.arange(T), side="right") - 1
+        start, L = cu[seq], cu[seq + 1] - cu[seq]
+    else:
+        start, L = np.zeros(T, dtype=np.int64), np.full(T, T)
+    t_rel = (np.arange(T) - start)[None, :, None, None]
+    valid = (np.arange(S)[None, None, None, :] < np.minimum(counts, S)[..., None]) & (idx >= 0) & \
+        (idx * bs < L[None, :, None, None])
+    if w.causal:
+        valid &= idx * bs <= t_rel
+    tok = (np.arange(B)[:, None] * T + np.arange(T)[None, :])[:, :, None, None]
+    first_row = np.broadcast_to(tok - t_rel + idx * bs, idx.shape)  # absolute first key row
+    group = np.broadcast_to(tok // NT, idx.shape)
+    head = np.broadcast_to(np.arange(Hkv)[None, None, :, None], idx.shape)
+    item = group[valid] * Hkv + head[valid]
+    pairs = np.unique(item * (B * T + bs) + first_row[valid])  # distinct (item, block)
+    per_item = np.bincount(pairs // (B * T + bs))
+    if bs >= tile_keys:
+        return int(per_item.sum()) * (bs // tile_keys)
+    return int((-(-per_item * bs // tile_keys)).sum())
+
+
+def profile_traffic(summary_name, source_rel):
+    """DRAM bytes per launch from a committed ncu summary, or None when the kernel
+    source changed since the capture (the summary records the source's SHA-256)."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", summary_name)).read()
+        src = open(os.path.join(ROOT, source_rel), "rb").read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip().strip("-* `")] = v.strip().strip("`")
+    if fields.get("source_sha256") != hashlib.sha256(src).hexdigest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def world_max(x, device):
+    """Maximum of a per-rank float over all ranks (the rank's own value when alone)."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(x)
+    if torch.distributed.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(units_per_rank, world, ms_max, scale=1e12):
+    """Whole-job throughput: all ranks' units over the slowest rank's step time."""
+    return units_per_rank * world / (ms_max * 1e-3) / scale
 
 
 class ClockSampler:
@@ -246,15 +320,13 @@ def run_cuda(args, rank, world, local_rank):
         torch.distributed.barrier()
     sba.check_error(dev)
     ms = sum(times) / len(times)
-    ms_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = world_max(ms, dev)
     clocks = sampler.summary(t0, t1)
     sampler.stop()
     log(f"timed steps done: {ms:.4f} ms/step")
-    value = flops * world / (ms_max * 1e-3) / 1e12
+    value = aggregate_value(flops, world, ms_max)
+    n_tiles = union_tiles(w)
+    exec_flops = 4.0 * 128 * 64 * w.q.shape[3] * n_tiles  # QK + PV of every union tile
 
     # e2e through the public API with host buffers (pinned), copies in the timed region
     host = {n: getattr(w, n).cpu().pin_memory() for n in ("q", "k", "v", "block_indices", "block_counts")}
@@ -304,9 +376,13 @@ def run_cuda(args, rank, world, local_rank):
             "peak": peaks["bf16_tflops"],
             "unit": "TFLOP/s",
             "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "traffic": None,
+            "traffic": profile_traffic("nsa_union_kernel_prefill.md",
+                                       "selected_block_attention_gb300/csrc/nsa_select.cu"),
             "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
-            "kernel": "nsa_select_kernel<bf16,128,64>",
+            "kernel": "nsa_union_kernel<128,64>",
+            "union_tiles": int(n_tiles),
+            "executed_mma_tflops": round(exec_flops / (ms * 1e-3) / 1e12, 1),
+            "executed_mma_frac": round(exec_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
             "terms_us": {
                 "tensor": round(flops / (peaks["bf16_tflops"] * 1e12) * 1e6, 2),
                 "hbm": round(hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6, 2)},
@@ -402,6 +478,51 @@ def measure_rows(sba, dev, stream, flush, peaks, args):
     return rows
 
 
+def run_case(args):
+    """Launch one workload's kernels ``--repeat`` times (no timing JSON): the command the
+    profiles are taken with.  Cases: nsa_prefill, nsa_varlen, blocksparse (bounds then
+    attention), decode (``--decode-batch`` rows of the decode workload)."""
+    import selected_block_attention_gb300 as sba
+    from selected_block_attention_gb300 import _build
+
+    _build.build()
+    sba.load_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.case in ("nsa_prefill", "nsa_varlen"):
+        w = workloads.nsa_prefill(device=dev) if args.case == "nsa_prefill" else workloads.nsa_varlen(device=dev)
+        fn = lambda: sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts,
+                                        w.block_size, cu_seqlens=w.cu_seqlens)
+    elif args.case == "blocksparse":
+        w = workloads.blocksparse(device=dev)
+        m = w.mask
+
+        def fn():
+            lo, up, lof, upf = sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions,
+                                                      m.kv_segment_ids, 128, 128, causal=True,
+                                                      window_left=1024, window_right=0)
+            sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids, m.kv_positions,
+                                     m.kv_segment_ids, lo, up, lof, upf, 128, 128, causal=True,
+                                     window_left=1024, window_right=0)
+    elif args.case == "decode":
+        w = workloads.decode(device=dev, B=args.decode_batch)
+
+        def fn():
+            sba.ragged_decode_fwd(w.q, w.k, w.v, w.sequence_start, w.sequence_end,
+                                  window_left=w.window_left, window_right=w.window_right,
+                                  logits_soft_cap=w.logits_soft_cap, sink_bias=w.sink_bias)
+    else:
+        raise SystemExit(f"unknown case {args.case}")
+    for i in range(args.repeat):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        print(f"{args.case} launch {i}: {s.elapsed_time(e):.4f} ms", file=sys.stderr)
+    sba.check_error(dev)
+
+
 def cpu_baseline(w, flops_per_group, seconds):
     """fp64 oracle on host cores over a bounded, seeded sample of token groups."""
     import oracle
@@ -487,7 +608,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None,
+                    help="profiling mode: launch one workload --repeat times, no JSON line")
+    ap.add_argument("--repeat", type=int, default=3)
+    ap.add_argument("--decode-batch", type=int, default=64)
     args = ap.parse_args()
+    if args.case is not None:
+        run_case(args)
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
