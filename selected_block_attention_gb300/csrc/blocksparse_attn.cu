@@ -6,18 +6,19 @@
 // per-token mask.  The token mask used elsewhere (same segment, neither padding,
 // causal and inclusive window on positions) is applied to every other block.
 //
-// Work item = (batch row, query block of 128 tokens, query head).  A persistent CTA
-// per SM runs a warp-specialised pipeline:
-//   warp 0      producer: TMA loads of the Q tile, then per key block of the item's
-//               range the K and V tiles plus the block's positions / segment ids
-//               (bulk copy) into a shared-memory ring;
-//   warp 1      MMA issuer (one thread): S = Q K^T (M = 128 queries, N = key block,
-//               fp32 in TMEM, double-buffered), O += P V (N = head dim, O kept in
-//               TMEM for the whole item);
-//   warps 4..7  softmax warpgroup, one thread per query row: mask, online softmax
-//               with a lazy rescale (O in TMEM is rescaled only when the running max
-//               grows by more than 2^8), P to shared memory in the 128-byte-swizzled
-//               K-major layout the MMA reads, and the epilogue O / l, LSE.
+// Work item = (batch row, query block of 128 tokens, query head): 128 rows of one
+// head.  Its key blocks are walked in tiles of 64 keys.  A persistent CTA per SM runs
+// the same warp-specialised pipeline as the NSA selection kernel:
+//   warp 0      loader: publishes the item (bounds of its query block), then TMA loads
+//               the Q rows (staging buffer) and per tile the K / V boxes plus the tile's
+//               key positions and segment ids (bulk copy) into a shared-memory ring;
+//   warp 1      QK issuer (one thread): copies Q into tensor memory (tcgen05.cp, in
+//               order with its MMAs), S = Q K^T (M = 128, N = 64, A from TMEM);
+//   warp 3      PV issuer (one thread): O_w += P_w V (A = P from TMEM);
+//   warps 4..11 two softmax warpgroups on alternate tiles, each with its own S buffer,
+//               P columns, O accumulator and running (m, l): token mask outside the
+//               full block range, lazy online softmax (O rescaled only when the max
+//               grows by > 2^8); the epilogue merges the two partial results.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -34,16 +35,18 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
-constexpr int kM = 128;  // query rows per tile
-constexpr int kItemSlots = 4;
+constexpr int kThreads = 384;   // warps 0-3: loader, QK issuer, spare, PV issuer; 4-11: softmax
+constexpr int kM = 128;         // query rows per item
+constexpr int kTileKeys = 64;   // keys per pipeline tile
+constexpr int kItemSlots = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct Item {
   int b, hq, qblk;
-  int lo, up, lof, upf;
+  int lo, up, lof, upf;  // kv blocks [lo, up); [lof, upf) need no token mask
+  int n_tiles;
 };
 
 struct Params {
@@ -62,37 +65,47 @@ struct Params {
   int n_items;
 };
 
+enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3 };
+enum BarId : unsigned {
+  kBarItemFull = 1, kBarItemEmpty, kBarQFull, kBarQEmpty, kBarKvFull, kBarKvEmpty, kBarSFull,
+  kBarSEmpty, kBarPFull, kBarPvDone, kBarOEmpty, kBarXch
+};
+
 template <int D, int KB>
 struct Cfg {
   static constexpr int kPanels = D / 64;
+  static constexpr int kTilesPerBlock = KB / kTileKeys;
+  static constexpr int kKVPanelBytes = kTileKeys * 128;    // 8 KB
+  static constexpr int kKTileBytes = kPanels * kKVPanelBytes;
+  static constexpr int kPosSegBytes = 2 * kTileKeys * 4;
+  static constexpr int kLoadBytes = 2 * kKTileBytes + kPosSegBytes;
+  static constexpr int kStageBytes = (kLoadBytes + 1023) & ~1023;  // [K][V][positions, segments]
   static constexpr int kQPanelBytes = kM * 128;
   static constexpr int kQBytes = kPanels * kQPanelBytes;
-  static constexpr int kKVPanelBytes = KB * 128;
-  static constexpr int kKVTileBytes = kPanels * kKVPanelBytes;
-  static constexpr int kPosSegBytes = 2 * KB * 4;
-  static constexpr int kStageBytes = 2 * kKVTileBytes + 1024;  // K, V, positions/segments (1024-padded)
-  static constexpr int kStages = (kStageBytes <= 40 * 1024) ? 3 : 2;
-  static constexpr int kPPanels = KB / 64;
-  static constexpr int kPBytes = kPPanels * kM * 128;
-  static constexpr int kTmemCols = (2 * KB + D <= 256) ? 256 : 512;
-  static constexpr int kOCol = 2 * KB;
-  static constexpr uint32_t kIdescQK = make_idesc(128, KB, 1u, false, false);
-  static constexpr uint32_t kIdescPV = make_idesc(128, D, 1u, false, true);
+  static constexpr int kItemBytes = (static_cast<int>(sizeof(Item)) + 15) & ~15;
+  static constexpr int kMlBytes = 2 * 2 * kM * 8;           // (m, l) per row: [item parity][wg]
   static constexpr int kOffQ = 0;
-  static constexpr int kOffStages = kOffQ + kQBytes;
-  static constexpr int kOffP = kOffStages + kStages * kStageBytes;
-  static constexpr int kOffItems = kOffP + kPBytes;
-  static constexpr int kOffBars = kOffItems + kItemSlots * (int)sizeof(Item) + 64;
-  static constexpr int kNumBars = 2 * kItemSlots + 2 + 2 * kStages + 4 + 3 + 2;
+  static constexpr int kOffStages = kQBytes;
+  static constexpr int kFixed = kQBytes + kItemSlots * kItemBytes + kMlBytes + 1024 + 1024;
+  static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kOffItems = kOffStages + kStages * kStageBytes;
+  static constexpr int kOffMl = kOffItems + kItemSlots * kItemBytes;
+  static constexpr int kOffBars = (kOffMl + kMlBytes + 7) & ~7;
+  static constexpr int kNumBars = 2 * kItemSlots + 3 + 2 * kStages + 8 + 4;
   static constexpr int kOffMisc = ((kOffBars + kNumBars * 8) + 15) & ~15;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // tensor memory columns: S, P and O per warpgroup, Q of the item
+  static constexpr int kSCol = 0;                    // S of wg w: 64 fp32 at w * 64
+  static constexpr int kOCol = 2 * kTileKeys;        // O of wg w: D fp32 at kOCol + w * D
+  static constexpr int kPCol = kOCol + 2 * D;        // P of wg w: 64 bf16 (32 cols) at kPCol + w * 32
+  static constexpr int kQCol = kPCol + kTileKeys;    // Q: D bf16 (D / 2 cols)
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdescQK = make_idesc(128, kTileKeys, 1u, false, false);
+  static constexpr uint32_t kIdescPV = make_idesc(128, D, 1u, false, true);
+  static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-};
-
-enum Role : unsigned { kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
-enum BarId : unsigned {
-  kBarItemFull = 1, kBarItemEmpty, kBarQFull, kBarQEmpty, kBarKvFull, kBarKvEmpty, kBarSFull,
-  kBarSEmpty, kBarPFull, kBarPvDone, kBarOEmpty, kBarWg
+  static_assert(kQCol + D / 2 <= kTmemCols, "tensor memory budget");
 };
 
 __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, int& hq, int& qblk) {
@@ -113,33 +126,40 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Item* items = reinterpret_cast<Item*>(smem + C::kOffItems);
+  float2* ml = reinterpret_cast<float2*>(smem + C::kOffMl);
   uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-  uint64_t* item_full = bb;            bb += kItemSlots;
-  uint64_t* item_empty = bb;           bb += kItemSlots;
-  uint64_t* q_full = bb;               bb += 1;
-  uint64_t* q_empty = bb;              bb += 1;
-  uint64_t* kv_full = bb;              bb += C::kStages;
-  uint64_t* kv_empty = bb;             bb += C::kStages;
-  uint64_t* s_full = bb;               bb += 2;
-  uint64_t* s_empty = bb;              bb += 2;
-  uint64_t* p_full = bb;               bb += 1;
-  uint64_t* pv_done = bb;              bb += 1;
-  uint64_t* o_empty = bb;              bb += 1;
-  uint64_t* mma_done = bb;             bb += 1;
-  uint64_t* wg_bar = bb;
+  uint64_t* item_full = bb;   bb += kItemSlots;
+  uint64_t* item_empty = bb;  bb += kItemSlots;
+  uint64_t* q_full = bb;      bb += 1;   // Q staging loaded
+  uint64_t* q_empty = bb;     bb += 1;   // Q staging copied into TMEM
+  uint64_t* q_used = bb;      bb += 1;   // last QK of an item done: TMEM Q may be replaced
+  uint64_t* kv_full = bb;     bb += C::kStages;
+  uint64_t* kv_empty = bb;    bb += C::kStages;
+  uint64_t* s_full = bb;      bb += 2;   // per warpgroup
+  uint64_t* s_empty = bb;     bb += 2;
+  uint64_t* p_full = bb;      bb += 2;
+  uint64_t* pv_done = bb;     bb += 2;
+  uint64_t* o_empty = bb;     bb += 1;
+  uint64_t* mma_done = bb;    bb += 2;   // per issuing thread
+  uint64_t* xch = bb;                    // (m, l) exchange between the two warpgroups
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Abort ab{abort_flag, &g_err_bsa, 2u};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto item_at = [&](int slot) -> Item& {
+    return *reinterpret_cast<Item*>(smem + C::kOffItems + slot * C::kItemBytes);
+  };
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 2); }
-    mbar_init(q_full, 1); mbar_init(q_empty, 1);
+    // item slots are released by the two MMA threads and the 8 softmax warps
+    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 10); }
+    mbar_init(q_full, 1); mbar_init(q_empty, 1); mbar_init(q_used, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1);
+    }
     for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
-    for (int i = 0; i < 2; ++i) { mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4); }
-    mbar_init(p_full, 4); mbar_init(pv_done, 1); mbar_init(o_empty, 4); mbar_init(mma_done, 1);
-    mbar_init(wg_bar, 4);
+    mbar_init(o_empty, 8); mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1); mbar_init(xch, 8);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -157,34 +177,37 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   const uint32_t smem_base = smem_u32(smem);
 
   if (warp == 0) {
-    // ------------------------------------------------------------------ producer
+    // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
     uint32_t qphase = 0;
     int stage = 0; uint32_t kvphase = 0;
-    bool kv_issued[4] = {false, false, false, false};
-    uint32_t last_kv_parity[4] = {0, 0, 0, 0};
+    bool kv_issued[8];
+    uint32_t last_kv_parity[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { kv_issued[i] = false; last_kv_parity[i] = 0; }
     bool q_issued = false;
     uint32_t last_q_parity = 0;
+    const int nbkv = p.T / KB;
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       int b, hq, qblk;
       decode_item(p, item, b, hq, qblk);
       const long long brow = (long long)b * p.nbq + qblk;
-      int lo = p.lower[brow], up = p.upper[brow], lof = p.lower_full[brow], upf = p.upper_full[brow];
-      const int nbkv = p.T / KB;
-      lo = max(lo, 0);
-      up = min(up, nbkv);
-      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleProducer, kBarItemEmpty, item)) break;
+      const int lo = max(p.lower[brow], 0), up = min(p.upper[brow], nbkv);
+      const int lof = p.lower_full[brow], upf = p.upper_full[brow];
+      const int nt = up > lo ? (up - lo) * C::kTilesPerBlock : 0;
+      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleLoader, kBarItemEmpty, item)) break;
       if (lane == 0) {
-        Item& it = items[islot];
-        it.b = b; it.hq = hq; it.qblk = qblk; it.lo = lo; it.up = up; it.lof = lof; it.upf = upf;
+        Item& it = item_at(islot);
+        it.b = b; it.hq = hq; it.qblk = qblk;
+        it.lo = lo; it.up = up; it.lof = lof; it.upf = upf; it.n_tiles = nt;
         mbar_arrive(&item_full[islot]);
       }
       __syncwarp();
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
-      if (up <= lo) continue;
+      if (nt == 0) continue;
       const int hkv = hq / p.G;
-      if (!warp_wait(q_empty, qphase ^ 1, ab, kRoleProducer, kBarQEmpty, item)) break;
+      if (!warp_wait(q_empty, qphase ^ 1, ab, kRoleLoader, kBarQEmpty, item)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, C::kQBytes);
 #pragma unroll
@@ -195,154 +218,181 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       q_issued = true;
       last_q_parity = qphase;
       qphase ^= 1;
-      for (int blk = lo; blk < up; ++blk) {
-        if (!warp_wait(&kv_empty[stage], kvphase ^ 1, ab, kRoleProducer, kBarKvEmpty, item)) { ok = false; break; }
+      for (int t = 0; t < nt; ++t) {
+        if (!warp_wait(&kv_empty[stage], kvphase ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
         if (lane == 0) {
           uint64_t* fb = &kv_full[stage];
-          mbar_arrive_expect_tx(fb, 2 * C::kKVTileBytes + C::kPosSegBytes);
+          mbar_arrive_expect_tx(fb, C::kLoadBytes);
           uint8_t* kdst = smem + C::kOffStages + stage * C::kStageBytes;
-          uint8_t* vdst = kdst + C::kKVTileBytes;
-          uint8_t* ps = vdst + C::kKVTileBytes;
-          const int tok0 = b * p.T + blk * KB;
+          uint8_t* vdst = kdst + C::kKTileBytes;
+          uint8_t* ps = vdst + C::kKTileBytes;
+          const int tok0 = b * p.T + lo * KB + t * kTileKeys;
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn) {
             tma_load_3d(kdst + pn * C::kKVPanelBytes, &tm_k, fb, pn * 64, hkv, tok0);
             tma_load_3d(vdst + pn * C::kKVPanelBytes, &tm_v, fb, pn * 64, hkv, tok0);
           }
-          bulk_load(ps, p.kv_pos + tok0, KB * 4, fb);
-          bulk_load(ps + KB * 4, p.kv_seg + tok0, KB * 4, fb);
+          bulk_load(ps, p.kv_pos + tok0, kTileKeys * 4, fb);
+          bulk_load(ps + kTileKeys * 4, p.kv_seg + tok0, kTileKeys * 4, fb);
         }
         kv_issued[stage] = true;
         last_kv_parity[stage] = kvphase;
         if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
       }
     }
+    // Drain: wait (bounded) for every copy this warp issued before the CTA exits.
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s)
         if (kv_issued[s]) drain_wait(&kv_full[s], last_kv_parity[s]);
       if (q_issued) drain_wait(q_full, last_q_parity);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ QK issuer
+    // Two threads issue the MMAs (QK here, PV in warp 3): a thread's wait on a barrier
+    // stalls only its own stream while the tensor core runs the other's MMAs.
     if (lane == 0) {
       int islot = 0; uint32_t iphase = 0;
-      uint32_t qphase = 0;
+      uint32_t qphase = 0, quphase = 0;
+      bool q_in_use = false;  // a QK of an earlier item may still read the TMEM copy of Q
       int stage = 0; uint32_t kvphase = 0;
-      int sbuf = 0; uint32_t sphase = 0;
-      uint32_t pphase = 0, ophase = 0;
-      int pending_stage = -1;
-      bool pending_first = false;
-      int cur_item = -1;
+      uint32_t sph[2] = {0u, 0u};
       bool ok = true;
-      auto issue_pv = [&](int st, bool first) -> bool {
-        if (!bounded_wait(p_full, pphase, ab, kRoleMma, kBarPFull, cur_item)) return false;
-        pphase ^= 1;
-        if (first) {
-          if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, cur_item)) return false;
-          ophase ^= 1;
-        }
-        tc_fence_after();
-        const uint32_t v_addr = smem_base + C::kOffStages + st * C::kStageBytes + C::kKVTileBytes;
-        const uint32_t p_addr = smem_base + C::kOffP;
-#pragma unroll
-        for (int k = 0; k < KB / 16; ++k) {
-          const uint64_t a = make_sdesc(p_addr + (k / 4) * (kM * 128) + (k % 4) * 32, 16, 1024, kLayoutSW128);
-          const uint64_t bd = make_sdesc(v_addr + k * 16 * 128, C::kKVPanelBytes, 1024, kLayoutSW128);
-          mma_f16_ss(tmem + C::kOCol, a, bd, C::kIdescPV, (first && k == 0) ? 0u : 1u);
-        }
-        mma_commit(&kv_empty[st]);
-        mma_commit(pv_done);
-        return true;
-      };
+      const uint64_t q_desc0 = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
+      const uint64_t k_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        cur_item = item;
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
-        const int n = items[islot].up - items[islot].lo;
-        if (n <= 0 && pending_stage >= 0) {
-          // nothing to compute: release the deferred PV now so the softmax group, which
-          // waits for it before finishing the previous item, never starves
-          if (!issue_pv(pending_stage, pending_first)) break;
-          pending_stage = -1;
-        }
-        if (n > 0) {
-          if (!bounded_wait(q_full, qphase, ab, kRoleMma, kBarQFull, item)) break;
-          qphase ^= 1;
-        }
-        for (int i = 0; i < n; ++i) {
-          if (!bounded_wait(&kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
-              !bounded_wait(&s_empty[sbuf], sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_base + C::kOffStages + stage * C::kStageBytes;
-          const uint32_t q_addr = smem_base + C::kOffQ;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const int pn = k / 4, kk = k % 4;
-            const uint64_t a = make_sdesc(q_addr + pn * C::kQPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
-            const uint64_t bd = make_sdesc(k_addr + pn * C::kKVPanelBytes + kk * 32, 16, 1024, kLayoutSW128);
-            mma_f16_ss(tmem + sbuf * KB, a, bd, C::kIdescQK, k > 0);
-          }
-          mma_commit(&s_full[sbuf]);
-          if (i == n - 1) mma_commit(q_empty);
-          if (pending_stage >= 0 && !issue_pv(pending_stage, pending_first)) { ok = false; break; }
-          pending_stage = stage;
-          pending_first = (i == 0);
-          if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
-          if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
-        }
-        if (!ok) break;
+        const int nt = item_at(islot).n_tiles;
         mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+        if (nt == 0) continue;
+        if (!bounded_wait(q_full, qphase, ab, kRoleMma, kBarQFull, item)) break;
+        qphase ^= 1;
+        if (q_in_use) {
+          if (!bounded_wait(q_used, quphase, ab, kRoleMma, kBarQEmpty, item)) break;
+          quphase ^= 1;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tmem_cp_128x256b(tmem + C::kQCol + kk * 8,
+                           q_desc0 + static_cast<uint64_t>(((kk / 4) * C::kQPanelBytes + (kk % 4) * 32) >> 4));
+        mma_commit(q_empty);
+        for (int t = 0; t < nt; ++t) {
+          const int w = t & 1;
+          if (!bounded_wait(&kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
+              !bounded_wait(&s_empty[w], sph[w] ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
+          sph[w] ^= 1;
+          tc_fence_after();
+          const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_ts(tmem + C::kSCol + w * kTileKeys, tmem + C::kQCol + kk * 8,
+                       kd + static_cast<uint64_t>(((kk / 4) * C::kKVPanelBytes + (kk % 4) * 32) >> 4),
+                       C::kIdescQK, kk > 0);
+          mma_commit(&s_full[w]);
+          if (t == nt - 1) {
+            mma_commit(q_used);
+            q_in_use = true;
+          }
+          if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
+        }
       }
-      if (ok && pending_stage >= 0) issue_pv(pending_stage, pending_first);
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
+      mma_commit(&mma_done[0]);
+      drain_wait(&mma_done[0], 0);
+    }
+    __syncwarp();
+  } else if (warp == 3) {
+    // ------------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      int islot = 0; uint32_t iphase = 0;
+      int stage = 0;
+      uint32_t pph[2] = {0u, 0u};
+      uint32_t ophase = 0;
+      bool ok = true;
+      const uint64_t v_desc0 =
+          make_sdesc(smem_base + C::kOffStages + C::kKTileBytes, C::kKVPanelBytes, 1024, kLayoutSW128);
+      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        const int nt = item_at(islot).n_tiles;
+        mbar_arrive(&item_empty[islot]);
+        if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+        // PV of tile t (A = P of warpgroup t & 1 in TMEM, B = V tile) goes to the O
+        // accumulator of warpgroup t & 1; each warpgroup's first tile of an item
+        // overwrites it.  A PV follows its tile's softmax, which follows the tile's QK,
+        // so the stage is free once the PV is done.
+        for (int t = 0; t < nt; ++t) {
+          const int w = t & 1;
+          if (!bounded_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+          pph[w] ^= 1;
+          if (t == 0) {
+            if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
+            ophase ^= 1;
+          }
+          tc_fence_after();
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int k = 0; k < kTileKeys / 16; ++k)
+            mma_f16_ts(tmem + C::kOCol + w * D, tmem + C::kPCol + w * (kTileKeys / 2) + k * 8,
+                       vd + static_cast<uint64_t>((k * 16 * 128) >> 4), C::kIdescPV,
+                       (t < 2 && k == 0) ? 0u : 1u);
+          mma_commit(&kv_empty[stage]);
+          mma_commit(&pv_done[w]);
+          if (++stage == C::kStages) stage = 0;
+        }
+      }
+      mma_commit(&mma_done[1]);
+      drain_wait(&mma_done[1], 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
-    const int q4 = warp - 4;
-    const int r = q4 * 32 + lane;  // query row of the tile = TMEM lane
+    const int w = (warp - 4) >> 2;   // warpgroup: tiles t with t & 1 == w
+    const int q4 = warp & 3;         // TMEM lane quadrant of this warp
+    const int r = q4 * 32 + lane;    // query row of the item = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + C::kSCol + w * kTileKeys;
+    const uint32_t o_col = tmem + lane_off + C::kOCol + w * D;
+    const uint32_t p_col = tmem + lane_off + C::kPCol + w * (kTileKeys / 2);
     int islot = 0; uint32_t iphase = 0;
     int stage = 0; uint32_t kvphase = 0;
-    int sbuf = 0; uint32_t sphase = 0;
-    uint32_t pvphase = 0;
-    uint32_t wg_phase = 0;
+    uint32_t sph = 0, pvph = 0, xph = 0;
+    int par = 0;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
-      const Item it = items[islot];
-      const int n = it.up - it.lo;
-      const int t = it.qblk * kM + r;
-      const long long orow = ((long long)it.b * p.T + t) * p.Hq + it.hq;
-      const int qp = p.q_pos[(long long)it.b * p.T + t];
-      const int qs = p.q_seg[(long long)it.b * p.T + t];
+      const Item it = item_at(islot);
+      const int nt = it.n_tiles;
+      const long long tok = (long long)it.b * p.T + it.qblk * kM + r;
+      const int qp = p.q_pos[tok];
+      const int qs = p.q_seg[tok];
       const bool q_pad = qs == p.pad_id;
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // log2 units, lazily moved reference max
+      int mine = 0;                  // tiles of this item handled by this warpgroup so far
       bool ok = true;
-      for (int i = 0; i < n; ++i) {
-        const int blk = it.lo + i;
-        if (!warp_wait(&s_full[sbuf], sphase, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+      for (int t = 0; t < nt; ++t) {
+        if ((t & 1) != w) {
+          if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
+          continue;
+        }
+        const int blk = it.lo + t / C::kTilesPerBlock;
+        const bool full = blk >= it.lof && blk < it.upf;
+        if (!warp_wait(&s_full[w], sph, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        sph ^= 1;
+        float x[kTileKeys];
         tc_fence_after();
-        float x[KB];
-#pragma unroll
-        for (int c = 0; c < KB / 32; ++c) tmem_ld_32x32b_x32(tmem + lane_off + sbuf * KB + c * 32, x + c * 32);
+        tmem_ld_32x32b_x32(s_col, x);
+        tmem_ld_32x32b_x32(s_col + 32, x + 32);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[sbuf]);
-        if (++sbuf == 2) { sbuf = 0; sphase ^= 1; }
-        const bool full = blk >= it.lof && blk < it.upf;
-        // the block's positions / segment ids arrived with the K/V tiles of this stage
-        if (!warp_wait(&kv_full[stage], kvphase, ab, kRoleSoftmax, kBarKvFull, item)) { ok = false; break; }
-        float tmax = -INFINITY;
-        if (full) {
+        if (lane == 0) mbar_arrive(&s_empty[w]);
+        if (!full) {
+          // the tile's key positions / segment ids arrived with its K / V
+          if (!warp_wait(&kv_full[stage], kvphase, ab, kRoleSoftmax, kBarKvFull, item)) { ok = false; break; }
+          const int* ps = reinterpret_cast<const int*>(smem + C::kOffStages + stage * C::kStageBytes +
+                                                       2 * C::kKTileBytes);
 #pragma unroll
-          for (int j = 0; j < KB; ++j) { x[j] *= p.scale_log2; tmax = fmaxf(tmax, x[j]); }
-        } else {
-          const int* ps = reinterpret_cast<const int*>(smem + C::kOffStages + stage * C::kStageBytes + 2 * C::kKVTileBytes);
-#pragma unroll
-          for (int j = 0; j < KB; j += 4) {
+          for (int j = 0; j < kTileKeys; j += 4) {
             const int4 kp4 = *reinterpret_cast<const int4*>(ps + j);
-            const int4 ks4 = *reinterpret_cast<const int4*>(ps + KB + j);
+            const int4 ks4 = *reinterpret_cast<const int4*>(ps + kTileKeys + j);
             const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
             const int ks[4] = {ks4.x, ks4.y, ks4.z, ks4.w};
 #pragma unroll
@@ -351,12 +401,15 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               if (p.causal) ok_k = ok_k && kp[u] <= qp;
               if (p.window_left >= 0) ok_k = ok_k && (long long)qp - kp[u] <= p.window_left;
               if (p.window_right >= 0) ok_k = ok_k && (long long)kp[u] - qp <= p.window_right;
-              x[j + u] = ok_k ? x[j + u] * p.scale_log2 : -INFINITY;
-              tmax = fmaxf(tmax, x[j + u]);
+              if (!ok_k) x[j + u] = -INFINITY;
             }
           }
         }
         if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int j = 0; j < kTileKeys; ++j) mx[j & 3] = fmaxf(mx[j & 3], x[j]);
+        const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
         // lazy online softmax: move the reference max only when it grows by > 2^8
         float m_new = m;
         if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
@@ -364,17 +417,32 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         float psum = 0.f;
         if (m_new == -INFINITY) {
 #pragma unroll
-          for (int j = 0; j < KB; ++j) x[j] = 0.f;
+          for (int j = 0; j < kTileKeys; ++j) x[j] = 0.f;
         } else {
+          float ps4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < KB; ++j) { x[j] = ex2(x[j] - m_new); psum += x[j]; }
+          for (int j = 0; j < kTileKeys; ++j) {
+            x[j] = ex2(fmaf(x[j], p.scale_log2, -m_new));
+            ps4[j & 3] += x[j];
+          }
+          psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         }
         l = l * alpha + psum;
-        // previous PV must be done: P buffer reusable and O stable
-        if (i > 0) {
-          if (!warp_wait(pv_done, pvphase, ab, kRoleSoftmax, kBarPvDone, item)) { ok = false; break; }
-          pvphase ^= 1;
+        uint32_t pk[kTileKeys / 2];
+#pragma unroll
+        for (int j = 0; j < kTileKeys / 2; ++j) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
+          pk[j] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        // this warpgroup's previous PV must be done before its P is replaced and its O
+        // rescaled
+        if (mine > 0) {
+          if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) { ok = false; break; }
+          pvph ^= 1;
           tc_fence_after();
+        }
+        tmem_st_32x32b_x32_u(p_col, pk);
+        if (mine > 0) {
           // TMEM loads/stores are warp-collective (.sync.aligned): the whole warp rescales
           // together when any of its rows moved its reference max; other rows use 1.
           const bool my_rescale = m_new != m && m != -INFINITY;
@@ -383,70 +451,75 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
               float ov[32];
-              tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+              tmem_ld_32x32b_x32(o_col + c * 32, ov);
 #pragma unroll
               for (int j = 0; j < 32; ++j) ov[j] *= f;
-              tmem_st_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+              tmem_st_32x32b_x32(o_col + c * 32, ov);
             }
           }
         }
         m = m_new;
-        // P row (bf16) -> shared memory, 128-byte swizzled K-major panels of 64 keys
-        const uint32_t prow = smem_base + C::kOffP + r * 128;
-#pragma unroll
-        for (int pp = 0; pp < C::kPPanels; ++pp) {
-#pragma unroll
-          for (int cchunk = 0; cchunk < 8; ++cchunk) {
-            uint32_t w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(x[pp * 64 + cchunk * 8 + 2 * u],
-                                                        x[pp * 64 + cchunk * 8 + 2 * u + 1]);
-              w[u] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            st_shared_v4(prow + pp * (kM * 128) + ((cchunk ^ (r & 7)) * 16), w[0], w[1], w[2], w[3]);
-          }
-        }
-        fence_proxy_async_smem();
+        ++mine;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[w]);
       }
       if (!ok) break;
-      __nv_bfloat16* orow_ptr = p.out + orow * D;
-      if (n > 0) {
-        if (!warp_wait(pv_done, pvphase, ab, kRoleSoftmax, kBarPvDone, item)) break;
-        pvphase ^= 1;
+      if (mine > 0) {
+        if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) break;
+        pvph ^= 1;
+      }
+      // merge the two warpgroups' partial results row by row
+      ml[(par * 2 + w) * kM + r] = make_float2(m, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xch);
+      if (!warp_wait(xch, xph, ab, kRoleSoftmax, kBarXch, item)) break;
+      xph ^= 1;
+      const float2 oth = ml[(par * 2 + (w ^ 1)) * kM + r];
+      const float mxr = fmaxf(m, oth.x);
+      const float a_me = l > 0.f ? ex2(m - mxr) : 0.f;
+      const float a_ot = oth.y > 0.f ? ex2(oth.x - mxr) : 0.f;
+      const float L = l * a_me + oth.y * a_ot;
+      const float a0 = w == 0 ? a_me : a_ot, a1 = w == 0 ? a_ot : a_me;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      constexpr int kOutHalf = D / 2;
+      __nv_bfloat16* orow = p.out + (tok * p.Hq + it.hq) * D;
+      if (nt > 0) {
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          float ov[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + c * 32, ov);
+        for (int c = 0; c < kOutHalf / 32; ++c) {
+          const int col = w * kOutHalf + c * 32;
+          float o0[32], o1[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + col, o0);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + D + col, o1);
 #pragma unroll
           for (int j = 0; j < 32; j += 8) {
-            uint32_t w[4];
+            uint32_t wv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[j + 2 * u] * inv, ov[j + 2 * u + 1] * inv);
-              w[u] = *reinterpret_cast<uint32_t*>(&h2);
+              // an accumulator that received no PV this item holds stale data: select
+              const int j0 = j + 2 * u;
+              const float v0 = ((a0 > 0.f) ? o0[j0] * a0 : 0.f) + ((a1 > 0.f) ? o1[j0] * a1 : 0.f);
+              const float v1 = ((a0 > 0.f) ? o0[j0 + 1] * a0 : 0.f) + ((a1 > 0.f) ? o1[j0 + 1] * a1 : 0.f);
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(v0 * inv, v1 * inv);
+              wv[u] = *reinterpret_cast<uint32_t*>(&h2);
             }
-            *reinterpret_cast<uint4*>(orow_ptr + c * 32 + j) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(orow + col + j) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty);
-        if (p.lse != nullptr) p.lse[orow] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       } else {
 #pragma unroll
-        for (int j = 0; j < D; j += 8)
-          *reinterpret_cast<uint4*>(orow_ptr + j) = make_uint4(0u, 0u, 0u, 0u);
-        if (p.lse != nullptr) p.lse[orow] = -INFINITY;
+        for (int j = 0; j < kOutHalf; j += 8)
+          *reinterpret_cast<uint4*>(orow + w * kOutHalf + j) = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (!warps_barrier(wg_bar, wg_phase, ab, kRoleSoftmax, kBarWg, item)) break;
-      if (r == 0) mbar_arrive(&item_empty[islot]);
+      if (w == 0 && p.lse != nullptr) p.lse[tok * p.Hq + it.hq] = L > 0.f ? (mxr + log2f(L)) * kLn2 : -INFINITY;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
+      par ^= 1;
     }
   }
 
@@ -473,7 +546,7 @@ int launch_impl(const void* q, const void* k, const void* v, const Params& p, cu
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.T};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)KB};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileKeys};
     if (encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims,
                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
         encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims,
