@@ -9,29 +9,28 @@
 // tokens and one KV head; its NT * G query rows (token-major, head-minor; NT = 8 when
 // G = 16) fill the M = 128 rows of one tcgen05 MMA.  The item's key set is the union
 // of the blocks its tokens selected (deduplicated, sorted by first key row), walked in
-// tiles of 64 keys; every row keeps only the keys of blocks its own token selected
-// (plus the causal / sequence-end limit), so a union block is gathered once per item
-// and shared by all tokens that picked it.  A persistent CTA per SM runs:
+// tiles of 64 keys, two tiles per QK; every row keeps only the keys of blocks its own
+// token selected (plus the causal / sequence-end limit), so a union block is gathered
+// once per item and shared by all tokens that picked it.  A persistent CTA per SM runs:
 //   warp 2      item builder: reads the NT tokens' index lists (cu_seqlens binary
 //               search for packed sequences), filters them, and forms the union with a
 //               warp bitonic sort plus a run merge into (first key row, token bitmask);
-//   warp 0      loader: TMA loads of the item's Q rows (one 3D box per 64-wide panel)
-//               into a staging buffer and of each K / V tile into a shared-memory ring;
+//   warp 0      loader: TMA loads into a shared-memory ring: the item's Q rows (one 3D
+//               box per 64-wide panel), then K and V of each pair of tiles;
 //   warp 1      QK issuer (one thread): copies Q into tensor memory (tcgen05.cp, in
-//               order with its MMAs), then S = Q K^T (M = 128 rows, N = 64 keys, A from
-//               TMEM, fp32 in TMEM);
-//   warp 3      PV issuer (one thread): O += P V (N = head dim, A = P from TMEM).  With
-//               both A operands in TMEM the MMAs read only K and V from shared memory,
-//               and with two issuing threads one's barrier waits overlap the other's
-//               MMAs;
-//   warps 4..11 two softmax warpgroups, one thread per row each.  Tiles alternate
-//               between them (tile t -> warpgroup t & 1), each with its own S buffer,
-//               running (m, l) and O accumulator, so two tiles' softmax overlap the MMAs.
-//               Per tile: selection / causal mask, lazy online softmax (O rescaled only
-//               when the running max grows by > 2^8), P (bf16) stored to TMEM.  The
-//               epilogue merges the two partial results ((m, l) exchanged through
-//               shared memory; each warpgroup writes half of the head-dim columns) and
-//               writes O / l and the LSE.
+//               order with its MMAs), then S = Q K^T for a pair (M = 128 rows, N = 128
+//               keys, A from TMEM, fp32 in TMEM);
+//   warp 3      PV issuer (one thread): O_w += P_w V_w (N = head dim, A = P_w from
+//               TMEM) for each warpgroup's half of the pair.  With both A operands in
+//               TMEM the MMAs read only K and V from shared memory, and with two
+//               issuing threads one's barrier waits overlap the other's MMAs;
+//   warps 4..11 two softmax warpgroups, one thread per row each; warpgroup w takes
+//               tile w of every pair (S columns 64 w .. 64 w + 63) with its own P
+//               columns, O accumulator and running (m, l).  Per tile: selection /
+//               causal mask, lazy online softmax (O rescaled only when the running max
+//               grows by > 2^8), P (bf16) stored to TMEM.  The epilogue merges the two
+//               partial results ((m, l) exchanged through shared memory; each
+//               warpgroup writes half of the head-dim columns) and writes O / l, LSE.
 //
 // fp32 path (CUDA cores, exact fp32 products and sums): one CTA per token group.
 // Tensor cores would round fp32 inputs to tf32, which is not accurate enough for the
@@ -97,33 +96,31 @@ struct Cfg {
   static constexpr int kPanels = D / 64;                   // 64-element (128-byte) panels
   static constexpr int kSegLen = BS < kTileKeys ? BS : kTileKeys;
   static constexpr int kSegs = kTileKeys / kSegLen;        // union blocks per tile (BS <= 64)
-  static constexpr int kKVPanelBytes = kTileKeys * 128;    // 8 KB
-  static constexpr int kKTileBytes = kPanels * kKVPanelBytes;
-  static constexpr int kStageBytes = 2 * kKTileBytes;      // [K][V]
-  static constexpr int kLoadBytes = 2 * kKTileBytes;
+  static constexpr int kPairKeys = 2 * kTileKeys;          // one QK covers two tiles
+  static constexpr int kPanelBytes = kPairKeys * 128;      // 16 KB: 128 keys x 64 elements
+  static constexpr int kKBytes = kPanels * kPanelBytes;    // K (or V) of a pair; also Q staging
+  static constexpr int kStageBytes = 2 * kKBytes;          // [K][V] of a pair, or an item's Q
   static constexpr int kQPanelBytes = kRows * 128;
-  static constexpr int kQBytes = kPanels * kQPanelBytes;   // Q staging (copied into TMEM)
   static constexpr int kItemBytes = (static_cast<int>(sizeof(Item)) + 127) & ~127;
   static constexpr int kMlBytes = 2 * 2 * kRows * 8;       // (m, l) per row: [item parity][wg]
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffStages = kQBytes;
-  static constexpr int kFixed = kQBytes + kItemSlots * kItemBytes + kMaxUnion * 8 + kMlBytes + 1024 + 1024;
+  static constexpr int kFixed = kItemSlots * kItemBytes + kMaxUnion * 8 + kMlBytes + 1024 + 1024;
   static constexpr int kStagesFit = (232448 - kFixed) / kStageBytes;
   static constexpr int kStages = kStagesFit > 6 ? 6 : kStagesFit;
+  static constexpr int kOffStages = 0;
   static constexpr int kOffItems = kOffStages + kStages * kStageBytes;
   static constexpr int kOffSort = kOffItems + kItemSlots * kItemBytes;
   static constexpr int kOffMl = kOffSort + kMaxUnion * 8;
   static constexpr int kOffBars = kOffMl + kMlBytes;
-  static constexpr int kNumBars = 2 * kItemSlots + 3 + 2 * kStages + 8 + 4;
+  static constexpr int kNumBars = 2 * kItemSlots + 2 * kStages + 1 + 2 + 4 + 1 + 2 + 1;
   static constexpr int kOffMisc = ((kOffBars + kNumBars * 8) + 15) & ~15;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  // tensor memory columns (512): S and P per warpgroup, O per warpgroup, Q of the item
-  static constexpr int kSCol = 0;                          // S of wg w: 64 fp32 at w * 64
-  static constexpr int kOCol = 2 * kTileKeys;              // O of wg w: D fp32 at kOCol + w * D
+  // tensor memory columns (512 at D = 128): S of a pair, O and P per warpgroup, Q
+  static constexpr int kSCol = 0;                          // S: 128 fp32, warpgroup w reads 64 at w * 64
+  static constexpr int kOCol = kPairKeys;                  // O of wg w: D fp32 at kOCol + w * D
   static constexpr int kPCol = kOCol + 2 * D;              // P of wg w: 64 bf16 (32 cols) at kPCol + w * 32
   static constexpr int kQCol = kPCol + kTileKeys;          // Q: D bf16 (D / 2 cols)
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdescQK = make_idesc(128, kTileKeys, 1u, false, false);
+  static constexpr uint32_t kIdescQK = make_idesc(128, kPairKeys, 1u, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(128, D, 1u, false, true);
   static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -311,18 +308,16 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
   uint64_t* item_full = bb;   bb += kItemSlots;
   uint64_t* item_empty = bb;  bb += kItemSlots;
-  uint64_t* q_full = bb;      bb += 1;   // Q staging loaded
-  uint64_t* q_empty = bb;     bb += 1;   // Q staging copied into TMEM
+  uint64_t* st_full = bb;     bb += C::kStages;  // ring: an item's Q, then one stage per pair
+  uint64_t* st_empty = bb;    bb += C::kStages;
   uint64_t* q_used = bb;      bb += 1;   // last QK of an item done: TMEM Q may be replaced
-  uint64_t* kv_full = bb;     bb += C::kStages;
-  uint64_t* kv_empty = bb;    bb += C::kStages;
-  uint64_t* s_full = bb;      bb += 2;   // per warpgroup
-  uint64_t* s_empty = bb;     bb += 2;
-  uint64_t* p_full = bb;      bb += 2;
+  uint64_t* s_full = bb;      bb += 1;   // S of the current pair written
+  uint64_t* s_empty = bb;     bb += 1;   // both warpgroups have read it
+  uint64_t* p_full = bb;      bb += 2;   // per warpgroup
   uint64_t* pv_done = bb;     bb += 2;
   uint64_t* o_empty = bb;     bb += 1;
   uint64_t* mma_done = bb;    bb += 2;   // per issuing thread
-  uint64_t* xch = bb;         // (m, l) exchange between the two warpgroups
+  uint64_t* xch = bb;                    // (m, l) exchange between the two warpgroups
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Abort ab{abort_flag, &g_err_nsa, 1u};
@@ -334,12 +329,10 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   if (threadIdx.x == 0) {
     // item slots are released by the loader, the two MMA threads and the 8 softmax warps
     for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 11); }
-    mbar_init(q_full, 1); mbar_init(q_empty, 1); mbar_init(q_used, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1); mbar_init(&s_empty[i], 4);
-      mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1);
-    }
-    for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&st_full[i], 1); mbar_init(&st_empty[i], 1); }
+    mbar_init(q_used, 1);
+    mbar_init(s_full, 1); mbar_init(s_empty, 8);
+    for (int i = 0; i < 2; ++i) { mbar_init(&p_full[i], 4); mbar_init(&pv_done[i], 1); }
     mbar_init(o_empty, 8); mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1); mbar_init(xch, 8);
     *abort_flag = 0;
     fence_mbar_init();
@@ -371,123 +364,119 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   } else if (warp == 0) {
     // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
-    uint32_t qphase = 0;
-    int stage = 0; uint32_t kvphase = 0;
-    bool kv_issued[8];
-    uint32_t last_kv_parity[8];
+    int stage = 0; uint32_t phase = 0;
+    bool issued[8];
+    uint32_t last_parity[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) { kv_issued[i] = false; last_kv_parity[i] = 0; }
-    bool q_issued = false;
-    uint32_t last_q_parity = 0;
+    for (int i = 0; i < 8; ++i) { issued[i] = false; last_parity[i] = 0; }
     const uint32_t q_box_bytes = static_cast<uint32_t>(C::kPanels * 128 * p.G * p.NT);
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, item)) break;
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union, hkv = it.hkv;
-      if (nt > 0) {
-        if (!warp_wait(q_empty, qphase ^ 1, ab, kRoleLoader, kBarQEmpty, item)) break;
+      const int np = (nt + 1) / 2;
+      for (int pp = np > 0 ? -1 : 0; pp < np; ++pp) {  // pp = -1: the item's Q
+        if (!warp_wait(&st_empty[stage], phase ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(q_full, q_box_bytes);
-          uint8_t* dst = smem + C::kOffQ;
+          uint64_t* fb = &st_full[stage];
+          uint8_t* kdst = smem + C::kOffStages + stage * C::kStageBytes;
+          uint8_t* vdst = kdst + C::kKBytes;
+          if (pp < 0) {
+            mbar_arrive_expect_tx(fb, q_box_bytes);
 #pragma unroll
-          for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(dst + pn * C::kQPanelBytes, &tm_q, q_full, pn * 64, hkv * p.G, it.g * p.NT);
-        }
-        q_issued = true;
-        last_q_parity = qphase;
-        qphase ^= 1;
-        for (int t = 0; t < nt; ++t) {
-          if (!warp_wait(&kv_empty[stage], kvphase ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
-          if (lane == 0) {
-            uint64_t* fb = &kv_full[stage];
-            mbar_arrive_expect_tx(fb, C::kLoadBytes);
-            uint8_t* kdst = smem + C::kOffStages + stage * C::kStageBytes;
-            uint8_t* vdst = kdst + C::kKTileBytes;
+            for (int pn = 0; pn < C::kPanels; ++pn)
+              tma_load_3d(kdst + pn * C::kQPanelBytes, &tm_q, fb, pn * 64, hkv * p.G, it.g * p.NT);
+          } else {
+            mbar_arrive_expect_tx(fb, C::kStageBytes);
 #pragma unroll
-            for (int e = 0; e < C::kSegs; ++e) {
-              int row0;
-              if constexpr (BS <= kTileKeys) {
-                const int ui = t * C::kSegs + e;
-                // a missing block is read from beyond the last token: TMA fills zeros
-                row0 = ui < nu ? it.ux[ui] : p.n_tok;
-              } else {
-                row0 = it.ux[t / (BS / kTileKeys)] + (t % (BS / kTileKeys)) * kTileKeys;
-              }
+            for (int hh = 0; hh < 2; ++hh) {
+              const int t = 2 * pp + hh;
 #pragma unroll
-              for (int pn = 0; pn < C::kPanels; ++pn) {
-                const int off = pn * C::kKVPanelBytes + e * C::kSegLen * 128;
-                tma_load_3d(kdst + off, &tm_k, fb, pn * 64, hkv, row0);
-                tma_load_3d(vdst + off, &tm_v, fb, pn * 64, hkv, row0);
+              for (int e = 0; e < C::kSegs; ++e) {
+                int row0;
+                if constexpr (BS <= kTileKeys) {
+                  const int ui = t * C::kSegs + e;
+                  // a missing block is read from beyond the last token: TMA fills zeros
+                  row0 = ui < nu ? it.ux[ui] : p.n_tok;
+                } else {
+                  const int ui = t / (BS / kTileKeys);
+                  row0 = ui < nu ? it.ux[ui] + (t % (BS / kTileKeys)) * kTileKeys : p.n_tok;
+                }
+#pragma unroll
+                for (int pn = 0; pn < C::kPanels; ++pn) {
+                  const int off = pn * C::kPanelBytes + (hh * kTileKeys + e * C::kSegLen) * 128;
+                  tma_load_3d(kdst + off, &tm_k, fb, pn * 64, hkv, row0);
+                  tma_load_3d(vdst + off, &tm_v, fb, pn * 64, hkv, row0);
+                }
               }
             }
           }
-          kv_issued[stage] = true;
-          last_kv_parity[stage] = kvphase;
-          if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
         }
+        issued[stage] = true;
+        last_parity[stage] = phase;
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
     }
     // Drain: wait (bounded) for every copy this warp issued before the CTA exits.
-    if (lane == 0) {
+    if (lane == 0)
       for (int s = 0; s < C::kStages; ++s)
-        if (kv_issued[s]) drain_wait(&kv_full[s], last_kv_parity[s]);
-      if (q_issued) drain_wait(q_full, last_q_parity);
-    }
+        if (issued[s]) drain_wait(&st_full[s], last_parity[s]);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ QK issuer
     // Two threads issue the MMAs (QK here, PV in warp 3): a thread's wait on a barrier
     // stalls only its own stream while the tensor core runs the other's MMAs.
     if (lane == 0) {
       int islot = 0; uint32_t iphase = 0;
-      uint32_t qphase = 0, quphase = 0;
+      uint32_t quphase = 0, sphase = 0;
       bool q_in_use = false;  // a QK of an earlier item may still read the TMEM copy of Q
-      int stage = 0; uint32_t kvphase = 0;
-      uint32_t sph[2] = {0u, 0u};
+      int stage = 0; uint32_t phase = 0;
       bool ok = true;
       // descriptors of the shared-memory operands; a byte offset x adds x >> 4
-      const uint64_t q_desc0 = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
-      const uint64_t k_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
+      const uint64_t st_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
         mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
-        if (nt == 0) continue;
-        // Q of this item: staging buffer -> TMEM, once the previous item's QKs are done
-        if (!bounded_wait(q_full, qphase, ab, kRoleMma, kBarQFull, item)) break;
-        qphase ^= 1;
+        const int np = (nt + 1) / 2;
+        if (np == 0) continue;
+        // Q of this item (its first ring stage) -> TMEM, once the previous item's QKs are done
+        if (!bounded_wait(&st_full[stage], phase, ab, kRoleMma, kBarQFull, item)) break;
         if (q_in_use) {
           if (!bounded_wait(q_used, quphase, ab, kRoleMma, kBarQEmpty, item)) break;
           quphase ^= 1;
         }
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          tmem_cp_128x256b(tmem + C::kQCol + kk * 8,
-                           q_desc0 + static_cast<uint64_t>(((kk / 4) * C::kQPanelBytes + (kk % 4) * 32) >> 4));
-        mma_commit(q_empty);
-        for (int t = 0; t < nt; ++t) {
-          const int w = t & 1;
-          if (!bounded_wait(&kv_full[stage], kvphase, ab, kRoleMma, kBarKvFull, item) ||
-              !bounded_wait(&s_empty[w], sph[w] ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
-          sph[w] ^= 1;
-          tc_fence_after();
-          const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
+        {
+          const uint64_t qd = st_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_f16_ts(tmem + C::kSCol + w * kTileKeys, tmem + C::kQCol + kk * 8,
-                       kd + static_cast<uint64_t>(((kk / 4) * C::kKVPanelBytes + (kk % 4) * 32) >> 4),
+            tmem_cp_128x256b(tmem + C::kQCol + kk * 8,
+                             qd + static_cast<uint64_t>(((kk / 4) * C::kQPanelBytes + (kk % 4) * 32) >> 4));
+        }
+        mma_commit(&st_empty[stage]);
+        if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+        for (int pp = 0; pp < np; ++pp) {
+          if (!bounded_wait(&st_full[stage], phase, ab, kRoleMma, kBarKvFull, item) ||
+              !bounded_wait(s_empty, sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
+          sphase ^= 1;
+          tc_fence_after();
+          const uint64_t kd = st_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_f16_ts(tmem + C::kSCol, tmem + C::kQCol + kk * 8,
+                       kd + static_cast<uint64_t>(((kk / 4) * C::kPanelBytes + (kk % 4) * 32) >> 4),
                        C::kIdescQK, kk > 0);
-          mma_commit(&s_full[w]);
-          if (t == nt - 1) {
+          mma_commit(s_full);
+          if (pp == np - 1) {
             mma_commit(q_used);
             q_in_use = true;
           }
-          if (++stage == C::kStages) { stage = 0; kvphase ^= 1; }
+          if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
       }
       // every tcgen05 op issued by this thread has finished once mma_done fires
@@ -504,33 +493,38 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       uint32_t ophase = 0;
       bool ok = true;
       const uint64_t v_desc0 =
-          make_sdesc(smem_base + C::kOffStages + C::kKTileBytes, C::kKVPanelBytes, 1024, kLayoutSW128);
+          make_sdesc(smem_base + C::kOffStages + C::kKBytes, C::kPanelBytes, 1024, kLayoutSW128);
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
         mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
-        // PV of tile t (A = P of warpgroup t & 1 in TMEM, B = V tile) goes to the O
-        // accumulator of warpgroup t & 1; each warpgroup's first tile of an item
-        // overwrites it.  A PV follows its tile's softmax, which follows the tile's QK,
-        // so the stage (K and V) is free once the PV is done.
-        for (int t = 0; t < nt; ++t) {
-          const int w = t & 1;
-          if (!bounded_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
-          pph[w] ^= 1;
-          if (t == 0) {
-            if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
-            ophase ^= 1;
-          }
-          tc_fence_after();
+        const int np = (nt + 1) / 2;
+        if (np == 0) continue;
+        if (++stage == C::kStages) stage = 0;  // the item's Q stage (released by the QK thread)
+        // Per pair, warpgroup w's half: O_w (+)= P_w (A in TMEM, 64 keys) * V[64 w ..
+        // 64 w + 63]; the first pair of an item overwrites O_w.  A PV follows its tile's
+        // softmax, which follows the pair's QK, so the stage is free once both are done.
+        for (int pp = 0; pp < np && ok; ++pp) {
           const uint64_t vd = v_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
 #pragma unroll
-          for (int k = 0; k < kTileKeys / 16; ++k)
-            mma_f16_ts(tmem + C::kOCol + w * D, tmem + C::kPCol + w * (kTileKeys / 2) + k * 8,
-                       vd + static_cast<uint64_t>((k * 16 * 128) >> 4), C::kIdescPV,
-                       (t < 2 && k == 0) ? 0u : 1u);
-          mma_commit(&kv_empty[stage]);
-          mma_commit(&pv_done[w]);
+          for (int w = 0; w < 2; ++w) {
+            if (!bounded_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+            pph[w] ^= 1;
+            if (pp == 0 && w == 0) {
+              if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
+              ophase ^= 1;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < kTileKeys / 16; ++k)
+              mma_f16_ts(tmem + C::kOCol + w * D, tmem + C::kPCol + w * (kTileKeys / 2) + k * 8,
+                         vd + static_cast<uint64_t>(((w * kTileKeys + k * 16) * 128) >> 4), C::kIdescPV,
+                         (pp == 0 && k == 0) ? 0u : 1u);
+            mma_commit(&pv_done[w]);
+          }
+          if (!ok) break;
+          mma_commit(&st_empty[stage]);
           if (++stage == C::kStages) stage = 0;
         }
       }
@@ -540,7 +534,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
-    const int w = (warp - 4) >> 2;   // warpgroup: tiles t with t & 1 == w
+    const int w = (warp - 4) >> 2;   // warpgroup: tile 2 pp + w of every pair pp
     const int q4 = warp & 3;         // TMEM lane quadrant of this warp
     const int r = q4 * 32 + lane;    // row of the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
@@ -550,7 +544,6 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int ti = r < p.rows ? r / p.G : 0;  // token of this row within the item
     const int h = r - ti * p.G;
     int islot = 0; uint32_t iphase = 0;
-    int stage = 0;
     uint32_t sph = 0, pvph = 0, xph = 0;
     int par = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -558,18 +551,15 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union;
+      const int np = (nt + 1) / 2;
       const bool row_ok = r < p.rows && ((it.tok_valid >> ti) & 1u);
       const int limit = r < p.rows ? it.limit[ti] : -1;
       const unsigned tbit = 1u << ti;
       float m = -INFINITY, l = 0.f;  // log2 units, lazily moved reference max
-      int mine = 0;                  // tiles of this item handled by this warpgroup so far
       bool ok = true;
-      for (int t = 0; t < nt; ++t) {
-        if ((t & 1) != w) {
-          if (++stage == C::kStages) stage = 0;
-          continue;
-        }
-        // valid keys of each segment of the tile for this row's token
+      for (int pp = 0; pp < np; ++pp) {
+        const int t = 2 * pp + w;
+        // valid keys of each segment of this warpgroup's tile for this row's token
         int nv[C::kSegs];
         int nvsum = 0;
 #pragma unroll
@@ -580,14 +570,14 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             x0 = ui < nu ? it.ux[ui] : 0;
           } else {
             ui = t / (BS / kTileKeys);
-            x0 = it.ux[ui] + (t % (BS / kTileKeys)) * kTileKeys;
+            x0 = ui < nu ? it.ux[ui] + (t % (BS / kTileKeys)) * kTileKeys : 0;
           }
           const bool sel = ui < nu && (it.ubits[ui] & tbit) != 0u;
           nv[e] = sel ? min(max(limit - x0 + 1, 0), C::kSegLen) : 0;
           nvsum += nv[e];
         }
         const bool any = __any_sync(0xffffffffu, nvsum > 0);
-        if (!warp_wait(&s_full[w], sph, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        if (!warp_wait(s_full, sph, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
         sph ^= 1;
         float x[kTileKeys];
         if (any) {
@@ -597,7 +587,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&s_empty[w]);
+        if (lane == 0) mbar_arrive(s_empty);
         float m_new = m, alpha = 1.f, psum = 0.f;
         if (any) {
           // masked raw scores; maximum with four independent chains
@@ -646,17 +636,16 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
           pk[j] = *reinterpret_cast<uint32_t*>(&h2);
         }
-        if (++stage == C::kStages) stage = 0;
         // this warpgroup's previous PV must be done before its P is replaced and its O
         // rescaled
-        if (mine > 0) {
+        if (pp > 0) {
           if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) { ok = false; break; }
           pvph ^= 1;
           tc_fence_after();
         }
         // P row (bf16 pairs, key order) into this warpgroup's TMEM P columns
         tmem_st_32x32b_x32_u(p_col, pk);
-        if (mine > 0) {
+        if (pp > 0) {
           // TMEM loads/stores are warp-collective (.sync.aligned): the whole warp rescales
           // together when any of its rows moved its reference max; other rows use 1.
           const bool my_rescale = m_new != m && m != -INFINITY;
@@ -673,13 +662,12 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           }
         }
         m = m_new;
-        ++mine;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&p_full[w]);
       }
       if (!ok) break;
-      if (mine > 0) {
+      if (np > 0) {
         if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) break;
         pvph ^= 1;
       }
@@ -696,12 +684,13 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const float L = l * a_me + oth.y * a_ot;
       const float a0 = w == 0 ? a_me : a_ot, a1 = w == 0 ? a_ot : a_me;
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      constexpr int kHalf = D / 2;
-      if (nt > 0) {
+      constexpr int kOutHalf = D / 2;
+      const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+      if (np > 0) {
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          const int col = w * kHalf + c * 32;
+        for (int c = 0; c < kOutHalf / 32; ++c) {
+          const int col = w * kOutHalf + c * 32;
           float o0[32], o1[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + col, o0);
           tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + D + col, o1);
@@ -711,14 +700,12 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               uint32_t wv[4];
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                // an accumulator that received no PV this item holds stale data: select
                 const int j0 = j + 2 * u;
-                const float v0 = ((a0 > 0.f) ? o0[j0] * a0 : 0.f) + ((a1 > 0.f) ? o1[j0] * a1 : 0.f);
-                const float v1 = ((a0 > 0.f) ? o0[j0 + 1] * a0 : 0.f) + ((a1 > 0.f) ? o1[j0 + 1] * a1 : 0.f);
+                const float v0 = o0[j0] * a0 + o1[j0] * a1;
+                const float v1 = o0[j0 + 1] * a0 + o1[j0 + 1] * a1;
                 __nv_bfloat162 h2 = __floats2bfloat162_rn(v0 * inv, v1 * inv);
                 wv[u] = *reinterpret_cast<uint32_t*>(&h2);
               }
-              const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
               *reinterpret_cast<uint4*>(out + orow * D + col + j) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
             }
           }
@@ -727,15 +714,11 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         __syncwarp();
         if (lane == 0) mbar_arrive(o_empty);
       } else if (row_ok) {
-        const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
 #pragma unroll
-        for (int j = 0; j < kHalf; j += 8)
-          *reinterpret_cast<uint4*>(out + orow * D + w * kHalf + j) = make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < kOutHalf; j += 8)
+          *reinterpret_cast<uint4*>(out + orow * D + w * kOutHalf + j) = make_uint4(0u, 0u, 0u, 0u);
       }
-      if (w == 0 && row_ok && p.lse != nullptr) {
-        const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
-        p.lse[orow] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
-      }
+      if (w == 0 && row_ok && p.lse != nullptr) p.lse[orow] = L > 0.f ? (mx + log2f(L)) * kLn2 : -INFINITY;
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
