@@ -65,6 +65,10 @@ SBA_API const char* sba_last_error(void);
  *
  *  q             [B, T, Hq, D]  dtype        (B == 1 when cu_seqlens != NULL)
  *  k, v          [B, T, Hkv, D] dtype
+ *  g_slc         [B, T, Hq] dtype, or NULL: gate of the selection branch (the
+ *                operation's g_slc argument); the output row of (b, t, hq) is
+ *                multiplied by g_slc[b, t, hq].  The LSE is not gated.  (The
+ *                compressed branch and its gate g_cmp are not part of this call.)
  *  block_indices [B, T, Hkv, S] int32: block ids relative to the start of the
  *                token's own sequence.  Entries < 0, >= ceil(L / block_size) (L = the
  *                sequence's length) or, when causal, after the token's own block are
@@ -77,10 +81,10 @@ SBA_API const char* sba_last_error(void);
  *  out           [B, T, Hq, D] dtype (written).
  *  lse           [B, T, Hq] float32 (written), or NULL.
  * Supported: D in {64, 128}; block_size in {32, 64, 128}; 1 <= Hq/Hkv <= 16;
- * 1 <= S <= 32; dtype bf16 (tensor cores, bf16 inputs, fp32 accumulation) or f32 with
- * D == 64 (tensor cores in tf32, fp32 accumulation).
+ * 1 <= S <= 32; dtype bf16 (tensor cores, bf16 inputs, fp32 accumulation, P rounded
+ * to bf16) or f32 (CUDA cores, exact fp32 products and sums).
  */
-SBA_API int sba_nsa_select_fwd(const void* q, const void* k, const void* v,
+SBA_API int sba_nsa_select_fwd(const void* q, const void* k, const void* v, const void* g_slc,
                        const int32_t* block_indices, const int32_t* block_counts,
                        int block_count_scalar, int S,
                        const int32_t* cu_seqlens, int num_seqs,

@@ -68,7 +68,7 @@ def _softmax_rows(scores, values):
 
 def nsa_select_attention(q, k, v, block_indices, block_counts, block_size, *,
                          cu_seqlens=None, causal=True, softmax_scale=None,
-                         rows=None):
+                         rows=None, g_slc=None):
     """Selection-branch attention output and LSE.
 
     Arguments (numpy, any float dtype; widened exactly to float64):
@@ -79,6 +79,10 @@ def nsa_select_attention(q, k, v, block_indices, block_counts, block_size, *,
       cu_seqlens    None, or int array [N + 1] (then B must be 1)
       rows          None (all tokens) or iterable of (b, t) pairs to compute;
                     rows not computed are left NaN.
+      g_slc         None, or the selection-branch gate [B, T, Hq]: the output of
+                    (b, t, hq) is scaled by g_slc[b, t, hq] (the operation's g_slc
+                    argument, read as a per-row gate of the selection output); the
+                    LSE is the attention's and is not gated.
 
     Returns ``(out [B, T, Hq, D] float64, lse [B, T, Hq] float64)``.
     """
@@ -125,4 +129,6 @@ def nsa_select_attention(q, k, v, block_indices, block_counts, block_size, *,
             o, l = _softmax_rows(scores, vv)
             out[b, t, heads] = o
             lse[b, t, heads] = l
+    if g_slc is not None:
+        out = out * np.asarray(g_slc, dtype=np.float64)[..., None]
     return out, lse

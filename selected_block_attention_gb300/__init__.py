@@ -65,7 +65,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     ci, cf, csz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.sba_version.restype = ctypes.c_char_p
     lib.sba_last_error.restype = ctypes.c_char_p
-    lib.sba_nsa_select_fwd.argtypes = [vp, vp, vp, i32p, i32p, ci, ci, i32p, ci, ci, ci, ci, ci,
+    lib.sba_nsa_select_fwd.argtypes = [vp, vp, vp, vp, i32p, i32p, ci, ci, i32p, ci, ci, ci, ci, ci,
                                        ci, ci, ci, cf, ci, vp, f32p, vp]
     lib.sba_nsa_select_fwd.restype = ci
     lib.sba_sparse_mask_bounds.argtypes = [i32p, i32p, i32p, i32p, ci, ci, ci, ci, ci, ci, ci, ci,
@@ -126,10 +126,12 @@ def _i32(t, name):
 
 
 def nsa_select_fwd(q, k, v, block_indices, block_counts, block_size, *, cu_seqlens=None,
-                   causal=True, softmax_scale=None, out=None, lse=None, return_lse=True):
-    """Selection-branch NSA forward.  q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16, or fp32 with
-    D=64), block_indices int32 [B,T,Hkv,S], block_counts int or int32 [B,T,Hkv],
-    cu_seqlens int32 [N+1] or None.  Returns (out, lse)."""
+                   causal=True, softmax_scale=None, g_slc=None, out=None, lse=None,
+                   return_lse=True):
+    """Selection-branch NSA forward.  q [B,T,Hq,D], k/v [B,T,Hkv,D] (bf16 or fp32),
+    block_indices int32 [B,T,Hkv,S], block_counts int or int32 [B,T,Hkv], cu_seqlens
+    int32 [N+1] or None, g_slc [B,T,Hq] (q's dtype) gate of the output rows or None.
+    Returns (out, lse)."""
     lib = load_library()
     B, T, Hq, D = q.shape
     Hkv = k.shape[2]
@@ -150,8 +152,12 @@ def nsa_select_fwd(q, k, v, block_indices, block_counts, block_size, *, cu_seqle
     if cu_seqlens is not None:
         _i32(cu_seqlens, "cu_seqlens")
         num_seqs = cu_seqlens.numel() - 1
+    if g_slc is not None:
+        if g_slc.dtype != q.dtype or tuple(g_slc.shape) != (B, T, Hq) or not g_slc.is_contiguous():
+            raise ValueError("g_slc must be a contiguous [B, T, Hq] tensor of q's dtype")
+        _dev(q, g_slc)
     _check(lib.sba_nsa_select_fwd(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(block_indices), _ptr(counts_t),
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_slc), _ptr(block_indices), _ptr(counts_t),
         int(block_counts) if counts_t is None else 0, S, _ptr(cu_seqlens), num_seqs,
         B, T, Hq, Hkv, D, int(block_size), int(bool(causal)),
         float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse), _stream(dev)))

@@ -75,7 +75,7 @@ const char* sba_version(void) { return "sba 0.1.0 sm_103a"; }
 
 const char* sba_last_error(void) { return g_last_error.c_str(); }
 
-int sba_nsa_select_fwd(const void* q, const void* k, const void* v,
+int sba_nsa_select_fwd(const void* q, const void* k, const void* v, const void* g_slc,
                        const int32_t* block_indices, const int32_t* block_counts,
                        int block_count_scalar, int S, const int32_t* cu_seqlens, int num_seqs,
                        int B, int T, int Hq, int Hkv, int D, int block_size, int causal,
@@ -101,7 +101,7 @@ int sba_nsa_select_fwd(const void* q, const void* k, const void* v,
   SBA_SUPPORT(S <= 32, "S must be <= 32");
   SBA_SUPPORT((long long)B * T * Hq < (1LL << 31), "B * T * Hq must be < 2^31");
   float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
-  return launch_nsa_select(q, k, v, block_indices, block_counts, block_count_scalar, S,
+  return launch_nsa_select(q, k, v, g_slc, block_indices, block_counts, block_count_scalar, S,
                            cu_seqlens, cu_seqlens ? num_seqs : 0, B, T, Hq, Hkv, D, block_size,
                            causal ? 1 : 0, scale, dtype, out, lse,
                            reinterpret_cast<cudaStream_t>(stream));

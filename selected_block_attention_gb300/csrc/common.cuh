@@ -33,7 +33,8 @@ unsigned read_and_clear_error_blocksparse(cudaStream_t s, std::string* where);
 unsigned read_and_clear_error_decode(cudaStream_t s, std::string* where);
 
 // Launch entry points implemented by the kernel files (arguments already validated).
-int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_indices,
+int launch_nsa_select(const void* q, const void* k, const void* v, const void* g_slc,
+                      const int32_t* block_indices,
                       const int32_t* block_counts, int block_count_scalar, int S,
                       const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
                       int D, int block_size, int causal, float scale, int dtype, void* out,

@@ -70,6 +70,7 @@ enum BarId : unsigned {
 };
 
 struct Params {
+  const void* g_slc;  // [B, T, Hq] gate of the output rows (query dtype), or NULL
   const int* block_indices;
   const int* block_counts;
   const int* cu_seqlens;
@@ -683,9 +684,11 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const float a_ot = oth.y > 0.f ? ex2(oth.x - mx) : 0.f;
       const float L = l * a_me + oth.y * a_ot;
       const float a0 = w == 0 ? a_me : a_ot, a1 = w == 0 ? a_ot : a_me;
-      const float inv = L > 0.f ? 1.f / L : 0.f;
       constexpr int kOutHalf = D / 2;
       const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+      const float gate =
+          (p.g_slc != nullptr && row_ok) ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.g_slc)[orow]) : 1.f;
+      const float inv = L > 0.f ? gate / L : 0.f;
       if (np > 0) {
         tc_fence_after();
 #pragma unroll
@@ -841,10 +844,14 @@ nsa_select_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
       m_s[tid] = m_run;
     }
     __syncthreads();
+    const float* gates = static_cast<const float*>(p.g_slc);
     if (tid < D) {
 #pragma unroll
       for (int h = 0; h < kNH; ++h)
-        if (h < p.G) out[(out_row0 + h) * D + tid] = a_s[h] > 0.f ? o[h] / a_s[h] : 0.f;
+        if (h < p.G) {
+          const float g = gates != nullptr ? gates[out_row0 + h] : 1.f;
+          out[(out_row0 + h) * D + tid] = a_s[h] > 0.f ? g * (o[h] / a_s[h]) : 0.f;
+        }
     }
     if (p.lse != nullptr && tid < p.G)
       p.lse[out_row0 + tid] = a_s[tid] > 0.f ? m_s[tid] + logf(a_s[tid]) : -INFINITY;
@@ -917,12 +924,14 @@ unsigned read_and_clear_error_nsa(cudaStream_t, std::string* where) {
   return w.flags;
 }
 
-int launch_nsa_select(const void* q, const void* k, const void* v, const int32_t* block_indices,
+int launch_nsa_select(const void* q, const void* k, const void* v, const void* g_slc,
+                      const int32_t* block_indices,
                       const int32_t* block_counts, int block_count_scalar, int S,
                       const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
                       int D, int block_size, int causal, float scale, int dtype, void* out,
                       float* lse, cudaStream_t stream) {
   Params p;
+  p.g_slc = g_slc;
   p.block_indices = block_indices;
   p.block_counts = block_counts;
   p.cu_seqlens = cu_seqlens;

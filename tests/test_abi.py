@@ -47,23 +47,23 @@ def test_argument_validation_without_launch(lib):
     c = ctypes
     fake = c.c_void_p(0x10000)  # never dereferenced: validation fails first
     # null pointers
-    r = lib.sba_nsa_select_fwd(None, None, None, None, None, 16, 16, None, 0, 1, 64, 4, 1, 128,
+    r = lib.sba_nsa_select_fwd(None, None, None, None, None, None, 16, 16, None, 0, 1, 64, 4, 1, 128,
                                64, 1, 0.0, 0, None, None, None)
     assert r == -1 and b"null" in lib.sba_last_error()
     # unsupported head dim
-    r = lib.sba_nsa_select_fwd(fake, fake, fake, fake, None, 16, 16, None, 0, 1, 64, 4, 1, 96,
+    r = lib.sba_nsa_select_fwd(fake, fake, fake, None, fake, None, 16, 16, None, 0, 1, 64, 4, 1, 96,
                                64, 1, 0.0, 0, fake, None, None)
     assert r == -2 and b"D must be" in lib.sba_last_error()
     # Hq not a multiple of Hkv
-    r = lib.sba_nsa_select_fwd(fake, fake, fake, fake, None, 16, 16, None, 0, 1, 64, 6, 4, 128,
+    r = lib.sba_nsa_select_fwd(fake, fake, fake, None, fake, None, 16, 16, None, 0, 1, 64, 6, 4, 128,
                                64, 1, 0.0, 0, fake, None, None)
     assert r == -1
     # misaligned pointer
-    r = lib.sba_nsa_select_fwd(c.c_void_p(0x10002), fake, fake, fake, None, 16, 16, None, 0, 1, 64,
+    r = lib.sba_nsa_select_fwd(c.c_void_p(0x10002), fake, fake, None, fake, None, 16, 16, None, 0, 1, 64,
                                4, 1, 128, 64, 1, 0.0, 0, fake, None, None)
     assert r == -1 and b"aligned" in lib.sba_last_error()
     # varlen with B > 1
-    r = lib.sba_nsa_select_fwd(fake, fake, fake, fake, None, 16, 16, fake, 3, 2, 64, 4, 1, 128,
+    r = lib.sba_nsa_select_fwd(fake, fake, fake, None, fake, None, 16, 16, fake, 3, 2, 64, 4, 1, 128,
                                64, 1, 0.0, 0, fake, None, None)
     assert r == -1
     # bounds: window below -1

@@ -179,3 +179,24 @@ def test_rejects_bad_arguments(sba):
         sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts, 48)
     with pytest.raises(ValueError):
         sba.nsa_select_fwd(w.q.cpu(), w.k, w.v, w.block_indices, w.block_counts, 64)
+
+
+@pytest.mark.parametrize("case", ["bf16", "f32"])
+def test_selection_gate(sba, case):
+    """g_slc scales each output row of the selection branch; the LSE is ungated."""
+    if case == "bf16":
+        w = workloads.nsa_prefill(device=DEV, B=2, T=300, Hq=32, Hkv=2, D=128, block_size=64,
+                                  S=6, max_count=6, seed=60)
+    else:
+        w = workloads.nsa_tiny(device=DEV)
+    # gates in (0, 1), as a sigmoid gate produces them (the absolute bound would
+    # otherwise scale with |gate|)
+    gate = torch.sigmoid(workloads.randn(tuple(w.q.shape[:3]), torch.float32, DEV, seed=61)).to(w.q.dtype)
+    out, lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts, w.block_size,
+                                  causal=w.causal, g_slc=gate)
+    sba.check_error()
+    counts = w.block_counts if isinstance(w.block_counts, int) else w.block_counts.cpu().numpy()
+    ref, ref_lse = oracle.nsa_select_attention(
+        to_np(w.q), to_np(w.k), to_np(w.v), w.block_indices.cpu().numpy(), counts, w.block_size,
+        causal=w.causal, g_slc=to_np(gate))
+    assert_attention_close(to_np(out), ref, to_np(lse), ref_lse, what=f"gate {case}")

@@ -211,3 +211,26 @@ def test_gqa_equals_repeated_heads():
     b, lb = nsa_select_attention(q, _expand_kv(k, G), _expand_kv(v, G), np.repeat(idx, G, axis=2), S, bs)
     np.testing.assert_allclose(a, b, rtol=1e-13, atol=1e-14)
     np.testing.assert_allclose(la, lb, rtol=1e-13, atol=1e-14)
+
+
+def test_selection_gate_scales_rows_and_leaves_lse():
+    """g_slc gates each (token, query head) output row of the selection branch; rows
+    with no admissible key stay 0 and the LSE is the ungated attention's."""
+    rng = np.random.default_rng(12)
+    B, T, Hq, Hkv, D, bs = 1, 40, 4, 2, 8, 8
+    q = rng.standard_normal((B, T, Hq, D))
+    k = rng.standard_normal((B, T, Hkv, D))
+    v = rng.standard_normal((B, T, Hkv, D))
+    idx = rng.integers(-1, 5, size=(B, T, Hkv, 3))
+    gate = rng.uniform(-2.0, 2.0, size=(B, T, Hq))
+    gate[0, 5, 1] = 0.0
+    o, l = nsa_select_attention(q, k, v, idx, 3, bs)
+    og, lg = nsa_select_attention(q, k, v, idx, 3, bs, g_slc=gate)
+    np.testing.assert_array_equal(lg, l)
+    assert np.all(og[0, 5, 1] == 0.0)
+    empty = np.isneginf(l)
+    assert np.all(og[empty] == 0.0)
+    # a gate of one is the ungated selection branch; any other gate scales its row
+    ones = nsa_select_attention(q, k, v, idx, 3, bs, g_slc=np.ones((B, T, Hq)))[0]
+    np.testing.assert_array_equal(ones, o)
+    np.testing.assert_allclose(og, o * gate[..., None], rtol=0, atol=1e-12)
