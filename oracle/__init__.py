@@ -17,6 +17,8 @@ source documentation pages named in its docstring:
 * ``ragged_decode_attention``  -- ejkernel.kernels._xla.ragged_decode_attention._xla_impl_fwd
   (API page), ``inner_decode_xla`` / ``create_attention_mask`` /
   ``apply_logits_soft_cap`` / ``apply_attention_sinks_block``.
+* ``ragged_flash_attention``   -- same page, ``ragged_flash_attention_xla`` (Q queries
+  per row, the last Q tokens of its range).
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 library routines (torch SDPA in float64), brute force on tiny inputs and the
@@ -27,6 +29,7 @@ from .nsa import nsa_select_attention, selected_key_set
 from .sparse_mask import sparse_mask_bounds
 from .blocksparse import blocksparse_attention
 from .ragged_decode import ragged_decode_attention
+from .ragged_attention import ragged_flash_attention
 
 __all__ = [
     "nsa_select_attention",
@@ -34,4 +37,5 @@ __all__ = [
     "sparse_mask_bounds",
     "blocksparse_attention",
     "ragged_decode_attention",
+    "ragged_flash_attention",
 ]
