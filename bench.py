@@ -10,11 +10,12 @@ The same JSON line carries ``roofline`` (dominant kernel vs the measured peak),
 ``cpu_baseline`` (the fp64 oracle on a bounded sample, host cores), ``e2e`` (same
 metric with host buffers, copies inside the timed region), ``clocks`` (nvidia-smi
 sampled during the timed region) and ``rows``: the other workloads of the path
-(varlen NSA, SparseMask bounds, block-sparse attention, ragged decode), each timed
-the same way.
+(varlen NSA, SparseMask bounds, block-sparse attention, ragged decode, ragged
+multi-query attention), each timed the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-  python bench.py --case {nsa_prefill,nsa_varlen,blocksparse,decode} [--repeat R]
+  python bench.py --case {nsa_prefill,nsa_varlen,blocksparse,decode,ragged_q4,ragged_chunk512}
+                  [--repeat R]
                   [--decode-batch B]      # profiling: launches only, no JSON line
 
 ``--impl reference`` times the fp64 CPU oracle on the same workload (bounded
@@ -266,6 +267,38 @@ def decode_work(w):
     return kv_bytes + w.q.numel() * 2 * 2 + B * Hq * 4, flops
 
 
+def ragged_attention_work(w):
+    """Algorithmic bytes and FLOPs of one multi-query call: per (row, query) the keys in
+    its window [p - left, p + right] inside [start, end) plus in-range sinks outside it;
+    HBM bytes = K/V of the union of a row's query windows (read once) + Q + O + LSE."""
+    ends = w.sequence_end.cpu().numpy().astype(np.int64)
+    starts = np.maximum(w.sequence_start.cpu().numpy().astype(np.int64), 0)
+    B, Q, Hq, D = w.q.shape
+    Hkv = w.k.shape[2]
+    ns = 0 if w.sink_bias is None else w.sink_bias.shape[-1]
+    wl, wr = w.window_left, w.window_right
+    pair_keys, union_keys = 0, 0
+
+    def window(lo_pos, hi_pos, s, e):
+        lo = np.maximum(s, lo_pos - wl) if wl >= 0 else s
+        hi = np.minimum(e, hi_pos + wr + 1) if wr >= 0 else e
+        hi = np.maximum(hi, lo)
+        sinks_out = max(0, min(ns, e, lo) - s) + max(0, min(ns, e) - max(hi, s))
+        return hi - lo, sinks_out
+
+    for s, e in zip(starts, ends):
+        if e <= s:
+            continue
+        for i in range(Q):
+            n, extra = window(e - Q + i, e - Q + i, s, e)
+            pair_keys += int(n) + extra
+        n, extra = window(e - Q, e - 1, s, e)
+        union_keys += int(n) + extra
+    kv_bytes = float(union_keys) * Hkv * D * 2 * 2
+    flops = 4.0 * D * Hq * pair_keys
+    return kv_bytes + 2 * w.q.numel() * 2 + B * Q * Hq * 4, flops
+
+
 def blocksparse_flops(w):
     m = w.mask
     pos = m.q_positions.cpu().numpy().astype(np.int64)
@@ -474,6 +507,34 @@ def measure_rows(sba, dev, stream, flush, peaks, args):
         "kernels_per_call": 2}
     del w
     torch.cuda.empty_cache()
+
+    # ragged multi-query attention: multi-token decode (4 tokens per row) and a chunked
+    # prefill (512-token chunks, causal over the whole prefix)
+    for key, w in (("ragged_attention_q4", workloads.ragged_attention(device=dev)),
+                   ("ragged_attention_chunk512",
+                    workloads.ragged_attention(device=dev, B=4, Q=512, S=16384, window=(-1, 0),
+                                               cap=0.0, num_sinks=0, seed=514))):
+        nbytes, mfl = ragged_attention_work(w)
+        B, Q, Hq, D = w.q.shape
+        ws = torch.empty(sba.ragged_flash_attention_workspace_size(
+            B, Q, Hq, w.k.shape[1], D, w.window_left, w.window_right), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(w.q)
+        t = timed_steps(lambda: sba.ragged_flash_attention_fwd(
+            w.q, w.k, w.v, w.sequence_start, w.sequence_end, window_left=w.window_left,
+            window_right=w.window_right, logits_soft_cap=w.logits_soft_cap, sink_bias=w.sink_bias,
+            out=out, workspace=ws), steps, warm, flush, stream)
+        ms = sum(t) / len(t)
+        log(f"{key} {ms * 1e3:.2f} us")
+        rows[key] = {
+            "workload": w.name, "us": round(ms * 1e3, 2),
+            "tok/s": round(B * Q / (ms * 1e-3), 1),
+            "GB/s": round(nbytes / ms / 1e6, 1),
+            "frac_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
+            "TFLOP/s": round(mfl / ms / 1e9, 2),
+            "frac_tensor": round(mfl / ms / 1e9 / peaks["bf16_tflops"], 4),
+            "kernels_per_call": 2}
+        del w, ws, out
+        torch.cuda.empty_cache()
     sba.check_error(dev)
     return rows
 
@@ -481,7 +542,8 @@ def measure_rows(sba, dev, stream, flush, peaks, args):
 def run_case(args):
     """Launch one workload's kernels ``--repeat`` times (no timing JSON): the command the
     profiles are taken with.  Cases: nsa_prefill, nsa_varlen, blocksparse (bounds then
-    attention), decode (``--decode-batch`` rows of the decode workload)."""
+    attention), decode (``--decode-batch`` rows of the decode workload), ragged_q4 and
+    ragged_chunk512 (the two multi-query workloads)."""
     import selected_block_attention_gb300 as sba
     from selected_block_attention_gb300 import _build
 
@@ -511,6 +573,15 @@ def run_case(args):
             sba.ragged_decode_fwd(w.q, w.k, w.v, w.sequence_start, w.sequence_end,
                                   window_left=w.window_left, window_right=w.window_right,
                                   logits_soft_cap=w.logits_soft_cap, sink_bias=w.sink_bias)
+    elif args.case in ("ragged_q4", "ragged_chunk512"):
+        w = (workloads.ragged_attention(device=dev) if args.case == "ragged_q4" else
+             workloads.ragged_attention(device=dev, B=4, Q=512, S=16384, window=(-1, 0), cap=0.0,
+                                        num_sinks=0, seed=514))
+
+        def fn():
+            sba.ragged_flash_attention_fwd(w.q, w.k, w.v, w.sequence_start, w.sequence_end,
+                                           window_left=w.window_left, window_right=w.window_right,
+                                           logits_soft_cap=w.logits_soft_cap, sink_bias=w.sink_bias)
     else:
         raise SystemExit(f"unknown case {args.case}")
     for i in range(args.repeat):

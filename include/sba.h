@@ -216,6 +216,55 @@ SBA_API int sba_ragged_decode_fwd_noalloc(const void* q, const void* k, const vo
                                           sba_stream_t stream);
 
 /*
+ * sba_ragged_flash_attention_workspace_size -- bytes of device workspace that
+ * sba_ragged_flash_attention_fwd needs for these sizes (fp32 split partials).  A window
+ * bound < 0 means unbounded on that side.  Returns 0 for invalid sizes.
+ */
+SBA_API size_t sba_ragged_flash_attention_workspace_size(int B, int Q, int Hq, int S, int D,
+                                                         int window_left, int window_right);
+
+/*
+ * sba_ragged_flash_attention_fwd -- ragged multi-query attention: Q query tokens per
+ * batch row against that row's slice of a KV cache.
+ *
+ * Defined by: "ejkernel.kernels._xla.ragged_decode_attention._xla_impl_fwd" (API
+ * page): ragged_flash_attention_xla (queries [B, Q, H, D], per-row key range
+ * [sequence_start, sequence_end), sliding window, logits soft cap, softmax_aux sink
+ * biases) with create_attention_mask (one mask for all heads; sinks are always
+ * attendable).  Readings of what the page leaves open: query i of a row sits at
+ * position p_i = end - Q + i (the row's last Q tokens; Q = 1 is sba_ragged_decode_fwd);
+ * there is no causal switch, so key k is attendable by query i iff start <= k < end and
+ * either p_i - window_left <= k <= p_i + window_right (a bound < 0 is unbounded) or
+ * k < num_sinks.  Logit = scale * <q, k>, then cap * tanh(logit / cap) when cap > 0,
+ * then + sink_bias for sink keys.  A query with no attendable key gets output 0 and
+ * LSE -inf.
+ *
+ *  q          [B, Q, Hq, D] bf16
+ *  k, v       [B, S, Hkv, D] bf16 (the KV cache; Hq % Hkv == 0, query head hq reads
+ *             KV head hq / (Hq / Hkv); the page's case is Hkv == Hq)
+ *  seq_start, seq_end  [B] int32 (clamped to [0, S])
+ *  sink_bias  float32 [Hq, num_sinks] (sink_bias_per_head != 0) or [num_sinks];
+ *             NULL with num_sinks == 0 for none.  num_sinks <= 16.
+ *  out        [B, Q, Hq, D] bf16 (written); lse [B, Q, Hq] float32 (written) or NULL
+ *  workspace  device scratch of at least
+ *             sba_ragged_flash_attention_workspace_size(B, Q, Hq, S, D, window_left,
+ *             window_right) bytes, 16-byte aligned, caller-owned; needs no initialisation.
+ * All pointers are caller-owned device memory.  Returns SBA_ERR_INVALID_ARG for null or
+ * misaligned pointers, bad sizes or a short workspace, SBA_ERR_UNSUPPORTED outside:
+ * D == 128, num_sinks <= 16, B * ceil(Q * Hq / Hkv / 16) <= 65535, Q <= 65535.
+ * Internally: split-KV partial kernel + combine kernel on `stream`.
+ */
+SBA_API int sba_ragged_flash_attention_fwd(const void* q, const void* k, const void* v,
+                                           const int32_t* seq_start, const int32_t* seq_end,
+                                           int B, int Q, int Hq, int Hkv, int S, int D,
+                                           float softmax_scale, int window_left,
+                                           int window_right, float logits_soft_cap,
+                                           const float* sink_bias, int num_sinks,
+                                           int sink_bias_per_head, void* out, float* lse,
+                                           void* workspace, size_t workspace_bytes,
+                                           sba_stream_t stream);
+
+/*
  * sba_check_error -- synchronise `stream`, then read and clear the device-side error
  * word of every kernel of this library.  Returns SBA_OK, SBA_ERR_TIMEOUT (a kernel
  * gave up on a bounded internal wait and returned early), SBA_ERR_DEVICE_INPUT (a

@@ -9,7 +9,8 @@ raises.
 
 Entry points (same names as the C ABI without the ``sba_`` prefix):
   nsa_select_fwd, sparse_mask_bounds, blocksparse_attn_fwd, ragged_decode_fwd,
-  ragged_decode_fwd_noalloc, ragged_decode_workspace_size, check_error.
+  ragged_decode_fwd_noalloc, ragged_decode_workspace_size, ragged_flash_attention_fwd,
+  ragged_flash_attention_workspace_size, check_error.
 """
 
 from __future__ import annotations
@@ -24,14 +25,15 @@ from . import _build
 __all__ = [
     "SBAError", "load_library", "library_path", "nsa_select_fwd", "sparse_mask_bounds",
     "blocksparse_attn_fwd", "ragged_decode_fwd", "ragged_decode_fwd_noalloc",
-    "ragged_decode_workspace_size",
-    "check_error", "EXPORTED_SYMBOLS",
+    "ragged_decode_workspace_size", "ragged_flash_attention_fwd",
+    "ragged_flash_attention_workspace_size", "check_error", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "sba_version", "sba_last_error", "sba_nsa_select_fwd", "sba_sparse_mask_bounds",
     "sba_blocksparse_attn_fwd", "sba_ragged_decode_workspace_size", "sba_ragged_decode_fwd",
-    "sba_ragged_decode_fwd_noalloc", "sba_check_error",
+    "sba_ragged_decode_fwd_noalloc", "sba_ragged_flash_attention_workspace_size",
+    "sba_ragged_flash_attention_fwd", "sba_check_error",
 )
 
 SBA_BF16, SBA_F32 = 0, 1
@@ -83,6 +85,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sba_ragged_decode_fwd_noalloc.argtypes = [vp, vp, vp, i32p, i32p, ci, ci, ci, ci, ci, cf,
                                                   ci, ci, cf, f32p, ci, ci, vp, f32p, vp]
     lib.sba_ragged_decode_fwd_noalloc.restype = ci
+    lib.sba_ragged_flash_attention_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci, ci]
+    lib.sba_ragged_flash_attention_workspace_size.restype = csz
+    lib.sba_ragged_flash_attention_fwd.argtypes = [vp, vp, vp, i32p, i32p, ci, ci, ci, ci, ci, ci,
+                                                   cf, ci, ci, cf, f32p, ci, ci, vp, f32p, vp,
+                                                   csz, vp]
+    lib.sba_ragged_flash_attention_fwd.restype = ci
     lib.sba_check_error.argtypes = [vp]
     lib.sba_check_error.restype = ci
     if path == _build.LIB_PATH:
@@ -276,6 +284,46 @@ def ragged_decode_fwd_noalloc(q, k, v, sequence_start, sequence_end, *, softmax_
         float(softmax_scale or 0.0), int(window_left), int(window_right),
         float(logits_soft_cap or 0.0), _ptr(sink_bias), num_sinks, per_head, _ptr(out), _ptr(lse),
         _stream(dev)))
+    return out, lse
+
+
+def ragged_flash_attention_workspace_size(B, Q, Hq, S, D, window_left=-1, window_right=-1) -> int:
+    return int(load_library().sba_ragged_flash_attention_workspace_size(
+        B, Q, Hq, S, D, window_left, window_right))
+
+
+def ragged_flash_attention_fwd(q, k, v, sequence_start, sequence_end, *, softmax_scale=None,
+                               window_left=-1, window_right=-1, logits_soft_cap=None,
+                               sink_bias=None, out=None, lse=None, workspace=None,
+                               return_lse=True):
+    """Ragged multi-query attention (bf16).  q [B,Q,Hq,D], k/v [B,S,Hkv,D],
+    sequence_start / sequence_end int32 [B] (query i of a row sits at end - Q + i),
+    sink_bias fp32 [Hq, num_sinks] or [num_sinks].  Returns (out [B,Q,Hq,D],
+    lse [B,Q,Hq])."""
+    lib = load_library()
+    _i32(sequence_start, "sequence_start")
+    _i32(sequence_end, "sequence_end")
+    dev = _dev(q, k, v, sequence_start, sequence_end, sink_bias, workspace, out, lse)
+    B, Q, Hq, D = q.shape
+    S, Hkv = k.shape[1], k.shape[2]
+    num_sinks, per_head = 0, 0
+    if sink_bias is not None:
+        if sink_bias.dtype != torch.float32:
+            raise TypeError("sink_bias must be float32")
+        num_sinks = sink_bias.shape[-1]
+        per_head = int(sink_bias.dim() == 2)
+    need = ragged_flash_attention_workspace_size(B, Q, Hq, S, D, window_left, window_right)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=dev)
+    _check(lib.sba_ragged_flash_attention_fwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(sequence_start), _ptr(sequence_end), B, Q, Hq, Hkv, S, D,
+        float(softmax_scale or 0.0), int(window_left), int(window_right),
+        float(logits_soft_cap or 0.0), _ptr(sink_bias), num_sinks, per_head, _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
     return out, lse
 
 

@@ -190,6 +190,44 @@ int sba_ragged_decode_fwd(const void* q, const void* k, const void* v, const int
                               reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t sba_ragged_flash_attention_workspace_size(int B, int Q, int Hq, int S, int D,
+                                                 int window_left, int window_right) {
+  if (B < 1 || Q < 1 || Hq < 1 || S < 1 || D < 1) return 0;
+  return ragged_mq_workspace_bytes(B, Q, Hq, S, window_left, window_right);
+}
+
+int sba_ragged_flash_attention_fwd(const void* q, const void* k, const void* v,
+                                   const int32_t* seq_start, const int32_t* seq_end, int B, int Q,
+                                   int Hq, int Hkv, int S, int D, float softmax_scale,
+                                   int window_left, int window_right, float logits_soft_cap,
+                                   const float* sink_bias, int num_sinks, int sink_bias_per_head,
+                                   void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                   sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q && k && v && seq_start && seq_end && out, "null pointer");
+  SBA_REQUIRE(B >= 1 && Q >= 1 && Hq >= 1 && Hkv >= 1 && S >= 1 && Hq % Hkv == 0, "bad sizes");
+  SBA_REQUIRE(window_left >= -1 && window_right >= -1, "windows must be >= -1");
+  SBA_REQUIRE(num_sinks >= 0 && (num_sinks == 0 || sink_bias != nullptr),
+              "num_sinks > 0 needs sink_bias");
+  SBA_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out),
+              "q, k, v and out must be 16-byte aligned");
+  SBA_REQUIRE(std::isfinite(softmax_scale) && std::isfinite(logits_soft_cap),
+              "scale and cap must be finite");
+  SBA_SUPPORT(D == 128, "D must be 128");
+  SBA_SUPPORT(num_sinks <= 16, "num_sinks must be <= 16");
+  SBA_SUPPORT((long long)B * Q * Hq < (1LL << 31) && (long long)B * S * Hkv < (1LL << 31),
+              "B * Q * Hq and B * S * Hkv must be < 2^31");
+  const size_t need = ragged_mq_workspace_bytes(B, Q, Hq, S, window_left, window_right);
+  SBA_REQUIRE(workspace != nullptr && aligned16(workspace) && workspace_bytes >= need,
+              "workspace missing, misaligned or smaller than "
+              "sba_ragged_flash_attention_workspace_size()");
+  float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_ragged_mq(q, k, v, seq_start, seq_end, B, Q, Hq, Hkv, S, scale, window_left,
+                          window_right, logits_soft_cap, sink_bias, num_sinks,
+                          sink_bias_per_head ? 1 : 0, out, lse, workspace,
+                          reinterpret_cast<cudaStream_t>(stream));
+}
+
 int sba_check_error(sba_stream_t stream) {
   g_last_error.clear();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

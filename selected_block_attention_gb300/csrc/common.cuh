@@ -58,6 +58,13 @@ int launch_ragged_decode(const void* q, const void* k, const void* v, const int3
                          const float* sink_bias, int num_sinks, int sink_per_head, void* out,
                          float* lse, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream);
+size_t ragged_mq_workspace_bytes(int B, int Qn, int Hq, int S, int window_left,
+                                 int window_right);
+int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                     const int32_t* seq_end, int B, int Qn, int Hq, int Hkv, int S, float scale,
+                     int window_left, int window_right, float cap, const float* sink_bias,
+                     int num_sinks, int sink_per_head, void* out, float* lse, void* workspace,
+                     cudaStream_t stream);
 
 // Driver entry point for tensor-map encoding, resolved once through the runtime.
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,

@@ -20,8 +20,13 @@
 // split 0 additionally folds in the sink tokens left of the window.  The combine
 // kernel merges the partials of a row with max / exp weights and writes the bf16
 // output and the natural-log LSE.
+//
+// The same file holds the multi-query form of the page's ragged_flash_attention_xla
+// (Q queries per row, query i at position end - Q + i), built on the same split /
+// combine scheme with (query, head) pairs as the MMA rows.
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <cmath>
 #include <mutex>
 #include <string>
@@ -106,17 +111,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Issue the cp.async copies of one 16-key K/V tile of KV head h (keys clamped into
 // the cache so no copy leaves the tensor; clamped rows are masked later).
-__device__ __forceinline__ void load_tile(const DecodeParams& p, int b, int h, int key0,
-                                          uint32_t k_dst, uint32_t v_dst, int lane) {
+__device__ __forceinline__ void load_tile(const __nv_bfloat16* k, const __nv_bfloat16* v, int S,
+                                          int Hkv, int b, int h, int key0, uint32_t k_dst,
+                                          uint32_t v_dst, int lane) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int u = lane + 32 * i;  // 256 chunks of 16 bytes per tensor
     const int key = u >> 4, part = u & 15;
-    const int kk = min(max(key0 + key, 0), p.S - 1);
-    const long long row = ((long long)b * p.S + kk) * p.Hkv + h;
+    const int kk = min(max(key0 + key, 0), S - 1);
+    const long long row = ((long long)b * S + kk) * Hkv + h;
     const uint32_t off = key * kRowBytes + part * 16;
-    cp_async16(k_dst + off, p.k + row * kD + part * 8);
-    cp_async16(v_dst + off, p.v + row * kD + part * 8);
+    cp_async16(k_dst + off, k + row * kD + part * 8);
+    cp_async16(v_dst + off, v + row * kD + part * 8);
   }
 }
 
@@ -183,7 +189,7 @@ decode_split_kernel(const DecodeParams p) {
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) {
     const int t = first_tile + i;
-    if (t <= last_tile) load_tile(p, b, h, tile_key0(t), k_stage(i), v_stage(i), lane);
+    if (t <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(t), k_stage(i), v_stage(i), lane);
     cp_async_commit();
   }
   int stage = 0;
@@ -191,7 +197,7 @@ decode_split_kernel(const DecodeParams p) {
     {  // prefetch tile t + kStages - 1
       const int tn = t + kStages - 1;
       const int sn = (stage + kStages - 1) % kStages;
-      if (tn <= last_tile) load_tile(p, b, h, tile_key0(tn), k_stage(sn), v_stage(sn), lane);
+      if (tn <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(tn), k_stage(sn), v_stage(sn), lane);
       cp_async_commit();
     }
     cp_async_wait<kStages - 1>();
@@ -381,6 +387,346 @@ decode_combine_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ out,
   if (lse != nullptr && d == 0) lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
 }
 
+
+// ---------------------------------------------------------------------------------------
+// Ragged multi-query attention ("ragged_flash_attention_xla" on the same page): Q queries
+// per batch row, query i at position end - Q + i, each with its own window.
+//
+// The rows of one KV head h are the Q * G (query, head) pairs, query-major; a row tile
+// is 16 consecutive rows, i.e. the G heads of up to 16 / G + 1 consecutive queries.  A
+// CTA (split s, KV head h, row tile rt of row b) walks kKeysPerCta keys of the union of
+// its rows' windows, [lo, hi); every element is then masked with its own row's window.
+// Sink keys outside [lo, hi) (left of it, or right of it when the tile's queries sit
+// before the sinks' end) go through the extra sink tile of split 0, sink keys inside
+// [lo, hi) through the per-row test (sinks are attendable from every query).
+struct MqParams {
+  const __nv_bfloat16* q;  // [B, Q, Hq, D]
+  const __nv_bfloat16* k;  // [B, S, Hkv, D]
+  const __nv_bfloat16* v;
+  const int* seq_start;
+  const int* seq_end;
+  const float* sink_bias;
+  float* o_part;   // [B][max_splits][Q][Hq][D]
+  float* ml_part;  // [B][max_splits][Q][Hq][2]
+  int B, Qn, Hq, Hkv, S, G, max_splits, row_tiles;
+  float scale, cap;
+  int window_left, window_right, num_sinks, sink_per_head;
+};
+
+struct MqRange {
+  int start, end;  // the row's clamped range [start, end)
+  int lo, hi;      // union of the tile's windows inside it
+  int sink_end;    // sink keys are [start, sink_end)
+  bool sink_tile;  // some sink key lies outside [lo, hi)
+  int n_split;
+};
+
+// Key range of row tile rt of batch row b.  Shared by the split and the combine kernel so
+// that both agree on the number of splits.
+__device__ __forceinline__ MqRange mq_tile_range(const MqParams& p, int b, int rt) {
+  MqRange R;
+  R.start = max(p.seq_start[b], 0);
+  R.end = min(p.seq_end[b], p.S);
+  R.n_split = 0;
+  R.sink_tile = false;
+  if (R.end <= R.start) {
+    R.start = R.lo = R.hi = R.sink_end = R.end;
+    return R;
+  }
+  const int nrows = p.Qn * p.G;
+  const int r0 = rt * 16, r1 = min(r0 + 15, nrows - 1);
+  const long long p_lo = (long long)R.end - p.Qn + r0 / p.G;
+  const long long p_hi = (long long)R.end - p.Qn + r1 / p.G;
+  long long lo = R.start, hi = R.end;
+  if (p.window_left >= 0) lo = max(lo, p_lo - p.window_left);
+  if (p.window_right >= 0) hi = min(hi, p_hi + p.window_right + 1);
+  if (hi <= lo) lo = hi = R.end;  // no window key: only sinks can remain
+  R.lo = static_cast<int>(lo);
+  R.hi = static_cast<int>(hi);
+  R.sink_end = min(p.num_sinks, R.end);
+  R.sink_tile = min(R.sink_end, R.lo) > R.start || R.sink_end > max(R.hi, R.start);
+  int n = (R.hi - R.lo + kKeysPerCta - 1) / kKeysPerCta;
+  if (n == 0 && R.sink_tile) n = 1;
+  R.n_split = min(n, p.max_splits);  // the host's bound already covers n; never read past it
+  return R;
+}
+
+// kHiRows: Q * G > 8, so the rows g + 8 of the m16n8k16 tiles are used.
+template <bool kHiRows>
+__global__ void __launch_bounds__(kWarps * 32)
+ragged_mq_split_kernel(const MqParams p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int s = blockIdx.x, h = blockIdx.y;
+  const int b = blockIdx.z / p.row_tiles, rt = blockIdx.z % p.row_tiles;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+
+  const MqRange R = mq_tile_range(p, b, rt);
+  if (s >= R.n_split) return;  // the combine kernel writes 0 / -inf for empty rows
+  const bool do_sinks = (s == 0) && (warp == 0) && R.sink_tile;
+  const int key_lo = R.lo + s * kKeysPerCta + warp * kKeysPerWarp;
+  const int key_hi = min(key_lo + kKeysPerWarp, R.hi);
+  const int n_tiles = key_hi > key_lo ? (key_hi - key_lo + kTileKeys - 1) / kTileKeys : 0;
+  const int first_tile = do_sinks ? -1 : 0;  // tile -1 = sink tile at keys [0, 16)
+
+  // This thread's two rows (g and g + 8 of the tile): query, head, window.
+  const int nrows = p.Qn * p.G;
+  const int rr0 = rt * 16 + g, rr1 = rr0 + 8;
+  const bool ok0 = rr0 < nrows, ok1 = kHiRows && rr1 < nrows;
+  const int i0 = ok0 ? rr0 / p.G : 0, i1 = ok1 ? rr1 / p.G : 0;
+  const int hq0 = h * p.G + (ok0 ? rr0 % p.G : 0), hq1 = h * p.G + (ok1 ? rr1 % p.G : 0);
+  auto win_lo = [&](int i) -> int {  // smallest window key of query i (keys are >= 0)
+    if (p.window_left < 0) return -1;
+    return static_cast<int>(max((long long)R.end - p.Qn + i - p.window_left, -1LL));
+  };
+  auto win_hi = [&](int i) -> int {  // largest window key of query i
+    if (p.window_right < 0) return INT_MAX;
+    return static_cast<int>(min((long long)R.end - p.Qn + i + p.window_right, (long long)INT_MAX));
+  };
+  const int wlo0 = win_lo(i0), whi0 = ok0 ? win_hi(i0) : -1;
+  const int wlo1 = win_lo(i1), whi1 = ok1 ? win_hi(i1) : -1;
+
+  // Query fragments (A operand): row r of the tile is (query, head) pair rt * 16 + r.
+  uint32_t qa[8][4];
+  {
+    auto row_ptr = [&](int r) -> const __nv_bfloat16* {
+      const int rr = rt * 16 + r;
+      if (rr >= nrows) return nullptr;
+      const int qi = rr / p.G, hq = h * p.G + rr % p.G;
+      return p.q + ((long long)(b * p.Qn + qi) * p.Hq + hq) * kD;
+    };
+    const __nv_bfloat16* qr0 = row_ptr(g);
+    const __nv_bfloat16* qr1 = kHiRows ? row_ptr(g + 8) : nullptr;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int d0 = ks * 16 + 2 * c;
+      auto ld = [&](const __nv_bfloat16* r, int d) -> uint32_t {
+        return r != nullptr ? *reinterpret_cast<const uint32_t*>(r + d) : 0u;
+      };
+      qa[ks][0] = ld(qr0, d0);
+      qa[ks][1] = ld(qr1, d0);
+      qa[ks][2] = ld(qr0, d0 + 8);
+      qa[ks][3] = ld(qr1, d0 + 8);
+    }
+  }
+  const float* bias_row0 = nullptr;
+  const float* bias_row1 = nullptr;
+  if (p.num_sinks > 0) {
+    bias_row0 = p.sink_bias + (p.sink_per_head ? (long long)hq0 * p.num_sinks : 0);
+    bias_row1 = p.sink_bias + (p.sink_per_head ? (long long)hq1 * p.num_sinks : 0);
+  }
+
+  const uint32_t wbase = ptx::smem_u32(smem) + warp * kWarpSmem;
+  auto k_stage = [&](int st) { return wbase + st * 2 * kTileBytes; };
+  auto v_stage = [&](int st) { return wbase + st * 2 * kTileBytes + kTileBytes; };
+  auto tile_key0 = [&](int t) { return t < 0 ? 0 : key_lo + t * kTileKeys; };
+
+  float o[16][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  const int last_tile = n_tiles - 1;
+#pragma unroll
+  for (int i = 0; i < kStages - 1; ++i) {
+    const int t = first_tile + i;
+    if (t <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(t), k_stage(i), v_stage(i), lane);
+    cp_async_commit();
+  }
+  int stage = 0;
+  const float two_log2e_over_cap = p.cap > 0.f ? 2.f * kLog2e / p.cap : 0.f;
+  for (int t = first_tile; t <= last_tile; ++t) {
+    {
+      const int tn = t + kStages - 1;
+      const int sn = (stage + kStages - 1) % kStages;
+      if (tn <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(tn), k_stage(sn), v_stage(sn), lane);
+      cp_async_commit();
+    }
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const uint32_t ks_base = k_stage(stage), vs_base = v_stage(stage);
+    const int key0 = tile_key0(t);
+
+    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const uint32_t row_addr = ks_base + ((mi >> 1) * 8 + ri) * kRowBytes + (mi & 1) * 16;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(row_addr + kk * 32, b00, b01, b10, b11);
+        mma_bf16(sc[0], qa[kk], b00, b01);
+        mma_bf16(sc[1], qa[kk], b10, b11);
+      }
+    }
+    float tmax0 = -INFINITY, tmax1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = key0 + nt * 8 + 2 * c + e;
+        const bool sink = key < p.num_sinks;
+        bool in0, in1;
+        if (t < 0) {  // sink tile: in-range sink keys outside the union window, every row
+          const bool outside = key >= R.start && key < R.sink_end && (key < R.lo || key >= R.hi);
+          in0 = ok0 && outside;
+          in1 = ok1 && outside;
+        } else {
+          const bool in_tile = key >= key_lo && key < key_hi;
+          in0 = ok0 && in_tile && ((key >= wlo0 && key <= whi0) || sink);
+          in1 = ok1 && in_tile && ((key >= wlo1 && key <= whi1) || sink);
+        }
+        float x0 = sc[nt][e] * p.scale;
+        if (p.cap > 0.f) x0 = soft_cap(x0, two_log2e_over_cap, p.cap);
+        if (sink) x0 += bias_row0[key];
+        sc[nt][e] = in0 ? x0 * kLog2e : -INFINITY;
+        tmax0 = fmaxf(tmax0, sc[nt][e]);
+        if constexpr (kHiRows) {
+          float x1 = sc[nt][2 + e] * p.scale;
+          if (p.cap > 0.f) x1 = soft_cap(x1, two_log2e_over_cap, p.cap);
+          if (sink) x1 += bias_row1[key];
+          sc[nt][2 + e] = in1 ? x1 * kLog2e : -INFINITY;
+          tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
+        } else {
+          sc[nt][2 + e] = -INFINITY;
+        }
+      }
+    }
+    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
+    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
+    if constexpr (kHiRows) {
+      tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
+      tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
+    }
+    const float mn0 = (tmax0 > m0 + kRescaleThreshold || (m0 == -INFINITY && tmax0 != -INFINITY)) ? tmax0 : m0;
+    const float mn1 = (tmax1 > m1 + kRescaleThreshold || (m1 == -INFINITY && tmax1 != -INFINITY)) ? tmax1 : m1;
+    const bool mv0 = mn0 != m0, mv1 = mn1 != m1;
+    const float alpha0 = (mv0 && m0 != -INFINITY) ? ptx::ex2(m0 - mn0) : 1.f;
+    const float alpha1 = (mv1 && m1 != -INFINITY) ? ptx::ex2(m1 - mn1) : 1.f;
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p0 = mn0 == -INFINITY ? 0.f : ptx::ex2(sc[nt][e] - mn0);
+        sc[nt][e] = p0;
+        ps0 += p0;
+        if constexpr (kHiRows) {
+          const float p1 = mn1 == -INFINITY ? 0.f : ptx::ex2(sc[nt][2 + e] - mn1);
+          sc[nt][2 + e] = p1;
+          ps1 += p1;
+        } else {
+          sc[nt][2 + e] = 0.f;
+        }
+      }
+    }
+    l0 = l0 * alpha0 + ps0;
+    l1 = l1 * alpha1 + ps1;
+    if (__any_sync(0xffffffffu, mv0 || mv1)) {
+#pragma unroll
+      for (int dn = 0; dn < 16; ++dn) {
+        o[dn][0] *= alpha0; o[dn][1] *= alpha0; o[dn][2] *= alpha1; o[dn][3] *= alpha1;
+      }
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+    pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+    pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+    pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+    {
+      const int mi = lane >> 3, ri = lane & 7;
+      const uint32_t row_addr = vs_base + ((mi & 1) * 8 + ri) * kRowBytes + (mi >> 1) * 16;
+#pragma unroll
+      for (int dn = 0; dn < 16; dn += 2) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4_t(row_addr + dn * 16, b00, b01, b10, b11);
+        mma_bf16(o[dn], pa, b00, b01);
+        mma_bf16(o[dn + 1], pa, b10, b11);
+      }
+    }
+    __syncwarp();
+    stage = (stage + 1) % kStages;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  m0 = m0 == -INFINITY ? m0 : m0 * kLn2;
+  m1 = m1 == -INFINITY ? m1 : m1 * kLn2;
+  float* s_o = reinterpret_cast<float*>(smem);  // [kWarps][16][kD]
+  float* s_ml = s_o + kWarps * 16 * kD;          // [kWarps][16][2]
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+#pragma unroll
+  for (int dn = 0; dn < 16; ++dn) {
+    const int d = dn * 8 + 2 * c;
+    s_o[(warp * 16 + g) * kD + d] = o[dn][0];
+    s_o[(warp * 16 + g) * kD + d + 1] = o[dn][1];
+    s_o[(warp * 16 + g + 8) * kD + d] = o[dn][2];
+    s_o[(warp * 16 + g + 8) * kD + d + 1] = o[dn][3];
+  }
+  if (c == 0) {
+    s_ml[(warp * 16 + g) * 2 + 0] = m0;
+    s_ml[(warp * 16 + g) * 2 + 1] = l0;
+    s_ml[(warp * 16 + g + 8) * 2 + 0] = m1;
+    s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
+  }
+  __syncthreads();
+  const int d = threadIdx.x;  // kD == blockDim.x
+  const int tile_rows = min(16, nrows - rt * 16);
+  for (int r = 0; r < tile_rows; ++r) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[(w * 16 + r) * 2]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float mw = s_ml[(w * 16 + r) * 2];
+        const float f = mw == -INFINITY ? 0.f : ptx::ex2((mw - M) * kLog2e);
+        L += f * s_ml[(w * 16 + r) * 2 + 1];
+        O += f * s_o[(w * 16 + r) * kD + d];
+      }
+    }
+    const int rr = rt * 16 + r;
+    const int qi = rr / p.G, hq = h * p.G + rr % p.G;
+    const long long slot = (((long long)b * p.max_splits + s) * p.Qn + qi) * p.Hq + hq;
+    p.o_part[slot * kD + d] = O;
+    if (d == 0) {
+      p.ml_part[slot * 2 + 0] = M;
+      p.ml_part[slot * 2 + 1] = L;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kD)
+ragged_mq_combine_kernel(const MqParams p, __nv_bfloat16* __restrict__ out,
+                         float* __restrict__ lse) {
+  const int hq = blockIdx.x, qi = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  const int rr = qi * p.G + hq % p.G;
+  const MqRange R = mq_tile_range(p, b, rr / 16);
+  const long long base = ((long long)b * p.max_splits * p.Qn + qi) * p.Hq + hq;
+  const long long split_stride = (long long)p.Qn * p.Hq;
+  float M = -INFINITY;
+  for (int s = 0; s < R.n_split; ++s) M = fmaxf(M, p.ml_part[(base + s * split_stride) * 2]);
+  float L = 0.f, O = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < R.n_split; ++s) {
+      const long long slot = base + s * split_stride;
+      const float ms = p.ml_part[slot * 2];
+      const float f = ms == -INFINITY ? 0.f : ptx::ex2((ms - M) * kLog2e);
+      L += f * p.ml_part[slot * 2 + 1];
+      O += f * p.o_part[slot * kD + d];
+    }
+  }
+  const long long orow = ((long long)b * p.Qn + qi) * p.Hq + hq;
+  out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+  if (lse != nullptr && d == 0) lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
+}
+
 }  // namespace
 
 unsigned read_and_clear_error_decode(cudaStream_t, std::string*) {
@@ -447,6 +793,74 @@ int launch_ragged_decode(const void* q, const void* k, const void* v, const int3
   decode_combine_kernel<<<dim3(Hq, B), kD, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out), lse);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "ragged_decode combine launch");
+  return SBA_OK;
+}
+
+
+static int mq_max_splits(int Qn, int S, int window_left, int window_right) {
+  // Longest union window of a 16-row tile: its rows span at most 16 consecutive queries.
+  long long win = S;
+  if (window_left >= 0) {
+    const long long span = window_right >= 0 ? (long long)window_left + window_right + 16
+                                             : (long long)window_left + Qn;
+    win = std::min<long long>(win, span);
+  }
+  return static_cast<int>(std::max<long long>(1, (win + kKeysPerCta - 1) / kKeysPerCta));
+}
+
+size_t ragged_mq_workspace_bytes(int B, int Qn, int Hq, int S, int window_left,
+                                 int window_right) {
+  const size_t splits = mq_max_splits(Qn, S, window_left, window_right);
+  return (size_t)B * splits * Qn * Hq * (kD + 2) * sizeof(float);
+}
+
+int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                     const int32_t* seq_end, int B, int Qn, int Hq, int Hkv, int S, float scale,
+                     int window_left, int window_right, float cap, const float* sink_bias,
+                     int num_sinks, int sink_per_head, void* out, float* lse, void* workspace,
+                     cudaStream_t stream) {
+  MqParams p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.seq_start = seq_start;
+  p.seq_end = seq_end;
+  p.sink_bias = sink_bias;
+  p.B = B; p.Qn = Qn; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.G = Hq / Hkv;
+  p.row_tiles = (Qn * p.G + 15) / 16;
+  p.max_splits = mq_max_splits(Qn, S, window_left, window_right);
+  if ((long long)B * p.row_tiles > 65535 || Hkv > 65535 || Qn > 65535)
+    return set_error(SBA_ERR_UNSUPPORTED,
+                     "ragged_flash_attention: B * ceil(Q * Hq / Hkv / 16), Hkv and Q must be <= 65535");
+  p.o_part = static_cast<float*>(workspace);
+  p.ml_part = p.o_part + (size_t)B * p.max_splits * Qn * Hq * kD;
+  p.scale = scale;
+  p.cap = cap > 0.f ? cap : 0.f;
+  p.window_left = window_left;
+  p.window_right = window_right;
+  p.num_sinks = num_sinks;
+  p.sink_per_head = sink_per_head;
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(ragged_mq_split_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(ragged_mq_split_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return cuda_error(e, "ragged_flash_attention: set smem attribute");
+    attr_done = true;
+  }
+  dim3 grid(p.max_splits, Hkv, B * p.row_tiles);
+  if (Qn * p.G > 8)
+    ragged_mq_split_kernel<true><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
+  else
+    ragged_mq_split_kernel<false><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "ragged_flash_attention split launch");
+  ragged_mq_combine_kernel<<<dim3(Hq, Qn, B), kD, 0, stream>>>(
+      p, static_cast<__nv_bfloat16*>(out), lse);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "ragged_flash_attention combine launch");
   return SBA_OK;
 }
 

@@ -257,3 +257,41 @@ def decode(device="cpu", seed=SEED_BASE + 5, B=64, Hq=32, Hkv=8, D=128, S=32768,
         window_left=window[0], window_right=window[1], logits_soft_cap=cap,
         sink_bias=sink,
         name=f"ragged_decode B={B} Hq={Hq} Hkv={Hkv} D={D} S={S} window={window} cap={cap} sinks={num_sinks} bf16")
+
+
+@dataclass
+class RaggedAttentionWorkload:
+    q: torch.Tensor               # [B, Q, Hq, D]
+    k: torch.Tensor               # [B, S, Hkv, D]
+    v: torch.Tensor
+    sequence_start: torch.Tensor  # int32 [B]
+    sequence_end: torch.Tensor    # int32 [B]
+    window_left: int
+    window_right: int
+    logits_soft_cap: float
+    sink_bias: torch.Tensor | None  # fp32 [Hq, num_sinks]
+    name: str = ""
+
+
+def ragged_attention(device="cpu", seed=SEED_BASE + 6, B=64, Q=4, Hq=32, Hkv=8, D=128, S=32768,
+                     window=(4096, 0), cap=50.0, num_sinks=4, sink_std=0.1,
+                     dtype=torch.bfloat16, ends=None, starts=None):
+    """Q query tokens per row against a KV cache (multi-token decode / chunked prefill).
+    Default: 64 rows verifying 4 tokens each; ends ~ U{Q..S}, so every query has a
+    position inside the cache."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    if ends is None:
+        ends = rng.integers(min(Q, S), S + 1, size=B)
+    ends = np.asarray(ends, dtype=np.int32)
+    starts = np.zeros(B, dtype=np.int32) if starts is None else np.asarray(starts, dtype=np.int32)
+    sink = randn((Hq, num_sinks), torch.float32, device, seed + 14, std=sink_std) if num_sinks else None
+    return RaggedAttentionWorkload(
+        q=randn((B, Q, Hq, D), dtype, device, seed + 11),
+        k=randn((B, S, Hkv, D), dtype, device, seed + 12),
+        v=randn((B, S, Hkv, D), dtype, device, seed + 13),
+        sequence_start=torch.from_numpy(starts).to(device),
+        sequence_end=torch.from_numpy(ends).to(device),
+        window_left=window[0], window_right=window[1], logits_soft_cap=cap,
+        sink_bias=sink,
+        name=f"ragged_attention B={B} Q={Q} Hq={Hq} Hkv={Hkv} D={D} S={S} window={window} "
+             f"cap={cap} sinks={num_sinks} bf16")

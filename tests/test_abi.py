@@ -86,6 +86,23 @@ def test_argument_validation_without_launch(lib):
                                   0.0, fake, 17, 1, fake, None, fake, need, None)
     assert r == -2
     assert lib.sba_ragged_decode_workspace_size(0, 8, 1024, 128, -1) == 0
+    # multi-query: workspace too small, unsupported head dim, Q < 1, too many sinks
+    need = lib.sba_ragged_flash_attention_workspace_size(4, 3, 8, 1024, 128, 100, 0)
+    assert need > 0
+    args = [fake, fake, fake, fake, fake, 4, 3, 8, 2, 1024, 128, 0.0, 100, 0, 0.0, None, 0, 0,
+            fake, None, fake, need - 1, None]
+    assert lib.sba_ragged_flash_attention_fwd(*args) == -1
+    assert b"workspace" in lib.sba_last_error()
+    args[-2] = need
+    args[10] = 64
+    assert lib.sba_ragged_flash_attention_fwd(*args) == -2
+    args[10] = 128
+    args[6] = 0
+    assert lib.sba_ragged_flash_attention_fwd(*args) == -1
+    args[6] = 3
+    args[15], args[16] = fake, 17
+    assert lib.sba_ragged_flash_attention_fwd(*args) == -2
+    assert lib.sba_ragged_flash_attention_workspace_size(4, 0, 8, 1024, 128, 100, 0) == 0
 
 
 def test_workspace_size_grows_with_window():
@@ -99,3 +116,21 @@ def test_workspace_size_grows_with_window():
     a = lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, 4096)
     b = lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, -1)
     assert 0 < a < b
+
+
+def test_multi_query_workspace_arithmetic():
+    """Split count of the multi-query workspace: a 16-row tile spans at most 16
+    queries, so with both window bounds it needs ceil((left + right + 16) / 512)
+    splits, with only a left bound ceil((left + Q) / 512), without one ceil(S / 512)."""
+    import selected_block_attention_gb300 as sba
+
+    try:
+        lib = sba.load_library()
+    except RuntimeError:
+        pytest.skip("library not built")
+    row = 4 * 32 * (128 + 2) * 4      # Q * Hq * (D + 2) fp32 per row and split
+    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 4096, 0) == 64 * 9 * row
+    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 4096, -1) == 64 * 9 * row
+    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, -1, 0) == 64 * 64 * row
+    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 496, 0) == 64 * 1 * row
+    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 497, 0) == 64 * 2 * row
