@@ -543,7 +543,8 @@ def run_case(args):
     """Launch one workload's kernels ``--repeat`` times (no timing JSON): the command the
     profiles are taken with.  Cases: nsa_prefill, nsa_varlen, blocksparse (bounds then
     attention), decode (``--decode-batch`` rows of the decode workload), ragged_q4 and
-    ragged_chunk512 (the two multi-query workloads)."""
+    ragged_chunk512 (the two multi-query workloads; ragged_q4 takes ``--decode-batch``
+    rows)."""
     import selected_block_attention_gb300 as sba
     from selected_block_attention_gb300 import _build
 
@@ -574,7 +575,7 @@ def run_case(args):
                                   window_left=w.window_left, window_right=w.window_right,
                                   logits_soft_cap=w.logits_soft_cap, sink_bias=w.sink_bias)
     elif args.case in ("ragged_q4", "ragged_chunk512"):
-        w = (workloads.ragged_attention(device=dev) if args.case == "ragged_q4" else
+        w = (workloads.ragged_attention(device=dev, B=args.decode_batch) if args.case == "ragged_q4" else
              workloads.ragged_attention(device=dev, B=4, Q=512, S=16384, window=(-1, 0), cap=0.0,
                                         num_sinks=0, seed=514))
 

@@ -1,29 +1,31 @@
-// Ragged single-token decode attention: split-KV partial kernel + combine kernel.
+// Ragged decode attention, one or several query tokens per batch row: split-KV partial
+// kernel + combine kernel.
 //
 // Follows "ejkernel.kernels._xla.ragged_decode_attention._xla_impl_fwd" (API page):
-// ragged_decode_mqa_xla / inner_decode_xla (per-row [sequence_start, sequence_end),
-// sliding window, logits soft cap, softmax_aux sinks), create_attention_mask (sinks
-// always attendable), apply_logits_soft_cap, apply_attention_sinks_block, and the
-// online-softmax carry of flash_attention_block.
+// ragged_decode_mqa_xla / inner_decode_xla (one query per row) and
+// ragged_flash_attention_xla (Q queries per row) over the per-row key range
+// [sequence_start, sequence_end) with sliding window, logits soft cap and softmax_aux
+// sinks; create_attention_mask (sinks always attendable), apply_logits_soft_cap,
+// apply_attention_sinks_block, and the online-softmax carry of flash_attention_block.
 //
-// The query sits at position end - 1.  Key k is attendable iff start <= k < end and
-// it is inside the inclusive window or k < num_sinks.  Logit: scale * <q, k>, then
-// cap * tanh(. / cap) when cap > 0, then + sink bias for k < num_sinks.
+// Query i of a row sits at position end - Q + i (Q = 1: the decode query at end - 1).
+// Key k is attendable by it iff start <= k < end and k is inside the query's inclusive
+// window or k < num_sinks.  Logit: scale * <q, k>, then cap * tanh(. / cap) when
+// cap > 0, then + sink bias for k < num_sinks.
 //
-// Work split: CTA (split s, KV head h, row b) covers kKeysPerCta keys of the
-// window [lo_w, end); its four warps each stream kKeysPerWarp of them.  Each warp
-// holds the G query heads of KV head h as the 16 rows of an m16n8k16 tile (rows
-// >= G are zero), streams 16-key K/V tiles with 16-byte cp.async (each key row of
-// one head is 256 contiguous bytes) through a 3-stage shared-memory ring, and keeps
-// the online-softmax state in registers.  The four warps merge through shared
-// memory and write one fp32 partial (o * exp(-m), m, l) per (row, split, q head);
-// split 0 additionally folds in the sink tokens left of the window.  The combine
-// kernel merges the partials of a row with max / exp weights and writes the bf16
-// output and the natural-log LSE.
-//
-// The same file holds the multi-query form of the page's ragged_flash_attention_xla
-// (Q queries per row, query i at position end - Q + i), built on the same split /
-// combine scheme with (query, head) pairs as the MMA rows.
+// Rows: the Q * G (query, head) pairs of one KV head, query-major; a row tile is 16
+// consecutive pairs, the 16 rows of an m16n8k16 MMA (the G heads of one query when
+// Q = 1; rows past the end are zero).  Work split: CTA (split s, KV head h, row tile
+// rt of batch row b) covers kKeysPerCta keys of the union [lo, hi) of its rows'
+// windows; its four warps each stream kKeysPerWarp of them as 16-key K/V tiles with
+// 16-byte cp.async (each key row of one head is 256 contiguous bytes) through a
+// 2-stage shared-memory ring, and keep the online-softmax state in registers.  Tiles
+// inside every row's window skip the per-element mask; edge tiles mask each element
+// with its own row's window.  Sink keys outside [lo, hi) go through an extra sink tile
+// of split 0.  The four warps merge through shared memory and write one fp32 partial
+// (o * exp(-m), m, l) per (row, split, query, head); the combine kernel merges the
+// partials of a (query, head) with max / exp weights and writes the bf16 output and
+// the natural-log LSE.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -42,10 +44,10 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kWarps = 4;
-constexpr int kKeysPerWarp = 128;
+constexpr int kKeysPerWarp = 256;
 constexpr int kKeysPerCta = kWarps * kKeysPerWarp;
 constexpr int kTileKeys = 16;
-constexpr int kStages = 3;
+constexpr int kStages = 2;  // 70 KB of ring per CTA: three CTAs (12 warps) per SM
 constexpr int kRowBytes = kD * 2 + 16;  // padded shared-memory row (ldmatrix without conflicts)
 constexpr int kTileBytes = kTileKeys * kRowBytes;
 constexpr int kWarpSmem = kStages * 2 * kTileBytes;
@@ -53,20 +55,6 @@ constexpr int kSmemBytes = kWarps * kWarpSmem;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-
-struct DecodeParams {
-  const __nv_bfloat16* q;
-  const __nv_bfloat16* k;
-  const __nv_bfloat16* v;
-  const int* seq_start;
-  const int* seq_end;
-  const float* sink_bias;
-  float* o_part;   // [B][max_splits][Hq][D]
-  float* ml_part;  // [B][max_splits][Hq][2]
-  int B, Hq, Hkv, S, G, max_splits;
-  float scale, cap;
-  int window_left, num_sinks, sink_per_head;
-};
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -95,15 +83,6 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, uint32_t b
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// cap * tanh(x / cap) from tanh(y) = 1 - 2 / (1 + e^(2y)): one ex2, one reciprocal.
-// Saturates to +-cap (e^(2y) -> inf or 0); near 0 the absolute error is a few ulp of cap.
-__device__ __forceinline__ float soft_cap(float x, float two_log2e_over_cap, float cap) {
-  const float t = ptx::ex2(x * two_log2e_over_cap);
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + t));
-  return fmaf(-2.f * cap, r, cap);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -126,279 +105,6 @@ __device__ __forceinline__ void load_tile(const __nv_bfloat16* k, const __nv_bfl
   }
 }
 
-// kHiRows: G > 8, so the rows g + 8 of the m16n8k16 tiles hold query heads too.
-template <bool kHiRows>
-__global__ void __launch_bounds__(kWarps * 32)
-decode_split_kernel(const DecodeParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int s = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-
-  const int start = p.seq_start[b], end = min(p.seq_end[b], p.S);
-  if (end <= max(start, 0)) return;  // empty row: the combine kernel writes 0 / -inf
-  const int pos = end - 1;
-  const int lo_w = p.window_left >= 0 ? max(max(start, 0), pos - p.window_left) : max(start, 0);
-  const int n_win = end - lo_w;
-  const int n_split = (n_win + kKeysPerCta - 1) / kKeysPerCta;
-  if (s >= n_split) return;
-  const int sink_hi = min(min(p.num_sinks, lo_w), end);  // sinks left of the window
-  const bool do_sinks = (s == 0) && (warp == 0) && (sink_hi > max(start, 0));
-
-  const int key_lo = lo_w + s * kKeysPerCta + warp * kKeysPerWarp;
-  const int key_hi = min(key_lo + kKeysPerWarp, end);
-  int n_tiles = key_hi > key_lo ? (key_hi - key_lo + kTileKeys - 1) / kTileKeys : 0;
-  const int first_tile = do_sinks ? -1 : 0;  // tile -1 = sink tile at keys [0, 16)
-
-  // Query fragments (A operand, 16 rows = q heads h*G + r, rows >= G zero).
-  uint32_t qa[8][4];
-  {
-    const __nv_bfloat16* qb = p.q + ((long long)b * p.Hq + (long long)h * p.G) * kD;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int d0 = ks * 16 + 2 * c;
-      auto ld = [&](int r, int d) -> uint32_t {
-        return r < p.G ? *reinterpret_cast<const uint32_t*>(qb + (long long)r * kD + d) : 0u;
-      };
-      qa[ks][0] = ld(g, d0);
-      qa[ks][1] = ld(g + 8, d0);
-      qa[ks][2] = ld(g, d0 + 8);
-      qa[ks][3] = ld(g + 8, d0 + 8);
-    }
-  }
-  const float* bias_row0 = nullptr;
-  const float* bias_row1 = nullptr;
-  if (p.num_sinks > 0) {
-    const int hq0 = h * p.G + g, hq1 = h * p.G + g + 8;
-    bias_row0 = p.sink_bias + (p.sink_per_head ? (long long)min(hq0, p.Hq - 1) * p.num_sinks : 0);
-    bias_row1 = p.sink_bias + (p.sink_per_head ? (long long)min(hq1, p.Hq - 1) * p.num_sinks : 0);
-  }
-
-  const uint32_t wbase = ptx::smem_u32(smem) + warp * kWarpSmem;
-  auto k_stage = [&](int st) { return wbase + st * 2 * kTileBytes; };
-  auto v_stage = [&](int st) { return wbase + st * 2 * kTileBytes + kTileBytes; };
-  auto tile_key0 = [&](int t) { return t < 0 ? 0 : key_lo + t * kTileKeys; };
-
-  float o[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  const int last_tile = n_tiles - 1;
-  // Prologue: stages for the first kStages-1 tiles.
-#pragma unroll
-  for (int i = 0; i < kStages - 1; ++i) {
-    const int t = first_tile + i;
-    if (t <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(t), k_stage(i), v_stage(i), lane);
-    cp_async_commit();
-  }
-  int stage = 0;
-  for (int t = first_tile; t <= last_tile; ++t) {
-    {  // prefetch tile t + kStages - 1
-      const int tn = t + kStages - 1;
-      const int sn = (stage + kStages - 1) % kStages;
-      if (tn <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(tn), k_stage(sn), v_stage(sn), lane);
-      cp_async_commit();
-    }
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const uint32_t ks_base = k_stage(stage), vs_base = v_stage(stage);
-    const int key0 = tile_key0(t);
-
-    // S = Q K^T for 16 keys: two n-tiles of 8 keys.
-    float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
-      const int mi = lane >> 3, ri = lane & 7;
-      const uint32_t row_addr = ks_base + ((mi >> 1) * 8 + ri) * kRowBytes + (mi & 1) * 16;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4(row_addr + kk * 32, b00, b01, b10, b11);
-        mma_bf16(sc[0], qa[kk], b00, b01);
-        mma_bf16(sc[1], qa[kk], b10, b11);
-      }
-    }
-    // Logits, mask, online softmax (rows g and g+8 of this thread), in log2 units with a
-    // lazily moved reference max (O is rescaled only when the max grows by > 2^8).
-    const float two_log2e_over_cap = p.cap > 0.f ? 2.f * kLog2e / p.cap : 0.f;
-    float tmax0 = -INFINITY, tmax1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = key0 + nt * 8 + 2 * c + e;
-        bool valid;
-        if (t < 0) valid = key >= max(start, 0) && key < sink_hi;
-        else valid = key >= key_lo && key < key_hi;
-        float x0 = sc[nt][e] * p.scale;
-        if (p.cap > 0.f) x0 = soft_cap(x0, two_log2e_over_cap, p.cap);
-        if (key < p.num_sinks) x0 += bias_row0[key];
-        sc[nt][e] = valid ? x0 * kLog2e : -INFINITY;
-        tmax0 = fmaxf(tmax0, sc[nt][e]);
-        if constexpr (kHiRows) {
-          float x1 = sc[nt][2 + e] * p.scale;
-          if (p.cap > 0.f) x1 = soft_cap(x1, two_log2e_over_cap, p.cap);
-          if (key < p.num_sinks) x1 += bias_row1[key];
-          sc[nt][2 + e] = valid ? x1 * kLog2e : -INFINITY;
-          tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
-        } else {
-          sc[nt][2 + e] = -INFINITY;
-        }
-      }
-    }
-    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
-    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
-    if constexpr (kHiRows) {
-      tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
-      tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
-    }
-    const float mn0 = (tmax0 > m0 + kRescaleThreshold || (m0 == -INFINITY && tmax0 != -INFINITY)) ? tmax0 : m0;
-    const float mn1 = (tmax1 > m1 + kRescaleThreshold || (m1 == -INFINITY && tmax1 != -INFINITY)) ? tmax1 : m1;
-    const bool mv0 = mn0 != m0, mv1 = mn1 != m1;
-    const float alpha0 = (mv0 && m0 != -INFINITY) ? ptx::ex2(m0 - mn0) : 1.f;
-    const float alpha1 = (mv1 && m1 != -INFINITY) ? ptx::ex2(m1 - mn1) : 1.f;
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float p0 = mn0 == -INFINITY ? 0.f : ptx::ex2(sc[nt][e] - mn0);
-        sc[nt][e] = p0;
-        ps0 += p0;
-        if constexpr (kHiRows) {
-          const float p1 = mn1 == -INFINITY ? 0.f : ptx::ex2(sc[nt][2 + e] - mn1);
-          sc[nt][2 + e] = p1;
-          ps1 += p1;
-        } else {
-          sc[nt][2 + e] = 0.f;
-        }
-      }
-    }
-    l0 = l0 * alpha0 + ps0;
-    l1 = l1 * alpha1 + ps1;
-    // the whole warp rescales O when any of its rows moved its reference max
-    if (__any_sync(0xffffffffu, mv0 || mv1)) {
-#pragma unroll
-      for (int dn = 0; dn < 16; ++dn) {
-        o[dn][0] *= alpha0; o[dn][1] *= alpha0; o[dn][2] *= alpha1; o[dn][3] *= alpha1;
-      }
-    }
-    uint32_t pa[4];
-    pa[0] = pack_bf16(sc[0][0], sc[0][1]);
-    pa[1] = pack_bf16(sc[0][2], sc[0][3]);
-    pa[2] = pack_bf16(sc[1][0], sc[1][1]);
-    pa[3] = pack_bf16(sc[1][2], sc[1][3]);
-    // O = O * alpha + P V  (16 n-tiles of 8 d columns).
-    {
-      const int mi = lane >> 3, ri = lane & 7;
-      const uint32_t row_addr = vs_base + ((mi & 1) * 8 + ri) * kRowBytes + (mi >> 1) * 16;
-#pragma unroll
-      for (int dn = 0; dn < 16; dn += 2) {
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4_t(row_addr + dn * 16, b00, b01, b10, b11);
-        mma_bf16(o[dn], pa, b00, b01);
-        mma_bf16(o[dn + 1], pa, b10, b11);
-      }
-    }
-    __syncwarp();
-    stage = (stage + 1) % kStages;
-  }
-  cp_async_wait<0>();
-  __syncthreads();
-
-  // back to natural-log units for the merge and the combine kernel
-  m0 = m0 == -INFINITY ? m0 : m0 * kLn2;
-  m1 = m1 == -INFINITY ? m1 : m1 * kLn2;
-  // Merge the four warps of the CTA through shared memory (reusing the ring).
-  float* s_o = reinterpret_cast<float*>(smem);           // [kWarps][16][kD]
-  float* s_ml = s_o + kWarps * 16 * kD;                    // [kWarps][16][2]
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-#pragma unroll
-  for (int dn = 0; dn < 16; ++dn) {
-    const int d = dn * 8 + 2 * c;
-    s_o[(warp * 16 + g) * kD + d] = o[dn][0];
-    s_o[(warp * 16 + g) * kD + d + 1] = o[dn][1];
-    s_o[(warp * 16 + g + 8) * kD + d] = o[dn][2];
-    s_o[(warp * 16 + g + 8) * kD + d + 1] = o[dn][3];
-  }
-  if (c == 0) {
-    s_ml[(warp * 16 + g) * 2 + 0] = m0;
-    s_ml[(warp * 16 + g) * 2 + 1] = l0;
-    s_ml[(warp * 16 + g + 8) * 2 + 0] = m1;
-    s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
-  }
-  __syncthreads();
-  const int d = threadIdx.x;  // kD == blockDim.x
-  for (int r = 0; r < p.G; ++r) {
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[(w * 16 + r) * 2]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = s_ml[(w * 16 + r) * 2];
-        const float f = mw == -INFINITY ? 0.f : ptx::ex2((mw - M) * kLog2e);
-        L += f * s_ml[(w * 16 + r) * 2 + 1];
-        O += f * s_o[(w * 16 + r) * kD + d];
-      }
-    }
-    const int hq = h * p.G + r;
-    const long long slot = ((long long)b * p.max_splits + s) * p.Hq + hq;
-    p.o_part[slot * kD + d] = O;
-    if (d == 0) {
-      p.ml_part[slot * 2 + 0] = M;
-      p.ml_part[slot * 2 + 1] = L;
-    }
-  }
-}
-
-__global__ void __launch_bounds__(kD)
-decode_combine_kernel(const DecodeParams p, __nv_bfloat16* __restrict__ out,
-                      float* __restrict__ lse) {
-  const int hq = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-  const int start = p.seq_start[b], end = min(p.seq_end[b], p.S);
-  int n_split = 0;
-  if (end > max(start, 0)) {
-    const int pos = end - 1;
-    const int lo_w = p.window_left >= 0 ? max(max(start, 0), pos - p.window_left) : max(start, 0);
-    n_split = (end - lo_w + kKeysPerCta - 1) / kKeysPerCta;
-  }
-  float M = -INFINITY;
-  for (int s = 0; s < n_split; ++s)
-    M = fmaxf(M, p.ml_part[(((long long)b * p.max_splits + s) * p.Hq + hq) * 2]);
-  float L = 0.f, O = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_split; ++s) {
-      const long long slot = ((long long)b * p.max_splits + s) * p.Hq + hq;
-      const float ms = p.ml_part[slot * 2];
-      const float f = ms == -INFINITY ? 0.f : ptx::ex2((ms - M) * kLog2e);
-      L += f * p.ml_part[slot * 2 + 1];
-      O += f * p.o_part[slot * kD + d];
-    }
-  }
-  const long long orow = (long long)b * p.Hq + hq;
-  out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-  if (lse != nullptr && d == 0) lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
-}
-
-
-// ---------------------------------------------------------------------------------------
-// Ragged multi-query attention ("ragged_flash_attention_xla" on the same page): Q queries
-// per batch row, query i at position end - Q + i, each with its own window.
-//
-// The rows of one KV head h are the Q * G (query, head) pairs, query-major; a row tile
-// is 16 consecutive rows, i.e. the G heads of up to 16 / G + 1 consecutive queries.  A
-// CTA (split s, KV head h, row tile rt of row b) walks kKeysPerCta keys of the union of
-// its rows' windows, [lo, hi); every element is then masked with its own row's window.
-// Sink keys outside [lo, hi) (left of it, or right of it when the tile's queries sit
-// before the sinks' end) go through the extra sink tile of split 0, sink keys inside
-// [lo, hi) through the per-row test (sinks are attendable from every query).
 struct MqParams {
   const __nv_bfloat16* q;  // [B, Q, Hq, D]
   const __nv_bfloat16* k;  // [B, S, Hkv, D]
@@ -451,9 +157,10 @@ __device__ __forceinline__ MqRange mq_tile_range(const MqParams& p, int b, int r
   return R;
 }
 
-// kHiRows: Q * G > 8, so the rows g + 8 of the m16n8k16 tiles are used.
-template <bool kHiRows>
-__global__ void __launch_bounds__(kWarps * 32)
+// kHiRows: Q * G > 8, so the rows g + 8 of the m16n8k16 tiles are used.  kCap: logits
+// soft cap on.
+template <bool kHiRows, bool kCap>
+__global__ void __launch_bounds__(kWarps * 32, 3)
 ragged_mq_split_kernel(const MqParams p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int s = blockIdx.x, h = blockIdx.y;
@@ -474,7 +181,7 @@ ragged_mq_split_kernel(const MqParams p) {
   const int rr0 = rt * 16 + g, rr1 = rr0 + 8;
   const bool ok0 = rr0 < nrows, ok1 = kHiRows && rr1 < nrows;
   const int i0 = ok0 ? rr0 / p.G : 0, i1 = ok1 ? rr1 / p.G : 0;
-  const int hq0 = h * p.G + (ok0 ? rr0 % p.G : 0), hq1 = h * p.G + (ok1 ? rr1 % p.G : 0);
+  const int hq0 = h * p.G + (rr0 - i0 * p.G) * ok0, hq1 = h * p.G + (rr1 - i1 * p.G) * ok1;
   auto win_lo = [&](int i) -> int {  // smallest window key of query i (keys are >= 0)
     if (p.window_left < 0) return -1;
     return static_cast<int>(max((long long)R.end - p.Qn + i - p.window_left, -1LL));
@@ -485,18 +192,21 @@ ragged_mq_split_kernel(const MqParams p) {
   };
   const int wlo0 = win_lo(i0), whi0 = ok0 ? win_hi(i0) : -1;
   const int wlo1 = win_lo(i1), whi1 = ok1 ? win_hi(i1) : -1;
+  // The part of the window that every row of the tile shares (rows past the end do not
+  // count): a key tile inside it, holding no sink, needs no per-element mask.
+  int all_lo = max(ok0 ? wlo0 : INT_MIN, ok1 ? wlo1 : INT_MIN);
+  int all_hi = min(ok0 ? whi0 : INT_MAX, ok1 ? whi1 : INT_MAX);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    all_lo = max(all_lo, __shfl_xor_sync(0xffffffffu, all_lo, off));
+    all_hi = min(all_hi, __shfl_xor_sync(0xffffffffu, all_hi, off));
+  }
 
   // Query fragments (A operand): row r of the tile is (query, head) pair rt * 16 + r.
   uint32_t qa[8][4];
   {
-    auto row_ptr = [&](int r) -> const __nv_bfloat16* {
-      const int rr = rt * 16 + r;
-      if (rr >= nrows) return nullptr;
-      const int qi = rr / p.G, hq = h * p.G + rr % p.G;
-      return p.q + ((long long)(b * p.Qn + qi) * p.Hq + hq) * kD;
-    };
-    const __nv_bfloat16* qr0 = row_ptr(g);
-    const __nv_bfloat16* qr1 = kHiRows ? row_ptr(g + 8) : nullptr;
+    const __nv_bfloat16* qr0 = ok0 ? p.q + ((long long)(b * p.Qn + i0) * p.Hq + hq0) * kD : nullptr;
+    const __nv_bfloat16* qr1 = ok1 ? p.q + ((long long)(b * p.Qn + i1) * p.Hq + hq1) * kD : nullptr;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       const int d0 = ks * 16 + 2 * c;
@@ -520,6 +230,39 @@ ragged_mq_split_kernel(const MqParams p) {
   auto k_stage = [&](int st) { return wbase + st * 2 * kTileBytes; };
   auto v_stage = [&](int st) { return wbase + st * 2 * kTileBytes + kTileBytes; };
   auto tile_key0 = [&](int t) { return t < 0 ? 0 : key_lo + t * kTileKeys; };
+  // Copies of one tile: lane copies 16-byte part (lane & 15) of keys 2 i + (lane >> 4).
+  // Tiles inside the cache step one pointer; the rare edge tile clamps key by key.
+  const long long key_stride = (long long)p.Hkv * kD;
+  const long long lane_off = ((long long)b * p.S * p.Hkv + h) * kD + (lane & 15) * 8;
+  const uint32_t lane_dst = (lane >> 4) * kRowBytes + (lane & 15) * 16;
+  auto issue_tile = [&](int key0, uint32_t k_dst, uint32_t v_dst) {
+    if (key0 >= 0 && key0 + kTileKeys <= p.S) {
+      const long long off = lane_off + (long long)(key0 + (lane >> 4)) * key_stride;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        cp_async16(k_dst + lane_dst + 2 * i * kRowBytes, p.k + off + 2 * i * key_stride);
+        cp_async16(v_dst + lane_dst + 2 * i * kRowBytes, p.v + off + 2 * i * key_stride);
+      }
+    } else {
+      load_tile(p.k, p.v, p.S, p.Hkv, b, h, key0, k_dst, v_dst, lane);
+    }
+  };
+  // Logits in log2 units: s * scale * log2(e), or with the cap
+  // log2(e) * cap * tanh(s * scale / cap) = c3 - c2 / (1 + 2^(s * c1)).
+  const float c0 = p.scale * kLog2e;
+  const float c1 = kCap ? p.scale * 2.f * kLog2e / p.cap : 0.f;
+  const float c2 = kCap ? 2.f * p.cap * kLog2e : 0.f;
+  const float c3 = kCap ? p.cap * kLog2e : 0.f;
+  auto logit = [&](float x) -> float {
+    if constexpr (kCap) {
+      const float e = ptx::ex2(x * c1);
+      float r;
+      asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+      return fmaf(-c2, r, c3);
+    } else {
+      return x * c0;
+    }
+  };
 
   float o[16][4];
 #pragma unroll
@@ -530,16 +273,15 @@ ragged_mq_split_kernel(const MqParams p) {
 #pragma unroll
   for (int i = 0; i < kStages - 1; ++i) {
     const int t = first_tile + i;
-    if (t <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(t), k_stage(i), v_stage(i), lane);
+    if (t <= last_tile) issue_tile(tile_key0(t), k_stage(i), v_stage(i));
     cp_async_commit();
   }
   int stage = 0;
-  const float two_log2e_over_cap = p.cap > 0.f ? 2.f * kLog2e / p.cap : 0.f;
   for (int t = first_tile; t <= last_tile; ++t) {
     {
       const int tn = t + kStages - 1;
       const int sn = (stage + kStages - 1) % kStages;
-      if (tn <= last_tile) load_tile(p.k, p.v, p.S, p.Hkv, b, h, tile_key0(tn), k_stage(sn), v_stage(sn), lane);
+      if (tn <= last_tile) issue_tile(tile_key0(tn), k_stage(sn), v_stage(sn));
       cp_async_commit();
     }
     cp_async_wait<kStages - 1>();
@@ -560,35 +302,53 @@ ragged_mq_split_kernel(const MqParams p) {
       }
     }
     float tmax0 = -INFINITY, tmax1 = -INFINITY;
+    const bool plain = t >= 0 && key0 >= p.num_sinks && key0 >= key_lo &&
+                       key0 + kTileKeys <= key_hi && key0 >= all_lo &&
+                       key0 + kTileKeys - 1 <= all_hi;  // warp-uniform
+    if (plain) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+      for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = key0 + nt * 8 + 2 * c + e;
-        const bool sink = key < p.num_sinks;
-        bool in0, in1;
-        if (t < 0) {  // sink tile: in-range sink keys outside the union window, every row
-          const bool outside = key >= R.start && key < R.sink_end && (key < R.lo || key >= R.hi);
-          in0 = ok0 && outside;
-          in1 = ok1 && outside;
-        } else {
-          const bool in_tile = key >= key_lo && key < key_hi;
-          in0 = ok0 && in_tile && ((key >= wlo0 && key <= whi0) || sink);
-          in1 = ok1 && in_tile && ((key >= wlo1 && key <= whi1) || sink);
+        for (int e = 0; e < 2; ++e) {
+          sc[nt][e] = logit(sc[nt][e]);
+          tmax0 = fmaxf(tmax0, sc[nt][e]);
+          if constexpr (kHiRows) {
+            sc[nt][2 + e] = logit(sc[nt][2 + e]);
+            tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
+          } else {
+            sc[nt][2 + e] = -INFINITY;
+          }
         }
-        float x0 = sc[nt][e] * p.scale;
-        if (p.cap > 0.f) x0 = soft_cap(x0, two_log2e_over_cap, p.cap);
-        if (sink) x0 += bias_row0[key];
-        sc[nt][e] = in0 ? x0 * kLog2e : -INFINITY;
-        tmax0 = fmaxf(tmax0, sc[nt][e]);
-        if constexpr (kHiRows) {
-          float x1 = sc[nt][2 + e] * p.scale;
-          if (p.cap > 0.f) x1 = soft_cap(x1, two_log2e_over_cap, p.cap);
-          if (sink) x1 += bias_row1[key];
-          sc[nt][2 + e] = in1 ? x1 * kLog2e : -INFINITY;
-          tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
-        } else {
-          sc[nt][2 + e] = -INFINITY;
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = key0 + nt * 8 + 2 * c + e;
+          const bool sink = key < p.num_sinks;
+          bool in0, in1;
+          if (t < 0) {  // sink tile: in-range sink keys outside the union window, every row
+            const bool outside = key >= R.start && key < R.sink_end && (key < R.lo || key >= R.hi);
+            in0 = ok0 && outside;
+            in1 = ok1 && outside;
+          } else {
+            const bool in_tile = key >= key_lo && key < key_hi;
+            in0 = ok0 && in_tile && ((key >= wlo0 && key <= whi0) || sink);
+            in1 = ok1 && in_tile && ((key >= wlo1 && key <= whi1) || sink);
+          }
+          float y0 = logit(sc[nt][e]);
+          if (sink) y0 = fmaf(bias_row0[key], kLog2e, y0);
+          sc[nt][e] = in0 ? y0 : -INFINITY;
+          tmax0 = fmaxf(tmax0, sc[nt][e]);
+          if constexpr (kHiRows) {
+            float y1 = logit(sc[nt][2 + e]);
+            if (sink) y1 = fmaf(bias_row1[key], kLog2e, y1);
+            sc[nt][2 + e] = in1 ? y1 : -INFINITY;
+            tmax1 = fmaxf(tmax1, sc[nt][2 + e]);
+          } else {
+            sc[nt][2 + e] = -INFINITY;
+          }
         }
       }
     }
@@ -675,22 +435,34 @@ ragged_mq_split_kernel(const MqParams p) {
     s_ml[(warp * 16 + g + 8) * 2 + 1] = l1;
   }
   __syncthreads();
-  const int d = threadIdx.x;  // kD == blockDim.x
-  const int tile_rows = min(16, nrows - rt * 16);
-  for (int r = 0; r < tile_rows; ++r) {
+  // Per row: the merged max and sum and each warp's weight, once (16 threads).
+  float* s_f = s_ml + kWarps * 16 * 2;  // [16][kWarps] weights
+  float* s_m = s_f + 16 * kWarps;       // [16] merged max
+  float* s_l = s_m + 16;                // [16] merged sum
+  if (threadIdx.x < 16) {
+    const int r = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_ml[(w * 16 + r) * 2]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
+    float L = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float mw = s_ml[(w * 16 + r) * 2];
-        const float f = mw == -INFINITY ? 0.f : ptx::ex2((mw - M) * kLog2e);
-        L += f * s_ml[(w * 16 + r) * 2 + 1];
-        O += f * s_o[(w * 16 + r) * kD + d];
-      }
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = s_ml[(w * 16 + r) * 2];
+      const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : ptx::ex2((mw - M) * kLog2e);
+      s_f[r * kWarps + w] = f;
+      L += f * s_ml[(w * 16 + r) * 2 + 1];
     }
+    s_m[r] = M;
+    s_l[r] = L;
+  }
+  __syncthreads();
+  const int d = threadIdx.x;  // kD == blockDim.x
+  const int tile_rows = min(16, nrows - rt * 16);
+  for (int r = 0; r < tile_rows; ++r) {
+    const float M = s_m[r], L = s_l[r];
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) O = fmaf(s_f[r * kWarps + w], s_o[(w * 16 + r) * kD + d], O);
     const int rr = rt * 16 + r;
     const int qi = rr / p.G, hq = h * p.G + rr % p.G;
     const long long slot = (((long long)b * p.max_splits + s) * p.Qn + qi) * p.Hq + hq;
@@ -736,73 +508,14 @@ unsigned read_and_clear_error_decode(cudaStream_t, std::string*) {
   return w;
 }
 
-static int decode_max_splits(int S, int window_left) {
-  const long long win = window_left >= 0 ? std::min<long long>(S, (long long)window_left + 1) : S;
-  return static_cast<int>(std::max<long long>(1, (win + kKeysPerCta - 1) / kKeysPerCta));
-}
-
-size_t decode_workspace_bytes(int B, int Hq, int S, int D, int window_left) {
-  (void)D;
-  const size_t splits = decode_max_splits(S, window_left);
-  return (size_t)B * splits * Hq * (kD + 2) * sizeof(float);
-}
-
-int launch_ragged_decode(const void* q, const void* k, const void* v, const int32_t* seq_start,
-                         const int32_t* seq_end, int B, int Hq, int Hkv, int S, int D,
-                         float scale, int window_left, int window_right, float cap,
-                         const float* sink_bias, int num_sinks, int sink_per_head, void* out,
-                         float* lse, void* workspace, size_t workspace_bytes,
-                         cudaStream_t stream) {
-  (void)D;
-  (void)window_right;  // the query is the last key: a right window never cuts
-  (void)workspace_bytes;
-  if (B > 65535 || Hkv > 65535) return set_error(SBA_ERR_UNSUPPORTED, "ragged_decode: B, Hkv <= 65535");
-  DecodeParams p;
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
-  p.seq_start = seq_start;
-  p.seq_end = seq_end;
-  p.sink_bias = sink_bias;
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.S = S; p.G = Hq / Hkv;
-  p.max_splits = decode_max_splits(S, window_left);
-  p.o_part = static_cast<float*>(workspace);
-  p.ml_part = p.o_part + (size_t)B * p.max_splits * Hq * kD;
-  p.scale = scale;
-  p.cap = cap > 0.f ? cap : 0.f;
-  p.window_left = window_left;
-  p.num_sinks = num_sinks;
-  p.sink_per_head = sink_per_head;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(decode_split_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kSmemBytes);
-    if (e != cudaSuccess) return cuda_error(e, "ragged_decode: set smem attribute");
-    attr_done = true;
-  }
-  dim3 grid(p.max_splits, Hkv, B);
-  if (p.G > 8)
-    decode_split_kernel<true><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
-  else
-    decode_split_kernel<false><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "ragged_decode split launch");
-  decode_combine_kernel<<<dim3(Hq, B), kD, 0, stream>>>(p, static_cast<__nv_bfloat16*>(out), lse);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "ragged_decode combine launch");
-  return SBA_OK;
-}
-
-
 static int mq_max_splits(int Qn, int S, int window_left, int window_right) {
-  // Longest union window of a 16-row tile: its rows span at most 16 consecutive queries.
+  // Longest union window of a 16-row tile.  Its rows belong to queries i_lo..i_hi
+  // (i_hi - i_lo <= 15), so hi - lo <= window_left + min(Q - i_lo, i_hi - i_lo + 1 +
+  // window_right) <= window_left + min(Q, window_right + 16); window_left + 1 when Q = 1.
   long long win = S;
   if (window_left >= 0) {
-    const long long span = window_right >= 0 ? (long long)window_left + window_right + 16
-                                             : (long long)window_left + Qn;
+    const long long span = (long long)window_left +
+                           (window_right >= 0 ? std::min<long long>(Qn, (long long)window_right + 16) : Qn);
     win = std::min<long long>(win, span);
   }
   return static_cast<int>(std::max<long long>(1, (win + kKeysPerCta - 1) / kKeysPerCta));
@@ -831,7 +544,7 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
   p.max_splits = mq_max_splits(Qn, S, window_left, window_right);
   if ((long long)B * p.row_tiles > 65535 || Hkv > 65535 || Qn > 65535)
     return set_error(SBA_ERR_UNSUPPORTED,
-                     "ragged_flash_attention: B * ceil(Q * Hq / Hkv / 16), Hkv and Q must be <= 65535");
+                     "ragged attention: B * ceil(Q * Hq / Hkv / 16), Hkv and Q must be <= 65535");
   p.o_part = static_cast<float*>(workspace);
   p.ml_part = p.o_part + (size_t)B * p.max_splits * Qn * Hq * kD;
   p.scale = scale;
@@ -842,26 +555,46 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
   p.sink_per_head = sink_per_head;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(ragged_mq_split_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ragged_mq_split_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return cuda_error(e, "ragged_flash_attention: set smem attribute");
+    cudaError_t e = cudaSuccess;
+    for (auto fn : {ragged_mq_split_kernel<false, false>, ragged_mq_split_kernel<false, true>,
+                    ragged_mq_split_kernel<true, false>, ragged_mq_split_kernel<true, true>})
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return cuda_error(e, "ragged attention: set smem attribute");
     attr_done = true;
   }
   dim3 grid(p.max_splits, Hkv, B * p.row_tiles);
-  if (Qn * p.G > 8)
-    ragged_mq_split_kernel<true><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
-  else
-    ragged_mq_split_kernel<false><<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
+  const bool hi_rows = Qn * p.G > 8, capped = p.cap > 0.f;
+  auto kernel = hi_rows ? (capped ? ragged_mq_split_kernel<true, true> : ragged_mq_split_kernel<true, false>)
+                        : (capped ? ragged_mq_split_kernel<false, true> : ragged_mq_split_kernel<false, false>);
+  kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "ragged_flash_attention split launch");
+  if (e != cudaSuccess) return cuda_error(e, "ragged attention split launch");
   ragged_mq_combine_kernel<<<dim3(Hq, Qn, B), kD, 0, stream>>>(
       p, static_cast<__nv_bfloat16*>(out), lse);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "ragged_flash_attention combine launch");
+  if (e != cudaSuccess) return cuda_error(e, "ragged attention combine launch");
   return SBA_OK;
+}
+
+
+// Single-token decode: the Q = 1 case (the query at end - 1; a right window never cuts).
+size_t decode_workspace_bytes(int B, int Hq, int S, int D, int window_left) {
+  (void)D;
+  return ragged_mq_workspace_bytes(B, 1, Hq, S, window_left, -1);
+}
+
+int launch_ragged_decode(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                         const int32_t* seq_end, int B, int Hq, int Hkv, int S, int D,
+                         float scale, int window_left, int window_right, float cap,
+                         const float* sink_bias, int num_sinks, int sink_per_head, void* out,
+                         float* lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  (void)D;
+  (void)workspace_bytes;
+  return launch_ragged_mq(q, k, v, seq_start, seq_end, B, 1, Hq, Hkv, S, scale, window_left,
+                          window_right, cap, sink_bias, num_sinks, sink_per_head, out, lse,
+                          workspace, stream);
 }
 
 }  // namespace sba

@@ -119,18 +119,28 @@ def test_workspace_size_grows_with_window():
 
 
 def test_multi_query_workspace_arithmetic():
-    """Split count of the multi-query workspace: a 16-row tile spans at most 16
-    queries, so with both window bounds it needs ceil((left + right + 16) / 512)
-    splits, with only a left bound ceil((left + Q) / 512), without one ceil(S / 512)."""
+    """Split count of the multi-query workspace: a 16-row tile spans queries
+    i_lo..i_hi (at most 16), so its key range is at most left + min(Q, right + 16)
+    keys with both window bounds, left + Q with only a left bound, S without one;
+    Q = 1 gives the decode workspace."""
     import selected_block_attention_gb300 as sba
 
     try:
         lib = sba.load_library()
     except RuntimeError:
         pytest.skip("library not built")
+    ws = lib.sba_ragged_flash_attention_workspace_size
     row = 4 * 32 * (128 + 2) * 4      # Q * Hq * (D + 2) fp32 per row and split
-    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 4096, 0) == 64 * 9 * row
-    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 4096, -1) == 64 * 9 * row
-    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, -1, 0) == 64 * 64 * row
-    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 496, 0) == 64 * 1 * row
-    assert lib.sba_ragged_flash_attention_workspace_size(64, 4, 32, 32768, 128, 497, 0) == 64 * 2 * row
+    assert ws(64, 4, 32, 32768, 128, 4096, 0) == 64 * 9 * row
+    assert ws(64, 4, 32, 32768, 128, 4096, -1) == 64 * 9 * row
+    assert ws(64, 4, 32, 32768, 128, -1, 0) == 64 * 64 * row
+    assert ws(64, 4, 32, 32768, 128, 508, 0) == 64 * 1 * row     # 512 keys
+    assert ws(64, 4, 32, 32768, 128, 509, 0) == 64 * 2 * row     # 513 keys
+    row64 = 64 * 32 * (128 + 2) * 4
+    assert ws(2, 64, 32, 32768, 128, 1000, 8) == 2 * 2 * row64  # 1000 + 24 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, -1) == 2 * 3 * row64  # 1000 + 64 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 40) == 2 * 3 * row64  # 1000 + 56 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 60) == 2 * 3 * row64  # 1000 + 64 keys
+    assert ws(2, 64, 32, 1000, 128, -1, 60) == 2 * 2 * row64     # S = 1000
+    for wl in (-1, 0, 4096, 5000):
+        assert ws(64, 1, 32, 32768, 128, wl, 7) == lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, wl)
