@@ -1,9 +1,11 @@
-"""fp64/int64 oracle: SparseMask block bounds for the forward pass.  (TEST INFRASTRUCTURE)
+"""int64 oracle: SparseMask block bounds, forward and dK/dV.  (TEST INFRASTRUCTURE)
 
 Source: ejkernel.kernels._triton.blocksparse_attention._mask (module source
-page): the ``SparseMask`` dataclass, the ``_compute_sparse_mask`` kernel taken
-with the query as the outer operand, and the padding, padding-segment remap and
-clip/fix-up steps of ``define_sparse_mask_fn``.
+page): the ``SparseMask`` dataclass, the ``_compute_sparse_mask`` kernel (taken
+with the query blocks as the outer operand for the forward / dQ bounds and with
+the key/value blocks as the outer operand when ``calculate_dkdv_mask`` is set),
+and the padding, padding-segment remap and clip/fix-up steps of
+``define_sparse_mask_fn``.
 
 The bounds are a block-level heuristic with an exact integer result, so this
 module takes the page's steps in the page's order, in plain loops:
@@ -11,11 +13,11 @@ module takes the page's steps in the page's order, in plain loops:
 1. pad both sides to a block multiple (query positions with -1, key/value
    positions with the int32 maximum, segment ids with the padding id);
 2. remap the padding segment id to ``padded_kv_len + 1`` on both sides;
-3. per query ("outer") block, take min/max of positions and segment ids; a
-   block made only of padding gets bounds (0, 0, 0, 0);
-4. sweep every key/value ("inner") block, evaluate the attend and full
-   predicates (segment-range overlap, causal, inclusive left/right window,
-   padding) and min/max-accumulate the four bounds;
+3. per outer block, take min/max of positions and segment ids; a block made
+   only of padding gets bounds (0, 0, 0, 0);
+4. sweep every inner block, evaluate the attend and full predicates
+   (segment-range overlap, causal, inclusive left/right window, inner block made
+   only of padding) and min/max-accumulate the four bounds;
 5. clip and order the bounds as the fix-up step does.
 
 Readings of what the page leaves open (each is also listed in the design notes):
@@ -25,7 +27,10 @@ Readings of what the page leaves open (each is also listed in the design notes):
   * position arithmetic is done in 64-bit integers.
 The window-left attend test compares the *smallest* key position of a block
 with ``min(query positions) - window_left``; it is reproduced as written, so a
-key block that straddles the window edge may be left out.
+key block that straddles the window edge may be left out.  The kv-outer
+(dK/dV) predicates are likewise taken as printed; they are not the transposed
+forward tests (under causal masking their left-window attend test never prunes
+a block, and their full tests compare the smallest positions).
 """
 
 from __future__ import annotations
@@ -45,12 +50,17 @@ def _pad_to_block(values, block, fill):
 
 def sparse_mask_bounds(q_positions, q_segment_ids, kv_positions, kv_segment_ids,
                        q_blocksize, kv_blocksize, *, causal=True,
-                       window_left=-1, window_right=-1, padding_segment_id=-1):
-    """Forward SparseMask bounds.
+                       window_left=-1, window_right=-1, padding_segment_id=-1,
+                       calculate_dkdv_mask=False):
+    """SparseMask bounds.
 
     Inputs are integer arrays ``[B, Tq]`` (query side) and ``[B, Tkv]``
-    (key/value side).  Returns four int32 arrays of shape ``[B, 1, NBq]``:
-    ``lower, upper, lower_full, upper_full`` with ``NBq = ceil(Tq / q_blocksize)``.
+    (key/value side).  Forward (``calculate_dkdv_mask=False``): the query blocks
+    are the outer operand and the result is four int32 arrays ``[B, 1, NBq]``
+    (``lower, upper, lower_full, upper_full`` ranges of key/value blocks).
+    Backward dK/dV (``calculate_dkdv_mask=True``): the key/value blocks are the
+    outer operand and the result is ``[B, 1, NBkv]`` ranges of query blocks, with
+    the kv-outer position predicates of the page.
     """
     q_pos = np.asarray(q_positions, dtype=np.int64)
     q_seg = np.asarray(q_segment_ids, dtype=np.int64)
@@ -63,55 +73,81 @@ def sparse_mask_bounds(q_positions, q_segment_ids, kv_positions, kv_segment_ids,
     q_seg = _pad_to_block(q_seg, q_blocksize, pad)
     kv_pos = _pad_to_block(kv_pos, kv_blocksize, INT32_MAX)
     kv_seg = _pad_to_block(kv_seg, kv_blocksize, pad)
-    B, Tq = q_pos.shape
     Tkv = kv_pos.shape[1]
-    nbq = Tq // q_blocksize
-    nbkv = Tkv // kv_blocksize
 
-    # Step 2: padding segment id -> padded kv length + 1.
+    # Step 2: padding segment id -> padded kv length + 1 (on both sides, either way).
     pad_inner = Tkv + 1
     q_seg = np.where(q_seg == pad, pad_inner, q_seg)
     kv_seg = np.where(kv_seg == pad, pad_inner, kv_seg)
 
-    use_window = window_left >= 0 or window_right >= 0
-    lower = np.zeros((B, 1, nbq), dtype=np.int64)
-    upper = np.zeros((B, 1, nbq), dtype=np.int64)
-    lower_full = np.zeros((B, 1, nbq), dtype=np.int64)
-    upper_full = np.zeros((B, 1, nbq), dtype=np.int64)
+    if calculate_dkdv_mask:
+        return _bounds(kv_pos, kv_seg, q_pos, q_seg, kv_blocksize, q_blocksize, False,
+                       causal, window_left, window_right, pad_inner)
+    return _bounds(q_pos, q_seg, kv_pos, kv_seg, q_blocksize, kv_blocksize, True,
+                   causal, window_left, window_right, pad_inner)
+
+
+def _position_predicates(query_is_outer, causal, window_left, window_right,
+                         o_min, o_max, i_min, i_max):
+    """(attend, full) position tests of one (outer block, inner block) pair, as the
+    page's kernel states them for each choice of outer operand."""
+    attend_pos, full_pos = True, True
+    if query_is_outer:      # outer = query block, inner = key/value block
+        if causal:
+            attend_pos = o_max >= i_min
+            full_pos = o_min >= i_max
+        if window_left >= 0:
+            attend_pos = attend_pos and (i_min >= o_min - window_left)
+            full_pos = full_pos and (i_min >= o_max - window_left)
+        if window_right >= 0:
+            attend_pos = attend_pos and (i_max <= o_max + window_right)
+            full_pos = full_pos and (i_max <= o_min + window_right)
+    else:                   # outer = key/value block, inner = query block
+        if causal:
+            attend_pos = i_max >= o_min
+            full_pos = i_min >= o_max
+        if window_left >= 0:
+            attend_pos = attend_pos and (i_max >= o_min - window_left)
+            full_pos = full_pos and (i_min >= o_min - window_left)
+        if window_right >= 0:
+            attend_pos = attend_pos and (i_min <= o_max + window_right)
+            full_pos = full_pos and (i_max <= o_max + window_right)
+    return attend_pos, full_pos
+
+
+def _bounds(o_pos, o_seg, i_pos, i_seg, o_block, i_block, query_is_outer, causal,
+            window_left, window_right, pad_inner):
+    B, To = o_pos.shape
+    Ti = i_pos.shape[1]
+    nbo = To // o_block
+    nbi = Ti // i_block
+    lower = np.zeros((B, 1, nbo), dtype=np.int64)
+    upper = np.zeros((B, 1, nbo), dtype=np.int64)
+    lower_full = np.zeros((B, 1, nbo), dtype=np.int64)
+    upper_full = np.zeros((B, 1, nbo), dtype=np.int64)
 
     for b in range(B):
-        for j in range(nbq):
-            # Step 3: summaries of the query (outer) block.
-            qs = slice(j * q_blocksize, (j + 1) * q_blocksize)
-            o_seg_min, o_seg_max = int(q_seg[b, qs].min()), int(q_seg[b, qs].max())
+        for j in range(nbo):
+            # Step 3: summaries of the outer block.
+            os_ = slice(j * o_block, (j + 1) * o_block)
+            o_seg_min, o_seg_max = int(o_seg[b, os_].min()), int(o_seg[b, os_].max())
             o_same = o_seg_min == o_seg_max
             if o_same and o_seg_min == pad_inner:
                 continue  # all four bounds stay 0
-            o_pos_min, o_pos_max = int(q_pos[b, qs].min()), int(q_pos[b, qs].max())
+            o_pos_min, o_pos_max = int(o_pos[b, os_].min()), int(o_pos[b, os_].max())
 
-            up, lo, up_full, lo_full = 0, nbkv, 0, nbkv
-            # Step 4: sweep the key/value (inner) blocks.
-            for i in range(nbkv):
-                ks = slice(i * kv_blocksize, (i + 1) * kv_blocksize)
-                i_seg_min, i_seg_max = int(kv_seg[b, ks].min()), int(kv_seg[b, ks].max())
+            up, lo, up_full, lo_full = 0, nbi, 0, nbi
+            # Step 4: sweep the inner blocks.
+            for i in range(nbi):
+                is_ = slice(i * i_block, (i + 1) * i_block)
+                i_seg_min, i_seg_max = int(i_seg[b, is_].min()), int(i_seg[b, is_].max())
                 i_same = i_seg_min == i_seg_max
                 attend_seg = (i_seg_min <= o_seg_max) and (o_seg_min <= i_seg_max)
                 full_seg = o_same and i_same
-                i_pos_min, i_pos_max = int(kv_pos[b, ks].min()), int(kv_pos[b, ks].max())
-
-                if causal:
-                    attend_pos = o_pos_max >= i_pos_min
-                    full_pos = o_pos_min >= i_pos_max
-                else:
-                    attend_pos = True
-                    full_pos = True
-                if use_window:
-                    if window_left >= 0:
-                        attend_pos = attend_pos and (i_pos_min >= o_pos_min - window_left)
-                        full_pos = full_pos and (i_pos_min >= o_pos_max - window_left)
-                    if window_right >= 0:
-                        attend_pos = attend_pos and (i_pos_max <= o_pos_max + window_right)
-                        full_pos = full_pos and (i_pos_max <= o_pos_min + window_right)
+                i_pos_min, i_pos_max = int(i_pos[b, is_].min()), int(i_pos[b, is_].max())
+                attend_pos, full_pos = _position_predicates(
+                    query_is_outer, causal, window_left, window_right,
+                    o_pos_min, o_pos_max, i_pos_min, i_pos_max)
 
                 attend = attend_pos and attend_seg and not (i_seg_min == pad_inner)
                 full = full_seg and full_pos and attend
@@ -123,11 +159,11 @@ def sparse_mask_bounds(q_positions, q_segment_ids, kv_positions, kv_segment_ids,
                     lo_full = min(lo_full, i)
 
             # Step 5: clip / order fix-up.
-            lo = min(max(lo, 0), nbkv)
-            up = min(max(up, 0), nbkv)
+            lo = min(max(lo, 0), nbi)
+            up = min(max(up, 0), nbi)
             lo = min(lo, up)
-            lo_full = max(min(max(lo_full, 0), nbkv), lo)
-            up_full = min(max(min(max(up_full, 0), nbkv), lo_full), up)
+            lo_full = max(min(max(lo_full, 0), nbi), lo)
+            up_full = min(max(min(max(up_full, 0), nbi), lo_full), up)
             lower[b, 0, j] = lo
             upper[b, 0, j] = up
             lower_full[b, 0, j] = lo_full
