@@ -472,6 +472,15 @@ def measure_rows(sba, dev, stream, flush, peaks, args):
     rows["sparse_mask_bounds"] = {
         "workload": m.name, "us": round(ms * 1e3, 2), "GB/s": round(in_bytes / ms / 1e6, 1),
         "frac_hbm": round(in_bytes / ms / 1e6 / peaks["hbm_gbs"], 4)}
+    t = timed_steps(lambda: sba.sparse_mask_bounds(
+        m.q_positions, m.q_segment_ids, m.kv_positions, m.kv_segment_ids, 128, 128, causal=True,
+        window_left=1024, window_right=0, calculate_dkdv_mask=True), steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    log(f"dkdv bounds {ms * 1e3:.2f} us")
+    rows["sparse_mask_dkdv_bounds"] = {
+        "workload": m.name + " (dK/dV, kv blocks outer)", "us": round(ms * 1e3, 2),
+        "GB/s": round(in_bytes / ms / 1e6, 1),
+        "frac_hbm": round(in_bytes / ms / 1e6 / peaks["hbm_gbs"], 4)}
     lo, up, lof, upf = bnd["b"]
     fl = blocksparse_flops(w)
     t = timed_steps(lambda: sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids,

@@ -121,6 +121,37 @@ SBA_API int sba_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg,
                            sba_stream_t stream);
 
 /*
+ * sba_sparse_mask_dkdv_bounds -- SparseMask block bounds for the dK/dV backward pass.
+ *
+ * Defined by: "ejkernel.kernels._triton.blocksparse_attention._mask" (module source
+ * page): define_sparse_mask_fn with calculate_dkdv_mask set, i.e. kernel
+ * _compute_sparse_mask with the key/value blocks as the outer operand and the query
+ * blocks as the inner one, then the same clip/fix-up against the number of query
+ * blocks.  Padding and the padding-segment remap are those of sba_sparse_mask_bounds.
+ * Position tests, as the page prints them for this operand order (o = key/value block,
+ * i = query block, min/max over the block's positions; 64-bit arithmetic):
+ *   causal:        attend  max_i >= min_o            full  min_i >= max_o
+ *   window_left:   attend  max_i >= min_o - left     full  min_i >= min_o - left
+ *   window_right:  attend  min_i <= max_o + right    full  max_i <= max_o + right
+ * Results are bit-exact integers.
+ *
+ *  q_pos, q_seg, kv_pos, kv_seg, window_left/right, padding_segment_id: as in
+ *                  sba_sparse_mask_bounds
+ *  lower, upper, lower_full, upper_full  [B, 1, ceil(Tkv / kv_block)] int32 (written):
+ *                  half-open ranges of query blocks per key/value block
+ * All pointers are caller-owned device memory.  Returns SBA_ERR_INVALID_ARG for null
+ * pointers or non-positive sizes, SBA_ERR_UNSUPPORTED for blocks > 4096 or B > 65535.
+ */
+SBA_API int sba_sparse_mask_dkdv_bounds(const int32_t* q_pos, const int32_t* q_seg,
+                                        const int32_t* kv_pos, const int32_t* kv_seg,
+                                        int B, int Tq, int Tkv, int q_block, int kv_block,
+                                        int causal, int window_left, int window_right,
+                                        int padding_segment_id,
+                                        int32_t* lower, int32_t* upper,
+                                        int32_t* lower_full, int32_t* upper_full,
+                                        sba_stream_t stream);
+
+/*
  * sba_blocksparse_attn_fwd -- attention restricted by SparseMask bounds.
  *
  * Defined by: "ejkernel.kernels._triton.blocksparse_attention._mask" (module source

@@ -8,7 +8,8 @@ fallback: if ``libsba.so`` is missing or a tensor is not on a CUDA device the ca
 raises.
 
 Entry points (same names as the C ABI without the ``sba_`` prefix):
-  nsa_select_fwd, sparse_mask_bounds, blocksparse_attn_fwd, ragged_decode_fwd,
+  nsa_select_fwd, sparse_mask_bounds (forward and dK/dV bounds), blocksparse_attn_fwd,
+  ragged_decode_fwd,
   ragged_decode_fwd_noalloc, ragged_decode_workspace_size, ragged_flash_attention_fwd,
   ragged_flash_attention_workspace_size, check_error.
 """
@@ -31,6 +32,7 @@ __all__ = [
 
 EXPORTED_SYMBOLS = (
     "sba_version", "sba_last_error", "sba_nsa_select_fwd", "sba_sparse_mask_bounds",
+    "sba_sparse_mask_dkdv_bounds",
     "sba_blocksparse_attn_fwd", "sba_ragged_decode_workspace_size", "sba_ragged_decode_fwd",
     "sba_ragged_decode_fwd_noalloc", "sba_ragged_flash_attention_workspace_size",
     "sba_ragged_flash_attention_fwd", "sba_check_error",
@@ -73,6 +75,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sba_sparse_mask_bounds.argtypes = [i32p, i32p, i32p, i32p, ci, ci, ci, ci, ci, ci, ci, ci,
                                            ci, i32p, i32p, i32p, i32p, vp]
     lib.sba_sparse_mask_bounds.restype = ci
+    lib.sba_sparse_mask_dkdv_bounds.argtypes = [i32p, i32p, i32p, i32p, ci, ci, ci, ci, ci, ci, ci,
+                                                ci, ci, i32p, i32p, i32p, i32p, vp]
+    lib.sba_sparse_mask_dkdv_bounds.restype = ci
     lib.sba_blocksparse_attn_fwd.argtypes = [vp, vp, vp, i32p, i32p, i32p, i32p, i32p, i32p, i32p,
                                              i32p, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, ci, cf,
                                              vp, f32p, vp]
@@ -174,9 +179,11 @@ def nsa_select_fwd(q, k, v, block_indices, block_counts, block_size, *, cu_seqle
 
 def sparse_mask_bounds(q_positions, q_segment_ids, kv_positions, kv_segment_ids, q_blocksize,
                        kv_blocksize, *, causal=True, window_left=-1, window_right=-1,
-                       padding_segment_id=-1):
-    """SparseMask forward bounds: returns (lower, upper, lower_full, upper_full), each
-    int32 [B, 1, ceil(Tq / q_blocksize)]."""
+                       padding_segment_id=-1, calculate_dkdv_mask=False):
+    """SparseMask bounds: returns (lower, upper, lower_full, upper_full), each int32
+    [B, 1, ceil(Tq / q_blocksize)] (forward / dQ: key/value block ranges per query
+    block), or with ``calculate_dkdv_mask`` [B, 1, ceil(Tkv / kv_blocksize)] (dK/dV:
+    query block ranges per key/value block)."""
     lib = load_library()
     for name, t in (("q_positions", q_positions), ("q_segment_ids", q_segment_ids),
                     ("kv_positions", kv_positions), ("kv_segment_ids", kv_segment_ids)):
@@ -184,9 +191,10 @@ def sparse_mask_bounds(q_positions, q_segment_ids, kv_positions, kv_segment_ids,
     dev = _dev(q_positions, q_segment_ids, kv_positions, kv_segment_ids)
     B, Tq = q_positions.shape
     Tkv = kv_positions.shape[1]
-    nbq = -(-Tq // q_blocksize)
-    outs = [torch.empty((B, 1, nbq), dtype=torch.int32, device=dev) for _ in range(4)]
-    _check(lib.sba_sparse_mask_bounds(
+    nb = -(-Tkv // kv_blocksize) if calculate_dkdv_mask else -(-Tq // q_blocksize)
+    outs = [torch.empty((B, 1, nb), dtype=torch.int32, device=dev) for _ in range(4)]
+    fn = lib.sba_sparse_mask_dkdv_bounds if calculate_dkdv_mask else lib.sba_sparse_mask_bounds
+    _check(fn(
         _ptr(q_positions), _ptr(q_segment_ids), _ptr(kv_positions), _ptr(kv_segment_ids),
         B, Tq, Tkv, int(q_blocksize), int(kv_blocksize), int(bool(causal)), int(window_left),
         int(window_right), int(padding_segment_id), *[_ptr(o) for o in outs], _stream(dev)))

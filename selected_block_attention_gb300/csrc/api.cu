@@ -123,7 +123,28 @@ int sba_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const int
   SBA_SUPPORT((long long)B * ((Tq + q_block - 1) / q_block) < (1LL << 31), "too many blocks");
   return launch_sparse_mask_bounds(q_pos, q_seg, kv_pos, kv_seg, B, Tq, Tkv, q_block, kv_block,
                                    causal ? 1 : 0, window_left, window_right, padding_segment_id,
-                                   lower, upper, lower_full, upper_full,
+                                   lower, upper, lower_full, upper_full, 0,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sba_sparse_mask_dkdv_bounds(const int32_t* q_pos, const int32_t* q_seg,
+                                const int32_t* kv_pos, const int32_t* kv_seg, int B, int Tq,
+                                int Tkv, int q_block, int kv_block, int causal, int window_left,
+                                int window_right, int padding_segment_id, int32_t* lower,
+                                int32_t* upper, int32_t* lower_full, int32_t* upper_full,
+                                sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q_pos && q_seg && kv_pos && kv_seg && lower && upper && lower_full && upper_full,
+              "null pointer");
+  SBA_REQUIRE(B >= 1 && Tq >= 1 && Tkv >= 1, "sizes must be positive");
+  SBA_REQUIRE(q_block >= 1 && kv_block >= 1, "block sizes must be positive");
+  SBA_REQUIRE(window_left >= -1 && window_right >= -1, "windows must be >= -1");
+  SBA_SUPPORT(q_block <= 4096 && kv_block <= 4096, "block sizes must be <= 4096");
+  SBA_SUPPORT(B <= 65535, "B must be <= 65535");
+  SBA_SUPPORT((long long)B * ((Tkv + kv_block - 1) / kv_block) < (1LL << 31), "too many blocks");
+  return launch_sparse_mask_bounds(q_pos, q_seg, kv_pos, kv_seg, B, Tq, Tkv, q_block, kv_block,
+                                   causal ? 1 : 0, window_left, window_right, padding_segment_id,
+                                   lower, upper, lower_full, upper_full, 1,
                                    reinterpret_cast<cudaStream_t>(stream));
 }
 

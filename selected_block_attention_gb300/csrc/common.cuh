@@ -43,7 +43,7 @@ int launch_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const 
                               const int32_t* kv_seg, int B, int Tq, int Tkv, int q_block,
                               int kv_block, int causal, int window_left, int window_right,
                               int pad_id, int32_t* lower, int32_t* upper, int32_t* lower_full,
-                              int32_t* upper_full, cudaStream_t stream);
+                              int32_t* upper_full, int dkdv, cudaStream_t stream);
 int launch_blocksparse_attn(const void* q, const void* k, const void* v, const int32_t* q_pos,
                             const int32_t* q_seg, const int32_t* kv_pos, const int32_t* kv_seg,
                             const int32_t* lower, const int32_t* upper, const int32_t* lower_full,

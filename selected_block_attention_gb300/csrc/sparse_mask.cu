@@ -1,14 +1,15 @@
-// SparseMask block bounds (forward pass, query = outer operand).
+// SparseMask block bounds: forward / dQ (query blocks outer) and dK/dV (key/value blocks
+// outer).
 //
 // Follows "ejkernel.kernels._triton.blocksparse_attention._mask" (module source page):
-// kernel _compute_sparse_mask and the padding / padding-segment remap / clip fix-up
-// of define_sparse_mask_fn, fused into one launch.
+// kernel _compute_sparse_mask (both choices of outer operand) and the padding /
+// padding-segment remap / clip fix-up of define_sparse_mask_fn, fused into one launch.
 //
-// Layout of the work: grid (ceil(NBq / kWarps), B); warp w of a CTA owns one query
-// block.  The CTA sweeps the key blocks of its batch row in chunks: every warp
-// summarises key blocks (min/max of positions and remapped segment ids) with
+// Layout of the work: grid (ceil(NB_outer / kWarps), B); warp w of a CTA owns one
+// outer block.  The CTA sweeps the inner blocks of its batch row in chunks: every warp
+// summarises inner blocks (min/max of positions and remapped segment ids) with
 // coalesced 16-byte loads and warp min/max reductions into shared memory, then each
-// warp tests its query block against the chunk with one key block per lane and
+// warp tests its outer block against the chunk with one inner block per lane and
 // folds the lane results with warp min/max reductions.  Integer results are exact.
 #include <climits>
 
@@ -22,7 +23,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kChunk = 1024;  // key-block summaries held in shared memory at once
+constexpr int kChunk = 1024;  // inner-block summaries held in shared memory at once
 
 struct BlockSummary {
   int pos_min, pos_max, seg_min, seg_max;
@@ -74,42 +75,79 @@ __device__ __forceinline__ BlockSummary summarize_block(const int* __restrict__ 
   return r;
 }
 
+// Position tests of one (outer block, inner block) pair, as the page's kernel states
+// them for each choice of outer operand (kQueryOuter: the query block is outer).
+template <bool kQueryOuter>
+__device__ __forceinline__ void position_tests(bool causal, int window_left, int window_right,
+                                               long long o_min, long long o_max, long long i_min,
+                                               long long i_max, bool& attend, bool& full) {
+  attend = true;
+  full = true;
+  if (kQueryOuter) {
+    if (causal) { attend = o_max >= i_min; full = o_min >= i_max; }
+    if (window_left >= 0) {
+      attend = attend && (i_min >= o_min - window_left);
+      full = full && (i_min >= o_max - window_left);
+    }
+    if (window_right >= 0) {
+      attend = attend && (i_max <= o_max + window_right);
+      full = full && (i_max <= o_min + window_right);
+    }
+  } else {
+    if (causal) { attend = i_max >= o_min; full = i_min >= o_max; }
+    if (window_left >= 0) {
+      attend = attend && (i_max >= o_min - window_left);
+      full = full && (i_min >= o_min - window_left);
+    }
+    if (window_right >= 0) {
+      attend = attend && (i_min <= o_max + window_right);
+      full = full && (i_max <= o_max + window_right);
+    }
+  }
+}
+
+// One outer side and one inner side: token arrays of one batch row set, their length,
+// block size, block count and the position that pads them to a block multiple.
+struct Side {
+  const int* pos;
+  const int* seg;
+  int T, block, nb, pos_fill;
+};
+
+template <bool kQueryOuter>
 __global__ void __launch_bounds__(kThreads)
-sparse_mask_bounds_kernel(const int* __restrict__ q_pos, const int* __restrict__ q_seg,
-                          const int* __restrict__ kv_pos, const int* __restrict__ kv_seg, int Tq,
-                          int Tkv, int q_block, int kv_block, int nbq, int nbkv, int causal,
-                          int window_left, int window_right, int pad_id, int* __restrict__ lower,
+sparse_mask_bounds_kernel(Side outer, Side inner, int causal, int window_left, int window_right,
+                          int pad_id, int pad_remap, int* __restrict__ lower,
                           int* __restrict__ upper, int* __restrict__ lower_full,
-                          int* __restrict__ upper_full, int vec_q, int vec_kv) {
+                          int* __restrict__ upper_full, int vec_outer, int vec_inner) {
   __shared__ int s_kmin[kChunk], s_kmax[kChunk], s_ksmin[kChunk], s_ksmax[kChunk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.y;
-  const int j = blockIdx.x * kWarps + warp;  // query block of this warp
-  const bool active = j < nbq;
-  const int pad_remap = nbkv * kv_block + 1;  // padded Tkv + 1
-  const int* qp = q_pos + (long long)b * Tq;
-  const int* qs = q_seg + (long long)b * Tq;
-  const int* kp = kv_pos + (long long)b * Tkv;
-  const int* ks = kv_seg + (long long)b * Tkv;
+  const int j = blockIdx.x * kWarps + warp;  // outer block of this warp
+  const bool active = j < outer.nb;
+  const int* op = outer.pos + (long long)b * outer.T;
+  const int* os = outer.seg + (long long)b * outer.T;
+  const int* ip = inner.pos + (long long)b * inner.T;
+  const int* is = inner.seg + (long long)b * inner.T;
+  const int nbi = inner.nb;
 
-  // Query (outer) block summary.
+  // Outer block summary.
   BlockSummary o{0, 0, 0, 0};
   bool all_pad = false;
   if (active) {
-    o = summarize_block(qp, qs, (long long)j * q_block, q_block, Tq, -1, pad_id, pad_remap,
-                        vec_q != 0);
+    o = summarize_block(op, os, (long long)j * outer.block, outer.block, outer.T, outer.pos_fill,
+                        pad_id, pad_remap, vec_outer != 0);
     all_pad = (o.seg_min == o.seg_max) && (o.seg_min == pad_remap);
   }
-  const bool use_window = window_left >= 0 || window_right >= 0;
   const long long o_min = o.pos_min, o_max = o.pos_max;
 
-  int up = 0, lo = nbkv, up_full = 0, lo_full = nbkv;
-  for (int c0 = 0; c0 < nbkv; c0 += kChunk) {
-    const int cn = min(kChunk, nbkv - c0);
+  int up = 0, lo = nbi, up_full = 0, lo_full = nbi;
+  for (int c0 = 0; c0 < nbi; c0 += kChunk) {
+    const int cn = min(kChunk, nbi - c0);
     __syncthreads();
     for (int i = warp; i < cn; i += kWarps) {
-      BlockSummary s = summarize_block(kp, ks, (long long)(c0 + i) * kv_block, kv_block, Tkv,
-                                       INT_MAX, pad_id, pad_remap, vec_kv != 0);
+      BlockSummary s = summarize_block(ip, is, (long long)(c0 + i) * inner.block, inner.block,
+                                       inner.T, inner.pos_fill, pad_id, pad_remap, vec_inner != 0);
       if (lane == 0) {
         s_kmin[i] = s.pos_min; s_kmax[i] = s.pos_max;
         s_ksmin[i] = s.seg_min; s_ksmax[i] = s.seg_max;
@@ -118,26 +156,13 @@ sparse_mask_bounds_kernel(const int* __restrict__ q_pos, const int* __restrict__
     __syncthreads();
     if (!active || all_pad) continue;
     for (int i = lane; i < cn; i += 32) {
-      const long long k_min = s_kmin[i], k_max = s_kmax[i];
-      const int ks_min = s_ksmin[i], ks_max = s_ksmax[i];
-      const bool attend_seg = (ks_min <= o.seg_max) && (o.seg_min <= ks_max);
-      const bool full_seg = (o.seg_min == o.seg_max) && (ks_min == ks_max);
-      bool attend_pos = true, full_pos = true;
-      if (causal) {
-        attend_pos = o_max >= k_min;
-        full_pos = o_min >= k_max;
-      }
-      if (use_window) {
-        if (window_left >= 0) {
-          attend_pos = attend_pos && (k_min >= o_min - window_left);
-          full_pos = full_pos && (k_min >= o_max - window_left);
-        }
-        if (window_right >= 0) {
-          attend_pos = attend_pos && (k_max <= o_max + window_right);
-          full_pos = full_pos && (k_max <= o_min + window_right);
-        }
-      }
-      const bool attend = attend_pos && attend_seg && !(ks_min == pad_remap);
+      const int is_min = s_ksmin[i], is_max = s_ksmax[i];
+      const bool attend_seg = (is_min <= o.seg_max) && (o.seg_min <= is_max);
+      const bool full_seg = (o.seg_min == o.seg_max) && (is_min == is_max);
+      bool attend_pos, full_pos;
+      position_tests<kQueryOuter>(causal != 0, window_left, window_right, o_min, o_max,
+                                  s_kmin[i], s_kmax[i], attend_pos, full_pos);
+      const bool attend = attend_pos && attend_seg && !(is_min == pad_remap);
       const bool full = full_seg && full_pos && attend;
       const int blk = c0 + i;
       if (attend) { up = max(up, blk + 1); lo = min(lo, blk); }
@@ -150,17 +175,17 @@ sparse_mask_bounds_kernel(const int* __restrict__ q_pos, const int* __restrict__
   up_full = __reduce_max_sync(0xffffffffu, up_full);
   lo_full = __reduce_min_sync(0xffffffffu, lo_full);
   if (lane != 0) return;
-  const long long out = (long long)b * nbq + j;
+  const long long out = (long long)b * outer.nb + j;
   if (all_pad) {
     lower[out] = 0; upper[out] = 0; lower_full[out] = 0; upper_full[out] = 0;
     return;
   }
   // Clip / order fix-up.
-  lo = min(max(lo, 0), nbkv);
-  up = min(max(up, 0), nbkv);
+  lo = min(max(lo, 0), nbi);
+  up = min(max(up, 0), nbi);
   lo = min(lo, up);
-  lo_full = max(min(max(lo_full, 0), nbkv), lo);
-  up_full = min(max(min(max(up_full, 0), nbkv), lo_full), up);
+  lo_full = max(min(max(lo_full, 0), nbi), lo);
+  up_full = min(max(min(max(up_full, 0), nbi), lo_full), up);
   lower[out] = lo; upper[out] = up; lower_full[out] = lo_full; upper_full[out] = up_full;
 }
 
@@ -177,16 +202,26 @@ int launch_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const 
                               const int32_t* kv_seg, int B, int Tq, int Tkv, int q_block,
                               int kv_block, int causal, int window_left, int window_right,
                               int pad_id, int32_t* lower, int32_t* upper, int32_t* lower_full,
-                              int32_t* upper_full, cudaStream_t stream) {
+                              int32_t* upper_full, int dkdv, cudaStream_t stream) {
   const int nbq = (Tq + q_block - 1) / q_block;
   const int nbkv = (Tkv + kv_block - 1) / kv_block;
   auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   const int vec_q = (Tq % 4 == 0) && (q_block % 4 == 0) && al16(q_pos) && al16(q_seg);
   const int vec_kv = (Tkv % 4 == 0) && (kv_block % 4 == 0) && al16(kv_pos) && al16(kv_seg);
-  dim3 grid((nbq + kWarps - 1) / kWarps, B);
-  sparse_mask_bounds_kernel<<<grid, kThreads, 0, stream>>>(
-      q_pos, q_seg, kv_pos, kv_seg, Tq, Tkv, q_block, kv_block, nbq, nbkv, causal, window_left,
-      window_right, pad_id, lower, upper, lower_full, upper_full, vec_q, vec_kv);
+  const Side qside{q_pos, q_seg, Tq, q_block, nbq, -1};
+  const Side kvside{kv_pos, kv_seg, Tkv, kv_block, nbkv, INT_MAX};
+  const int pad_remap = nbkv * kv_block + 1;  // padded Tkv + 1
+  if (dkdv) {
+    dim3 grid((nbkv + kWarps - 1) / kWarps, B);
+    sparse_mask_bounds_kernel<false><<<grid, kThreads, 0, stream>>>(
+        kvside, qside, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
+        lower_full, upper_full, vec_kv, vec_q);
+  } else {
+    dim3 grid((nbq + kWarps - 1) / kWarps, B);
+    sparse_mask_bounds_kernel<true><<<grid, kThreads, 0, stream>>>(
+        qside, kvside, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
+        lower_full, upper_full, vec_q, vec_kv);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "sparse_mask_bounds launch");
   return SBA_OK;

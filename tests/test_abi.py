@@ -70,6 +70,15 @@ def test_argument_validation_without_launch(lib):
     r = lib.sba_sparse_mask_bounds(fake, fake, fake, fake, 1, 64, 64, 16, 16, 1, -2, 0, -1, fake,
                                    fake, fake, fake, None)
     assert r == -1
+    r = lib.sba_sparse_mask_dkdv_bounds(fake, fake, fake, fake, 1, 64, 64, 16, 16, 1, -2, 0, -1,
+                                        fake, fake, fake, fake, None)
+    assert r == -1
+    r = lib.sba_sparse_mask_dkdv_bounds(fake, fake, fake, fake, 1, 64, 64, 16, 8192, 1, -1, -1,
+                                        -1, fake, fake, fake, fake, None)
+    assert r == -2
+    r = lib.sba_sparse_mask_dkdv_bounds(fake, None, fake, fake, 1, 64, 64, 16, 16, 1, -1, -1, -1,
+                                        fake, fake, fake, fake, None)
+    assert r == -1 and b"null" in lib.sba_last_error()
     # block-sparse: q_block must be 128
     r = lib.sba_blocksparse_attn_fwd(fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
                                      fake, 1, 256, 4, 2, 128, 64, 64, 1, -1, -1, -1, 0.0, fake,
@@ -119,10 +128,10 @@ def test_workspace_size_grows_with_window():
 
 
 def test_multi_query_workspace_arithmetic():
-    """Split count of the multi-query workspace: a 16-row tile spans queries
-    i_lo..i_hi (at most 16), so its key range is at most left + min(Q, right + 16)
-    keys with both window bounds, left + Q with only a left bound, S without one;
-    Q = 1 gives the decode workspace."""
+    """Split count of the multi-query workspace (1024 keys per split): a 16-row tile
+    spans queries i_lo..i_hi (at most 16), so its key range is at most
+    left + min(Q, right + 16) keys with both window bounds, left + Q with only a left
+    bound, S without one; Q = 1 gives the decode workspace."""
     import selected_block_attention_gb300 as sba
 
     try:
@@ -131,16 +140,16 @@ def test_multi_query_workspace_arithmetic():
         pytest.skip("library not built")
     ws = lib.sba_ragged_flash_attention_workspace_size
     row = 4 * 32 * (128 + 2) * 4      # Q * Hq * (D + 2) fp32 per row and split
-    assert ws(64, 4, 32, 32768, 128, 4096, 0) == 64 * 9 * row
-    assert ws(64, 4, 32, 32768, 128, 4096, -1) == 64 * 9 * row
-    assert ws(64, 4, 32, 32768, 128, -1, 0) == 64 * 64 * row
-    assert ws(64, 4, 32, 32768, 128, 508, 0) == 64 * 1 * row     # 512 keys
-    assert ws(64, 4, 32, 32768, 128, 509, 0) == 64 * 2 * row     # 513 keys
+    assert ws(64, 4, 32, 32768, 128, 4096, 0) == 64 * 5 * row     # 4100 keys
+    assert ws(64, 4, 32, 32768, 128, 4096, -1) == 64 * 5 * row
+    assert ws(64, 4, 32, 32768, 128, -1, 0) == 64 * 32 * row
+    assert ws(64, 4, 32, 32768, 128, 1020, 0) == 64 * 1 * row     # 1024 keys
+    assert ws(64, 4, 32, 32768, 128, 1021, 0) == 64 * 2 * row     # 1025 keys
     row64 = 64 * 32 * (128 + 2) * 4
-    assert ws(2, 64, 32, 32768, 128, 1000, 8) == 2 * 2 * row64  # 1000 + 24 keys
-    assert ws(2, 64, 32, 32768, 128, 1000, -1) == 2 * 3 * row64  # 1000 + 64 keys
-    assert ws(2, 64, 32, 32768, 128, 1000, 40) == 2 * 3 * row64  # 1000 + 56 keys
-    assert ws(2, 64, 32, 32768, 128, 1000, 60) == 2 * 3 * row64  # 1000 + 64 keys
-    assert ws(2, 64, 32, 1000, 128, -1, 60) == 2 * 2 * row64     # S = 1000
+    assert ws(2, 64, 32, 32768, 128, 1000, 8) == 2 * 1 * row64  # 1000 + 24 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, -1) == 2 * 2 * row64  # 1000 + 64 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 40) == 2 * 2 * row64  # 1000 + 56 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 60) == 2 * 2 * row64  # 1000 + 64 keys
+    assert ws(2, 64, 32, 1000, 128, -1, 60) == 2 * 1 * row64     # S = 1000
     for wl in (-1, 0, 4096, 5000):
         assert ws(64, 1, 32, 32768, 128, wl, 7) == lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, wl)

@@ -1,4 +1,4 @@
-"""GPU parity: SparseMask bounds kernel vs the oracle, bit-exact."""
+"""GPU parity: SparseMask bounds kernel (forward and dK/dV) vs the oracle, bit-exact."""
 
 import os
 
@@ -89,3 +89,51 @@ def test_many_kv_blocks_chunked(sba):
     pos = np.arange(T)[None]
     seg = (np.arange(T) // 5000)[None]
     _check(sba, pos, seg, pos, seg, 512, 32, causal=True, window_left=2000, window_right=-1)
+
+
+# --------------------------------------------------------------------------- dK/dV bounds
+
+def test_dkdv_page_example_transposed(sba):
+    pos = np.arange(256)[None]
+    seg = np.zeros((1, 256), np.int64)
+    lo, up, lof, upf = _check(sba, pos, seg, pos, seg, 64, 64, causal=True,
+                              calculate_dkdv_mask=True)
+    assert lo[0, 0].tolist() == [0, 1, 2, 3] and up[0, 0].tolist() == [4] * 4
+    assert lof[0, 0].tolist() == [1, 2, 3, 4] and upf[0, 0].tolist() == [4] * 4
+
+
+def test_dkdv_full_size_workload(sba):
+    """The forward workload's inputs (B=4, T=16384, block 128, window (1024, 0))."""
+    m = workloads.mask(device="cpu")
+    _check(sba, m.q_positions.numpy(), m.q_segment_ids.numpy(), m.kv_positions.numpy(),
+           m.kv_segment_ids.numpy(), 128, 128, causal=True, window_left=1024, window_right=0,
+           padding_segment_id=-1, calculate_dkdv_mask=True)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_dkdv_random_ragged(sba, seed):
+    rng = np.random.default_rng(100 + seed)
+    B = int(rng.integers(1, 4))
+    Tq, Tkv = int(rng.integers(1, 700)), int(rng.integers(1, 700))
+    qb, kb = int(rng.choice([7, 16, 33, 64, 128])), int(rng.choice([5, 16, 32, 100, 128]))
+    qp = np.sort(rng.integers(-5, 900, size=(B, Tq)), axis=1)
+    kp = np.sort(rng.integers(-5, 900, size=(B, Tkv)), axis=1)
+    if seed % 2:
+        rng.shuffle(kp, axis=1)
+    qs = np.sort(rng.integers(0, 6, size=(B, Tq)), axis=1)
+    ks = np.sort(rng.integers(0, 6, size=(B, Tkv)), axis=1)
+    qs[:, -int(rng.integers(0, 40)) or Tq:] = -1
+    ks[:, -int(rng.integers(0, 40)) or Tkv:] = -1
+    wl = int(rng.choice([-1, 0, 37, 128]))
+    wr = int(rng.choice([-1, 0, 64]))
+    _check(sba, qp, qs, kp, ks, qb, kb, causal=bool(seed % 3), window_left=wl, window_right=wr,
+           padding_segment_id=-1, calculate_dkdv_mask=True)
+
+
+def test_dkdv_many_query_blocks_chunked(sba):
+    """More query blocks (the inner operand here) than one shared-memory chunk holds."""
+    T = 40000
+    pos = np.arange(T)[None]
+    seg = (np.arange(T) // 5000)[None]
+    _check(sba, pos, seg, pos, seg, 32, 512, causal=True, window_left=2000, window_right=-1,
+           calculate_dkdv_mask=True)
