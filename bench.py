@@ -106,9 +106,11 @@ def nsa_work(w):
 
 
 def union_tiles(w, rows=128, tile_keys=64):
-    """Tiles the union walk executes: per (group of NT = rows // G consecutive tokens,
-    KV head), the number of distinct selected blocks (each block of <= 64 keys is one
-    64-key tile)."""
+    """Tiles the union walk executes: per (item, KV head), the number of distinct selected
+    blocks (each block of <= 64 keys is one 64-key tile).  An item holds NT = rows // G
+    tokens: for G >= 8 the tokens of each window of 8 * NT tokens ranked by selection
+    count (clipped to [0, S], ties by position), NT consecutive ranks per item, as the
+    kernel forms them; otherwise NT consecutive tokens."""
     idx = w.block_indices.cpu().numpy().astype(np.int64)
     B, T, Hkv, S = idx.shape
     G = w.q.shape[2] // Hkv
@@ -129,7 +131,21 @@ def union_tiles(w, rows=128, tile_keys=64):
         valid &= idx * bs <= t_rel
     tok = (np.arange(B)[:, None] * T + np.arange(T)[None, :])[:, :, None, None]
     first_row = np.broadcast_to(tok - t_rel + idx * bs, idx.shape)  # absolute first key row
-    group = np.broadcast_to(tok // NT, idx.shape)
+    if G >= 8:
+        wn = 8 * NT
+        n_tok = B * T
+        nw = -(-n_tok // wn)
+        cnt = np.full((nw * wn, Hkv), 0xFFFF, dtype=np.int64)
+        cnt[:n_tok] = np.clip(counts.reshape(n_tok, Hkv), 0, S)
+        li = np.arange(nw * wn) % wn
+        key = (cnt << 8) | li[:, None]
+        order = np.argsort(key.reshape(nw, wn, Hkv), axis=1, kind="stable")
+        rank = np.empty_like(order)
+        np.put_along_axis(rank, order, np.arange(wn)[None, :, None], axis=1)
+        grp = (np.arange(nw)[:, None, None] * 8 + rank // NT).reshape(nw * wn, Hkv)[:n_tok]
+        group = np.broadcast_to(grp.reshape(B, T, Hkv)[..., None], idx.shape)
+    else:
+        group = np.broadcast_to(tok // NT, idx.shape)
     head = np.broadcast_to(np.arange(Hkv)[None, None, :, None], idx.shape)
     item = group[valid] * Hkv + head[valid]
     pairs = np.unique(item * (B * T + bs) + first_row[valid])  # distinct (item, block)

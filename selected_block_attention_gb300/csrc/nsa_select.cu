@@ -79,6 +79,7 @@ struct Params {
   int count_scalar, S, num_seqs;
   int B, T, Hq, Hkv, G, causal, bs;
   int NT, rows;  // tokens per item, rows used (NT * G <= 128)
+  int ranked;    // items are formed from count-ranked windows (see build_item)
   float scale, scale_log2;
   int n_items, n_tok;
 };
@@ -86,7 +87,8 @@ struct Params {
 // One union-walk item as the builder hands it to the other roles.
 struct Item {
   int g, hkv, n_union, n_tiles;
-  unsigned tok_valid;              // bit i: token g * NT + i exists
+  unsigned tok_valid;              // bit i: token slot i holds a token
+  int tok[kMaxNT];                 // token of slot i (-1: none)
   int limit[kMaxNT];               // last key row (absolute) token i may see; -1 if none
   int ux[kMaxUnion];               // first key row (absolute) of each union block
   unsigned short ubits[kMaxUnion]; // tokens of the group that selected it
@@ -184,16 +186,57 @@ __device__ __forceinline__ unsigned select_blocks(const Params& p, long long row
 }
 
 // ------------------------------------------------------------------ item builder
-// Forms the union of the selected blocks of tokens g*NT .. g*NT+NT-1 for KV head hkv.
+// Forms the union of the selected blocks of the item's NT tokens for KV head hkv.
 // Keys (first key row << 16 | token bit) are sorted by one warp (bitonic network in
 // shared memory); equal rows are merged by OR-ing their token bits.
+//
+// Tokens of an item: without ranking g*NT .. g*NT+NT-1.  With ranking the tokens of a
+// window of 8*NT consecutive tokens are ranked by their selection count (ties by
+// position) and item g takes ranks (g % 8)*NT .. (g % 8)*NT+NT-1 of window g / 8: tokens
+// that select few blocks share items with each other, so the unions (and the tiles every
+// row of an item walks) are smaller than for consecutive tokens.
 template <int BS>
 __device__ __forceinline__ void build_item(const Params& p, int g, int hkv, int lane,
                                            int& cached_seq, Item& it, uint64_t* keys) {
   const unsigned kFull = 0xffffffffu;
   const unsigned lt_mask = (1u << lane) - 1u;
-  const int tok = g * p.NT + lane;
-  const bool tv = lane < p.NT && tok < p.n_tok;
+  if (p.ranked) {
+    const int wn = 8 * p.NT;            // window of 8 items (64 or 128 tokens)
+    const int base = (g >> 3) * wn, r = g & 7;
+    constexpr int kPer = 128 / 32;      // tokens per lane for the largest window
+    int key[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int li = j * 32 + lane, t = base + li;
+      int cnt = 0xFFFF;                 // past the window / the tokens: ranked last
+      if (li < wn && t < p.n_tok) {
+        cnt = p.block_counts ? p.block_counts[(long long)t * p.Hkv + hkv] : p.count_scalar;
+        cnt = min(max(cnt, 0), p.S);
+      }
+      key[j] = (cnt << 8) | li;
+    }
+    int rank[kPer] = {0, 0, 0, 0};
+    for (int src = 0; src < 32; ++src) {
+#pragma unroll
+      for (int jj = 0; jj < kPer; ++jj) {
+        const int other = __shfl_sync(kFull, key[jj], src);
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) rank[j] += other < key[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int li = j * 32 + lane, t = base + li;
+      const int slot = rank[j] - r * p.NT;
+      if (li < wn && slot >= 0 && slot < p.NT) it.tok[slot] = t < p.n_tok ? t : -1;
+    }
+    if (lane >= p.NT && lane < kMaxNT) it.tok[lane] = -1;
+  } else {
+    if (lane < kMaxNT) it.tok[lane] = (lane < p.NT && g * p.NT + lane < p.n_tok) ? g * p.NT + lane : -1;
+  }
+  __syncwarp();
+  const int tok = lane < kMaxNT ? it.tok[lane] : -1;
+  const bool tv = lane < p.NT && tok >= 0;
   int seq0 = 0, slen = 0, trel = 0, cnt = 0, limit = -1;
   if (tv) {
     const int b = p.cu_seqlens ? 0 : tok / p.T;
@@ -212,11 +255,10 @@ __device__ __forceinline__ void build_item(const Params& p, int g, int hkv, int 
   for (int c = 0; c < kChunks; ++c) {
     const int idx = c * 32 + lane;
     ev[c] = -1;
-    if (idx < total) {
-      const int i = idx / p.S, j = idx - i * p.S;
-      const int trow = g * p.NT + i;
-      if (trow < p.n_tok) ev[c] = p.block_indices[((long long)trow * p.Hkv + hkv) * p.S + j];
-    }
+    if (c * 32 >= total) continue;  // warp-uniform
+    const int i = idx < total ? idx / p.S : 0, j = idx - i * p.S;
+    const int trow = __shfl_sync(kFull, tok, i);
+    if (idx < total && trow >= 0) ev[c] = p.block_indices[((long long)trow * p.Hkv + hkv) * p.S + j];
   }
   int n = 0;
 #pragma unroll
@@ -385,9 +427,20 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           uint8_t* vdst = kdst + C::kKBytes;
           if (pp < 0) {
             mbar_arrive_expect_tx(fb, q_box_bytes);
+            if (p.ranked) {
+              // one box (G heads) per token slot; an empty slot reads zeros past the end
+              for (int i = 0; i < p.NT; ++i) {
+                const int tk = it.tok[i] >= 0 ? it.tok[i] : p.n_tok;
 #pragma unroll
-            for (int pn = 0; pn < C::kPanels; ++pn)
-              tma_load_3d(kdst + pn * C::kQPanelBytes, &tm_q, fb, pn * 64, hkv * p.G, it.g * p.NT);
+                for (int pn = 0; pn < C::kPanels; ++pn)
+                  tma_load_3d(kdst + pn * C::kQPanelBytes + i * p.G * 128, &tm_q, fb, pn * 64,
+                              hkv * p.G, tk);
+              }
+            } else {
+#pragma unroll
+              for (int pn = 0; pn < C::kPanels; ++pn)
+                tma_load_3d(kdst + pn * C::kQPanelBytes, &tm_q, fb, pn * 64, hkv * p.G, it.g * p.NT);
+            }
           } else {
             mbar_arrive_expect_tx(fb, C::kStageBytes);
 #pragma unroll
@@ -685,7 +738,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const float L = l * a_me + oth.y * a_ot;
       const float a0 = w == 0 ? a_me : a_ot, a1 = w == 0 ? a_ot : a_me;
       constexpr int kOutHalf = D / 2;
-      const long long orow = (long long)(it.g * p.NT + ti) * p.Hq + (long long)it.hkv * p.G + h;
+      const long long orow = (long long)(row_ok ? it.tok[ti] : 0) * p.Hq + (long long)it.hkv * p.G + h;
       const float gate =
           (p.g_slc != nullptr && row_ok) ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.g_slc)[orow]) : 1.f;
       const float inv = L > 0.f ? gate / L : 0.f;
@@ -736,6 +789,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tmem_dealloc(tmem, C::kTmemCols);
   }
 }
+
 
 // ---------------------------------------------------------------------------- fp32
 constexpr int kF32Threads = 128;
@@ -868,7 +922,7 @@ int launch_bf16(const void* q, const void* k, const void* v, const Params& p, cu
     // rows (token-major, head-minor) of one item
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.n_tok};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hq * D * 2};
-    cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)p.NT};
+    cuuint32_t box[3] = {64, (cuuint32_t)p.G, (cuuint32_t)(p.ranked ? 1 : p.NT)};
     if (encode_tensor_map(&tq, dt, 3, const_cast<void*>(q), dims, strides, box,
                           CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return set_error(SBA_ERR_CUDA, "nsa_select: tensor map (q) failed");
@@ -947,10 +1001,15 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const void* g
   p.scale_log2 = scale * kLog2e;
   p.NT = std::min(kMaxNT, kRows / p.G);
   p.rows = p.NT * p.G;
+  p.ranked = 0;
   if ((long long)B * T * Hkv >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "nsa_select: too many items");
   p.n_tok = B * T;
   if (dtype == SBA_BF16) {
-    const long long groups = (p.n_tok + p.NT - 1) / p.NT;
+    // Count-ranked items need a token's Q rows to start a 1024-byte swizzle atom in the
+    // item's Q stage (G >= 8); smaller groups take consecutive tokens.
+    p.ranked = p.G >= 8 ? 1 : 0;
+    const long long groups = p.ranked ? (p.n_tok + 8 * p.NT - 1) / (8 * p.NT) * 8
+                                      : (p.n_tok + p.NT - 1) / p.NT;
     p.n_items = static_cast<int>(groups * Hkv);
     if (D == 128) return dispatch_bs<128>(block_size, q, k, v, p, stream);
     return dispatch_bs<64>(block_size, q, k, v, p, stream);
