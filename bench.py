@@ -335,6 +335,27 @@ def blocksparse_flops(w):
 
 
 # ----------------------------------------------------------------------------- arms
+def l2_read_gbs(sba, dev, stream, mb=48, reps=200):
+    """L2-to-SM read bandwidth from the library's probe: a 48 MB buffer (under half of
+    the 129 MB L2) read `reps` times (about 10 GB in all, so launch overhead is
+    negligible) with 16-byte L1-bypassing loads on every SM, after
+    one warm-up pass; best of 3 timings."""
+    buf = torch.ones(mb * (1 << 20) // 4, dtype=torch.int32, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    sba.l2_read_probe(buf, 1, sink)
+    best = None
+    for _ in range(3):
+        s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        sba.l2_read_probe(buf, reps, sink)
+        e0.record(stream)
+        e0.synchronize()
+        ms = s0.elapsed_time(e0)
+        best = ms if best is None else min(best, ms)
+    sba.check_error(dev)
+    return reps * buf.numel() * 4 / (best * 1e-3) / 1e9
+
+
 def run_cuda(args, rank, world, local_rank):
     import selected_block_attention_gb300 as sba
     from selected_block_attention_gb300 import _build
@@ -398,6 +419,13 @@ def run_cuda(args, rank, world, local_rank):
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
 
     log(f"e2e done: {e2e_ms:.4f} ms/step")
+    bw_l2 = l2_read_gbs(sba, dev, stream)
+    log(f"L2 read bandwidth {bw_l2:.0f} GB/s")
+    union_bytes = float(n_tiles) * 64 * w.q.shape[3] * 2 * 2  # K and V of every union tile
+    terms = {"tensor": flops / (peaks["bf16_tflops"] * 1e12) * 1e6,
+             "hbm": hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
+             "l2_gather": gather_bytes / (bw_l2 * 1e9) * 1e6}
+    t_roof = max(terms.values())
     rows = {} if args.no_rows else measure_rows(sba, dev, stream, flush, peaks, args)
 
     result = {
@@ -432,9 +460,14 @@ def run_cuda(args, rank, world, local_rank):
             "union_tiles": int(n_tiles),
             "executed_mma_tflops": round(exec_flops / (ms * 1e-3) / 1e12, 1),
             "executed_mma_frac": round(exec_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
-            "terms_us": {
-                "tensor": round(flops / (peaks["bf16_tflops"] * 1e12) * 1e6, 2),
-                "hbm": round(hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6, 2)},
+            # t_roof = max(F_alg / P_tensor, B_hbm / BW_hbm, B_gather / BW_l2) with the
+            # per-token selection gather and the probe's L2 read bandwidth
+            "terms_us": {k: round(v, 2) for k, v in terms.items()},
+            "l2_read_gbs": round(bw_l2, 1),
+            "t_roof_us": round(t_roof, 2),
+            "frac_t_roof": round(t_roof / (ms * 1e3), 4),
+            "union_gather_bytes": union_bytes,
+            "union_gather_us_at_l2": round(union_bytes / (bw_l2 * 1e9) * 1e6, 2),
             "hbm_achieved_gbs": round(hbm_bytes / (ms * 1e-3) / 1e9, 1),
             "hbm_frac": round(hbm_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "gathered_kv_bytes": gather_bytes,

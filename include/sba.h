@@ -296,6 +296,20 @@ SBA_API int sba_ragged_flash_attention_fwd(const void* q, const void* k, const v
                                            sba_stream_t stream);
 
 /*
+ * sba_l2_read_probe -- measurement helper for the roofline's L2 term; computes nothing
+ * of the attention method.
+ *
+ * Reads buf (bytes bytes) reps times with 16-byte loads that bypass L1, from four
+ * 512-thread blocks per SM, and XORs what it read into *sink (so no load is dead).
+ * With bytes at most half the L2 size, reps * bytes / elapsed time is the L2-to-SM read
+ * bandwidth.  buf: caller-owned device memory, 16-byte aligned, bytes a positive
+ * multiple of 16; sink: one caller-owned device word.  Returns SBA_ERR_INVALID_ARG
+ * otherwise.  Asynchronous on `stream`.
+ */
+SBA_API int sba_l2_read_probe(const void* buf, size_t bytes, int reps, uint32_t* sink,
+                              sba_stream_t stream);
+
+/*
  * sba_check_error -- synchronise `stream`, then read and clear the device-side error
  * word of every kernel of this library.  Returns SBA_OK, SBA_ERR_TIMEOUT (a kernel
  * gave up on a bounded internal wait and returned early), SBA_ERR_DEVICE_INPUT (a

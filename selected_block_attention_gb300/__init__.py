@@ -27,7 +27,7 @@ __all__ = [
     "SBAError", "load_library", "library_path", "nsa_select_fwd", "sparse_mask_bounds",
     "blocksparse_attn_fwd", "ragged_decode_fwd", "ragged_decode_fwd_noalloc",
     "ragged_decode_workspace_size", "ragged_flash_attention_fwd",
-    "ragged_flash_attention_workspace_size", "check_error", "EXPORTED_SYMBOLS",
+    "ragged_flash_attention_workspace_size", "l2_read_probe", "check_error", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -35,7 +35,7 @@ EXPORTED_SYMBOLS = (
     "sba_sparse_mask_dkdv_bounds",
     "sba_blocksparse_attn_fwd", "sba_ragged_decode_workspace_size", "sba_ragged_decode_fwd",
     "sba_ragged_decode_fwd_noalloc", "sba_ragged_flash_attention_workspace_size",
-    "sba_ragged_flash_attention_fwd", "sba_check_error",
+    "sba_ragged_flash_attention_fwd", "sba_l2_read_probe", "sba_check_error",
 )
 
 SBA_BF16, SBA_F32 = 0, 1
@@ -96,6 +96,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                    cf, ci, ci, cf, f32p, ci, ci, vp, f32p, vp,
                                                    csz, vp]
     lib.sba_ragged_flash_attention_fwd.restype = ci
+    lib.sba_l2_read_probe.argtypes = [vp, csz, ci, vp, vp]
+    lib.sba_l2_read_probe.restype = ci
     lib.sba_check_error.argtypes = [vp]
     lib.sba_check_error.restype = ci
     if path == _build.LIB_PATH:
@@ -333,6 +335,15 @@ def ragged_flash_attention_fwd(q, k, v, sequence_start, sequence_end, *, softmax
         float(logits_soft_cap or 0.0), _ptr(sink_bias), num_sinks, per_head, _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
     return out, lse
+
+
+def l2_read_probe(buf, reps, sink):
+    """Measurement helper (not part of the method): read ``buf`` (a CUDA tensor) ``reps``
+    times with 16-byte L1-bypassing loads on every SM; XOR of the data into ``sink``
+    (an int32 CUDA tensor of one element)."""
+    _dev(buf, sink)
+    _check(load_library().sba_l2_read_probe(_ptr(buf), buf.numel() * buf.element_size(), int(reps),
+                                            _ptr(sink), _stream(buf.device)))
 
 
 def check_error(device=None):

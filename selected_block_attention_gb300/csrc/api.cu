@@ -249,6 +249,16 @@ int sba_ragged_flash_attention_fwd(const void* q, const void* k, const void* v,
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+int sba_l2_read_probe(const void* buf, size_t bytes, int reps, uint32_t* sink,
+                      sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(buf && sink, "null pointer");
+  SBA_REQUIRE(aligned16(buf) && bytes >= 16 && bytes % 16 == 0,
+              "buf must be 16-byte aligned and bytes a positive multiple of 16");
+  SBA_REQUIRE(reps >= 1, "reps must be >= 1");
+  return launch_l2_read_probe(buf, bytes, reps, sink, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int sba_check_error(sba_stream_t stream) {
   g_last_error.clear();
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

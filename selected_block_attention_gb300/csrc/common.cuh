@@ -66,6 +66,9 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
                      int num_sinks, int sink_per_head, void* out, float* lse, void* workspace,
                      cudaStream_t stream);
 
+int launch_l2_read_probe(const void* buf, size_t bytes, int reps, unsigned* sink,
+                         cudaStream_t stream);
+
 // Driver entry point for tensor-map encoding, resolved once through the runtime.
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32_t rank,
                            void* gaddr, const cuuint64_t* dims, const cuuint64_t* strides_bytes,

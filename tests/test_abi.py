@@ -112,6 +112,11 @@ def test_argument_validation_without_launch(lib):
     args[15], args[16] = fake, 17
     assert lib.sba_ragged_flash_attention_fwd(*args) == -2
     assert lib.sba_ragged_flash_attention_workspace_size(4, 0, 8, 1024, 128, 100, 0) == 0
+    # L2 probe: misaligned buffer, size not a multiple of 16, no sink
+    assert lib.sba_l2_read_probe(c.c_void_p(0x10008), 4096, 1, fake, None) == -1
+    assert lib.sba_l2_read_probe(fake, 4100, 1, fake, None) == -1
+    assert lib.sba_l2_read_probe(fake, 4096, 1, None, None) == -1
+    assert lib.sba_l2_read_probe(fake, 4096, 0, fake, None) == -1
 
 
 def test_workspace_size_grows_with_window():

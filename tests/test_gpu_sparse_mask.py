@@ -137,3 +137,16 @@ def test_dkdv_many_query_blocks_chunked(sba):
     seg = (np.arange(T) // 5000)[None]
     _check(sba, pos, seg, pos, seg, 32, 512, causal=True, window_left=2000, window_right=-1,
            calculate_dkdv_mask=True)
+
+
+def test_l2_read_probe_reads_everything(sba):
+    """The roofline's L2 probe XORs every 32-bit word it reads into its sink: an even
+    number of passes over any buffer gives 0, an odd number the XOR of the buffer."""
+    vals = (np.arange(1 << 16, dtype=np.int64) * 2654435761) % (1 << 31)
+    buf = torch.from_numpy(vals.astype(np.int32)).to(DEV)
+    want = int(np.bitwise_xor.reduce(vals.astype(np.uint32)))
+    for reps, expect in ((1, want), (2, 0), (3, want)):
+        sink = torch.zeros(1, dtype=torch.int32, device=DEV)
+        sba.l2_read_probe(buf, reps, sink)
+        sba.check_error()
+        assert int(sink.cpu().numpy().astype(np.uint32)[0]) == expect
