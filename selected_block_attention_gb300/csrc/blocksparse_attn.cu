@@ -452,21 +452,28 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             }
           }
         }
+        // row maximum: eight chains of three-input max (two new scores per instruction)
         float mx[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) mx[j] = x[j];
 #pragma unroll
-        for (int j = 8; j < KB; ++j) mx[j & 7] = fmaxf(mx[j & 7], x[j]);
-        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * p.scale_log2;
+        for (int j = 8; j < KB; j += 16) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = fmax3f(mx[u], x[j + 2 * u], x[j + 2 * u + 1]);
+        }
+        const float tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                                  fmaxf(mx[6], mx[7])) * p.scale_log2;
         // lazy online softmax: move the reference max only when it grows by > 2^8
         float m_new = m;
         if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
         const float alpha = (m == -INFINITY || m_new == m) ? (m_new == m ? 1.f : 0.f) : ex2(m - m_new);
-        // exponentials; P (bf16 pairs) over the S_w columns, 32 keys at a time
+        // exponentials; P (bf16 pairs) over the S_w columns, 32 keys at a time.  The
+        // argument x * scale - m and the row sum run two lanes per instruction.
         float psum = 0.f;
         {
-          float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
+          const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
+          const uint64_t negm2 = pack_f32x2(-m_new, -m_new);
 #pragma unroll
           for (int c = 0; c < KB / 32; ++c) {
             uint32_t pk[16];
@@ -475,10 +482,14 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               for (int j = 0; j < 16; ++j) pk[j] = 0u;
             } else {
 #pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float e = ex2(fmaf(x[c * 32 + j], p.scale_log2, -m_new));
-                x[c * 32 + j] = e;
-                ps8[j & 7] += e;
+              for (int j = 0; j < 32; j += 2) {
+                const uint64_t a2 = fma_f32x2(pack_f32x2(x[c * 32 + j], x[c * 32 + j + 1]), scale2, negm2);
+                float a0, a1;
+                unpack_f32x2(a2, a0, a1);
+                const float e0 = ex2(a0), e1 = ex2(a1);
+                x[c * 32 + j] = e0;
+                x[c * 32 + j + 1] = e1;
+                ps2[(j >> 1) & 3] = add_f32x2(ps2[(j >> 1) & 3], pack_f32x2(e0, e1));
               }
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -489,7 +500,10 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tmem_st_32x32b_x16_u_nw(s_col + c * 16, pk);
           }
           tmem_wait_st();
-          psum = ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+          const uint64_t s01 = add_f32x2(ps2[0], ps2[1]), s23 = add_f32x2(ps2[2], ps2[3]);
+          float lo, hi;
+          unpack_f32x2(add_f32x2(s01, s23), lo, hi);
+          psum = lo + hi;
         }
         if (t > 0) {
           // S_w(t) implies PV_w(t - 1) is done: O_w may be rescaled.  TMEM loads/stores
