@@ -60,6 +60,7 @@ struct Item {
   int b, hkv, qblk, h0, nh;  // heads h0 .. h0 + nh - 1 (nh = 1 or 2)
   int lo, up, lof, upf;      // kv blocks [lo, up); [lof, upf) need no token mask
   int n_tiles;               // = up - lo (one key block per tile)
+  int start, end;            // ragged mode: the row's key range
 };
 
 struct Params {
@@ -71,9 +72,12 @@ struct Params {
   const int* upper;
   const int* lower_full;
   const int* upper_full;
+  const int* seq_start;  // ragged mode: per batch row [start, end) of the key range
+  const int* seq_end;
   __nv_bfloat16* out;
   float* lse;
   int B, T, Hq, Hkv, G, nbq, causal, window_left, window_right, pad_id;
+  int q_rows, kv_rows;   // query / key rows per batch row (T and T; ragged: Q and S)
   float scale_log2;
   int n_pairs, n_items;
 };
@@ -130,7 +134,11 @@ __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, i
   nh = min(2, p.G - 2 * pair);
 }
 
-template <int D, int KB>
+// kRagged: the ragged multi-query form of the same computation (queries are the last Q
+// tokens of [start, end) of a KV cache, each with its own inclusive window); the key
+// range and the full blocks of a query block follow from start, end and the window, and
+// the per-row key range replaces the position / segment test.
+template <int D, int KB, bool kRagged>
 __global__ void __launch_bounds__(kThreads, 1)
 blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const Params p) {
@@ -188,7 +196,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t smem_base = smem_u32(smem);
-  const int nbkv = p.T / KB;
+  const int nbkv = (p.kv_rows + KB - 1) / KB;
 
   if (warp < 4) {
     setmaxnreg_dec<kRegsLow>();
@@ -208,15 +216,44 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       int b, hkv, qblk, h0, nh;
       decode_item(p, item, b, hkv, qblk, h0, nh);
-      const long long brow = (long long)b * p.nbq + qblk;
-      const int lo = max(p.lower[brow], 0), up = min(p.upper[brow], nbkv);
+      int lo = 0, up = 0, lof = 0, upf = 0, start = 0, end = 0;
+      if constexpr (kRagged) {
+        // rows i0 .. i1 of this query block sit at end - Q + i; their windows' union is
+        // [kmin(i0), kmax(i1)] and the keys every row sees are [kmin(i1), kmax(i0)]
+        start = min(max(p.seq_start[b], 0), p.kv_rows);
+        end = min(max(p.seq_end[b], 0), p.kv_rows);
+        const int i0 = qblk * kM, i1 = min(i0 + kM, p.q_rows) - 1;
+        auto kmin = [&](int i) -> long long {
+          const long long pos = (long long)end - p.q_rows + i;
+          return p.window_left >= 0 ? max((long long)start, pos - p.window_left) : (long long)start;
+        };
+        auto kmax = [&](int i) -> long long {
+          const long long pos = (long long)end - p.q_rows + i;
+          return p.window_right >= 0 ? min((long long)end - 1, pos + p.window_right) : (long long)end - 1;
+        };
+        const long long klo = kmin(i0), khi = kmax(i1);
+        if (end > start && khi >= klo) {
+          lo = static_cast<int>(klo / KB);
+          up = static_cast<int>(khi / KB) + 1;
+          const long long flo = kmin(i1), fhi = kmax(i0);
+          lof = static_cast<int>((flo + KB - 1) / KB);
+          upf = fhi >= flo ? static_cast<int>((fhi + 1) / KB) : lof;
+        }
+      } else {
+        const long long brow = (long long)b * p.nbq + qblk;
+        lo = max(p.lower[brow], 0);
+        up = min(p.upper[brow], nbkv);
+        lof = p.lower_full[brow];
+        upf = p.upper_full[brow];
+      }
       const int nt = up > lo ? up - lo : 0;
       if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleLoader, kBarItemEmpty, item)) break;
       if (lane == 0) {
         Item& it = item_at(islot);
         it.b = b; it.hkv = hkv; it.qblk = qblk; it.h0 = h0; it.nh = nh;
-        it.lo = lo; it.up = up; it.lof = p.lower_full[brow]; it.upf = p.upper_full[brow];
+        it.lo = lo; it.up = up; it.lof = lof; it.upf = upf;
         it.n_tiles = nt;
+        it.start = start; it.end = end;
         mbar_arrive(&item_full[islot]);
       }
       __syncwarp();
@@ -229,7 +266,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
             tma_load_3d(smem + C::kOffQ + w * C::kQBytes + pn * C::kQPanelBytes, &tm_q, &q_full[w],
-                        pn * 64, h0 + w, b * p.T + qblk * kM);
+                        pn * 64, h0 + w, b * p.q_rows + qblk * kM);
         }
         q_issued[w] = true;
         q_last[w] = qphase[w];
@@ -237,7 +274,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       }
       if (!ok) break;
       for (int t = 0; t < nt; ++t) {
-        const int tok0 = b * p.T + (lo + t) * KB;
+        const int tok0 = b * p.kv_rows + (lo + t) * KB;
         if (!warp_wait(&k_empty[ks], kphase ^ 1, ab, kRoleLoader, kBarKEmpty, item)) { ok = false; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&k_full[ks], C::kKBytes);
@@ -252,12 +289,14 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (!warp_wait(&v_empty[vs], vphase ^ 1, ab, kRoleLoader, kBarVEmpty, item)) { ok = false; break; }
         if (lane == 0) {
           uint8_t* vdst = smem + C::kOffV + vs * C::kVStageBytes;
-          mbar_arrive_expect_tx(&v_full[vs], C::kKBytes + C::kPosSegBytes);
+          mbar_arrive_expect_tx(&v_full[vs], C::kKBytes + (kRagged ? 0 : C::kPosSegBytes));
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
             tma_load_3d(vdst + pn * C::kKPanelBytes, &tm_v, &v_full[vs], pn * 64, hkv, tok0);
-          bulk_load(vdst + C::kKBytes, p.kv_pos + tok0, KB * 4, &v_full[vs]);
-          bulk_load(vdst + C::kKBytes + KB * 4, p.kv_seg + tok0, KB * 4, &v_full[vs]);
+          if (!kRagged) {
+            bulk_load(vdst + C::kKBytes, p.kv_pos + tok0, KB * 4, &v_full[vs]);
+            bulk_load(vdst + C::kKBytes + KB * 4, p.kv_seg + tok0, KB * 4, &v_full[vs]);
+          }
         }
         v_issued[vs] = true;
         v_last[vs] = vphase;
@@ -387,11 +426,12 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const Item it = item_at(islot);
       const int nt = it.n_tiles;
       const bool mine = w < it.nh;
-      const long long tok = (long long)it.b * p.T + it.qblk * kM + r;
+      const long long tok = (long long)it.b * p.q_rows + it.qblk * kM + r;
       const int hq = it.h0 + w;
+      const bool row_ok = !kRagged || it.qblk * kM + r < p.q_rows;  // ragged: last block partial
       bool ok = true;
       if (!mine || nt == 0) {
-        if (mine) {  // nothing attended: zeros and -inf
+        if (mine && row_ok) {  // nothing attended: zeros and -inf
           __nv_bfloat16* orow = p.out + (tok * p.Hq + hq) * D;
 #pragma unroll
           for (int j = 0; j < D; j += 8) *reinterpret_cast<uint4*>(orow + j) = make_uint4(0u, 0u, 0u, 0u);
@@ -405,15 +445,26 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         continue;
       }
-      const int qp = p.q_pos[tok];
-      const int qs = p.q_seg[tok];
-      // key positions this row may attend (causal and inclusive window, exact in 64 bits,
-      // then clamped to the int32 range of the positions); a padding row sees none
+      int qs = 0;
       long long klo = INT_MIN, khi = INT_MAX;
-      if (p.causal) khi = min(khi, (long long)qp);
-      if (p.window_left >= 0) klo = max(klo, (long long)qp - p.window_left);
-      if (p.window_right >= 0) khi = min(khi, (long long)qp + p.window_right);
-      if (qs == p.pad_id) { klo = 1; khi = 0; }
+      if constexpr (kRagged) {
+        // keys of this row: [start, end) inside the inclusive window of its position
+        const long long qpos = (long long)it.end - p.q_rows + it.qblk * kM + r;
+        klo = it.start;
+        khi = (long long)it.end - 1;
+        if (p.window_left >= 0) klo = max(klo, qpos - p.window_left);
+        if (p.window_right >= 0) khi = min(khi, qpos + p.window_right);
+        if (!row_ok) { klo = 1; khi = 0; }
+      } else {
+        const int qp = p.q_pos[tok];
+        qs = p.q_seg[tok];
+        // key positions this row may attend (causal and inclusive window, exact in 64
+        // bits, then clamped to the int32 range of the positions); padding sees none
+        if (p.causal) khi = min(khi, (long long)qp);
+        if (p.window_left >= 0) klo = max(klo, (long long)qp - p.window_left);
+        if (p.window_right >= 0) khi = min(khi, (long long)qp + p.window_right);
+        if (qs == p.pad_id) { klo = 1; khi = 0; }
+      }
       const int kmin = static_cast<int>(max(klo, (long long)INT_MIN));
       const int kmax = static_cast<int>(min(khi, (long long)INT_MAX));
       const bool none = klo > khi;
@@ -424,7 +475,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (!warp_wait(&s_full[w], sph, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
         sph ^= 1;
         const int* ps = nullptr;
-        if (!full) {
+        if (!full && !kRagged) {
           // the block's key positions / segment ids arrived with its V
           if (!warp_wait(&v_full[vs], vphase, ab, kRoleSoftmax, kBarVFull, item)) { ok = false; break; }
           ps = reinterpret_cast<const int*>(smem + C::kOffV + vs * C::kVStageBytes + C::kKBytes);
@@ -438,7 +489,12 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < KB; ++j) tmem_ld_ready(x[j]);
-        if (!full) {
+        if (!full && kRagged) {
+          const int key0 = blk * KB;  // key index of column 0
+#pragma unroll
+          for (int j = 0; j < KB; ++j)
+            if (!(!none && key0 + j >= kmin && key0 + j <= kmax)) x[j] = -INFINITY;
+        } else if (!full) {
 #pragma unroll
           for (int j = 0; j < KB; j += 4) {
             const int4 kp4 = *reinterpret_cast<const int4*>(ps + j);
@@ -537,6 +593,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       for (int c = 0; c < D / 32; ++c) {
         float ov[32];
         tmem_ld_32x32b_x32(o_col + c * 32, ov);
+        if (!row_ok) continue;  // warp-collective load above, no store for a padded row
 #pragma unroll
         for (int j = 0; j < 32; j += 8) {
           uint32_t wv[4];
@@ -548,7 +605,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           *reinterpret_cast<uint4*>(orow + c * 32 + j) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
         }
       }
-      if (p.lse != nullptr) p.lse[tok * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (p.lse != nullptr && row_ok) p.lse[tok * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -567,12 +624,12 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   }
 }
 
-template <int D, int KB>
+template <int D, int KB, bool kRagged>
 int launch_impl(const void* q, const void* k, const void* v, const Params& p, cudaStream_t stream) {
   using C = Cfg<D, KB>;
   CUtensorMap tq, tk, tv;
   {
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.B * p.T};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.B * p.q_rows};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hq * D * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)kM};
     if (encode_tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims,
@@ -580,7 +637,7 @@ int launch_impl(const void* q, const void* k, const void* v, const Params& p, cu
       return set_error(SBA_ERR_CUDA, "blocksparse_attn: tensor map (q) failed");
   }
   {
-    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.T};
+    cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.kv_rows};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
     cuuint32_t box[3] = {64, 1, (cuuint32_t)KB};
     if (encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims,
@@ -591,13 +648,13 @@ int launch_impl(const void* q, const void* k, const void* v, const Params& p, cu
   }
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(blocksparse_attn_kernel<D, KB>,
+    cudaError_t e = cudaFuncSetAttribute(blocksparse_attn_kernel<D, KB, kRagged>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return cuda_error(e, "blocksparse_attn: set smem attribute");
     attr_done = true;
   }
   const int grid = std::min(p.n_items, num_sms());
-  blocksparse_attn_kernel<D, KB><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  blocksparse_attn_kernel<D, KB, kRagged><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "blocksparse_attn launch");
   return SBA_OK;
@@ -634,6 +691,10 @@ int launch_blocksparse_attn(const void* q, const void* k, const void* v, const i
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
+  p.q_rows = T;
+  p.kv_rows = T;
+  p.seq_start = nullptr;
+  p.seq_end = nullptr;
   p.nbq = T / kM;
   p.causal = causal;
   p.window_left = window_left;
@@ -644,10 +705,38 @@ int launch_blocksparse_attn(const void* q, const void* k, const void* v, const i
   const long long n_items = (long long)B * Hkv * p.nbq * p.n_pairs;
   if (n_items >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "blocksparse_attn: too many items");
   p.n_items = static_cast<int>(n_items);
-  if (D == 128 && kv_block == 128) return launch_impl<128, 128>(q, k, v, p, stream);
-  if (D == 128 && kv_block == 64) return launch_impl<128, 64>(q, k, v, p, stream);
-  if (D == 64 && kv_block == 128) return launch_impl<64, 128>(q, k, v, p, stream);
-  return launch_impl<64, 64>(q, k, v, p, stream);
+  if (D == 128 && kv_block == 128) return launch_impl<128, 128, false>(q, k, v, p, stream);
+  if (D == 128 && kv_block == 64) return launch_impl<128, 64, false>(q, k, v, p, stream);
+  if (D == 64 && kv_block == 128) return launch_impl<64, 128, false>(q, k, v, p, stream);
+  return launch_impl<64, 64, false>(q, k, v, p, stream);
+}
+
+// Ragged multi-query attention on the block pipeline (no soft cap, no sinks): queries
+// q [B, Q, Hq, 128] at positions end - Q + i, keys / values [B, S, Hkv, 128].
+int launch_ragged_chunk(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                        const int32_t* seq_end, int B, int Qn, int Hq, int Hkv, int S,
+                        float scale, int window_left, int window_right, void* out, float* lse,
+                        cudaStream_t stream) {
+  Params p{};
+  p.seq_start = seq_start;
+  p.seq_end = seq_end;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.B = B; p.T = 0; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
+  p.q_rows = Qn;
+  p.kv_rows = S;
+  p.nbq = (Qn + kM - 1) / kM;
+  p.causal = 0;  // causality comes from window_right = 0
+  p.window_left = window_left;
+  p.window_right = window_right;
+  p.pad_id = 0;
+  p.scale_log2 = scale * kLog2e;
+  p.n_pairs = (p.G + 1) / 2;
+  const long long n_items = (long long)B * Hkv * p.nbq * p.n_pairs;
+  if (n_items >= (1LL << 31) || (long long)B * S >= (1LL << 31) || (long long)B * Qn >= (1LL << 31))
+    return set_error(SBA_ERR_UNSUPPORTED, "ragged attention: too many rows");
+  p.n_items = static_cast<int>(n_items);
+  return launch_impl<128, 128, true>(q, k, v, p, stream);
 }
 
 }  // namespace sba

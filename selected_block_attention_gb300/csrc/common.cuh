@@ -66,6 +66,10 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
                      int num_sinks, int sink_per_head, void* out, float* lse, void* workspace,
                      cudaStream_t stream);
 
+int launch_ragged_chunk(const void* q, const void* k, const void* v, const int32_t* seq_start,
+                        const int32_t* seq_end, int B, int Qn, int Hq, int Hkv, int S,
+                        float scale, int window_left, int window_right, void* out, float* lse,
+                        cudaStream_t stream);
 int launch_l2_read_probe(const void* buf, size_t bytes, int reps, unsigned* sink,
                          cudaStream_t stream);
 

@@ -532,6 +532,11 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
                      int window_left, int window_right, float cap, const float* sink_bias,
                      int num_sinks, int sink_per_head, void* out, float* lse, void* workspace,
                      cudaStream_t stream) {
+  // Long chunks without a soft cap or sinks run on the tensor-memory block pipeline
+  // (query blocks of 128 rows, two heads of a KV head per item, key blocks of 128).
+  if (Qn >= 128 && cap <= 0.f && num_sinks == 0)
+    return launch_ragged_chunk(q, k, v, seq_start, seq_end, B, Qn, Hq, Hkv, S, scale, window_left,
+                               window_right, out, lse, stream);
   MqParams p;
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);

@@ -152,3 +152,24 @@ def test_workspace_contract(sba):
     with pytest.raises(sba.SBAError):
         sba.ragged_flash_attention_fwd(w.q, w.k, w.v, w.sequence_start, w.sequence_end,
                                        window_left=32, window_right=0, workspace=short)
+
+
+@pytest.mark.parametrize("Q,Hq,Hkv,S,window", [
+    (128, 4, 2, 1000, (-1, 0)),      # exactly one query block, causal prefix
+    (200, 4, 2, 1000, (300, 0)),     # partial last query block, left window
+    (300, 3, 1, 777, (-1, -1)),      # odd G (a head slot of its own), no window, S % 128 != 0
+    (256, 2, 2, 900, (100, 20)),     # G = 1 (the page's Hkv = Hq), look-ahead right window
+    (160, 8, 2, 640, (0, 0)),        # one key per query
+])
+def test_long_chunks_on_the_block_pipeline(sba, Q, Hq, Hkv, S, window):
+    """Q >= 128 without cap or sinks runs on the tensor-memory block pipeline: every
+    (query, head) row against the oracle, with ragged starts / ends, an empty row and a
+    row whose first queries sit left of its range."""
+    ends = [S, S - 37, Q // 2, 600 % S + 1]
+    starts = [0, 5, 0, 600 % S + 1]          # the last row is empty (end == start)
+    w = workloads.ragged_attention(device=DEV, B=4, Q=Q, Hq=Hq, Hkv=Hkv, S=S, window=window,
+                                   cap=0.0, num_sinks=0, ends=ends, starts=starts,
+                                   seed=520 + Q)
+    _compare(sba, w, what=f"mq block pipeline Q={Q} Hq={Hq} Hkv={Hkv} S={S} {window}")
+    _, lse = _gpu(sba, w)
+    assert torch.isneginf(lse[3]).all()
