@@ -283,7 +283,9 @@ SBA_API size_t sba_ragged_flash_attention_workspace_size(int B, int Q, int Hq, i
  * All pointers are caller-owned device memory.  Returns SBA_ERR_INVALID_ARG for null or
  * misaligned pointers, bad sizes or a short workspace, SBA_ERR_UNSUPPORTED outside:
  * D == 128, num_sinks <= 16, B * ceil(Q * Hq / Hkv / 16) <= 65535, Q <= 65535.
- * Internally: split-KV partial kernel + combine kernel on `stream`.
+ * Internally, on `stream`: with Q >= 128, no soft cap and no sinks, one launch of the
+ * tensor-memory block kernel (query blocks of 128 rows, key blocks of 128; the workspace
+ * is not touched); otherwise a split-KV partial kernel + combine kernel.
  */
 SBA_API int sba_ragged_flash_attention_fwd(const void* q, const void* k, const void* v,
                                            const int32_t* seq_start, const int32_t* seq_end,
