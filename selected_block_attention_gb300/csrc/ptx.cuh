@@ -182,21 +182,21 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, float* out) {
 
 // 32 lanes x 32 consecutive 32-bit columns from TMEM without the completion wait: the
 // values may be used only after tmem_wait_ld() and a tmem_ld_ready() on each of them.
+// The destinations are the caller's float registers themselves, so nothing reads them
+// (not even a bit-cast move between register classes) before the wait.
 __device__ __forceinline__ void tmem_ld_32x32b_x32_nw(uint32_t taddr, float* out) {
-  uint32_t r[32];
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
       "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
       "%28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "=f"(out[0]), "=f"(out[1]), "=f"(out[2]), "=f"(out[3]), "=f"(out[4]), "=f"(out[5]),
+        "=f"(out[6]), "=f"(out[7]), "=f"(out[8]), "=f"(out[9]), "=f"(out[10]), "=f"(out[11]),
+        "=f"(out[12]), "=f"(out[13]), "=f"(out[14]), "=f"(out[15]), "=f"(out[16]),
+        "=f"(out[17]), "=f"(out[18]), "=f"(out[19]), "=f"(out[20]), "=f"(out[21]),
+        "=f"(out[22]), "=f"(out[23]), "=f"(out[24]), "=f"(out[25]), "=f"(out[26]),
+        "=f"(out[27]), "=f"(out[28]), "=f"(out[29]), "=f"(out[30]), "=f"(out[31])
       : "r"(taddr)
       : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) out[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
