@@ -426,7 +426,7 @@ def run_cuda(args, rank, world, local_rank):
              "hbm": hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
              "l2_gather": gather_bytes / (bw_l2 * 1e9) * 1e6}
     t_roof = max(terms.values())
-    rows = {} if args.no_rows else measure_rows(sba, dev, stream, flush, peaks, args)
+    rows = {} if args.no_rows else measure_rows(sba, dev, stream, flush, peaks, args, bw_l2)
 
     result = {
         "metric": METRIC,
@@ -485,7 +485,17 @@ def run_cuda(args, rank, world, local_rank):
     return result
 
 
-def measure_rows(sba, dev, stream, flush, peaks, args):
+def t_roof_terms(flops, hbm_bytes, peaks, gather_bytes=None, bw_l2=None):
+    """Roofline terms in us (tensor, HBM, and the per-token gather at the measured L2
+    read bandwidth when given) and their maximum."""
+    terms = {"tensor": flops / (peaks["bf16_tflops"] * 1e12) * 1e6,
+             "hbm": hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6}
+    if gather_bytes is not None:
+        terms["l2_gather"] = gather_bytes / (bw_l2 * 1e9) * 1e6
+    return {k: round(v, 2) for k, v in terms.items()}, max(terms.values())
+
+
+def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
     rows = {}
     steps, warm = max(3, min(args.steps, 20)), 3
 
@@ -497,10 +507,13 @@ def measure_rows(sba, dev, stream, flush, peaks, args):
                     steps, warm, flush, stream)
     ms = sum(t) / len(t)
     log(f"varlen nsa {ms:.4f} ms")
+    terms, t_roof = t_roof_terms(flops, hbm, peaks, gather, bw_l2)
     rows["nsa_select_varlen"] = {
         "workload": w.name, "ms": round(ms, 4), "TFLOP/s": round(flops / ms / 1e9, 2),
         "frac_tensor": round(flops / ms / 1e9 / peaks["bf16_tflops"], 4),
-        "hbm_GB/s": round(hbm / ms / 1e6, 1), "gather_GB/s": round(gather / ms / 1e6, 1)}
+        "hbm_GB/s": round(hbm / ms / 1e6, 1), "gather_GB/s": round(gather / ms / 1e6, 1),
+        "terms_us": terms, "t_roof_us": round(t_roof, 2),
+        "frac_t_roof": round(t_roof / (ms * 1e3), 4)}
     del w
     torch.cuda.empty_cache()
 
@@ -539,9 +552,16 @@ def measure_rows(sba, dev, stream, flush, peaks, args):
                     steps, warm, flush, stream)
     ms = sum(t) / len(t)
     log(f"blocksparse {ms:.4f} ms")
+    # HBM bytes: Q, K, V read once, O and LSE written, positions / segment ids, bounds
+    B, T, Hq, D = w.q.shape
+    bsa_hbm = (2 * w.q.numel() * 2 + 2 * w.k.numel() * 2 + B * T * Hq * 4 + 4 * B * T * 4
+               + 4 * lo.numel() * 4)
+    terms, t_roof = t_roof_terms(fl, bsa_hbm, peaks)
     rows["blocksparse_attn"] = {
         "workload": w.name, "ms": round(ms, 4), "TFLOP/s": round(fl / ms / 1e9, 2),
-        "frac_tensor": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4)}
+        "frac_tensor": round(fl / ms / 1e9 / peaks["bf16_tflops"], 4),
+        "hbm_bytes": int(bsa_hbm), "terms_us": terms, "t_roof_us": round(t_roof, 2),
+        "frac_t_roof": round(t_roof / (ms * 1e3), 4)}
     del w, m, bnd
     torch.cuda.empty_cache()
 
