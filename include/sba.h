@@ -93,6 +93,48 @@ SBA_API int sba_nsa_select_fwd(const void* q, const void* k, const void* v, cons
                        void* out, float* lse, sba_stream_t stream);
 
 /*
+ * sba_nsa_select_host_workspace_size -- bytes of device staging memory that
+ * sba_nsa_select_fwd_host needs for the given shapes: device copies of q, k, v,
+ * block_indices, block_counts (has_counts), g_slc (has_gate), out and lse (has_lse),
+ * each starting on a 256-byte boundary.  Returns 0 for sizes < 1 or an unknown dtype.
+ */
+SBA_API size_t sba_nsa_select_host_workspace_size(int B, int T, int Hq, int Hkv, int D, int S,
+                                                  int dtype, int has_counts, int has_gate,
+                                                  int has_lse);
+
+/*
+ * sba_nsa_select_fwd_host -- sba_nsa_select_fwd on HOST buffers, fixed-length rows
+ * (no cu_seqlens).  Same operation, arguments, layouts and support limits as
+ * sba_nsa_select_fwd; every tensor argument (q_h, k_h, v_h, g_slc_h, block_indices_h,
+ * block_counts_h, out_h, lse_h) is a host pointer.  Page-locked (pinned) host memory
+ * makes the copies asynchronous; pageable memory works but copies synchronously.
+ *
+ *  workspace        device memory of at least sba_nsa_select_host_workspace_size(B, T,
+ *                   Hq, Hkv, D, S, dtype, block_counts_h != NULL, g_slc_h != NULL,
+ *                   lse_h != NULL) bytes, 256-byte aligned, owned by the caller; its
+ *                   contents are scratch.
+ *
+ * The batch is split into up to four chunks of rows.  Each chunk's inputs are copied
+ * to the device on a library stream, computed on `stream`, and its outputs copied
+ * back on a second library stream, so that the copy of one chunk overlaps the
+ * computation of its neighbours (the library keeps these two non-blocking streams
+ * per device from the first call on).  Ordering: the call's work starts after the
+ * work already enqueued on `stream`, and its end (the last copy to out_h / lse_h) is
+ * enqueued on `stream`: synchronize `stream` before reading out_h or lse_h, and do not
+ * reuse the workspace or the host buffers before that.
+ * Errors: SBA_ERR_INVALID_ARG (null pointer, misaligned or short workspace, sizes),
+ * SBA_ERR_UNSUPPORTED (as sba_nsa_select_fwd), SBA_ERR_CUDA (a copy, event or launch
+ * failed; work enqueued before the failure may still run).
+ */
+SBA_API int sba_nsa_select_fwd_host(const void* q_h, const void* k_h, const void* v_h,
+                                    const void* g_slc_h, const int32_t* block_indices_h,
+                                    const int32_t* block_counts_h, int block_count_scalar, int S,
+                                    int B, int T, int Hq, int Hkv, int D, int block_size,
+                                    int causal, float softmax_scale, int dtype, void* out_h,
+                                    float* lse_h, void* workspace, size_t workspace_bytes,
+                                    sba_stream_t stream);
+
+/*
  * sba_sparse_mask_bounds -- SparseMask block bounds for the forward pass.
  *
  * Defined by: "ejkernel.kernels._triton.blocksparse_attention._mask" (module source

@@ -24,7 +24,8 @@ import torch
 from . import _build
 
 __all__ = [
-    "SBAError", "load_library", "library_path", "nsa_select_fwd", "sparse_mask_bounds",
+    "SBAError", "load_library", "library_path", "nsa_select_fwd", "nsa_select_fwd_host",
+    "nsa_select_host_workspace_size", "sparse_mask_bounds",
     "blocksparse_attn_fwd", "ragged_decode_fwd", "ragged_decode_fwd_noalloc",
     "ragged_decode_workspace_size", "ragged_flash_attention_fwd",
     "ragged_flash_attention_workspace_size", "l2_read_probe", "check_error", "EXPORTED_SYMBOLS",
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "sba_blocksparse_attn_fwd", "sba_ragged_decode_workspace_size", "sba_ragged_decode_fwd",
     "sba_ragged_decode_fwd_noalloc", "sba_ragged_flash_attention_workspace_size",
     "sba_ragged_flash_attention_fwd", "sba_l2_read_probe", "sba_check_error",
+    "sba_nsa_select_host_workspace_size", "sba_nsa_select_fwd_host",
 )
 
 SBA_BF16, SBA_F32 = 0, 1
@@ -69,6 +71,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     ci, cf, csz = ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.sba_version.restype = ctypes.c_char_p
     lib.sba_last_error.restype = ctypes.c_char_p
+    lib.sba_nsa_select_host_workspace_size.argtypes = [ci] * 10
+    lib.sba_nsa_select_host_workspace_size.restype = csz
+    lib.sba_nsa_select_fwd_host.argtypes = [vp, vp, vp, vp, i32p, i32p, ci, ci, ci, ci, ci, ci, ci,
+                                            ci, ci, cf, ci, vp, f32p, vp, csz, vp]
+    lib.sba_nsa_select_fwd_host.restype = ci
     lib.sba_nsa_select_fwd.argtypes = [vp, vp, vp, vp, i32p, i32p, ci, ci, i32p, ci, ci, ci, ci, ci,
                                        ci, ci, ci, cf, ci, vp, f32p, vp]
     lib.sba_nsa_select_fwd.restype = ci
@@ -176,6 +183,55 @@ def nsa_select_fwd(q, k, v, block_indices, block_counts, block_size, *, cu_seqle
         int(block_counts) if counts_t is None else 0, S, _ptr(cu_seqlens), num_seqs,
         B, T, Hq, Hkv, D, int(block_size), int(bool(causal)),
         float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse), _stream(dev)))
+    return out, lse
+
+
+def nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, dtype=SBA_BF16, has_counts=True,
+                                   has_gate=False, has_lse=True) -> int:
+    return int(load_library().sba_nsa_select_host_workspace_size(
+        B, T, Hq, Hkv, D, S, dtype, int(bool(has_counts)), int(bool(has_gate)), int(bool(has_lse))))
+
+
+def nsa_select_fwd_host(q, k, v, block_indices, block_counts, block_size, *, causal=True,
+                        softmax_scale=None, g_slc=None, out=None, lse=None, return_lse=True,
+                        workspace=None, device=None):
+    """Selection-branch NSA forward on CPU tensors (pinned for asynchronous copies):
+    the library stages them in a device workspace, overlapping the copies of batch-row
+    chunks with the computation.  Fixed-length rows only.  Returns (out, lse) as CPU
+    tensors; they are complete when the current stream of ``device`` is."""
+    lib = load_library()
+    for t in (q, k, v, block_indices, g_slc, out, lse,
+              None if isinstance(block_counts, int) else block_counts):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("host entry point: tensors must be contiguous CPU tensors")
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    S = block_indices.shape[-1]
+    counts_t = None if isinstance(block_counts, int) else block_counts
+    if block_indices.dtype != torch.int32 or (counts_t is not None and counts_t.dtype != torch.int32):
+        raise TypeError("block_indices / block_counts must be int32")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    dtype = {torch.bfloat16: SBA_BF16, torch.float32: SBA_F32}.get(q.dtype)
+    if dtype is None:
+        raise TypeError("q must be bfloat16 or float32")
+    if g_slc is not None and (g_slc.dtype != q.dtype or tuple(g_slc.shape) != (B, T, Hq)):
+        raise ValueError("g_slc must be a [B, T, Hq] tensor of q's dtype")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=pin)
+    if lse is None and return_lse:
+        lse = torch.empty((B, T, Hq), dtype=torch.float32, pin_memory=pin)
+    need = nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, dtype, counts_t is not None,
+                                          g_slc is not None, lse is not None)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    _check(lib.sba_nsa_select_fwd_host(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g_slc), _ptr(block_indices), _ptr(counts_t),
+        int(block_counts) if counts_t is None else 0, S, B, T, Hq, Hkv, D, int(block_size),
+        int(bool(causal)), float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
     return out, lse
 
 

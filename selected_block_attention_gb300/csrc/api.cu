@@ -56,6 +56,67 @@ int num_sms() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+constexpr int kHostChunks = 4;  // batch-row chunks of the host-buffer entry point
+
+// Two non-blocking streams per device for the host-buffer entry point: one carries the
+// host-to-device copies, the other the device-to-host copies.  Created on first use and
+// kept for the life of the process; calls that share a device share them.
+struct CopyStreams {
+  cudaStream_t in = nullptr, out = nullptr;
+};
+static std::mutex g_copy_mutex;
+static CopyStreams g_copy_streams[64];
+
+static int copy_streams(CopyStreams** cs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(SBA_ERR_UNSUPPORTED, "device ordinal must be < 64");
+  std::lock_guard<std::mutex> lock(g_copy_mutex);
+  CopyStreams& c = g_copy_streams[dev];
+  if (c.in == nullptr) {
+    if ((e = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking)) != cudaSuccess)
+      return cuda_error(e, "copy stream");
+    if ((e = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking)) != cudaSuccess) {
+      cudaStreamDestroy(c.in);
+      c.in = nullptr;
+      return cuda_error(e, "copy stream");
+    }
+  }
+  *cs = &c;
+  return SBA_OK;
+}
+
+// Device staging layout of the host-buffer NSA entry: every array whole (all B rows),
+// each starting on a 256-byte boundary.
+struct NsaHostLayout {
+  size_t q, k, v, idx, cnt, g, out, lse, total;
+  size_t q_row, kv_row, idx_row, cnt_row, g_row, lse_row;  // bytes per batch row
+};
+static size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+static NsaHostLayout nsa_host_layout(int B, int T, int Hq, int Hkv, int D, int S, int dtype,
+                                     bool has_counts, bool has_gate, bool has_lse) {
+  NsaHostLayout L{};
+  const size_t esz = dtype == SBA_F32 ? 4 : 2;
+  L.q_row = static_cast<size_t>(T) * Hq * D * esz;
+  L.kv_row = static_cast<size_t>(T) * Hkv * D * esz;
+  L.idx_row = static_cast<size_t>(T) * Hkv * S * 4;
+  L.cnt_row = has_counts ? static_cast<size_t>(T) * Hkv * 4 : 0;
+  L.g_row = has_gate ? static_cast<size_t>(T) * Hq * esz : 0;
+  L.lse_row = has_lse ? static_cast<size_t>(T) * Hq * 4 : 0;
+  size_t off = 0;
+  L.q = off;   off += round256(L.q_row * B);
+  L.k = off;   off += round256(L.kv_row * B);
+  L.v = off;   off += round256(L.kv_row * B);
+  L.idx = off; off += round256(L.idx_row * B);
+  L.cnt = off; off += round256(L.cnt_row * B);
+  L.g = off;   off += round256(L.g_row * B);
+  L.out = off; off += round256(L.q_row * B);
+  L.lse = off; off += round256(L.lse_row * B);
+  L.total = off;
+  return L;
+}
+
 }  // namespace sba
 
 using namespace sba;
@@ -105,6 +166,112 @@ int sba_nsa_select_fwd(const void* q, const void* k, const void* v, const void* 
                            cu_seqlens, cu_seqlens ? num_seqs : 0, B, T, Hq, Hkv, D, block_size,
                            causal ? 1 : 0, scale, dtype, out, lse,
                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t sba_nsa_select_host_workspace_size(int B, int T, int Hq, int Hkv, int D, int S,
+                                          int dtype, int has_counts, int has_gate,
+                                          int has_lse) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || D < 1 || S < 1) return 0;
+  if (dtype != SBA_BF16 && dtype != SBA_F32) return 0;
+  return nsa_host_layout(B, T, Hq, Hkv, D, S, dtype, has_counts != 0, has_gate != 0,
+                         has_lse != 0).total;
+}
+
+int sba_nsa_select_fwd_host(const void* q_h, const void* k_h, const void* v_h,
+                            const void* g_slc_h, const int32_t* block_indices_h,
+                            const int32_t* block_counts_h, int block_count_scalar, int S, int B,
+                            int T, int Hq, int Hkv, int D, int block_size, int causal,
+                            float softmax_scale, int dtype, void* out_h, float* lse_h,
+                            void* workspace, size_t workspace_bytes, sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q_h && k_h && v_h && block_indices_h && out_h, "null host pointer");
+  SBA_REQUIRE(workspace != nullptr, "null workspace");
+  SBA_REQUIRE((reinterpret_cast<uintptr_t>(workspace) & 255u) == 0,
+              "workspace must be 256-byte aligned");
+  SBA_REQUIRE(B >= 1 && T >= 1 && Hq >= 1 && Hkv >= 1, "sizes must be positive");
+  SBA_REQUIRE(Hq % Hkv == 0, "Hq must be a multiple of Hkv");
+  SBA_REQUIRE(S >= 1, "S (selected-block slots) must be >= 1");
+  SBA_REQUIRE(dtype == SBA_BF16 || dtype == SBA_F32, "dtype must be SBA_BF16 or SBA_F32");
+  SBA_REQUIRE(block_counts_h != nullptr || block_count_scalar >= 0,
+              "block_count_scalar must be >= 0");
+  SBA_REQUIRE(std::isfinite(softmax_scale), "softmax_scale must be finite");
+  SBA_SUPPORT(D == 64 || D == 128, "D must be 64 or 128");
+  SBA_SUPPORT(block_size == 32 || block_size == 64 || block_size == 128,
+              "block_size must be 32, 64 or 128");
+  SBA_SUPPORT(Hq / Hkv <= 16, "Hq / Hkv must be <= 16");
+  SBA_SUPPORT(S <= 32, "S must be <= 32");
+  SBA_SUPPORT((long long)B * T * Hq < (1LL << 31), "B * T * Hq must be < 2^31");
+  const NsaHostLayout L = nsa_host_layout(B, T, Hq, Hkv, D, S, dtype, block_counts_h != nullptr,
+                                          g_slc_h != nullptr, lse_h != nullptr);
+  SBA_REQUIRE(workspace_bytes >= L.total,
+              "workspace too small (see sba_nsa_select_host_workspace_size)");
+  CopyStreams* cs = nullptr;
+  if (int rc = copy_streams(&cs)) return rc;
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int nchunks = B < kHostChunks ? B : kHostChunks;
+
+  // events: start, then per chunk "inputs copied" and "computed", then "outputs copied"
+  cudaEvent_t ev[2 + 2 * kHostChunks];
+  int nev = 0;
+  auto cleanup = [&]() {
+    for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);  // released once they complete
+  };
+  for (; nev < 2 + 2 * nchunks; ++nev) {
+    cudaError_t e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
+    if (e != cudaSuccess) { cleanup(); return cuda_error(e, "event create"); }
+  }
+  cudaEvent_t ev_start = ev[0], ev_done = ev[1];
+  cudaError_t e = cudaEventRecord(ev_start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->in, ev_start, 0);
+  if (e != cudaSuccess) { cleanup(); return cuda_error(e, "stream ordering"); }
+
+  auto h2d = [&](size_t off, const void* src, size_t row_bytes, int r0, int rows) {
+    if (row_bytes == 0) return cudaSuccess;
+    return cudaMemcpyAsync(ws + off + row_bytes * r0,
+                           static_cast<const uint8_t*>(src) + row_bytes * r0, row_bytes * rows,
+                           cudaMemcpyHostToDevice, cs->in);
+  };
+  auto d2h = [&](void* dst, size_t off, size_t row_bytes, int r0, int rows) {
+    if (row_bytes == 0) return cudaSuccess;
+    return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + row_bytes * r0, ws + off + row_bytes * r0,
+                           row_bytes * rows, cudaMemcpyDeviceToHost, cs->out);
+  };
+  for (int c = 0; c < nchunks; ++c) {
+    const int r0 = static_cast<int>(static_cast<long long>(B) * c / nchunks);
+    const int rows = static_cast<int>(static_cast<long long>(B) * (c + 1) / nchunks) - r0;
+    cudaEvent_t ev_in = ev[2 + 2 * c], ev_k = ev[3 + 2 * c];
+    // rows r0 .. r0 + rows - 1: inputs in, selection forward, outputs out
+    e = h2d(L.q, q_h, L.q_row, r0, rows);
+    if (e == cudaSuccess) e = h2d(L.k, k_h, L.kv_row, r0, rows);
+    if (e == cudaSuccess) e = h2d(L.v, v_h, L.kv_row, r0, rows);
+    if (e == cudaSuccess) e = h2d(L.idx, block_indices_h, L.idx_row, r0, rows);
+    if (e == cudaSuccess && block_counts_h) e = h2d(L.cnt, block_counts_h, L.cnt_row, r0, rows);
+    if (e == cudaSuccess && g_slc_h) e = h2d(L.g, g_slc_h, L.g_row, r0, rows);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, cs->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
+    if (e != cudaSuccess) { cleanup(); return cuda_error(e, "host-to-device copy"); }
+    const int rc = launch_nsa_select(
+        ws + L.q + L.q_row * r0, ws + L.k + L.kv_row * r0, ws + L.v + L.kv_row * r0,
+        g_slc_h ? ws + L.g + L.g_row * r0 : nullptr,
+        reinterpret_cast<const int32_t*>(ws + L.idx + L.idx_row * r0),
+        block_counts_h ? reinterpret_cast<const int32_t*>(ws + L.cnt + L.cnt_row * r0) : nullptr,
+        block_count_scalar, S, nullptr, 0, rows, T, Hq, Hkv, D, block_size, causal ? 1 : 0, scale,
+        dtype, ws + L.out + L.q_row * r0,
+        lse_h ? reinterpret_cast<float*>(ws + L.lse + L.lse_row * r0) : nullptr, st);
+    if (rc != SBA_OK) { cleanup(); return rc; }
+    e = cudaEventRecord(ev_k, st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->out, ev_k, 0);
+    if (e == cudaSuccess) e = d2h(out_h, L.out, L.q_row, r0, rows);
+    if (e == cudaSuccess && lse_h) e = d2h(lse_h, L.lse, L.lse_row, r0, rows);
+    if (e != cudaSuccess) { cleanup(); return cuda_error(e, "device-to-host copy"); }
+  }
+  e = cudaEventRecord(ev_done, cs->out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_done, 0);
+  cleanup();
+  if (e != cudaSuccess) return cuda_error(e, "stream ordering");
+  return SBA_OK;
 }
 
 int sba_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const int32_t* kv_pos,

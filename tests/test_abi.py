@@ -112,6 +112,22 @@ def test_argument_validation_without_launch(lib):
     args[15], args[16] = fake, 17
     assert lib.sba_ragged_flash_attention_fwd(*args) == -2
     assert lib.sba_ragged_flash_attention_workspace_size(4, 0, 8, 1024, 128, 100, 0) == 0
+    # host-buffer NSA entry: null host pointer, misaligned / short workspace, unsupported D
+    need = lib.sba_nsa_select_host_workspace_size(2, 64, 4, 2, 128, 4, 0, 1, 0, 1)
+    assert need > 0
+    hargs = [fake, fake, fake, None, fake, fake, 0, 4, 2, 64, 4, 2, 128, 64, 1, 0.0, 0, fake, fake,
+             c.c_void_p(0x100000), need, None]
+    r = lib.sba_nsa_select_fwd_host(None, *hargs[1:])
+    assert r == -1 and b"null" in lib.sba_last_error()
+    hargs[19] = c.c_void_p(0x100010)
+    assert lib.sba_nsa_select_fwd_host(*hargs) == -1 and b"aligned" in lib.sba_last_error()
+    hargs[19] = c.c_void_p(0x100000)
+    hargs[20] = need - 1
+    assert lib.sba_nsa_select_fwd_host(*hargs) == -1 and b"workspace" in lib.sba_last_error()
+    hargs[20] = need
+    hargs[12] = 96
+    assert lib.sba_nsa_select_fwd_host(*hargs) == -2
+    assert lib.sba_nsa_select_host_workspace_size(0, 64, 4, 2, 128, 4, 0, 1, 0, 1) == 0
     # L2 probe: misaligned buffer, size not a multiple of 16, no sink
     assert lib.sba_l2_read_probe(c.c_void_p(0x10008), 4096, 1, fake, None) == -1
     assert lib.sba_l2_read_probe(fake, 4100, 1, fake, None) == -1
@@ -158,3 +174,25 @@ def test_multi_query_workspace_arithmetic():
     assert ws(2, 64, 32, 1000, 128, -1, 60) == 2 * 1 * row64     # S = 1000
     for wl in (-1, 0, 4096, 5000):
         assert ws(64, 1, 32, 32768, 128, wl, 7) == lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, wl)
+
+
+def test_nsa_host_workspace_arithmetic():
+    """Staging layout of the host-buffer NSA entry: q, k, v, indices, counts, gate, out,
+    lse for all rows, each rounded up to 256 bytes (host-only arithmetic)."""
+    import selected_block_attention_gb300 as sba
+
+    try:
+        lib = sba.load_library()
+    except RuntimeError:
+        pytest.skip("library not built")
+    r = lambda x: (x + 255) // 256 * 256
+    B, T, Hq, Hkv, D, S = 3, 100, 4, 2, 64, 5
+    q = B * T * Hq * D * 2
+    kv = B * T * Hkv * D * 2
+    full = r(q) + 2 * r(kv) + r(B * T * Hkv * S * 4) + r(B * T * Hkv * 4) + r(B * T * Hq * 2) + r(q) + r(B * T * Hq * 4)
+    assert lib.sba_nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, 0, 1, 1, 1) == full
+    bare = r(q) + 2 * r(kv) + r(B * T * Hkv * S * 4) + r(q)
+    assert lib.sba_nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, 0, 0, 0, 0) == bare
+    f32 = 2 * r(2 * q) + 2 * r(2 * kv) + r(B * T * Hkv * S * 4) + r(B * T * Hq * 4)
+    assert lib.sba_nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, 1, 0, 0, 1) == f32
+    assert lib.sba_nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, 7, 0, 0, 1) == 0

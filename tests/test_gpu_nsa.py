@@ -200,3 +200,61 @@ def test_selection_gate(sba, case):
         to_np(w.q), to_np(w.k), to_np(w.v), w.block_indices.cpu().numpy(), counts, w.block_size,
         causal=w.causal, g_slc=to_np(gate))
     assert_attention_close(to_np(out), ref, to_np(lse), ref_lse, what=f"gate {case}")
+
+
+@pytest.mark.parametrize("B,dtype,gate,counts_tensor,with_lse,pinned", [
+    (3, torch.bfloat16, True, True, True, True),      # three row chunks, gate, counts array
+    (6, torch.bfloat16, False, False, False, True),   # 4 chunks of 1-2 rows, scalar count, no LSE
+    (1, torch.float32, False, True, True, False),     # fp32, one chunk, pageable host memory
+])
+def test_host_entry_against_oracle(sba, B, dtype, gate, counts_tensor, with_lse, pinned):
+    """The host-buffer entry point (inputs and outputs in host memory, batch rows staged
+    and computed in chunks) against the fp64 oracle, every row.  Chunks change which
+    tokens share an item (items are windows of consecutive tokens), so the result is
+    held to the attention tolerances, not to the device entry's bits."""
+    w = workloads.nsa_prefill(device=DEV, B=B, T=300, Hq=8, Hkv=2, D=128, block_size=64, S=5,
+                              max_count=5, seed=300 + B, dtype=dtype)
+    counts = w.block_counts if counts_tensor else 3
+    g = None
+    if gate:
+        g = torch.sigmoid(workloads.randn(tuple(w.q.shape[:3]), torch.float32, DEV, seed=301)).to(dtype)
+    host = lambda t: None if t is None else (t.cpu().pin_memory() if pinned else t.cpu())
+    out, lse = sba.nsa_select_fwd_host(
+        host(w.q), host(w.k), host(w.v), host(w.block_indices),
+        host(counts) if counts_tensor else counts, w.block_size, causal=True, g_slc=host(g),
+        return_lse=with_lse)
+    torch.cuda.synchronize()
+    sba.check_error()
+    assert not out.is_cuda and out.is_pinned() == pinned
+    ref, ref_lse = oracle.nsa_select_attention(
+        to_np(w.q), to_np(w.k), to_np(w.v), w.block_indices.cpu().numpy(),
+        w.block_counts.cpu().numpy() if counts_tensor else counts, w.block_size, causal=True,
+        g_slc=None if g is None else to_np(g))
+    if with_lse:
+        assert_attention_close(to_np(out), ref, to_np(lse), ref_lse, what=f"host entry B={B}")
+    else:
+        assert lse is None
+        assert_attention_close(to_np(out), ref, what=f"host entry B={B}")
+
+
+def test_host_entry_in_stream_order(sba):
+    """Two back-to-back host calls that share one workspace, synchronized once at the
+    end: each call starts after the work already on the stream, so the second call's
+    staging copies wait for the first call's kernels and copies.  With T = 256 (a
+    multiple of the 32-token item window at G = 4) the row chunks form the same items
+    as one whole-batch launch, so both results equal the device entry's bit for bit."""
+    w1 = workloads.nsa_prefill(device=DEV, B=2, T=256, Hq=8, Hkv=2, D=128, S=4, max_count=4, seed=401)
+    w2 = workloads.nsa_prefill(device=DEV, B=2, T=256, Hq=8, Hkv=2, D=128, S=4, max_count=4, seed=402)
+    res = []
+    ws = torch.empty(sba.nsa_select_host_workspace_size(2, 256, 8, 2, 128, 4), dtype=torch.uint8,
+                     device=DEV)
+    for w in (w1, w2):
+        pin = lambda t: t.cpu().pin_memory()
+        res.append(sba.nsa_select_fwd_host(pin(w.q), pin(w.k), pin(w.v), pin(w.block_indices),
+                                           pin(w.block_counts), w.block_size, workspace=ws))
+    torch.cuda.synchronize()
+    sba.check_error()
+    for w, (out, lse) in zip((w1, w2), res):
+        ref_out, ref_lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts,
+                                              w.block_size)
+        assert torch.equal(out, ref_out.cpu()) and torch.equal(lse, ref_lse.cpu())
