@@ -427,6 +427,8 @@ def run_cuda(args, rank, world, local_rank):
              "hbm": hbm_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6,
              "l2_gather": gather_bytes / (bw_l2 * 1e9) * 1e6}
     t_roof = max(terms.values())
+    exec_floor_us = max(exec_flops / (peaks["bf16_tflops"] * 1e12),
+                        union_bytes / (bw_l2 * 1e9)) * 1e6
     rows = {} if args.no_rows else measure_rows(sba, dev, stream, flush, peaks, args, bw_l2)
 
     result = {
@@ -456,13 +458,22 @@ def run_cuda(args, rank, world, local_rank):
             "frac": round(flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
             "traffic": profile_traffic("nsa_union_kernel_prefill.md",
                                        "selected_block_attention_gb300/csrc/nsa_select.cu"),
+            "traffic_source": "stored: dram__bytes_read.sum + dram__bytes_write.sum of one ncu "
+                              "capture (profiles/nsa_union_kernel_prefill.md), reported only while "
+                              "the kernel source still has the SHA-256 recorded there",
             "peak_source": f"{peak_src} bf16_tflops (burst; kernel timed alone)",
             "kernel": "nsa_union_kernel<128,64>",
             "union_tiles": int(n_tiles),
             "executed_mma_tflops": round(exec_flops / (ms * 1e-3) / 1e12, 1),
             "executed_mma_frac": round(exec_flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"], 4),
+            # the union walk's own floor: its executed MMA work at the tensor peak or its
+            # gathered K/V bytes at the measured L2 read bandwidth, whichever is larger
+            "exec_floor_us": round(exec_floor_us, 2),
+            "frac_exec_floor": round(exec_floor_us / (ms * 1e3), 4),
             # t_roof = max(F_alg / P_tensor, B_hbm / BW_hbm, B_gather / BW_l2) with the
-            # per-token selection gather and the probe's L2 read bandwidth
+            # per-token selection gather and the probe's L2 read bandwidth: the floor of a
+            # kernel that gathers each token's blocks separately, which the union walk does
+            # not (frac is the tensor-peak fraction; frac_exec_floor the union walk's own)
             "terms_us": {k: round(v, 2) for k, v in terms.items()},
             "l2_read_gbs": round(bw_l2, 1),
             "t_roof_us": round(t_roof, 2),
@@ -483,8 +494,6 @@ def run_cuda(args, rank, world, local_rank):
         "clocks": clocks,
         "rows": rows,
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(w, flops / groups, args.cpu_seconds)
     return result
 
 
@@ -501,6 +510,19 @@ def t_roof_terms(flops, hbm_bytes, peaks, gather_bytes=None, bw_l2=None):
 def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
     rows = {}
     steps, warm = max(3, min(args.steps, 20)), 3
+
+    # the fp32 correctness workload (B=1 T=256 Hq=4 Hkv=1 D=64, CUDA cores): latency only
+    w = workloads.nsa_tiny(device=dev)
+    flops, hbm, _g, _n = nsa_work(w)
+    t = timed_steps(lambda: sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts,
+                                               w.block_size, causal=True),
+                    steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    log(f"nsa tiny {ms * 1e3:.2f} us")
+    rows["nsa_select_tiny_fp32"] = {
+        "workload": w.name, "us": round(ms * 1e3, 2), "GFLOP/s": round(flops / ms / 1e6, 2),
+        "hbm_bytes": int(hbm), "bound": "launch latency (0.7 MB, fp32 on CUDA cores)"}
+    del w
 
     # varlen NSA (8 packed sequences)
     w = workloads.nsa_varlen(device=dev)
@@ -676,68 +698,107 @@ def run_case(args):
     sba.check_error(dev)
 
 
-def cpu_baseline(w, flops_per_group, seconds):
-    """fp64 oracle on host cores over a bounded, seeded sample of token groups."""
+# ----------------------------------------------------------------------------- oracle legs
+# The fp64 oracle runs in worker processes started with "spawn" (never forked from a
+# process that has touched the GPU), one per host core.  Every worker builds the same
+# seeded prefill workload on the CPU (the dense values differ from the GPU-generated
+# ones, the shapes, counts and selection structure are the recipe's) and evaluates the
+# oracle on the rows it is handed; the algorithmic FLOPs of those rows are counted the
+# same way as for the GPU line.
+_ORACLE = {}
+
+
+def _oracle_init():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    w = workloads.nsa_prefill(device="cpu")
+    _ORACLE["w"] = w
+    _ORACLE["q"] = w.q.double().numpy()
+    _ORACLE["k"] = w.k.double().numpy()
+    _ORACLE["v"] = w.v.double().numpy()
+    _ORACLE["idx"] = w.block_indices.numpy()
+    _ORACLE["counts"] = w.block_counts.numpy()
+
+
+def _row_flops(idx, counts, rows, bs, D, G):
+    fl = 0.0
+    for b, t in rows:
+        hi = np.minimum(idx[b, t] * bs + bs, t + 1)
+        valid = (np.arange(idx.shape[-1])[None, :] < counts[b, t][:, None]) & (idx[b, t] >= 0)
+        fl += 4.0 * D * G * np.where(valid, hi - idx[b, t] * bs, 0).sum()
+    return fl
+
+
+def _oracle_rows(rows):
+    """Oracle on the given (b, t) rows of the prefill workload; returns their FLOPs."""
     import oracle
 
-    q = w.q.cpu().double().numpy()
-    k = w.k.cpu().double().numpy()
-    v = w.v.cpu().double().numpy()
-    idx = w.block_indices.cpu().numpy()
-    counts = w.block_counts.cpu().numpy()
-    B, T = q.shape[:2]
+    o = _ORACLE
+    oracle.nsa_select_attention(o["q"], o["k"], o["v"], o["idx"], o["counts"], o["w"].block_size,
+                                rows=rows)
+    return _row_flops(o["idx"], o["counts"], rows, o["w"].block_size, o["q"].shape[3],
+                      o["q"].shape[2] // o["k"].shape[2])
+
+
+def _oracle_ping(_):
+    return len(_ORACLE)
+
+
+class OraclePool:
+    """One spawn-started worker per host core, each holding the workload."""
+
+    def __init__(self, cores=None):
+        import multiprocessing as mp
+
+        self.cores = cores or os.cpu_count() or 1
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_oracle_init)
+        self.pool.map(_oracle_ping, range(self.cores), chunksize=1)  # every worker ready
+
+    def run(self, rows_per_worker, rng):
+        """One parallel sample: rows_per_worker random tokens per worker.  Returns
+        (FLOPs, wall seconds, rows)."""
+        B, T = 2, 8192
+        chunks = [[(int(b), int(t)) for b, t in zip(rng.integers(0, B, rows_per_worker),
+                                                   rng.integers(0, T, rows_per_worker))]
+                  for _ in range(self.cores)]
+        t0 = time.perf_counter()
+        fl = self.pool.map(_oracle_rows, chunks, chunksize=1)
+        return float(sum(fl)), time.perf_counter() - t0, rows_per_worker * self.cores
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+
+
+def cpu_baseline(pool, seconds):
+    """fp64 oracle on all host cores over a bounded, seeded sample of prefill tokens."""
     rng = np.random.default_rng(0)
-    done_rows = 0
-    t0 = time.perf_counter()
-    flops = 0.0
-    while time.perf_counter() - t0 < seconds:
-        rows = [(int(b), int(t)) for b, t in zip(rng.integers(0, B, 32), rng.integers(0, T, 32))]
-        oracle.nsa_select_attention(q, k, v, idx, counts, w.block_size, rows=rows)
-        for b, t in rows:
-            hi = np.minimum(idx[b, t] * w.block_size + w.block_size, t + 1)
-            valid = (np.arange(idx.shape[-1])[None, :] < counts[b, t][:, None]) & (idx[b, t] >= 0)
-            flops += 4.0 * q.shape[3] * (q.shape[2] // k.shape[2]) * np.where(valid, hi - idx[b, t] * w.block_size, 0).sum()
-        done_rows += len(rows)
-    dt = time.perf_counter() - t0
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{done_rows} random tokens (all {k.shape[2]} KV heads x {q.shape[2]} query heads) "
-                      f"of the prefill workload, {dt:.1f} s, numpy float64, 1 thread"}
+    flops, dt, rows = 0.0, 0.0, 0
+    while dt < seconds:
+        f, d, r = pool.run(32, rng)
+        flops, dt, rows = flops + f, dt + d, rows + r
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": pool.cores,
+            "kind": "oracle",
+            "sample": f"{rows} random tokens (all 4 KV heads x 64 query heads) of the prefill "
+                      f"workload, {dt:.1f} s, numpy float64, {pool.cores} processes x 1 thread"}
 
 
 def run_reference(args):
-    """The fp64 oracle on host cores, same workload, bounded sample per step."""
-    import oracle
-
-    w = workloads.nsa_prefill(device="cpu")
-    q = w.q.double().numpy()
-    k = w.k.double().numpy()
-    v = w.v.double().numpy()
-    idx = w.block_indices.numpy()
-    counts = w.block_counts.numpy()
+    """The fp64 oracle on all host cores, same workload, bounded sample per step."""
+    pool = OraclePool()
     rng = np.random.default_rng(0)
-    per_step = 48
-
-    def one():
-        rows = [(int(b), int(t)) for b, t in zip(rng.integers(0, 2, per_step), rng.integers(0, 8192, per_step))]
-        t0 = time.perf_counter()
-        oracle.nsa_select_attention(q, k, v, idx, counts, w.block_size, rows=rows)
-        dt = time.perf_counter() - t0
-        fl = 0.0
-        for b, t in rows:
-            hi = np.minimum(idx[b, t] * 64 + 64, t + 1)
-            valid = (np.arange(16)[None, :] < counts[b, t][:, None]) & (idx[b, t] >= 0)
-            fl += 4.0 * 128 * 16 * np.where(valid, hi - idx[b, t] * 64, 0).sum()
-        return dt, fl
-
+    per_worker = 32
     for _ in range(args.warmup):
-        one()
+        pool.run(per_worker, rng)
     tot_t, tot_f = 0.0, 0.0
     for _ in range(args.steps):
-        dt, fl = one()
-        tot_t += dt
-        tot_f += fl
+        f, d, _r = pool.run(per_worker, rng)
+        tot_t += d
+        tot_f += f
+    pool.close()
     value = tot_f / tot_t / 1e12
-    sample = f"{per_step} random tokens per step (all 4 KV heads x 64 query heads), numpy float64, 1 thread"
+    sample = (f"{per_worker * pool.cores} random tokens per step (all 4 KV heads x 64 query heads), "
+              f"numpy float64, {pool.cores} processes x 1 thread")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -745,8 +806,8 @@ def run_reference(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "nsa_select_prefill B=2 T=8192 Hq=64 Hkv=4 D=128 block_size=64 causal "
                                "(bounded sample per step)"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": pool.cores,
+                         "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -771,9 +832,22 @@ def main():
         return
     args.warmup = max(args.warmup, 3)
 
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1 and args.impl == "cuda":
+        # launched without torchrun: start one rank per GPU on this node
+        import socket
+
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               "--master-port", str(port), os.path.abspath(__file__), *sys.argv[1:]]
+        raise SystemExit(subprocess.call(cmd))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "cuda" and world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} disagrees with WORLD_SIZE={world}")
 
     if args.impl == "reference":
         if rank != 0:
@@ -781,9 +855,14 @@ def main():
         print(json.dumps(run_reference(args)))
         return
 
+    # the oracle's worker processes start before the first GPU call (spawn in any case)
+    pool = OraclePool() if rank == 0 and not args.no_cpu_baseline else None
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_cuda(args, rank, world, local_rank)
+    if pool is not None:
+        res["cpu_baseline"] = cpu_baseline(pool, args.cpu_seconds)
+        pool.close()
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

@@ -54,6 +54,23 @@ SBA_API const char* sba_version(void);
 SBA_API const char* sba_last_error(void);
 
 /*
+ * sba_set_wait_timeout_cycles -- limit, in SM clock cycles, on every internal wait of
+ * the warp-specialised kernels (the NSA selection forward on tensor cores and the
+ * block-sparse / ragged block attention).  No counterpart on the pages: it is the
+ * library's failure detection.  A wait that runs past the limit records the kernel,
+ * role, barrier and work item in the device error word, makes every other wait of its
+ * CTA return at once, drains the copies already issued, frees its tensor memory and
+ * returns; sba_check_error() then reports SBA_ERR_TIMEOUT with that location and the
+ * outputs of that launch are undefined.  Applies to launches made after the call, from
+ * any host thread (process-wide).  cycles == 0 restores the default (4e9 cycles, about
+ * two seconds at the boost clock); a limit far below a kernel's normal wait times
+ * makes its launches fail.  Returns SBA_ERR_INVALID_ARG for cycles < 0.
+ * sba_get_wait_timeout_cycles returns the limit in force.
+ */
+SBA_API int sba_set_wait_timeout_cycles(long long cycles);
+SBA_API long long sba_get_wait_timeout_cycles(void);
+
+/*
  * sba_nsa_select_fwd -- native-sparse-attention forward, selection branch.
  *
  * Defined by: "ejkernel.modules.operations.native_sparse_attention" (operation API
@@ -273,11 +290,18 @@ SBA_API int sba_ragged_decode_fwd(const void* q, const void* k, const void* v,
  *  - Sizes whose sba_ragged_decode_workspace_size() exceeds 16 MiB are rejected with
  *    SBA_ERR_INVALID_ARG (use sba_ragged_decode_fwd with a workspace instead).
  *  - The first call on each device looks up the array's device address (with that device
- *    current) and caches it; make that first call before any stream capture.
+ *    current: `stream` must belong to the current device) and caches it for the life of
+ *    the process; make that first call before any stream capture.  The cached address
+ *    belongs to the device's context: after cudaDeviceReset() on a device, do not call
+ *    this entry point on that device again in the same process.
  *  - All calls on a device share the array: calls that may overlap on the GPU (different
  *    streams, no ordering between them) race and corrupt each other's results.  Calls on
- *    one stream are ordered and safe.
- *  - Nothing is allocated, here or in the first-call set-up.
+ *    one stream are ordered and safe.  The array keeps the last call's partials; every
+ *    slot a call reads was written by that call, so nothing needs clearing.
+ *  - Neither the call nor its first-call set-up calls cudaMalloc, cudaFree or any
+ *    allocating routine.  The 16 MiB are reserved when the library's device code is
+ *    loaded onto the GPU; with lazy module loading (CUDA_MODULE_LOADING=LAZY, the
+ *    default) that load may happen during the first call.
  */
 SBA_API int sba_ragged_decode_fwd_noalloc(const void* q, const void* k, const void* v,
                                           const int32_t* seq_start, const int32_t* seq_end,

@@ -28,7 +28,8 @@ __all__ = [
     "nsa_select_host_workspace_size", "sparse_mask_bounds",
     "blocksparse_attn_fwd", "ragged_decode_fwd", "ragged_decode_fwd_noalloc",
     "ragged_decode_workspace_size", "ragged_flash_attention_fwd",
-    "ragged_flash_attention_workspace_size", "l2_read_probe", "check_error", "EXPORTED_SYMBOLS",
+    "ragged_flash_attention_workspace_size", "l2_read_probe", "check_error",
+    "set_wait_timeout_cycles", "get_wait_timeout_cycles", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -38,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "sba_ragged_decode_fwd_noalloc", "sba_ragged_flash_attention_workspace_size",
     "sba_ragged_flash_attention_fwd", "sba_l2_read_probe", "sba_check_error",
     "sba_nsa_select_host_workspace_size", "sba_nsa_select_fwd_host",
+    "sba_set_wait_timeout_cycles", "sba_get_wait_timeout_cycles",
 )
 
 SBA_BF16, SBA_F32 = 0, 1
@@ -107,6 +109,10 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sba_l2_read_probe.restype = ci
     lib.sba_check_error.argtypes = [vp]
     lib.sba_check_error.restype = ci
+    lib.sba_set_wait_timeout_cycles.argtypes = [ctypes.c_longlong]
+    lib.sba_set_wait_timeout_cycles.restype = ci
+    lib.sba_get_wait_timeout_cycles.argtypes = []
+    lib.sba_get_wait_timeout_cycles.restype = ctypes.c_longlong
     if path == _build.LIB_PATH:
         _lib = lib
     return lib
@@ -139,6 +145,14 @@ def _dev(*tensors):
 
 def _stream(dev):
     return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _call(dev, fn, *args):
+    """Call a library entry point with ``dev`` current: the library launches on the
+    current device (and looks up per-device state there), so the stream's device must
+    be the current one."""
+    with torch.cuda.device(dev):
+        _check(fn(*args))
 
 
 def _i32(t, name):
@@ -178,11 +192,11 @@ def nsa_select_fwd(q, k, v, block_indices, block_counts, block_size, *, cu_seqle
         if g_slc.dtype != q.dtype or tuple(g_slc.shape) != (B, T, Hq) or not g_slc.is_contiguous():
             raise ValueError("g_slc must be a contiguous [B, T, Hq] tensor of q's dtype")
         _dev(q, g_slc)
-    _check(lib.sba_nsa_select_fwd(
+    _call(dev, lib.sba_nsa_select_fwd,
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_slc), _ptr(block_indices), _ptr(counts_t),
         int(block_counts) if counts_t is None else 0, S, _ptr(cu_seqlens), num_seqs,
         B, T, Hq, Hkv, D, int(block_size), int(bool(causal)),
-        float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse), _stream(dev)))
+        float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse), _stream(dev))
     return out, lse
 
 
@@ -227,11 +241,11 @@ def nsa_select_fwd_host(q, k, v, block_indices, block_counts, block_size, *, cau
                                           g_slc is not None, lse is not None)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
-    _check(lib.sba_nsa_select_fwd_host(
+    _call(dev, lib.sba_nsa_select_fwd_host,
         _ptr(q), _ptr(k), _ptr(v), _ptr(g_slc), _ptr(block_indices), _ptr(counts_t),
         int(block_counts) if counts_t is None else 0, S, B, T, Hq, Hkv, D, int(block_size),
         int(bool(causal)), float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev))
     return out, lse
 
 
@@ -252,10 +266,10 @@ def sparse_mask_bounds(q_positions, q_segment_ids, kv_positions, kv_segment_ids,
     nb = -(-Tkv // kv_blocksize) if calculate_dkdv_mask else -(-Tq // q_blocksize)
     outs = [torch.empty((B, 1, nb), dtype=torch.int32, device=dev) for _ in range(4)]
     fn = lib.sba_sparse_mask_dkdv_bounds if calculate_dkdv_mask else lib.sba_sparse_mask_bounds
-    _check(fn(
+    _call(dev, fn,
         _ptr(q_positions), _ptr(q_segment_ids), _ptr(kv_positions), _ptr(kv_segment_ids),
         B, Tq, Tkv, int(q_blocksize), int(kv_blocksize), int(bool(causal)), int(window_left),
-        int(window_right), int(padding_segment_id), *[_ptr(o) for o in outs], _stream(dev)))
+        int(window_right), int(padding_segment_id), *[_ptr(o) for o in outs], _stream(dev))
     return tuple(outs)
 
 
@@ -278,11 +292,11 @@ def blocksparse_attn_fwd(q, k, v, q_positions, q_segment_ids, kv_positions, kv_s
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, T, Hq), dtype=torch.float32, device=dev)
-    _check(lib.sba_blocksparse_attn_fwd(
+    _call(dev, lib.sba_blocksparse_attn_fwd,
         _ptr(q), _ptr(k), _ptr(v), *[_ptr(t) for t in ints], B, T, Hq, Hkv, D,
         int(q_blocksize), int(kv_blocksize), int(bool(causal)), int(window_left),
         int(window_right), int(padding_segment_id), float(softmax_scale or 0.0), _ptr(out),
-        _ptr(lse), _stream(dev)))
+        _ptr(lse), _stream(dev))
     return out, lse
 
 
@@ -315,11 +329,11 @@ def ragged_decode_fwd(q, k, v, sequence_start, sequence_end, *, softmax_scale=No
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    _check(lib.sba_ragged_decode_fwd(
+    _call(dev, lib.sba_ragged_decode_fwd,
         _ptr(q), _ptr(k), _ptr(v), _ptr(sequence_start), _ptr(sequence_end), B, Hq, Hkv, S, D,
         float(softmax_scale or 0.0), int(window_left), int(window_right),
         float(logits_soft_cap or 0.0), _ptr(sink_bias), num_sinks, per_head, _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev))
     return out, lse
 
 
@@ -345,11 +359,11 @@ def ragged_decode_fwd_noalloc(q, k, v, sequence_start, sequence_end, *, softmax_
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
-    _check(lib.sba_ragged_decode_fwd_noalloc(
+    _call(dev, lib.sba_ragged_decode_fwd_noalloc,
         _ptr(q), _ptr(k), _ptr(v), _ptr(sequence_start), _ptr(sequence_end), B, Hq, Hkv, S, D,
         float(softmax_scale or 0.0), int(window_left), int(window_right),
         float(logits_soft_cap or 0.0), _ptr(sink_bias), num_sinks, per_head, _ptr(out), _ptr(lse),
-        _stream(dev)))
+        _stream(dev))
     return out, lse
 
 
@@ -385,11 +399,11 @@ def ragged_flash_attention_fwd(q, k, v, sequence_start, sequence_end, *, softmax
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty((B, Q, Hq), dtype=torch.float32, device=dev)
-    _check(lib.sba_ragged_flash_attention_fwd(
+    _call(dev, lib.sba_ragged_flash_attention_fwd,
         _ptr(q), _ptr(k), _ptr(v), _ptr(sequence_start), _ptr(sequence_end), B, Q, Hq, Hkv, S, D,
         float(softmax_scale or 0.0), int(window_left), int(window_right),
         float(logits_soft_cap or 0.0), _ptr(sink_bias), num_sinks, per_head, _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev)))
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(dev))
     return out, lse
 
 
@@ -406,3 +420,14 @@ def check_error(device=None):
     """Synchronise the current stream and raise if a kernel flagged an error."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     _check(load_library().sba_check_error(_stream(dev)))
+
+
+def set_wait_timeout_cycles(cycles):
+    """Limit (SM cycles) on every internal wait of the warp-specialised kernels launched
+    from now on; 0 restores the default (about two seconds).  A launch whose wait runs
+    past it returns early and check_error() raises SBAError with code -4 (timeout)."""
+    _check(load_library().sba_set_wait_timeout_cycles(int(cycles)))
+
+
+def get_wait_timeout_cycles() -> int:
+    return int(load_library().sba_get_wait_timeout_cycles())

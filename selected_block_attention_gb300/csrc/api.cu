@@ -3,6 +3,7 @@
 // kernels of the other translation units.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -43,6 +44,10 @@ CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, cuuint32
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
+
+static std::atomic<long long> g_wait_limit{kWaitTimeoutCycles};
+
+long long wait_timeout_cycles() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 int num_sms() {
   static int n = 0;
@@ -135,6 +140,15 @@ extern "C" {
 const char* sba_version(void) { return "sba 0.1.0 sm_103a"; }
 
 const char* sba_last_error(void) { return g_last_error.c_str(); }
+
+int sba_set_wait_timeout_cycles(long long cycles) {
+  g_last_error.clear();
+  SBA_REQUIRE(cycles >= 0, "cycles must be >= 0 (0 restores the default)");
+  g_wait_limit.store(cycles == 0 ? kWaitTimeoutCycles : cycles, std::memory_order_relaxed);
+  return SBA_OK;
+}
+
+long long sba_get_wait_timeout_cycles(void) { return wait_timeout_cycles(); }
 
 int sba_nsa_select_fwd(const void* q, const void* k, const void* v, const void* g_slc,
                        const int32_t* block_indices, const int32_t* block_counts,

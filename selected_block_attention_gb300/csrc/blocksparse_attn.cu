@@ -18,10 +18,11 @@
 //               so that the tensor core runs one head's MMAs while the other head's
 //               softmax works;
 //   warps 4..7  softmax of head slot 0, warps 8..11 of head slot 1: one thread per query
-//               row; S_w is read from tensor memory twice (row maximum, then
-//               exponentials), masked outside the full block range, and P_w (bf16) is
-//               written over the S_w columns already read; lazy online softmax (O_w
-//               rescaled only when the row maximum grows by > 2^8); epilogue O_w / l.
+//               row; the row's scores of S_w come out of tensor memory in one pass (four
+//               loads under one wait) into registers, are masked outside the full block
+//               range, and P_w (bf16) is written in place over the S_w columns; lazy
+//               online softmax (O_w rescaled only when the row maximum grows by > 2^8);
+//               epilogue O_w / l.
 // Tensor memory: S0, S1 (one key block of fp32 columns each, P aliased in place), O0,
 // O1 (D columns each).  A commit after S_w(j + 1) also covers PV_w(j), so a softmax
 // warpgroup that sees S_w(j + 1) may rescale O_w without a further wait.
@@ -80,6 +81,7 @@ struct Params {
   int q_rows, kv_rows;   // query / key rows per batch row (T and T; ragged: Q and S)
   float scale_log2;
   int n_pairs, n_items;
+  long long wait_limit;  // cycles a bounded wait may take
 };
 
 enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3 };
@@ -162,7 +164,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   uint64_t* mma_done = reinterpret_cast<uint64_t*>(smem + C::kOffMisc + 8);
-  const Abort ab{abort_flag, &g_err_bsa, 2u};
+  const Abort ab{abort_flag, &g_err_bsa, 2u, p.wait_limit};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto item_at = [&](int slot) -> Item& {
     return *reinterpret_cast<Item*>(smem + C::kOffItems + slot * C::kItemBytes);
@@ -702,6 +704,7 @@ int launch_blocksparse_attn(const void* q, const void* k, const void* v, const i
   p.pad_id = pad_id;
   p.scale_log2 = scale * kLog2e;
   p.n_pairs = (p.G + 1) / 2;
+  p.wait_limit = wait_timeout_cycles();
   const long long n_items = (long long)B * Hkv * p.nbq * p.n_pairs;
   if (n_items >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "blocksparse_attn: too many items");
   p.n_items = static_cast<int>(n_items);
@@ -732,6 +735,7 @@ int launch_ragged_chunk(const void* q, const void* k, const void* v, const int32
   p.pad_id = 0;
   p.scale_log2 = scale * kLog2e;
   p.n_pairs = (p.G + 1) / 2;
+  p.wait_limit = wait_timeout_cycles();
   const long long n_items = (long long)B * Hkv * p.nbq * p.n_pairs;
   if (n_items >= (1LL << 31) || (long long)B * S >= (1LL << 31) || (long long)B * Qn >= (1LL << 31))
     return set_error(SBA_ERR_UNSUPPORTED, "ragged attention: too many rows");

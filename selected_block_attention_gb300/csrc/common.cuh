@@ -17,9 +17,14 @@ enum : unsigned {
   kDevErrInput = 2u,    // malformed device-side input (e.g. cu_seqlens)
 };
 
-// Roughly two seconds at the GB300 boost clock: every spin-wait on an mbarrier
-// gives up after this many SM cycles, flags kDevErrTimeout and unwinds.
+// Roughly two seconds at the GB300 boost clock: by default every spin-wait on an
+// mbarrier gives up after this many SM cycles, flags kDevErrTimeout and unwinds.  The
+// limit a launch uses is wait_timeout_cycles() (settable through the C ABI); the
+// teardown drains of copies already in flight always use this default.
 constexpr long long kWaitTimeoutCycles = 4000000000LL;
+
+// Current limit for the bounded waits of the next launches (api.cu).
+long long wait_timeout_cycles();
 
 // Host-side error reporting (defined in api.cu).
 int set_error(int code, const std::string& msg);

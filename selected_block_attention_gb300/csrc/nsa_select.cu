@@ -82,6 +82,7 @@ struct Params {
   int ranked;    // items are formed from count-ranked windows (see build_item)
   float scale, scale_log2;
   int n_items, n_tok;
+  long long wait_limit;  // cycles a bounded wait may take
 };
 
 // One union-walk item as the builder hands it to the other roles.
@@ -363,7 +364,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
   uint64_t* xch = bb;                    // (m, l) exchange between the two warpgroups
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-  const Abort ab{abort_flag, &g_err_nsa, 1u};
+  const Abort ab{abort_flag, &g_err_nsa, 1u, p.wait_limit};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto item_at = [&](int slot) -> Item& {
     return *reinterpret_cast<Item*>(smem + C::kOffItems + slot * C::kItemBytes);
@@ -1002,6 +1003,7 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const void* g
   p.NT = std::min(kMaxNT, kRows / p.G);
   p.rows = p.NT * p.G;
   p.ranked = 0;
+  p.wait_limit = wait_timeout_cycles();
   if ((long long)B * T * Hkv >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "nsa_select: too many items");
   p.n_tok = B * T;
   if (dtype == SBA_BF16) {

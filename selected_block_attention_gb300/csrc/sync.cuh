@@ -1,6 +1,7 @@
 // Bounded synchronisation for the warp-specialised kernels.
 //
-// Every wait gives up after kWaitTimeoutCycles: it records where it gave up in the
+// Every wait gives up after the launch's limit (Abort::limit; by default
+// kWaitTimeoutCycles): it records where it gave up in the
 // kernel's error word (first failure wins), raises the CTA's abort flag and returns
 // false; every later wait of the CTA then returns false at once, so all roles unwind
 // to the kernel's final barrier.  No role loop uses an unbounded hardware barrier
@@ -22,6 +23,7 @@ struct Abort {
   volatile int* flag;
   DevError* err;
   unsigned kernel_id;
+  long long limit;  // SM cycles a wait may take before the CTA gives up
 };
 
 // Bounded wait of one thread on an mbarrier phase.
@@ -33,7 +35,7 @@ __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, con
   while (true) {
     if (ptx::mbar_try_wait(a, parity)) return true;
     if (*ab.flag) return false;
-    if (clock64() - t0 > kWaitTimeoutCycles) {
+    if (clock64() - t0 > ab.limit) {
       atomicOr(&ab.err->flags, kDevErrTimeout);
       const unsigned code = (ab.kernel_id << 24) | (role << 16) | (bar_id & 0xFFFFu);
       if (atomicCAS(&ab.err->where, 0u, code) == 0u) ab.err->item = item;

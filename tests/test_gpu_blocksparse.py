@@ -23,7 +23,15 @@ def sba():
 
 
 def _run(sba, w, kv_block=128, rows=None, heads=None, softmax_scale=None):
+    """Bounds from the oracle on the host arrays feed the oracle's attention, so the
+    reference key set never comes from the CUDA path; the GPU bounds (which the GPU
+    attention consumes) must equal them bit for bit."""
     m = w.mask
+    np_ = lambda t: t.cpu().numpy()
+    ref_bounds = oracle.sparse_mask_bounds(
+        np_(m.q_positions), np_(m.q_segment_ids), np_(m.kv_positions), np_(m.kv_segment_ids),
+        m.q_blocksize, kv_block, causal=m.causal, window_left=m.window_left,
+        window_right=m.window_right, padding_segment_id=m.padding_segment_id)
     bounds = sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions,
                                     m.kv_segment_ids, m.q_blocksize, kv_block, causal=m.causal,
                                     window_left=m.window_left, window_right=m.window_right,
@@ -35,10 +43,11 @@ def _run(sba, w, kv_block=128, rows=None, heads=None, softmax_scale=None):
                                         padding_segment_id=m.padding_segment_id,
                                         softmax_scale=softmax_scale)
     sba.check_error()
-    np_ = lambda t: t.cpu().numpy()
+    for name, g, r in zip(("lower", "upper", "lower_full", "upper_full"), bounds, ref_bounds):
+        assert np.array_equal(np_(g), r), f"GPU {name} bounds differ from the oracle's"
     ref, ref_lse = oracle.blocksparse_attention(
         to_np(w.q), to_np(w.k), to_np(w.v), np_(m.q_positions), np_(m.q_segment_ids),
-        np_(m.kv_positions), np_(m.kv_segment_ids), np_(bounds[0]), np_(bounds[1]),
+        np_(m.kv_positions), np_(m.kv_segment_ids), ref_bounds[0], ref_bounds[1],
         m.q_blocksize, kv_block, causal=m.causal, window_left=m.window_left,
         window_right=m.window_right, padding_segment_id=m.padding_segment_id, rows=rows,
         heads=heads, softmax_scale=softmax_scale)

@@ -15,7 +15,6 @@ import pytest
 import torch
 
 from selected_block_attention_gb300 import workloads
-from tests._parity import assert_attention_close, to_np
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -53,8 +52,11 @@ def test_noalloc_matches_workspace_entry_point_twice(sba):
                                                      **_kwargs(w))
         sba.check_error()
         assert got.data_ptr() == out.data_ptr()
-        assert_attention_close(to_np(got), to_np(ref), to_np(got_lse), to_np(ref_lse),
-                               what=f"noalloc seed {seed}")
+        # same kernels, same split count, same inputs: the results must be identical
+        # (a loose tolerance could hide partials left in the shared array by the
+        # previous call)
+        assert torch.equal(got, ref), f"noalloc seed {seed}: output differs"
+        assert torch.equal(got_lse, ref_lse), f"noalloc seed {seed}: LSE differs"
 
 
 def test_noalloc_full_decode_workload(sba):
@@ -65,8 +67,7 @@ def test_noalloc_full_decode_workload(sba):
     got, got_lse = sba.ragged_decode_fwd_noalloc(w.q, w.k, w.v, w.sequence_start,
                                                  w.sequence_end, **_kwargs(w))
     sba.check_error()
-    assert_attention_close(to_np(got), to_np(ref), to_np(got_lse), to_np(ref_lse),
-                           what="noalloc full")
+    assert torch.equal(got, ref) and torch.equal(got_lse, ref_lse), "noalloc full: differs"
 
 
 def test_noalloc_rejects_sizes_beyond_the_scratch(sba):
