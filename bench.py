@@ -14,7 +14,7 @@ sampled during the timed region) and ``rows``: the other workloads of the path
 multi-query attention), each timed the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-  python bench.py --case {nsa_prefill,nsa_varlen,blocksparse,decode,ragged_q4,ragged_chunk512}
+  python bench.py --case {nsa_prefill,nsa_varlen,blocksparse,mask_sweep,decode,ragged_q4,ragged_chunk512}
                   [--repeat R]
                   [--decode-batch B]      # profiling: launches only, no JSON line
 
@@ -568,6 +568,25 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
         "workload": m.name + " (dK/dV, kv blocks outer)", "us": round(ms * 1e3, 2),
         "GB/s": round(in_bytes / ms / 1e6, 1),
         "frac_hbm": round(in_bytes / ms / 1e6 / peaks["hbm_gbs"], 4)}
+    # the scaled sweep of the same recipe (B=64, T=131072): large enough to show bandwidth
+    ms_w = workloads.mask(device=dev, B=64, T=131072)
+    sweep = lambda: sba.sparse_mask_bounds(ms_w.q_positions, ms_w.q_segment_ids, ms_w.kv_positions,
+                                           ms_w.kv_segment_ids, 128, 128, causal=True,
+                                           window_left=1024, window_right=0)
+    for key, dk in (("sparse_mask_bounds_b64_t128k", False), ("sparse_mask_dkdv_bounds_b64_t128k", True)):
+        t = timed_steps(lambda: sba.sparse_mask_bounds(
+            ms_w.q_positions, ms_w.q_segment_ids, ms_w.kv_positions, ms_w.kv_segment_ids, 128, 128,
+            causal=True, window_left=1024, window_right=0, calculate_dkdv_mask=dk),
+            steps, warm, flush, stream)
+        ms = sum(t) / len(t)
+        sw_bytes = 4 * ms_w.q_positions.numel() * 4 + 4 * 64 * 1024 * 4
+        log(f"{key} {ms * 1e3:.2f} us")
+        rows[key] = {
+            "workload": ms_w.name + (" (dK/dV, kv blocks outer)" if dk else ""),
+            "us": round(ms * 1e3, 2), "GB/s": round(sw_bytes / ms / 1e6, 1),
+            "frac_hbm": round(sw_bytes / ms / 1e6 / peaks["hbm_gbs"], 4),
+            "bytes": int(sw_bytes)}
+    del ms_w, sweep
     lo, up, lof, upf = bnd["b"]
     fl = blocksparse_flops(w)
     t = timed_steps(lambda: sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids,
@@ -670,6 +689,11 @@ def run_case(args):
             sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids, m.kv_positions,
                                      m.kv_segment_ids, lo, up, lof, upf, 128, 128, causal=True,
                                      window_left=1024, window_right=0)
+    elif args.case == "mask_sweep":
+        m = workloads.mask(device=dev, B=64, T=131072)
+        fn = lambda: sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions,
+                                            m.kv_segment_ids, 128, 128, causal=True,
+                                            window_left=1024, window_right=0)
     elif args.case == "decode":
         w = workloads.decode(device=dev, B=args.decode_batch)
 

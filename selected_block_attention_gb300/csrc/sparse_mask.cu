@@ -5,12 +5,29 @@
 // kernel _compute_sparse_mask (both choices of outer operand) and the padding /
 // padding-segment remap / clip fix-up of define_sparse_mask_fn, fused into one launch.
 //
-// Layout of the work: grid (ceil(NB_outer / kWarps), B); warp w of a CTA owns one
-// outer block.  The CTA sweeps the inner blocks of its batch row in chunks: every warp
-// summarises inner blocks (min/max of positions and remapped segment ids) with
-// coalesced 16-byte loads and warp min/max reductions into shared memory, then each
-// warp tests its outer block against the chunk with one inner block per lane and
-// folds the lane results with warp min/max reductions.  Integer results are exact.
+// Main kernel (sparse_mask_cluster_kernel): one cluster of kCluster CTAs per batch row.
+//   1. every block of the row is summarised exactly once (min/max of positions and of
+//      remapped segment ids, coalesced 16-byte loads, several blocks in flight per
+//      warp, warp min/max reductions): CTA r of the cluster takes the r-th slice of the
+//      inner blocks and of the outer blocks;
+//   2. after a cluster barrier each CTA copies the whole row of inner summaries out of
+//      its peers' shared memory (distributed shared memory) and builds prefix maxima /
+//      suffix minima of the summary fields the attend test compares;
+//   3. per outer block (one lane each, so the searches of 32 outer blocks run side by
+//      side) those monotone arrays give, by binary search, a candidate range of inner
+//      blocks outside of which the attend test provably fails (e.g. under causal
+//      masking, once every later key block starts after the query block's last
+//      position, no later block can attend); the page's predicates are then evaluated
+//      exactly on the candidates only (by the same lane when every range of the warp
+//      is short, else one inner block per lane with warp min/max reductions) and
+//      clipped as the fix-up does.
+// Pruning never changes a result: a pruned block fails a necessary condition of the
+// attend test, and a full block must attend.  Integer results are exact.
+// Rows with more than kMaxInner inner blocks use the fallback kernel
+// (sparse_mask_bounds_kernel): one warp per outer block, inner summaries recomputed per
+// CTA in chunks.
+#include <cooperative_groups.h>
+
 #include <climits>
 
 #include "common.cuh"
@@ -189,6 +206,322 @@ sparse_mask_bounds_kernel(Side outer, Side inner, int causal, int window_left, i
   lower[out] = lo; upper[out] = up; lower_full[out] = lo_full; upper_full[out] = up_full;
 }
 
+// ------------------------------------------------------------------ cluster kernel
+namespace cg = cooperative_groups;
+
+constexpr int kCluster = 8;          // CTAs per batch row (portable cluster size)
+constexpr int kCWarps = 8;
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kMaxInner = 4096;      // inner blocks of a row held in shared memory
+constexpr int kMaxOuterSlice = 1024; // outer blocks per CTA
+constexpr int kUnroll = 4;           // blocks a warp summarises at once (loads in flight)
+
+// Summaries (pos_min, pos_max, seg_min, seg_max) of up to kUnroll blocks of one row at
+// once; blk[u] < 0 marks an unused slot.  Tokens at or beyond sd.T are padding.
+__device__ __forceinline__ void summarize_unrolled(const int* __restrict__ pos,
+                                                   const int* __restrict__ seg, const Side& sd,
+                                                   const int (&blk)[kUnroll], bool vec,
+                                                   int pad_id, int pad_remap,
+                                                   int4 (&out)[kUnroll]) {
+  const int lane = threadIdx.x & 31;
+  int pmin[kUnroll], pmax[kUnroll], smin[kUnroll], smax[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) {
+    pmin[u] = INT_MAX; pmax[u] = INT_MIN; smin[u] = INT_MAX; smax[u] = INT_MIN;
+  }
+  if (vec) {
+    for (int o = lane * 4; o < sd.block; o += 128) {
+      int4 pv[kUnroll], sv[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long t = (long long)blk[u] * sd.block + o;
+        if (blk[u] >= 0 && t < sd.T) {
+          pv[u] = __ldcs(reinterpret_cast<const int4*>(pos + t));
+          sv[u] = __ldcs(reinterpret_cast<const int4*>(seg + t));
+        } else {
+          pv[u] = make_int4(sd.pos_fill, sd.pos_fill, sd.pos_fill, sd.pos_fill);
+          sv[u] = make_int4(pad_id, pad_id, pad_id, pad_id);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int p4[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+        const int s4[4] = {sv[u].x, sv[u].y, sv[u].z, sv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int sg = s4[e] == pad_id ? pad_remap : s4[e];
+          pmin[u] = min(pmin[u], p4[e]); pmax[u] = max(pmax[u], p4[e]);
+          smin[u] = min(smin[u], sg); smax[u] = max(smax[u], sg);
+        }
+      }
+    }
+  } else {
+    for (int o = lane; o < sd.block; o += 32) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const long long t = (long long)blk[u] * sd.block + o;
+        int pp = sd.pos_fill, sg = pad_id;
+        if (blk[u] >= 0 && t < sd.T) { pp = pos[t]; sg = seg[t]; }
+        sg = sg == pad_id ? pad_remap : sg;
+        pmin[u] = min(pmin[u], pp); pmax[u] = max(pmax[u], pp);
+        smin[u] = min(smin[u], sg); smax[u] = max(smax[u], sg);
+      }
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u)
+    out[u] = make_int4(__reduce_min_sync(0xffffffffu, pmin[u]), __reduce_max_sync(0xffffffffu, pmax[u]),
+                       __reduce_min_sync(0xffffffffu, smin[u]), __reduce_max_sync(0xffffffffu, smax[u]));
+}
+
+// Summaries of blocks [b0, b0 + n) of one side into dst[0 .. n), kUnroll per warp step.
+__device__ __forceinline__ void summarize_slice(const int* pos, const int* seg, const Side& sd,
+                                                int b0, int n, bool vec, int pad_id,
+                                                int pad_remap, int4* dst) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int base = warp * kUnroll; base < n; base += kCWarps * kUnroll) {
+    int blk[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) blk[u] = base + u < n ? b0 + base + u : -1;
+    int4 sm[kUnroll];
+    summarize_unrolled(pos, seg, sd, blk, vec, pad_id, pad_remap, sm);
+    if (lane == 0) {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u)
+        if (base + u < n) dst[base + u] = sm[u];
+    }
+  }
+}
+
+// The six monotone arrays of one row from its inner summaries `v`, in one pass over the
+// CTA: out[0..2] = prefix maxima of pos_min, pos_max, seg_max (out[f][i] = max over
+// v[0..i]) and out[3..5] = suffix minima of pos_min, pos_max, seg_min (out[f][i] = min
+// over v[i..n-1]).  Thread t owns a contiguous chunk (from the left for the prefix
+// arrays, from the right for the suffix arrays); chunk totals are combined with warp
+// shuffles and one exchange of warp totals through `tmp` (6 * kCWarps ints), then each
+// thread rescans its chunk with that offset and writes it.  Ends with the CTA
+// synchronised.
+__device__ void cta_scans(const int4* v, int n, int* const (&out)[6], int* tmp) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = (n + kCThreads - 1) / kCThreads;
+  const int plo = min(tid * chunk, n), phi = min(plo + chunk, n);       // prefix chunk
+  const int shi = max(n - tid * chunk, 0), slo = max(shi - chunk, 0);   // suffix chunk
+  int run[6] = {INT_MIN, INT_MIN, INT_MIN, INT_MAX, INT_MAX, INT_MAX};
+  for (int i = plo; i < phi; ++i) {
+    const int4 x = v[i];
+    run[0] = max(run[0], x.x); run[1] = max(run[1], x.y); run[2] = max(run[2], x.w);
+  }
+  for (int i = slo; i < shi; ++i) {
+    const int4 x = v[i];
+    run[3] = min(run[3], x.x); run[4] = min(run[4], x.y); run[5] = min(run[5], x.z);
+  }
+  // inclusive scan of the chunk totals in thread order, within the warp
+  int incl[6];
+#pragma unroll
+  for (int f = 0; f < 6; ++f) incl[f] = run[f];
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+#pragma unroll
+    for (int f = 0; f < 6; ++f) {
+      const int o = __shfl_up_sync(0xffffffffu, incl[f], d);
+      if (lane >= d) incl[f] = f < 3 ? max(incl[f], o) : min(incl[f], o);
+    }
+  }
+  if (lane == 31) {
+#pragma unroll
+    for (int f = 0; f < 6; ++f) tmp[f * kCWarps + warp] = incl[f];
+  }
+  __syncthreads();
+  // exclusive offset of this thread: earlier warps' totals, then earlier lanes'
+  int ex[6];
+#pragma unroll
+  for (int f = 0; f < 6; ++f) {
+    int wt = lane < warp ? tmp[f * kCWarps + lane] : (f < 3 ? INT_MIN : INT_MAX);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+      const int o = __shfl_xor_sync(0xffffffffu, wt, d);
+      wt = f < 3 ? max(wt, o) : min(wt, o);
+    }
+    int e = __shfl_up_sync(0xffffffffu, incl[f], 1);
+    if (lane == 0) e = f < 3 ? INT_MIN : INT_MAX;
+    ex[f] = f < 3 ? max(e, wt) : min(e, wt);
+  }
+  for (int i = plo; i < phi; ++i) {
+    const int4 x = v[i];
+    ex[0] = max(ex[0], x.x); ex[1] = max(ex[1], x.y); ex[2] = max(ex[2], x.w);
+    out[0][i] = ex[0]; out[1][i] = ex[1]; out[2][i] = ex[2];
+  }
+  for (int i = shi - 1; i >= slo; --i) {
+    const int4 x = v[i];
+    ex[3] = min(ex[3], x.x); ex[4] = min(ex[4], x.y); ex[5] = min(ex[5], x.z);
+    out[3][i] = ex[3]; out[4][i] = ex[4]; out[5][i] = ex[5];
+  }
+  __syncthreads();
+}
+
+// First index i in [0, n) with pred(i) true, for a predicate that is false then true
+// along i (n if it never holds).
+template <typename P>
+__device__ __forceinline__ int first_true(int n, P pred) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pred(mid)) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+template <bool kQueryOuter>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kCThreads, 4)
+sparse_mask_cluster_kernel(Side outer, Side inner, int causal, int window_left, int window_right,
+                           int pad_id, int pad_remap, int* __restrict__ lower,
+                           int* __restrict__ upper, int* __restrict__ lower_full,
+                           int* __restrict__ upper_full, int vec_outer, int vec_inner) {
+  extern __shared__ int4 csm[];
+  __shared__ int scan_tmp[6 * kCWarps];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int r = static_cast<int>(cluster.block_rank());
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.y;
+  const int nbi = inner.nb, nbo = outer.nb;
+  const int islice = (nbi + kCluster - 1) / kCluster;
+  const int oslice = (nbo + kCluster - 1) / kCluster;
+  int4* own_inner = csm;                  // [islice]: read by the whole cluster
+  int4* all_inner = own_inner + islice;   // [nbi]
+  int4* own_outer = all_inner + nbi;      // [oslice]
+  int* pmx_pmin = reinterpret_cast<int*>(own_outer + oslice);  // prefix max of pos_min
+  int* pmx_pmax = pmx_pmin + nbi;                               // prefix max of pos_max
+  int* pmx_smax = pmx_pmax + nbi;                               // prefix max of seg_max
+  int* smn_pmin = pmx_smax + nbi;                               // suffix min of pos_min
+  int* smn_pmax = smn_pmin + nbi;                               // suffix min of pos_max
+  int* smn_smin = smn_pmax + nbi;                               // suffix min of seg_min
+
+  // 1. this CTA's slices of the row, each block summarised once
+  const int i0 = r * islice, ni = max(0, min(islice, nbi - i0));
+  const int o0 = r * oslice, no = max(0, min(oslice, nbo - o0));
+  summarize_slice(inner.pos + (long long)b * inner.T, inner.seg + (long long)b * inner.T, inner,
+                  i0, ni, vec_inner != 0, pad_id, pad_remap, own_inner);
+  summarize_slice(outer.pos + (long long)b * outer.T, outer.seg + (long long)b * outer.T, outer,
+                  o0, no, vec_outer != 0, pad_id, pad_remap, own_outer);
+
+  // 2. the whole row of inner summaries from the cluster's shared memory
+  cluster.sync();
+  for (int i = threadIdx.x; i < nbi; i += kCThreads) {
+    const int4* peer = cluster.map_shared_rank(own_inner, i / islice);
+    all_inner[i] = peer[i % islice];
+  }
+  // This CTA's slice must stay in place until every peer has copied it: arrive now,
+  // wait at the very end of the kernel (the barrier's latency hides behind the work).
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  __syncthreads();
+  {
+    int* const arrays[6] = {pmx_pmin, pmx_pmax, pmx_smax, smn_pmin, smn_pmax, smn_smin};
+    cta_scans(all_inner, nbi, arrays, scan_tmp);
+  }
+
+  // 3. candidate ranges with one lane per outer block (the binary searches run in
+  // parallel across lanes), then per outer block the exact predicates on its candidates
+  // with one inner block per lane.  Outer block jl goes to warp jl % kCWarps, lane
+  // (jl / kCWarps) % 32, so every warp gets work.
+  for (int g0 = 0; g0 < no; g0 += kCWarps * 32) {
+    const int jl = g0 + lane * kCWarps + warp;
+    int4 o = make_int4(0, 0, 0, 0);
+    int clo = 0, cup = 0;
+    if (jl < no) {
+      o = own_outer[jl];
+      const long long o_min = o.x, o_max = o.y;
+      // lower end: the first block from which every necessary "inner >= threshold"
+      // condition can hold (prefix maxima: each condition, and so their conjunction, is
+      // false then true along the row); upper end: the first block from which some
+      // necessary "inner <= threshold" condition fails for it and every later block
+      // (suffix minima: the disjunction is false then true as well)
+      const bool wl_on = window_left >= 0, wr_on = window_right >= 0, causal_on = causal != 0;
+      const long long thr_l = o_min - window_left, thr_r = o_max + window_right;
+      if (kQueryOuter) {
+        clo = first_true(nbi, [&](int i) {
+          return pmx_smax[i] >= o.z && (!wl_on || (long long)pmx_pmin[i] >= thr_l);
+        });
+        cup = first_true(nbi, [&](int i) {
+          return smn_smin[i] > o.w || (causal_on && (long long)smn_pmin[i] > o_max) ||
+                 (wr_on && (long long)smn_pmax[i] > thr_r);
+        });
+      } else {
+        clo = first_true(nbi, [&](int i) {
+          return pmx_smax[i] >= o.z && (!causal_on || (long long)pmx_pmax[i] >= o_min) &&
+                 (!wl_on || (long long)pmx_pmax[i] >= thr_l);
+        });
+        cup = first_true(nbi, [&](int i) {
+          return smn_smin[i] > o.w || (wr_on && (long long)smn_pmin[i] > thr_r);
+        });
+      }
+    }
+    // the page's predicates on the candidates of one outer block, folded into the
+    // four bounds (clipped as the fix-up does) and stored
+    auto eval_range = [&](const int4& ob, int i_begin, int i_end, int i_step, int& lo, int& up,
+                          int& lo_full, int& up_full) {
+      const long long o_min = ob.x, o_max = ob.y;
+      for (int i = i_begin; i < i_end; i += i_step) {
+        const int4 in = all_inner[i];
+        const bool attend_seg = (in.z <= ob.w) && (ob.z <= in.w);
+        const bool full_seg = (ob.z == ob.w) && (in.z == in.w);
+        bool attend_pos, full_pos;
+        position_tests<kQueryOuter>(causal != 0, window_left, window_right, o_min, o_max, in.x,
+                                    in.y, attend_pos, full_pos);
+        const bool attend = attend_pos && attend_seg && !(in.z == pad_remap);
+        const bool full = full_seg && full_pos && attend;
+        if (attend) { up = max(up, i + 1); lo = min(lo, i); }
+        if (full) { up_full = max(up_full, i + 1); lo_full = min(lo_full, i); }
+      }
+    };
+    auto store = [&](long long out, bool all_pad, int lo, int up, int lo_full, int up_full) {
+      if (all_pad) {  // query / key block made only of padding
+        lower[out] = 0; upper[out] = 0; lower_full[out] = 0; upper_full[out] = 0;
+        return;
+      }
+      lo = min(max(lo, 0), nbi);
+      up = min(max(up, 0), nbi);
+      lo = min(lo, up);
+      lo_full = max(min(max(lo_full, 0), nbi), lo);
+      up_full = min(max(min(max(up_full, 0), nbi), lo_full), up);
+      lower[out] = lo; upper[out] = up; lower_full[out] = lo_full; upper_full[out] = up_full;
+    };
+    const bool mine = jl < no;
+    const bool pad_blk = mine && (o.z == o.w) && (o.z == pad_remap);
+    const int ncand = mine && !pad_blk ? max(cup - clo, 0) : 0;
+    if (__reduce_max_sync(0xffffffffu, ncand) <= 64) {
+      // short ranges: each lane evaluates its own outer block
+      if (mine) {
+        int up = 0, lo = nbi, up_full = 0, lo_full = nbi;
+        if (!pad_blk) eval_range(o, clo, cup, 1, lo, up, lo_full, up_full);
+        store((long long)b * nbo + o0 + jl, pad_blk, lo, up, lo_full, up_full);
+      }
+      continue;
+    }
+    // long ranges: the warp evaluates one outer block at a time, one inner block per lane
+    for (int k = 0; k < 32; ++k) {
+      const int jk = g0 + k * kCWarps + warp;
+      if (jk >= no) break;  // warp-uniform
+      const int4 ok4 = make_int4(__shfl_sync(0xffffffffu, o.x, k), __shfl_sync(0xffffffffu, o.y, k),
+                                 __shfl_sync(0xffffffffu, o.z, k), __shfl_sync(0xffffffffu, o.w, k));
+      const int klo = __shfl_sync(0xffffffffu, clo, k), kup = __shfl_sync(0xffffffffu, cup, k);
+      const bool kpad = (ok4.z == ok4.w) && (ok4.z == pad_remap);
+      int up = 0, lo = nbi, up_full = 0, lo_full = nbi;
+      if (!kpad) eval_range(ok4, klo + lane, kup, 32, lo, up, lo_full, up_full);
+      up = __reduce_max_sync(0xffffffffu, up);
+      lo = __reduce_min_sync(0xffffffffu, lo);
+      up_full = __reduce_max_sync(0xffffffffu, up_full);
+      lo_full = __reduce_min_sync(0xffffffffu, lo_full);
+      if (lane == 0) store((long long)b * nbo + o0 + jk, kpad, lo, up, lo_full, up_full);
+    }
+  }
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+size_t cluster_smem_bytes(int nbi, int nbo) {
+  const size_t islice = (nbi + kCluster - 1) / kCluster, oslice = (nbo + kCluster - 1) / kCluster;
+  return 16 * (islice + nbi + oslice) + 6 * 4 * static_cast<size_t>(nbi);
+}
+
 }  // namespace
 
 unsigned read_and_clear_error_mask(cudaStream_t, std::string*) {
@@ -211,16 +544,45 @@ int launch_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const 
   const Side qside{q_pos, q_seg, Tq, q_block, nbq, -1};
   const Side kvside{kv_pos, kv_seg, Tkv, kv_block, nbkv, INT_MAX};
   const int pad_remap = nbkv * kv_block + 1;  // padded Tkv + 1
-  if (dkdv) {
-    dim3 grid((nbkv + kWarps - 1) / kWarps, B);
-    sparse_mask_bounds_kernel<false><<<grid, kThreads, 0, stream>>>(
-        kvside, qside, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
-        lower_full, upper_full, vec_kv, vec_q);
+  const Side& outer = dkdv ? kvside : qside;
+  const Side& inner = dkdv ? qside : kvside;
+  const int vec_o = dkdv ? vec_kv : vec_q, vec_i = dkdv ? vec_q : vec_kv;
+  const int oslice = (outer.nb + kCluster - 1) / kCluster;
+  if (inner.nb <= kMaxInner && oslice <= kMaxOuterSlice) {
+    // one cluster per batch row, each block summarised once
+    const size_t smem = cluster_smem_bytes(inner.nb, outer.nb);
+    // the largest request (kMaxInner inner blocks, kMaxOuterSlice outer blocks per CTA)
+    static const size_t kSmemMax = cluster_smem_bytes(kMaxInner, kMaxOuterSlice * kCluster);
+    static bool attr_done[2] = {false, false};
+    if (!attr_done[dkdv]) {
+      cudaError_t e = dkdv ? cudaFuncSetAttribute(sparse_mask_cluster_kernel<false>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(kSmemMax))
+                           : cudaFuncSetAttribute(sparse_mask_cluster_kernel<true>,
+                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  static_cast<int>(kSmemMax));
+      if (e != cudaSuccess) return cuda_error(e, "sparse_mask_bounds: set smem attribute");
+      attr_done[dkdv] = true;
+    }
+    dim3 grid(kCluster, B);
+    if (dkdv)
+      sparse_mask_cluster_kernel<false><<<grid, kCThreads, smem, stream>>>(
+          outer, inner, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
+          lower_full, upper_full, vec_o, vec_i);
+    else
+      sparse_mask_cluster_kernel<true><<<grid, kCThreads, smem, stream>>>(
+          outer, inner, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
+          lower_full, upper_full, vec_o, vec_i);
   } else {
-    dim3 grid((nbq + kWarps - 1) / kWarps, B);
-    sparse_mask_bounds_kernel<true><<<grid, kThreads, 0, stream>>>(
-        qside, kvside, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
-        lower_full, upper_full, vec_q, vec_kv);
+    dim3 grid((outer.nb + kWarps - 1) / kWarps, B);
+    if (dkdv)
+      sparse_mask_bounds_kernel<false><<<grid, kThreads, 0, stream>>>(
+          outer, inner, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
+          lower_full, upper_full, vec_o, vec_i);
+    else
+      sparse_mask_bounds_kernel<true><<<grid, kThreads, 0, stream>>>(
+          outer, inner, causal, window_left, window_right, pad_id, pad_remap, lower, upper,
+          lower_full, upper_full, vec_o, vec_i);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "sparse_mask_bounds launch");

@@ -91,6 +91,77 @@ def test_many_kv_blocks_chunked(sba):
     _check(sba, pos, seg, pos, seg, 512, 32, causal=True, window_left=2000, window_right=-1)
 
 
+@pytest.mark.parametrize("dkdv", [False, True])
+@pytest.mark.parametrize("seed", range(8))
+def test_random_unsorted(sba, seed, dkdv):
+    """Positions and segment ids in no order at all (the candidate-range pruning must hold
+    for any input, not only monotone ones), padding scattered inside the rows, both
+    window sides, causal or not."""
+    rng = np.random.default_rng(300 + seed)
+    B = int(rng.integers(1, 5))
+    Tq, Tkv = int(rng.integers(200, 3000)), int(rng.integers(200, 3000))
+    qb, kb = int(rng.choice([4, 16, 33, 64])), int(rng.choice([4, 16, 31, 64]))
+    span = int(rng.choice([50, 3000, 1 << 30]))
+    qp = rng.integers(-span, span, size=(B, Tq))
+    kp = rng.integers(-span, span, size=(B, Tkv))
+    if seed % 4 == 1:  # mostly sorted with a few swaps
+        qp.sort(axis=1); kp.sort(axis=1)
+        for a in (qp, kp):
+            for _ in range(5):
+                i, j = rng.integers(0, a.shape[1], 2)
+                a[:, [i, j]] = a[:, [j, i]]
+    qs = rng.integers(0, 8, size=(B, Tq))
+    ks = rng.integers(0, 8, size=(B, Tkv))
+    if seed % 2:
+        qs.sort(axis=1); ks.sort(axis=1)
+    qs[rng.random((B, Tq)) < 0.05] = -1
+    ks[rng.random((B, Tkv)) < 0.05] = -1
+    wl = int(rng.choice([-1, 0, 37, 1000]))
+    wr = int(rng.choice([-1, 0, 64, 2000]))
+    _check(sba, qp, qs, kp, ks, qb, kb, causal=bool(seed % 3), window_left=wl, window_right=wr,
+           padding_segment_id=-1, calculate_dkdv_mask=dkdv)
+
+
+@pytest.mark.parametrize("dkdv", [False, True])
+def test_more_inner_blocks_than_shared_memory_holds(sba, dkdv):
+    """5,000 inner blocks per row: beyond the 4,096 the one-cluster-per-row kernel keeps
+    in shared memory, so the chunked kernel runs."""
+    T = 40000
+    pos = np.arange(T)[None]
+    seg = (np.arange(T) // 5000)[None]
+    qb, kb = (512, 8) if not dkdv else (8, 512)
+    _check(sba, pos, seg, pos, seg, qb, kb, causal=True, window_left=2000, window_right=-1,
+           calculate_dkdv_mask=dkdv)
+
+
+def test_many_batch_rows(sba):
+    """300 batch rows (one cluster each), ragged tail, both directions."""
+    m = workloads.mask(device="cpu", B=300, T=1000, mean_doc=150, pad_tail=37, block=64,
+                       window=(200, 0))
+    a = [m.q_positions.numpy(), m.q_segment_ids.numpy(), m.kv_positions.numpy(),
+         m.kv_segment_ids.numpy()]
+    for dkdv in (False, True):
+        _check(sba, *a, 64, 32, causal=True, window_left=200, window_right=0,
+               calculate_dkdv_mask=dkdv)
+
+
+def test_scaled_sweep_sampled(sba):
+    """The scaled bandwidth workload (B=64, T=131072, block 128, window (1024, 0)) in the
+    launch the bench times; the oracle checks rows 0, 31 and 63 (one long row costs it
+    a few seconds)."""
+    m = workloads.mask(device=DEV, B=64, T=131072)
+    got = sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions, m.kv_segment_ids,
+                                 128, 128, causal=True, window_left=1024, window_right=0)
+    sba.check_error()
+    for b in (0, 31, 63):
+        sl = lambda t: t[b:b + 1].cpu().numpy()
+        ref = oracle.sparse_mask_bounds(sl(m.q_positions), sl(m.q_segment_ids), sl(m.kv_positions),
+                                        sl(m.kv_segment_ids), 128, 128, causal=True,
+                                        window_left=1024, window_right=0)
+        for name, g, r in zip(("lower", "upper", "lower_full", "upper_full"), got, ref):
+            np.testing.assert_array_equal(g[b:b + 1].cpu().numpy(), r, err_msg=f"{name} row {b}")
+
+
 # --------------------------------------------------------------------------- dK/dV bounds
 
 def test_dkdv_page_example_transposed(sba):
