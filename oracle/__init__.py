@@ -19,6 +19,8 @@ source documentation pages named in its docstring:
   ``apply_logits_soft_cap`` / ``apply_attention_sinks_block``.
 * ``ragged_flash_attention``   -- same page, ``ragged_flash_attention_xla`` (Q queries
   per row, the last Q tokens of its range).
+* ``nsa_select_attention_backward`` -- gradients (dq, dk, dv) of the selection
+  forward, the softmax backward over the same explicit key sets.
 
 Every function is pinned by ``tests/test_oracle_*.py`` against closed forms,
 library routines (torch SDPA in float64), brute force on tiny inputs and the
@@ -30,6 +32,7 @@ from .sparse_mask import sparse_mask_bounds
 from .blocksparse import blocksparse_attention
 from .ragged_decode import ragged_decode_attention
 from .ragged_attention import ragged_flash_attention
+from .nsa_backward import nsa_select_attention_backward
 
 __all__ = [
     "nsa_select_attention",
@@ -38,4 +41,5 @@ __all__ = [
     "blocksparse_attention",
     "ragged_decode_attention",
     "ragged_flash_attention",
+    "nsa_select_attention_backward",
 ]
