@@ -110,6 +110,54 @@ SBA_API int sba_nsa_select_fwd(const void* q, const void* k, const void* v, cons
                        void* out, float* lse, sba_stream_t stream);
 
 /*
+ * sba_nsa_select_bwd_workspace_size -- bytes of device workspace sba_nsa_select_bwd
+ * needs (Delta per query row, and the per-key-block token lists).  num_seqs = 0 for
+ * fixed-length rows.  Returns 0 for invalid sizes.
+ */
+SBA_API size_t sba_nsa_select_bwd_workspace_size(int B, int T, int Hq, int Hkv, int S,
+                                                 int num_seqs);
+
+/*
+ * sba_nsa_select_bwd -- gradients of sba_nsa_select_fwd with respect to q, k and v.
+ *
+ * Defined by: "ejkernel.modules.operations.native_sparse_attention" (operation API
+ * page), NativeSparseAttention.run / native_sparse_attention, which is differentiable
+ * in query, key and value.  The page gives no gradient algorithm; the result is the
+ * gradient of the forward above (no gate): for each row (token, query head) with its
+ * explicit key set and P = exp(scale * q.k - LSE) over that set,
+ *   dV_k += P_k dO,  dS_k = P_k (dO.v_k - dO.O),  dQ = scale * sum_k dS_k k_k,
+ *   dK_k += scale * dS_k q.
+ * A gate g_slc applied in the forward is handled by the caller: pass dO * g_slc as
+ * d_out (the gate's own gradient is rowsum(dO * O_ungated)).
+ *
+ *  q, k, v, block_indices, block_counts, block_count_scalar, S, cu_seqlens, num_seqs,
+ *  B, T, Hq, Hkv, D, block_size, causal, softmax_scale, dtype: exactly as passed to
+ *                the forward that produced `out` and `lse`
+ *  out           [B, T, Hq, D] dtype: the forward's output (ungated)
+ *  lse           [B, T, Hq] float32: the forward's log-sum-exp (required)
+ *  d_out         [B, T, Hq, D] dtype: gradient of the loss with respect to out
+ *  dq            [B, T, Hq, D] dtype (written)
+ *  dk, dv        [B, T, Hkv, D] dtype (written; keys no token selected get 0)
+ *  workspace     device scratch of at least sba_nsa_select_bwd_workspace_size(B, T, Hq,
+ *                Hkv, S, cu_seqlens ? num_seqs : 0) bytes, 256-byte aligned, caller-owned;
+ *                needs no initialisation.
+ * Supported: dtype bf16 (tensor cores, fp32 accumulation; P and dS rounded to bf16
+ * before their products), D == 128, block_size == 64, Hq / Hkv in {8, 16}, S <= 32;
+ * other valid arguments return SBA_ERR_UNSUPPORTED.  dK / dV sum many tokens in an
+ * order set by atomics, so results may differ in the last bits between runs.
+ * Internally, on `stream`: a memset, three small index kernels (Delta and counts, offsets,
+ * token lists), the dQ kernel and the dK/dV kernel.
+ */
+SBA_API int sba_nsa_select_bwd(const void* q, const void* k, const void* v, const void* out,
+                               const float* lse, const void* d_out,
+                               const int32_t* block_indices, const int32_t* block_counts,
+                               int block_count_scalar, int S, const int32_t* cu_seqlens,
+                               int num_seqs, int B, int T, int Hq, int Hkv, int D, int block_size,
+                               int causal, float softmax_scale, int dtype, void* dq, void* dk,
+                               void* dv, void* workspace, size_t workspace_bytes,
+                               sba_stream_t stream);
+
+/*
  * sba_nsa_select_host_workspace_size -- bytes of device staging memory that
  * sba_nsa_select_fwd_host needs for the given shapes: device copies of q, k, v,
  * block_indices, block_counts (has_counts), g_slc (has_gate), out and lse (has_lse),

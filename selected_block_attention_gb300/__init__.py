@@ -29,7 +29,8 @@ __all__ = [
     "blocksparse_attn_fwd", "ragged_decode_fwd", "ragged_decode_fwd_noalloc",
     "ragged_decode_workspace_size", "ragged_flash_attention_fwd",
     "ragged_flash_attention_workspace_size", "l2_read_probe", "check_error",
-    "set_wait_timeout_cycles", "get_wait_timeout_cycles", "EXPORTED_SYMBOLS",
+    "set_wait_timeout_cycles", "get_wait_timeout_cycles", "nsa_select_bwd",
+    "nsa_select_bwd_workspace_size", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -40,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "sba_ragged_flash_attention_fwd", "sba_l2_read_probe", "sba_check_error",
     "sba_nsa_select_host_workspace_size", "sba_nsa_select_fwd_host",
     "sba_set_wait_timeout_cycles", "sba_get_wait_timeout_cycles",
+    "sba_nsa_select_bwd", "sba_nsa_select_bwd_workspace_size",
 )
 
 SBA_BF16, SBA_F32 = 0, 1
@@ -109,6 +111,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
     lib.sba_l2_read_probe.restype = ci
     lib.sba_check_error.argtypes = [vp]
     lib.sba_check_error.restype = ci
+    lib.sba_nsa_select_bwd_workspace_size.argtypes = [ci] * 6
+    lib.sba_nsa_select_bwd_workspace_size.restype = csz
+    lib.sba_nsa_select_bwd.argtypes = [vp, vp, vp, vp, f32p, vp, i32p, i32p, ci, ci, i32p, ci, ci, ci,
+                                       ci, ci, ci, ci, ci, cf, ci, vp, vp, vp, vp, csz, vp]
+    lib.sba_nsa_select_bwd.restype = ci
     lib.sba_set_wait_timeout_cycles.argtypes = [ctypes.c_longlong]
     lib.sba_set_wait_timeout_cycles.restype = ci
     lib.sba_get_wait_timeout_cycles.argtypes = []
@@ -198,6 +205,49 @@ def nsa_select_fwd(q, k, v, block_indices, block_counts, block_size, *, cu_seqle
         B, T, Hq, Hkv, D, int(block_size), int(bool(causal)),
         float(softmax_scale or 0.0), dtype, _ptr(out), _ptr(lse), _stream(dev))
     return out, lse
+
+
+def nsa_select_bwd_workspace_size(B, T, Hq, Hkv, S, num_seqs=0) -> int:
+    return int(load_library().sba_nsa_select_bwd_workspace_size(B, T, Hq, Hkv, S, num_seqs))
+
+
+def nsa_select_bwd(q, k, v, out, lse, d_out, block_indices, block_counts, block_size, *,
+                   cu_seqlens=None, causal=True, softmax_scale=None, dq=None, dk=None, dv=None,
+                   workspace=None):
+    """Gradients (dq, dk, dv) of the selection forward (bf16): ``out`` and ``lse`` are
+    the forward's results for the same arguments, ``d_out`` the gradient of the loss
+    with respect to ``out``."""
+    lib = load_library()
+    B, T, Hq, D = q.shape
+    Hkv = k.shape[2]
+    S = block_indices.shape[-1]
+    counts_t = None if isinstance(block_counts, int) else _i32(block_counts, "block_counts")
+    dev = _dev(q, k, v, out, lse, d_out, block_indices, counts_t, cu_seqlens, dq, dk, dv, workspace)
+    _i32(block_indices, "block_indices")
+    if any(t.dtype != q.dtype for t in (k, v, out, d_out)):
+        raise TypeError("q, k, v, out and d_out must share a dtype")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
+    dtype = {torch.bfloat16: SBA_BF16, torch.float32: SBA_F32}.get(q.dtype)
+    if dtype is None:
+        raise TypeError("q must be bfloat16 or float32")
+    num_seqs = 0
+    if cu_seqlens is not None:
+        _i32(cu_seqlens, "cu_seqlens")
+        num_seqs = cu_seqlens.numel() - 1
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if workspace is None:
+        need = nsa_select_bwd_workspace_size(B, T, Hq, Hkv, S, num_seqs)
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _call(dev, lib.sba_nsa_select_bwd,
+          _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(d_out), _ptr(block_indices),
+          _ptr(counts_t), int(block_counts) if counts_t is None else 0, S, _ptr(cu_seqlens),
+          num_seqs, B, T, Hq, Hkv, D, int(block_size), int(bool(causal)),
+          float(softmax_scale or 0.0), dtype, _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+          workspace.numel() * workspace.element_size(), _stream(dev))
+    return dq, dk, dv
 
 
 def nsa_select_host_workspace_size(B, T, Hq, Hkv, D, S, dtype=SBA_BF16, has_counts=True,

@@ -20,8 +20,8 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsba.so")
 
-SOURCES = ["api.cu", "sparse_mask.cu", "nsa_select.cu", "blocksparse_attn.cu", "ragged_decode.cu",
-           "probe.cu"]
+SOURCES = ["api.cu", "sparse_mask.cu", "nsa_select.cu", "nsa_backward.cu", "blocksparse_attn.cu",
+           "ragged_decode.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr", "-I", INCLUDE]

@@ -182,6 +182,50 @@ int sba_nsa_select_fwd(const void* q, const void* k, const void* v, const void* 
                            reinterpret_cast<cudaStream_t>(stream));
 }
 
+size_t sba_nsa_select_bwd_workspace_size(int B, int T, int Hq, int Hkv, int S, int num_seqs) {
+  if (B < 1 || T < 1 || Hq < 1 || Hkv < 1 || S < 1 || num_seqs < 0) return 0;
+  return nsa_bwd_workspace_bytes(B, T, Hq, Hkv, S, num_seqs);
+}
+
+int sba_nsa_select_bwd(const void* q, const void* k, const void* v, const void* out,
+                       const float* lse, const void* d_out, const int32_t* block_indices,
+                       const int32_t* block_counts, int block_count_scalar, int S,
+                       const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv, int D,
+                       int block_size, int causal, float softmax_scale, int dtype, void* dq,
+                       void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                       sba_stream_t stream) {
+  g_last_error.clear();
+  SBA_REQUIRE(q && k && v && out && lse && d_out && block_indices && dq && dk && dv,
+              "null tensor pointer");
+  SBA_REQUIRE(B >= 1 && T >= 1 && Hq >= 1 && Hkv >= 1, "sizes must be positive");
+  SBA_REQUIRE(Hq % Hkv == 0, "Hq must be a multiple of Hkv");
+  SBA_REQUIRE(S >= 1, "S (selected-block slots) must be >= 1");
+  SBA_REQUIRE(dtype == SBA_BF16 || dtype == SBA_F32, "dtype must be SBA_BF16 or SBA_F32");
+  SBA_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) && aligned16(d_out) &&
+                  aligned16(dq) && aligned16(dk) && aligned16(dv) && aligned16(lse),
+              "tensors must be 16-byte aligned");
+  SBA_REQUIRE(cu_seqlens == nullptr || (num_seqs >= 1 && B == 1),
+              "cu_seqlens needs num_seqs >= 1 and B == 1");
+  SBA_REQUIRE(block_counts != nullptr || block_count_scalar >= 0,
+              "block_count_scalar must be >= 0");
+  SBA_REQUIRE(std::isfinite(softmax_scale), "softmax_scale must be finite");
+  SBA_SUPPORT(dtype == SBA_BF16, "the backward supports bf16 only");
+  SBA_SUPPORT(D == 128, "the backward supports D == 128 only");
+  SBA_SUPPORT(block_size == 64, "the backward supports block_size == 64 only");
+  SBA_SUPPORT(Hq / Hkv == 8 || Hq / Hkv == 16, "the backward supports Hq / Hkv in {8, 16}");
+  SBA_SUPPORT(S <= 32, "S must be <= 32");
+  SBA_SUPPORT((long long)B * T * Hq < (1LL << 31), "B * T * Hq must be < 2^31");
+  const int ns = cu_seqlens ? num_seqs : 0;
+  SBA_REQUIRE(workspace != nullptr && (reinterpret_cast<uintptr_t>(workspace) & 255u) == 0 &&
+                  workspace_bytes >= nsa_bwd_workspace_bytes(B, T, Hq, Hkv, S, ns),
+              "workspace missing, not 256-byte aligned or smaller than "
+              "sba_nsa_select_bwd_workspace_size()");
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
+  return launch_nsa_select_bwd(q, k, v, out, lse, d_out, block_indices, block_counts,
+                               block_count_scalar, S, cu_seqlens, ns, B, T, Hq, Hkv, causal ? 1 : 0,
+                               scale, dq, dk, dv, workspace, reinterpret_cast<cudaStream_t>(stream));
+}
+
 size_t sba_nsa_select_host_workspace_size(int B, int T, int Hq, int Hkv, int D, int S,
                                           int dtype, int has_counts, int has_gate,
                                           int has_lse) {
@@ -447,7 +491,8 @@ int sba_check_error(sba_stream_t stream) {
   if (e != cudaSuccess) return cuda_error(e, "sba_check_error: stream synchronize");
   std::string where;
   unsigned w = read_and_clear_error_nsa(s, &where) | read_and_clear_error_mask(s, &where) |
-               read_and_clear_error_blocksparse(s, &where) | read_and_clear_error_decode(s, &where);
+               read_and_clear_error_blocksparse(s, &where) | read_and_clear_error_decode(s, &where) |
+               read_and_clear_error_nsa_bwd(s, &where);
   if (w & kDevErrTimeout)
     return set_error(SBA_ERR_TIMEOUT, "a kernel gave up on a bounded internal wait" + where);
   if (w & kDevErrInput)

@@ -36,6 +36,7 @@ unsigned read_and_clear_error_nsa(cudaStream_t s, std::string* where);
 unsigned read_and_clear_error_mask(cudaStream_t s, std::string* where);
 unsigned read_and_clear_error_blocksparse(cudaStream_t s, std::string* where);
 unsigned read_and_clear_error_decode(cudaStream_t s, std::string* where);
+unsigned read_and_clear_error_nsa_bwd(cudaStream_t s, std::string* where);
 
 // Launch entry points implemented by the kernel files (arguments already validated).
 int launch_nsa_select(const void* q, const void* k, const void* v, const void* g_slc,
@@ -75,6 +76,13 @@ int launch_ragged_chunk(const void* q, const void* k, const void* v, const int32
                         const int32_t* seq_end, int B, int Qn, int Hq, int Hkv, int S,
                         float scale, int window_left, int window_right, void* out, float* lse,
                         cudaStream_t stream);
+size_t nsa_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int S, int num_seqs);
+int launch_nsa_select_bwd(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* d_out, const int32_t* block_indices,
+                          const int32_t* block_counts, int block_count_scalar, int S,
+                          const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
+                          int causal, float scale, void* dq, void* dk, void* dv, void* workspace,
+                          cudaStream_t stream);
 int launch_l2_read_probe(const void* buf, size_t bytes, int reps, unsigned* sink,
                          cudaStream_t stream);
 

@@ -1,0 +1,1134 @@
+// Native-sparse-attention backward, selection branch, for sm_103a: dQ, dK, dV.
+//
+// Follows "ejkernel.modules.operations.native_sparse_attention" (operation API page),
+// NativeSparseAttention.run / native_sparse_attention, which is differentiable in
+// q, k and v.  The page prints no gradient algorithm; the gradient of the forward is
+// the softmax backward over each row's explicit key set:
+//   P = exp(scale * Q K^T - LSE) on the selected keys, dP = dO V^T,
+//   Delta = rowsum(dO * O), dS = P * (dP - Delta),
+//   dQ = scale * dS K,  dK = scale * dS^T Q,  dV = P^T dO,
+// where a key of a block the row's token did not select (or past its causal /
+// sequence limit) has P = 0.
+//
+// Launch sequence (all on the caller's stream, scratch in the caller's workspace):
+//   1. prep (count): Delta per (token, query head); for every (token, KV head) its
+//      filtered, de-duplicated selected blocks are counted per key-block slot;
+//   2. scan: offsets of each slot's token list;
+//   3. prep (fill): the token lists (the reverse of block_indices: which tokens chose a
+//      key block of a KV head);
+//   4. dQ kernel (query-centric, tensor cores): a work item is NT = 128 / G consecutive
+//      tokens and one KV head, 128 query rows; the union of the tokens' selected blocks
+//      is walked in 64-key tiles gathered by TMA.  Per tile: S = Q K^T and dP = dO V^T
+//      (both operands in shared memory, fp32 in tensor memory), then four softmax warps
+//      (one row each) form dS in bf16 into tensor memory, and dQ += dS K accumulates in
+//      tensor memory (A = dS from TMEM).  S/dP and dS are double-buffered so the next
+//      tile's MMAs run while the softmax warps work;
+//   5. dK/dV kernel (key-centric, tensor cores): a work item is one key block of one KV
+//      head; the tokens that selected it are processed in chunks of NT tokens (their Q
+//      and dO rows gathered by TMA, one box of G heads per token).  Per chunk: S and dP
+//      as above, the softmax warps write P and dS (bf16) to shared memory, and
+//      dV^T += dO^T P, dK^T += Q^T dS accumulate in tensor memory (M = head dim,
+//      N = the block's 64 keys); the block's dK and dV are written once at the end.
+// No atomics touch the gradients; the order of a list's tokens (filled with atomics)
+// decides the fp32 summation order of dK/dV, so results may differ in the last bits
+// between runs.
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "sync.cuh"
+
+namespace sba {
+
+static __device__ DevError g_err_nsab = {0u, 0u, 0};
+
+namespace {
+
+using namespace ptx;
+
+constexpr int kD = 128;                     // head dimension of the tensor-core path
+constexpr int kBS = 64;                     // selection block = key tile
+constexpr int kRows = 128;                  // MMA M: NT tokens x G query heads
+constexpr int kMaxNT = 16;
+constexpr int kMaxSel = 32;
+constexpr int kMaxUnion = kMaxNT * kMaxSel;
+constexpr int kThreads = 256;               // warps 0-3: loader, MMA, builder, spare; 4-7 softmax
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleBuilder = 4 };
+enum BarId : unsigned {
+  kBarItemFull = 1, kBarItemEmpty, kBarQdoFull, kBarQdoEmpty, kBarKvFull, kBarKvEmpty,
+  kBarSdpFull, kBarSdpEmpty, kBarDsFull, kBarDsEmpty, kBarAccFull, kBarAccEmpty
+};
+
+struct Params {
+  const __nv_bfloat16* out;
+  const __nv_bfloat16* dout;
+  const float* lse;
+  float* delta;                 // [n_tok, Hq]
+  const int* block_indices;
+  const int* block_counts;
+  const int* cu_seqlens;
+  int count_scalar, S, num_seqs;
+  int B, T, Hq, Hkv, G, causal;
+  int NT;                       // tokens per item / chunk (128 / G)
+  float scale, scale_log2;
+  int n_tok;                    // B * T
+  int nbr;                      // key-block slots per (batch row, KV head)
+  int n_slots;                  // B * Hkv * nbr
+  int* slot_cnt;
+  int* slot_off;
+  int* slot_cur;
+  int* slot_tok;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  int n_items_dq;
+  long long wait_limit;
+};
+
+// ------------------------------------------------------------------ token / slot helpers
+// Sequence of token t of batch row b: first row (absolute), length, position inside.
+__device__ __forceinline__ bool locate(const Params& p, int b, int t, int& seq, int& seq0, int& slen,
+                                       int& trel) {
+  seq = 0;
+  seq0 = b * p.T;
+  slen = p.T;
+  trel = t;
+  if (p.cu_seqlens == nullptr) return true;
+  int lo = 0, hi = p.num_seqs;  // largest s with cu[s] <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.cu_seqlens[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int c0 = p.cu_seqlens[lo], c1 = p.cu_seqlens[lo + 1];
+  if (!(c0 <= t && t < c1) || p.cu_seqlens[0] != 0 || p.cu_seqlens[p.num_seqs] != p.T) {
+    atomicOr(&g_err_nsab.flags, kDevErrInput);
+    return false;
+  }
+  seq = lo;
+  seq0 = c0;
+  slen = c1 - c0;
+  trel = t - c0;
+  return true;
+}
+
+// First slot of a sequence inside its (batch row, KV head) range: sequence s starting
+// at row c0 gets slots [c0 / 64 + s, ...), one per key block; consecutive sequences
+// never overlap since floor((c0 + L) / 64) - floor(c0 / 64) + 1 >= ceil(L / 64).
+__device__ __forceinline__ int seq_slot_base(int seq, int seq0_in_row) { return seq0_in_row / kBS + seq; }
+
+// Key block of slot (b, hkv, sidx): absolute first key row and number of keys; false
+// when the slot holds no block (a gap between packed sequences or past the row).
+__device__ __forceinline__ bool decode_slot(const Params& p, int b, int sidx, int& row0, int& nkeys) {
+  if (p.cu_seqlens == nullptr) {
+    const int nb = (p.T + kBS - 1) / kBS;
+    if (sidx >= nb) return false;
+    row0 = b * p.T + sidx * kBS;
+    nkeys = min(kBS, p.T - sidx * kBS);
+    return true;
+  }
+  int lo = 0, hi = p.num_seqs;  // largest s with base(s) <= sidx
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (seq_slot_base(mid, p.cu_seqlens[mid]) <= sidx) lo = mid; else hi = mid;
+  }
+  const int c0 = p.cu_seqlens[lo], len = p.cu_seqlens[lo + 1] - c0;
+  const int j = sidx - seq_slot_base(lo, c0);
+  if (j < 0 || len <= 0 || j * kBS >= len) return false;
+  row0 = c0 + j * kBS;
+  nkeys = min(kBS, len - j * kBS);
+  return true;
+}
+
+// ------------------------------------------------------------------ 1/3. prep
+// One warp per (token, KV head).  kFill == false: Delta of the token's G query heads and
+// the count of each selected block's slot; kFill == true: the token into each slot's list.
+template <bool kFill>
+__global__ void __launch_bounds__(256) nsa_bwd_prep_kernel(const Params p) {
+  const int lane = threadIdx.x & 31;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < (long long)p.n_tok * p.Hkv;
+       w += warps) {
+    const int tok = static_cast<int>(w / p.Hkv), hkv = static_cast<int>(w - (long long)tok * p.Hkv);
+    if (!kFill) {
+      // Delta[tok, hq] = <dO, O> in fp32, one head per iteration, 4 elements per lane
+      for (int h = 0; h < p.G; ++h) {
+        const long long base = ((long long)tok * p.Hq + hkv * p.G + h) * kD + lane * 4;
+        const uint2 ov = *reinterpret_cast<const uint2*>(p.out + base);
+        const uint2 dv = *reinterpret_cast<const uint2*>(p.dout + base);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const float2 a = __bfloat1622float2(o2[u]), c = __bfloat1622float2(d2[u]);
+          acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) p.delta[(long long)tok * p.Hq + hkv * p.G + h] = acc;
+      }
+    }
+    const int b = p.cu_seqlens ? 0 : tok / p.T;
+    const int t = p.cu_seqlens ? tok : tok - b * p.T;
+    int seq, seq0, slen, trel;
+    if (!locate(p, b, t, seq, seq0, slen, trel)) continue;
+    int cnt = p.block_counts ? p.block_counts[(long long)tok * p.Hkv + hkv] : p.count_scalar;
+    cnt = min(max(cnt, 0), p.S);
+    const int nb = (slen + kBS - 1) / kBS;
+    int e = -1;
+    if (lane < cnt) e = p.block_indices[((long long)tok * p.Hkv + hkv) * p.S + lane];
+    const bool valid = lane < cnt && e >= 0 && e < nb && (!p.causal || e * kBS <= trel);
+    bool dup = false;
+    for (int j = 0; j < kMaxSel; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, e, j);
+      const bool vj = __shfl_sync(0xffffffffu, valid, j);
+      if (j < lane && vj && ej == e) dup = true;
+    }
+    if (valid && !dup) {
+      const int base = seq_slot_base(seq, seq0 - b * p.T);
+      const long long slot = ((long long)b * p.Hkv + hkv) * p.nbr + base + e;
+      if (!kFill) {
+        atomicAdd(&p.slot_cnt[slot], 1);
+      } else {
+        const int pos = p.slot_off[slot] + atomicAdd(&p.slot_cur[slot], 1);
+        p.slot_tok[pos] = tok;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ 2. scan
+// Exclusive prefix sum of the slot counts (one CTA of 1024 threads, chunks of 1024),
+// and the fill cursors reset to zero.
+__global__ void __launch_bounds__(1024) nsa_bwd_scan_kernel(const Params p) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < p.n_slots; c0 += 1024) {
+    const int i = c0 + tid;
+    const int v = i < p.n_slots ? p.slot_cnt[i] : 0;
+    int incl = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += o;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int ws = warp_sums[lane];
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, ws, d);
+        if (lane >= d) ws += o;
+      }
+      warp_sums[lane] = ws;  // inclusive over warps
+    }
+    __syncthreads();
+    const int before = carry + (warp > 0 ? warp_sums[warp - 1] : 0) + incl - v;
+    if (i < p.n_slots) {
+      p.slot_off[i] = before;
+      p.slot_cur[i] = 0;
+    }
+    __syncthreads();
+    if (tid == 0) carry += warp_sums[31];
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ shared pieces
+// K-major 128-byte-swizzled operand of `rows` rows: byte offset of K-step kk (16 elements)
+__device__ __forceinline__ uint64_t kmajor_step(int kk, int panel_bytes) {
+  return static_cast<uint64_t>(((kk / 4) * panel_bytes + (kk % 4) * 32) >> 4);
+}
+
+// 64 fp32 columns of one TMEM lane row (two loads, one wait)
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* x) {
+  tmem_ld_32x32b_x32_nw(taddr, x);
+  tmem_ld_32x32b_x32_nw(taddr + 32, x + 32);
+  tmem_wait_ld();
+#pragma unroll
+  for (int j = 0; j < 64; ++j) tmem_ld_ready(x[j]);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h2);
+}
+
+// P and dS of one row from its S and dP columns: the first nvalid keys are admissible.
+__device__ __forceinline__ void row_grads(const float* s, const float* dp, int nvalid, float scale_log2,
+                                          float lse2, float delta, uint32_t* p_pk, uint32_t* ds_pk) {
+#pragma unroll
+  for (int j = 0; j < 64; j += 2) {
+    const float p0 = j < nvalid ? ex2(fmaf(s[j], scale_log2, -lse2)) : 0.f;
+    const float p1 = j + 1 < nvalid ? ex2(fmaf(s[j + 1], scale_log2, -lse2)) : 0.f;
+    if (p_pk != nullptr) p_pk[j >> 1] = pack_bf16(p0, p1);
+    ds_pk[j >> 1] = pack_bf16(p0 * (dp[j] - delta), p1 * (dp[j + 1] - delta));
+  }
+}
+
+// ------------------------------------------------------------------ 4. dQ kernel
+struct DqItem {
+  int n_union;
+  unsigned tok_valid;
+  int tok[kMaxNT];                  // token of slot i (-1: none)
+  int limit[kMaxNT];                // last key row (absolute) token i may see; -1 if none
+  int ux[kMaxUnion];                // first key row (absolute) of each union block
+  unsigned short ubits[kMaxUnion];  // tokens of the item that selected it
+};
+
+struct DqCfg {
+  static constexpr int kQBytes = kRows * kD * 2;           // 32 KB: 2 panels of 128 rows x 128 B
+  static constexpr int kQPanel = kRows * 128;
+  static constexpr int kTileBytes = kBS * kD * 2;          // 16 KB: K (or V) of one 64-key tile
+  static constexpr int kTilePanel = kBS * 128;
+  static constexpr int kStages = 3;
+  static constexpr int kItemSlots = 2;
+  static constexpr int kItemBytes = (static_cast<int>(sizeof(DqItem)) + 127) & ~127;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kQBytes;
+  static constexpr int kOffRing = 2 * kQBytes;             // stage s: K at s * 32 KB, V + 16 KB
+  static constexpr int kOffItems = kOffRing + kStages * 2 * kTileBytes;
+  static constexpr int kOffSort = kOffItems + kItemSlots * kItemBytes;
+  static constexpr int kOffBars = kOffSort + kMaxUnion * 8;
+  static constexpr int kNumBars = 2 * kItemSlots + 2 + 2 * kStages + 8 + 2 + 1;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // tensor memory: S[2], dP[2] (64 fp32 each), dS[2] (64 bf16 = 32 columns each), dQ (128)
+  static constexpr int kSCol = 0, kDpCol = 128, kDsCol = 256, kDqCol = 320;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdescS = make_idesc(128, kBS, 1u, false, false);
+  static constexpr uint32_t kIdescDq = make_idesc(128, kD, 1u, false, true);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+// Union of the selected blocks of the item's tokens for one KV head (one warp): entries
+// (first key row << 16 | token bit) sorted with a bitonic network in shared memory, equal
+// rows merged by OR-ing their token bits.
+__device__ void build_dq_item(const Params& p, int g, int hkv, int lane, DqItem& it, uint64_t* keys) {
+  const unsigned kFull = 0xffffffffu;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int tok = (lane < p.NT && g * p.NT + lane < p.n_tok) ? g * p.NT + lane : -1;
+  int seq = 0, seq0 = 0, slen = 0, trel = 0, cnt = 0, limit = -1;
+  if (tok >= 0) {
+    const int b = p.cu_seqlens ? 0 : tok / p.T;
+    const int t = p.cu_seqlens ? tok : tok - b * p.T;
+    if (locate(p, b, t, seq, seq0, slen, trel)) {
+      cnt = p.block_counts ? p.block_counts[(long long)tok * p.Hkv + hkv] : p.count_scalar;
+      cnt = min(max(cnt, 0), p.S);
+      limit = p.causal ? tok : seq0 + slen - 1;
+    }
+  }
+  const int total = p.NT * p.S;
+  int n = 0;
+  for (int c0 = 0; c0 < total; c0 += 32) {
+    const int idx = c0 + lane;
+    const int i = idx < total ? idx / p.S : 0, j = idx - i * p.S;
+    const int trow = __shfl_sync(kFull, tok, i);
+    const int cnt_i = __shfl_sync(kFull, cnt, i);
+    const int seq0_i = __shfl_sync(kFull, seq0, i);
+    const int slen_i = __shfl_sync(kFull, slen, i);
+    const int trel_i = __shfl_sync(kFull, trel, i);
+    int e = -1;
+    if (idx < total && trow >= 0 && j < cnt_i) e = p.block_indices[((long long)trow * p.Hkv + hkv) * p.S + j];
+    const int nb = (slen_i + kBS - 1) / kBS;
+    const bool valid = idx < total && trow >= 0 && j < cnt_i && e >= 0 && e < nb &&
+                       (!p.causal || e * kBS <= trel_i);
+    const unsigned bal = __ballot_sync(kFull, valid);
+    if (valid)
+      keys[n + __popc(bal & lt_mask)] =
+          (static_cast<uint64_t>(static_cast<uint32_t>(seq0_i + e * kBS)) << 16) | (1u << i);
+    n += __popc(bal);
+  }
+  int N = 32;
+  while (N < n) N <<= 1;
+  for (int idx = n + lane; idx < N; idx += 32) keys[idx] = ~0ull;
+  __syncwarp();
+  for (int k = 2; k <= N; k <<= 1) {
+    for (int jj = k >> 1; jj > 0; jj >>= 1) {
+      for (int idx = lane; idx < N; idx += 32) {
+        const int ixj = idx ^ jj;
+        if (ixj > idx) {
+          const uint64_t a = keys[idx], b = keys[ixj];
+          if ((a > b) == ((idx & k) == 0)) {
+            keys[idx] = b;
+            keys[ixj] = a;
+          }
+        }
+      }
+      __syncwarp();
+    }
+  }
+  int nu = 0;
+  for (int base = 0; base < n; base += 32) {
+    const int idx = base + lane;
+    bool head = false;
+    uint32_t x = 0;
+    unsigned bits = 0;
+    if (idx < n) {
+      const uint64_t key = keys[idx];
+      x = static_cast<uint32_t>(key >> 16);
+      head = idx == 0 || static_cast<uint32_t>(keys[idx - 1] >> 16) != x;
+      if (head) {
+        bits = static_cast<unsigned>(key & 0xFFFFu);
+        for (int u = idx + 1; u < n; ++u) {
+          const uint64_t k2 = keys[u];
+          if (static_cast<uint32_t>(k2 >> 16) != x) break;
+          bits |= static_cast<unsigned>(k2 & 0xFFFFu);
+        }
+      }
+    }
+    const unsigned bal = __ballot_sync(kFull, head);
+    if (head) {
+      const int pos = nu + __popc(bal & lt_mask);
+      it.ux[pos] = static_cast<int>(x);
+      it.ubits[pos] = static_cast<unsigned short>(bits);
+    }
+    nu += __popc(bal);
+  }
+  if (lane < kMaxNT) {
+    it.tok[lane] = tok;
+    it.limit[lane] = limit;
+  }
+  const unsigned tv_bits = __ballot_sync(kFull, tok >= 0);
+  if (lane == 0) {
+    it.n_union = nu;
+    it.tok_valid = tv_bits;
+  }
+  __syncwarp();
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                  const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const Params p) {
+  using C = DqCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* keys = reinterpret_cast<uint64_t*>(smem + C::kOffSort);
+  uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* item_full = bb;  bb += C::kItemSlots;
+  uint64_t* item_empty = bb; bb += C::kItemSlots;
+  uint64_t* qdo_full = bb;   bb += 1;
+  uint64_t* qdo_empty = bb;  bb += 1;
+  uint64_t* kv_full = bb;    bb += C::kStages;
+  uint64_t* kv_empty = bb;   bb += C::kStages;
+  uint64_t* sdp_full = bb;   bb += 2;
+  uint64_t* sdp_empty = bb;  bb += 2;
+  uint64_t* ds_full = bb;    bb += 2;
+  uint64_t* ds_empty = bb;   bb += 2;
+  uint64_t* dq_full = bb;    bb += 1;
+  uint64_t* dq_empty = bb;   bb += 1;
+  uint64_t* mma_done = bb;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  const Abort ab{abort_flag, &g_err_nsab, 3u, p.wait_limit};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto item_at = [&](int slot) -> DqItem& {
+    return *reinterpret_cast<DqItem*>(smem + C::kOffItems + slot * C::kItemBytes);
+  };
+
+  if (threadIdx.x == 0) {
+    // an item slot is released by the loader, the MMA thread and the 4 softmax warps
+    for (int i = 0; i < C::kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 6); }
+    mbar_init(qdo_full, 1); mbar_init(qdo_empty, 1);
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1); mbar_init(&sdp_empty[i], 4);
+      mbar_init(&ds_full[i], 4); mbar_init(&ds_empty[i], 1);
+    }
+    mbar_init(dq_full, 1); mbar_init(dq_empty, 4); mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 2) {
+    // ------------------------------------------------------------------ item builder
+    int islot = 0; uint32_t iphase = 0;
+    for (int item = blockIdx.x; item < p.n_items_dq; item += gridDim.x) {
+      const int g = item / p.Hkv, hkv = item - g * p.Hkv;
+      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, item)) break;
+      build_dq_item(p, g, hkv, lane, item_at(islot), keys);
+      if (lane == 0) mbar_arrive(&item_full[islot]);
+      if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ loader
+    int islot = 0; uint32_t iphase = 0;
+    uint32_t qph = 0;
+    int stage = 0; uint32_t kph = 0;
+    bool issued[C::kStages] = {false, false, false};
+    uint32_t last[C::kStages] = {0u, 0u, 0u};
+    bool q_issued = false; uint32_t q_last = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < p.n_items_dq && ok; item += gridDim.x) {
+      const int g = item / p.Hkv, hkv = item - g * p.Hkv;
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, item)) break;
+      const DqItem& it = item_at(islot);
+      const int nu = it.n_union;
+      if (nu > 0) {
+        if (!warp_wait(qdo_empty, qph ^ 1, ab, kRoleLoader, kBarQdoEmpty, item)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(qdo_full, 2 * C::kQBytes);
+#pragma unroll
+          for (int pn = 0; pn < kD / 64; ++pn) {
+            tma_load_3d(smem + C::kOffQ + pn * C::kQPanel, &tm_q, qdo_full, pn * 64, hkv * p.G, g * p.NT);
+            tma_load_3d(smem + C::kOffDO + pn * C::kQPanel, &tm_do, qdo_full, pn * 64, hkv * p.G, g * p.NT);
+          }
+        }
+        q_issued = true; q_last = qph; qph ^= 1;
+        for (int u = 0; u < nu; ++u) {
+          if (!warp_wait(&kv_empty[stage], kph ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
+          if (lane == 0) {
+            uint8_t* kdst = smem + C::kOffRing + stage * 2 * C::kTileBytes;
+            mbar_arrive_expect_tx(&kv_full[stage], 2 * C::kTileBytes);
+#pragma unroll
+            for (int pn = 0; pn < kD / 64; ++pn) {
+              tma_load_3d(kdst + pn * C::kTilePanel, &tm_k, &kv_full[stage], pn * 64, hkv, it.ux[u]);
+              tma_load_3d(kdst + C::kTileBytes + pn * C::kTilePanel, &tm_v, &kv_full[stage], pn * 64, hkv,
+                          it.ux[u]);
+            }
+          }
+          issued[stage] = true; last[stage] = kph;
+          if (++stage == C::kStages) { stage = 0; kph ^= 1; }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
+      if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
+    }
+    if (lane == 0) {
+      for (int s = 0; s < C::kStages; ++s)
+        if (issued[s]) drain_wait(&kv_full[s], last[s]);
+      if (q_issued) drain_wait(qdo_full, q_last);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int islot = 0; uint32_t iphase = 0;
+      uint32_t qph = 0, dqph = 0;
+      int stage = 0; uint32_t kph = 0;
+      uint32_t sdp_ph[2] = {0u, 0u}, ds_ph[2] = {0u, 0u};
+      int sbuf = 0, dbuf = 0;  // next S/dP buffer to fill, next dS buffer to consume
+      bool ok = true;
+      const uint64_t q_desc = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
+      const uint64_t do_desc = make_sdesc(smem_base + C::kOffDO, 16, 1024, kLayoutSW128);
+      const uint64_t ring_k = make_sdesc(smem_base + C::kOffRing, 16, 1024, kLayoutSW128);
+      const uint64_t ring_kmn = make_sdesc(smem_base + C::kOffRing, C::kTilePanel, 1024, kLayoutSW128);
+      for (int item = blockIdx.x; item < p.n_items_dq && ok; item += gridDim.x) {
+        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        const int nu = item_at(islot).n_union;
+        mbar_arrive(&item_empty[islot]);
+        if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
+        if (nu == 0) continue;
+        if (!bounded_wait(qdo_full, qph, ab, kRoleMma, kBarQdoFull, item)) break;
+        qph ^= 1;
+        int st_u = stage;  // stage of the tile whose dQ MMA is next
+        // S = Q K^T and dP = dO V^T of tile u into S/dP buffer sbuf
+        auto issue_sdp = [&](int u) -> bool {
+          if (!bounded_wait(&kv_full[stage], kph, ab, kRoleMma, kBarKvFull, item)) return false;
+          if (!bounded_wait(&sdp_empty[sbuf], sdp_ph[sbuf] ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) return false;
+          tc_fence_after();
+          const uint64_t kd = ring_k + static_cast<uint64_t>((stage * 2 * C::kTileBytes) >> 4);
+          const uint64_t vd = kd + static_cast<uint64_t>(C::kTileBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ss(tmem + C::kSCol + sbuf * kBS, q_desc + kmajor_step(kk, C::kQPanel),
+                       kd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ss(tmem + C::kDpCol + sbuf * kBS, do_desc + kmajor_step(kk, C::kQPanel),
+                       vd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+          mma_commit(&sdp_full[sbuf]);
+          if (u == nu - 1) mma_commit(qdo_empty);
+          sdp_ph[sbuf] ^= 1;
+          sbuf ^= 1;
+          if (++stage == C::kStages) { stage = 0; kph ^= 1; }
+          return true;
+        };
+        if (!issue_sdp(0)) break;
+        for (int u = 0; u < nu && ok; ++u) {
+          if (u + 1 < nu && !issue_sdp(u + 1)) { ok = false; break; }
+          // dQ += dS(u) K(u)
+          if (!bounded_wait(&ds_full[dbuf], ds_ph[dbuf], ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+          ds_ph[dbuf] ^= 1;
+          if (u == 0) {
+            if (!bounded_wait(dq_empty, dqph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
+            dqph ^= 1;
+          }
+          tc_fence_after();
+          const uint64_t kmn = ring_kmn + static_cast<uint64_t>((st_u * 2 * C::kTileBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kBS / 16; ++kk)
+            mma_f16_ts(tmem + C::kDqCol, tmem + C::kDsCol + dbuf * (kBS / 2) + kk * 8,
+                       kmn + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::kIdescDq,
+                       (u == 0 && kk == 0) ? 0u : 1u);
+          mma_commit(&kv_empty[st_u]);
+          mma_commit(&ds_empty[dbuf]);
+          dbuf ^= 1;
+          if (++st_u == C::kStages) st_u = 0;
+        }
+        if (!ok) break;
+        mma_commit(dq_full);
+      }
+      mma_commit(mma_done);
+      drain_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax / epilogue
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;          // row of the item = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int ti = r / p.G, h = r - (r / p.G) * p.G;
+    int islot = 0; uint32_t iphase = 0;
+    uint32_t sdp_ph[2] = {0u, 0u}, ds_ph[2] = {0u, 0u}, dqph = 0;
+    int buf = 0;
+    for (int item = blockIdx.x; item < p.n_items_dq; item += gridDim.x) {
+      const int hkv = item % p.Hkv;
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
+      const DqItem& it = item_at(islot);
+      const int nu = it.n_union;
+      const int tok = ti < p.NT ? it.tok[ti] : -1;
+      const int limit = ti < p.NT ? it.limit[ti] : -1;
+      const long long hrow = (long long)(tok >= 0 ? tok : 0) * p.Hq + hkv * p.G + h;
+      float lse2 = -INFINITY, delta = 0.f;
+      if (tok >= 0) {
+        lse2 = p.lse[hrow] * kLog2e;
+        delta = p.delta[hrow];
+      }
+      const bool live = tok >= 0 && lse2 != -INFINITY;
+      const unsigned tbit = 1u << ti;
+      bool ok = true;
+      for (int u = 0; u < nu; ++u) {
+        const int x0 = it.ux[u];
+        const bool sel = live && (it.ubits[u] & tbit) != 0u;
+        const int nvalid = sel ? min(max(limit - x0 + 1, 0), kBS) : 0;
+        if (!warp_wait(&sdp_full[buf], sdp_ph[buf], ab, kRoleSoftmax, kBarSdpFull, item)) { ok = false; break; }
+        sdp_ph[buf] ^= 1;
+        tc_fence_after();
+        float s[64], dp[64];
+        tmem_ld64(tmem + lane_off + C::kSCol + buf * kBS, s);
+        tmem_ld64(tmem + lane_off + C::kDpCol + buf * kBS, dp);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sdp_empty[buf]);
+        uint32_t ds_pk[32];
+        row_grads(s, dp, nvalid, p.scale_log2, lse2, delta, nullptr, ds_pk);
+        // the dQ MMA that read this dS buffer two tiles ago must be done
+        if (!warp_wait(&ds_empty[buf], ds_ph[buf] ^ 1, ab, kRoleSoftmax, kBarDsEmpty, item)) { ok = false; break; }
+        ds_ph[buf] ^= 1;
+        tc_fence_after();
+        tmem_st_32x32b_x32_u(tmem + lane_off + C::kDsCol + buf * (kBS / 2), ds_pk);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ds_full[buf]);
+        buf ^= 1;
+      }
+      if (!ok) break;
+      __nv_bfloat16* drow = p.dq + hrow * kD;
+      if (nu > 0) {
+        if (!warp_wait(dq_full, dqph, ab, kRoleSoftmax, kBarAccFull, item)) break;
+        dqph ^= 1;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < kD / 32; ++c) {
+          float v[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kDqCol + c * 32, v);
+          if (tok >= 0) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+              uint4 w4;
+              w4.x = pack_bf16(v[j] * p.scale, v[j + 1] * p.scale);
+              w4.y = pack_bf16(v[j + 2] * p.scale, v[j + 3] * p.scale);
+              w4.z = pack_bf16(v[j + 4] * p.scale, v[j + 5] * p.scale);
+              w4.w = pack_bf16(v[j + 6] * p.scale, v[j + 7] * p.scale);
+              *reinterpret_cast<uint4*>(drow + c * 32 + j) = w4;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dq_empty);
+      } else if (tok >= 0) {
+#pragma unroll
+        for (int j = 0; j < kD; j += 8) *reinterpret_cast<uint4*>(drow + j) = make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
+      if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ 5. dK/dV kernel
+struct KvCfg {
+  static constexpr int kQBytes = kRows * kD * 2;           // 32 KB (Q or dO of a chunk)
+  static constexpr int kQPanel = kRows * 128;
+  static constexpr int kTileBytes = kBS * kD * 2;          // 16 KB
+  static constexpr int kTilePanel = kBS * 128;
+  static constexpr int kPBytes = kRows * kBS * 2;          // 16 KB: P (or dS), 128 rows x 128 B
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTileBytes;
+  static constexpr int kOffQ = 2 * kTileBytes;             // buffer b: Q at + b * 64 KB, dO + 32 KB
+  static constexpr int kOffP = kOffQ + 4 * kQBytes;
+  static constexpr int kOffDs = kOffP + kPBytes;
+  static constexpr int kOffBars = kOffDs + kPBytes;
+  static constexpr int kNumBars = 2 + 4 + 2 + 2 + 2 + 1;
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // tensor memory: S, dP (64 fp32 each), dV^T, dK^T (lanes = head dim, 64 key columns)
+  static constexpr int kSCol = 0, kDpCol = 64, kDvCol = 128, kDkCol = 192;
+  static constexpr int kTmemCols = 256;
+  static constexpr uint32_t kIdescS = make_idesc(128, kBS, 1u, false, false);
+  static constexpr uint32_t kIdescAcc = make_idesc(128, kBS, 1u, true, true);
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void kv_item(const Params& p, int item, int& b, int& hkv, int& sidx) {
+  sidx = item % p.nbr;
+  const int r = item / p.nbr;
+  hkv = r % p.Hkv;
+  b = r / p.Hkv;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const Params p) {
+  using C = KvCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bb = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+  uint64_t* kv_full = bb;    bb += 1;
+  uint64_t* kv_empty = bb;   bb += 1;
+  uint64_t* qdo_full = bb;   bb += 2;
+  uint64_t* qdo_empty = bb;  bb += 2;
+  uint64_t* sdp_full = bb;   bb += 1;
+  uint64_t* sdp_empty = bb;  bb += 1;
+  uint64_t* pds_full = bb;   bb += 1;
+  uint64_t* pds_empty = bb;  bb += 1;
+  uint64_t* acc_full = bb;   bb += 1;
+  uint64_t* acc_empty = bb;  bb += 1;
+  uint64_t* mma_done = bb;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  const Abort ab{abort_flag, &g_err_nsab, 4u, p.wait_limit};
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_items = p.n_slots;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1); mbar_init(kv_empty, 1);
+    for (int i = 0; i < 2; ++i) { mbar_init(&qdo_full[i], 1); mbar_init(&qdo_empty[i], 1); }
+    mbar_init(sdp_full, 1); mbar_init(sdp_empty, 4);
+    mbar_init(pds_full, 4); mbar_init(pds_empty, 1);
+    mbar_init(acc_full, 1); mbar_init(acc_empty, 4);
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ loader
+    uint32_t kvph = 0;
+    uint32_t qph[2] = {0u, 0u};
+    int qb = 0;
+    bool kv_issued = false; uint32_t kv_last = 0;
+    bool q_issued[2] = {false, false}; uint32_t q_last[2] = {0u, 0u};
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      int b, hkv, sidx, row0 = 0, nkeys = 0;
+      kv_item(p, item, b, hkv, sidx);
+      if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
+      const int cnt = p.slot_cnt[item], off = p.slot_off[item];
+      if (cnt == 0) continue;
+      if (!warp_wait(kv_empty, kvph ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(kv_full, 2 * C::kTileBytes);
+#pragma unroll
+        for (int pn = 0; pn < kD / 64; ++pn) {
+          tma_load_3d(smem + C::kOffK + pn * C::kTilePanel, &tm_k, kv_full, pn * 64, hkv, row0);
+          tma_load_3d(smem + C::kOffV + pn * C::kTilePanel, &tm_v, kv_full, pn * 64, hkv, row0);
+        }
+      }
+      kv_issued = true; kv_last = kvph; kvph ^= 1;
+      const int nch = (cnt + p.NT - 1) / p.NT;
+      for (int c = 0; c < nch; ++c) {
+        if (!warp_wait(&qdo_empty[qb], qph[qb] ^ 1, ab, kRoleLoader, kBarQdoEmpty, item)) { ok = false; break; }
+        // lane i < NT: token of slot i of this chunk (past the list: a row past the end,
+        // which the TMA fills with zeros)
+        const int k = c * p.NT + lane;
+        const int tk = (lane < p.NT && k < cnt) ? p.slot_tok[off + k] : p.n_tok;
+        if (lane == 0) mbar_arrive_expect_tx(&qdo_full[qb], 2 * C::kQBytes);
+        __syncwarp();
+        uint8_t* qdst = smem + C::kOffQ + qb * 2 * C::kQBytes;
+        for (int i = 0; i < p.NT; ++i) {
+          const int ti = __shfl_sync(0xffffffffu, tk, i);
+          if (lane == 0) {
+#pragma unroll
+            for (int pn = 0; pn < kD / 64; ++pn) {
+              tma_load_3d(qdst + pn * C::kQPanel + i * p.G * 128, &tm_q, &qdo_full[qb], pn * 64, hkv * p.G, ti);
+              tma_load_3d(qdst + C::kQBytes + pn * C::kQPanel + i * p.G * 128, &tm_do, &qdo_full[qb], pn * 64,
+                          hkv * p.G, ti);
+            }
+          }
+        }
+        q_issued[qb] = true; q_last[qb] = qph[qb]; qph[qb] ^= 1;
+        qb ^= 1;
+      }
+    }
+    if (lane == 0) {
+      if (kv_issued) drain_wait(kv_full, kv_last);
+      for (int i = 0; i < 2; ++i)
+        if (q_issued[i]) drain_wait(&qdo_full[i], q_last[i]);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t kvph = 0, sdph = 0, pdph = 0, accph = 0;
+      uint32_t qph[2] = {0u, 0u};
+      int qb = 0;
+      bool ok = true;
+      const uint64_t k_desc = make_sdesc(smem_base + C::kOffK, 16, 1024, kLayoutSW128);
+      const uint64_t v_desc = make_sdesc(smem_base + C::kOffV, 16, 1024, kLayoutSW128);
+      const uint64_t qk_desc = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
+      const uint64_t qmn_desc = make_sdesc(smem_base + C::kOffQ, C::kQPanel, 1024, kLayoutSW128);
+      const uint64_t p_desc = make_sdesc(smem_base + C::kOffP, C::kPBytes, 1024, kLayoutSW128);
+      const uint64_t ds_desc = make_sdesc(smem_base + C::kOffDs, C::kPBytes, 1024, kLayoutSW128);
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        int b, hkv, sidx, row0 = 0, nkeys = 0;
+        kv_item(p, item, b, hkv, sidx);
+        if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
+        const int cnt = p.slot_cnt[item];
+        if (cnt == 0) continue;
+        if (!bounded_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
+        kvph ^= 1;
+        const int nch = (cnt + p.NT - 1) / p.NT;
+        // S = Q K^T and dP = dO V^T of chunk c (Q / dO buffer c & 1 of this item's run)
+        int sq = qb;  // buffer of the next chunk to start
+        auto issue_sdp = [&]() -> bool {
+          if (!bounded_wait(&qdo_full[sq], qph[sq], ab, kRoleMma, kBarQdoFull, item) ||
+              !bounded_wait(sdp_empty, sdph ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) return false;
+          qph[sq] ^= 1;
+          sdph ^= 1;
+          tc_fence_after();
+          const uint64_t qo = static_cast<uint64_t>((sq * 2 * C::kQBytes) >> 4);
+          const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ss(tmem + C::kSCol, qk_desc + qo + kmajor_step(kk, C::kQPanel),
+                       k_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_f16_ss(tmem + C::kDpCol, qk_desc + doo + kmajor_step(kk, C::kQPanel),
+                       v_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+          mma_commit(sdp_full);
+          sq ^= 1;
+          return true;
+        };
+        if (!issue_sdp()) break;
+        for (int c = 0; c < nch && ok; ++c) {
+          // the next chunk's S / dP run while the softmax warps work on this one (they
+          // release S / dP as soon as they have loaded them)
+          if (c + 1 < nch && !issue_sdp()) { ok = false; break; }
+          // dV^T += dO^T P and dK^T += Q^T dS over the chunk's 128 rows (K = rows)
+          if (!bounded_wait(pds_full, pdph, ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+          pdph ^= 1;
+          if (c == 0) {
+            if (!bounded_wait(acc_empty, accph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
+            accph ^= 1;
+          }
+          tc_fence_after();
+          const uint64_t qo = static_cast<uint64_t>((qb * 2 * C::kQBytes) >> 4);
+          const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+            mma_f16_ss(tmem + C::kDvCol, qmn_desc + doo + step, p_desc + step, C::kIdescAcc,
+                       (c == 0 && kk == 0) ? 0u : 1u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kRows / 16; ++kk) {
+            const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+            mma_f16_ss(tmem + C::kDkCol, qmn_desc + qo + step, ds_desc + step, C::kIdescAcc,
+                       (c == 0 && kk == 0) ? 0u : 1u);
+          }
+          mma_commit(&qdo_empty[qb]);
+          mma_commit(pds_empty);
+          qb ^= 1;
+        }
+        if (!ok) break;
+        mma_commit(kv_empty);
+        mma_commit(acc_full);
+      }
+      mma_commit(mma_done);
+      drain_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ softmax / epilogue
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;          // row of the chunk = TMEM lane; head-dim row in the epilogue
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int ti = r / p.G, h = r - (r / p.G) * p.G;
+    uint32_t sdph = 0, pdph = 0, accph = 0;
+    uint8_t* prow = smem + C::kOffP + r * 128;
+    uint8_t* dsrow = smem + C::kOffDs + r * 128;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      int b, hkv, sidx, row0 = 0, nkeys = 0;
+      kv_item(p, item, b, hkv, sidx);
+      if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
+      const int cnt = p.slot_cnt[item], off = p.slot_off[item];
+      if (cnt == 0) {
+        // no token chose this block: its keys get zero gradients
+        for (int i = r; i < nkeys * (kD / 8); i += kRows) {
+          const long long o = ((long long)(row0 + i / (kD / 8)) * p.Hkv + hkv) * kD + (i % (kD / 8)) * 8;
+          *reinterpret_cast<uint4*>(p.dk + o) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(p.dv + o) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
+      const int nch = (cnt + p.NT - 1) / p.NT;
+      bool ok = true;
+      for (int c = 0; c < nch; ++c) {
+        const int k = c * p.NT + ti;
+        const int tok = k < cnt ? p.slot_tok[off + k] : -1;
+        float lse2 = -INFINITY, delta = 0.f;
+        if (tok >= 0) {
+          const long long hrow = (long long)tok * p.Hq + hkv * p.G + h;
+          lse2 = p.lse[hrow] * kLog2e;
+          delta = p.delta[hrow];
+        }
+        // keys of the block this row may see: causal limit of its token, the block's end
+        int nvalid = 0;
+        if (tok >= 0 && lse2 != -INFINITY) nvalid = p.causal ? min(max(tok - row0 + 1, 0), nkeys) : nkeys;
+        if (!warp_wait(sdp_full, sdph, ab, kRoleSoftmax, kBarSdpFull, item)) { ok = false; break; }
+        sdph ^= 1;
+        tc_fence_after();
+        float s[64], dp[64];
+        tmem_ld64(tmem + lane_off + C::kSCol, s);
+        tmem_ld64(tmem + lane_off + C::kDpCol, dp);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sdp_empty);
+        uint32_t p_pk[32], ds_pk[32];
+        row_grads(s, dp, nvalid, p.scale_log2, lse2, delta, p_pk, ds_pk);
+        // the previous chunk's dV/dK MMAs must be done with the P / dS buffers
+        if (!warp_wait(pds_empty, pdph ^ 1, ab, kRoleSoftmax, kBarDsEmpty, item)) { ok = false; break; }
+        pdph ^= 1;
+        // row r of P and dS, 128-byte swizzle: 16-byte chunk j at position j ^ (r & 7)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int pos = (j ^ (r & 7)) * 16;
+          *reinterpret_cast<uint4*>(prow + pos) = make_uint4(p_pk[4 * j], p_pk[4 * j + 1], p_pk[4 * j + 2], p_pk[4 * j + 3]);
+          *reinterpret_cast<uint4*>(dsrow + pos) =
+              make_uint4(ds_pk[4 * j], ds_pk[4 * j + 1], ds_pk[4 * j + 2], ds_pk[4 * j + 3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pds_full);
+      }
+      if (!ok) break;
+      // epilogue: lane r of dV^T / dK^T is head-dim index r; 64 key columns each
+      if (!warp_wait(acc_full, accph, ab, kRoleSoftmax, kBarAccFull, item)) break;
+      accph ^= 1;
+      tc_fence_after();
+      float av[64], ak[64];
+      tmem_ld64(tmem + lane_off + C::kDvCol, av);
+      tmem_ld64(tmem + lane_off + C::kDkCol, ak);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+#pragma unroll
+      for (int key = 0; key < 64; ++key) {
+        if (key < nkeys) {
+          const long long o = ((long long)(row0 + key) * p.Hkv + hkv) * kD + r;
+          p.dv[o] = __float2bfloat16_rn(av[key]);
+          p.dk[o] = __float2bfloat16_rn(ak[key] * p.scale);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+struct BwdLayout {
+  size_t delta, cnt, off, cur, tok, total;
+};
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+BwdLayout bwd_layout(int B, int T, int Hq, int Hkv, int S, int num_seqs) {
+  BwdLayout L{};
+  const size_t nbr = static_cast<size_t>((T + kBS - 1) / kBS) + static_cast<size_t>(num_seqs) + 1;
+  const size_t n_slots = static_cast<size_t>(B) * Hkv * nbr;
+  size_t o = 0;
+  L.delta = o; o += round256(static_cast<size_t>(B) * T * Hq * 4);
+  L.cnt = o;   o += round256(n_slots * 4);
+  L.off = o;   o += round256(n_slots * 4);
+  L.cur = o;   o += round256(n_slots * 4);
+  L.tok = o;   o += round256(static_cast<size_t>(B) * T * Hkv * std::min(S, kMaxSel) * 4);
+  L.total = o;
+  return L;
+}
+
+}  // namespace
+
+unsigned read_and_clear_error_nsa_bwd(cudaStream_t, std::string* where) {
+  DevError w{0u, 0u, 0}, zero{0u, 0u, 0};
+  cudaMemcpyFromSymbol(&w, g_err_nsab, sizeof(w));
+  if (w.flags) {
+    cudaMemcpyToSymbol(g_err_nsab, &zero, sizeof(zero));
+    if (where && w.where) {
+      char buf[96];
+      snprintf(buf, sizeof(buf), " [nsa_select_bwd %s role %u barrier %u item %d]",
+               ((w.where >> 24) & 0xFFu) == 3u ? "dq" : "dkdv", (w.where >> 16) & 0xFFu,
+               w.where & 0xFFFFu, w.item);
+      *where += buf;
+    }
+  }
+  return w.flags;
+}
+
+size_t nsa_bwd_workspace_bytes(int B, int T, int Hq, int Hkv, int S, int num_seqs) {
+  return bwd_layout(B, T, Hq, Hkv, S, num_seqs).total;
+}
+
+int launch_nsa_select_bwd(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, const void* d_out, const int32_t* block_indices,
+                          const int32_t* block_counts, int block_count_scalar, int S,
+                          const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
+                          int causal, float scale, void* dq, void* dk, void* dv, void* workspace,
+                          cudaStream_t stream) {
+  const BwdLayout L = bwd_layout(B, T, Hq, Hkv, S, num_seqs);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Params p{};
+  p.out = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(d_out);
+  p.lse = lse;
+  p.delta = reinterpret_cast<float*>(ws + L.delta);
+  p.block_indices = block_indices;
+  p.block_counts = block_counts;
+  p.cu_seqlens = cu_seqlens;
+  p.count_scalar = block_count_scalar;
+  p.S = S;
+  p.num_seqs = num_seqs;
+  p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
+  p.causal = causal;
+  p.NT = kRows / p.G;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.n_tok = B * T;
+  p.nbr = (T + kBS - 1) / kBS + num_seqs + 1;
+  p.n_slots = B * Hkv * p.nbr;
+  p.slot_cnt = reinterpret_cast<int*>(ws + L.cnt);
+  p.slot_off = reinterpret_cast<int*>(ws + L.off);
+  p.slot_cur = reinterpret_cast<int*>(ws + L.cur);
+  p.slot_tok = reinterpret_cast<int*>(ws + L.tok);
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.n_items_dq = ((p.n_tok + p.NT - 1) / p.NT) * Hkv;
+  p.wait_limit = wait_timeout_cycles();
+
+  // tensor maps: Q and dO [n_tok, Hq, D] (boxes of G heads x NT tokens, or x 1 token for
+  // the per-token gather), K and V [n_tok, Hkv, D] (boxes of 64 keys)
+  CUtensorMap tq_dq, tdo_dq, tq_kv, tdo_kv, tk, tv;
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hq, (cuuint64_t)p.n_tok};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hq * kD * 2};
+    cuuint32_t box_dq[3] = {64, (cuuint32_t)p.G, (cuuint32_t)p.NT};
+    cuuint32_t box_kv[3] = {64, (cuuint32_t)p.G, 1};
+    if (encode_tensor_map(&tq_dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                          box_dq, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tensor_map(&tdo_dq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(d_out), dims,
+                          strides, box_dq, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tensor_map(&tq_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                          box_kv, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tensor_map(&tdo_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(d_out), dims,
+                          strides, box_kv, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return set_error(SBA_ERR_CUDA, "nsa_select_bwd: tensor map (q / d_out) failed");
+  }
+  {
+    cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)Hkv, (cuuint64_t)p.n_tok};
+    cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)Hkv * kD * 2};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kBS};
+    if (encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
+        encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return set_error(SBA_ERR_CUDA, "nsa_select_bwd: tensor map (k / v) failed");
+  }
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(nsa_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         DqCfg::kSmemBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(nsa_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               KvCfg::kSmemBytes);
+    if (e != cudaSuccess) return cuda_error(e, "nsa_select_bwd: set smem attribute");
+    attr_done = true;
+  }
+  cudaError_t e = cudaMemsetAsync(p.slot_cnt, 0, static_cast<size_t>(p.n_slots) * 4, stream);
+  if (e != cudaSuccess) return cuda_error(e, "nsa_select_bwd: clear slot counts");
+  const int prep_blocks = std::min<long long>(((long long)p.n_tok * Hkv + 7) / 8, 8LL * num_sms());
+  nsa_bwd_prep_kernel<false><<<prep_blocks, 256, 0, stream>>>(p);
+  nsa_bwd_scan_kernel<<<1, 1024, 0, stream>>>(p);
+  nsa_bwd_prep_kernel<true><<<prep_blocks, 256, 0, stream>>>(p);
+  nsa_bwd_dq_kernel<<<std::min(p.n_items_dq, num_sms()), kThreads, DqCfg::kSmemBytes, stream>>>(
+      tq_dq, tdo_dq, tk, tv, p);
+  nsa_bwd_dkdv_kernel<<<std::min(p.n_slots, num_sms()), kThreads, KvCfg::kSmemBytes, stream>>>(
+      tq_kv, tdo_kv, tk, tv, p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_error(e, "nsa_select_bwd launch");
+  return SBA_OK;
+}
+
+}  // namespace sba
