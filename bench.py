@@ -14,7 +14,7 @@ sampled during the timed region) and ``rows``: the other workloads of the path
 multi-query attention), each timed the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-  python bench.py --case {nsa_prefill,nsa_varlen,blocksparse,mask_sweep,decode,ragged_q4,ragged_chunk512}
+  python bench.py --case {nsa_prefill,nsa_varlen,nsa_bwd,blocksparse,mask_sweep,decode,ragged_q4,ragged_chunk512}
                   [--repeat R]
                   [--decode-batch B]      # profiling: launches only, no JSON line
 
@@ -103,6 +103,28 @@ def nsa_work(w):
         (0 if isinstance(w.block_counts, int) else counts.size * 4)
     gather = float(n_blocks) * bs * D * 2 * elt
     return flops, float(hbm), gather, int(B * T * Hkv)
+
+
+def nsa_selected_pairs(w, rows=128):
+    """Per (batch row, KV head, key block): the number of tokens whose filtered selection
+    holds it; "chunks" = the dK/dV kernel's chunks of rows // G tokens over all of them."""
+    idx = w.block_indices.cpu().numpy().astype(np.int64)
+    B, T, Hkv, S = idx.shape
+    G = w.q.shape[2] // Hkv
+    bs = w.block_size
+    counts = (np.full((B, T, Hkv), w.block_counts, dtype=np.int64) if isinstance(w.block_counts, int)
+              else w.block_counts.cpu().numpy().astype(np.int64))
+    t = np.arange(T)[None, :, None, None]
+    valid = (np.arange(S)[None, None, None, :] < np.minimum(counts, S)[..., None]) & (idx >= 0) & \
+        (idx * bs < T) & (idx * bs <= t)
+    nb = -(-T // bs)
+    slot = (np.arange(B)[:, None, None, None] * Hkv + np.arange(Hkv)[None, None, :, None]) * nb + idx
+    # a duplicate entry in one token's list counts once
+    tok = np.broadcast_to(np.arange(B * T).reshape(B, T, 1, 1), idx.shape)
+    pairs = np.unique(slot[valid] * (B * T) + tok[valid])
+    per_slot = np.bincount(pairs // (B * T))
+    nt = rows // G
+    return {"pairs": int(pairs.size), "chunks": int((-(-per_slot // nt)).sum())}
 
 
 def union_tiles(w, rows=128, tile_keys=64):
@@ -524,6 +546,42 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
         "hbm_bytes": int(hbm), "bound": "launch latency (0.7 MB, fp32 on CUDA cores)"}
     del w
 
+    # NSA selection backward on the prefill workload (dq, dk, dv from the forward's out / LSE)
+    w = workloads.nsa_prefill(device=dev)
+    flops, hbm, _g, _n = nsa_work(w)
+    out, lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts, w.block_size,
+                                  causal=True)
+    gen = torch.Generator(device=dev).manual_seed(7)
+    do = torch.randn(w.q.shape, generator=gen, device=dev, dtype=torch.float32).to(w.q.dtype)
+    B, T, Hq, D = w.q.shape
+    Hkv = w.k.shape[2]
+    bws = torch.empty(sba.nsa_select_bwd_workspace_size(B, T, Hq, Hkv, w.block_indices.shape[-1]),
+                      dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(w.q), torch.empty_like(w.k), torch.empty_like(w.v)
+    t = timed_steps(lambda: sba.nsa_select_bwd(w.q, w.k, w.v, out, lse, do, w.block_indices,
+                                               w.block_counts, w.block_size, causal=True, dq=dq,
+                                               dk=dk, dv=dv, workspace=bws),
+                    steps, warm, flush, stream)
+    ms = sum(t) / len(t)
+    bflops = 2.5 * flops  # S and dP recomputed, dV, dK, dQ: 10 D per (row, key) vs 4 D forward
+    n_tiles = union_tiles(w)
+    # executed MMA work: dQ kernel 3 MMAs (S, dP, dQ) of 128 x 64 x 128 per union tile;
+    # dK/dV kernel 4 such MMAs per chunk of 8 tokens of a block's token list
+    sel = nsa_selected_pairs(w)
+    exec_fl = 2.0 * 128 * 64 * D * (3 * n_tiles + 4 * sel["chunks"])
+    bhbm = hbm + 2 * (w.q.numel() + w.k.numel() + w.v.numel()) * 2  # + d_out, dq, dk, dv
+    log(f"nsa backward {ms:.4f} ms")
+    rows["nsa_select_bwd"] = {
+        "workload": w.name + " (dq, dk, dv)", "ms": round(ms, 4),
+        "TFLOP/s": round(bflops / ms / 1e9, 2),
+        "frac_tensor": round(bflops / ms / 1e9 / peaks["bf16_tflops"], 4),
+        "executed_mma_tflops": round(exec_fl / ms / 1e9, 1),
+        "executed_mma_frac": round(exec_fl / ms / 1e9 / peaks["bf16_tflops"], 4),
+        "hbm_bytes": int(bhbm), "kernels_per_call": 5,
+        "flop_per_call": bflops, "token_list_chunks": sel["chunks"]}
+    del w, out, lse, do, dq, dk, dv, bws
+    torch.cuda.empty_cache()
+
     # varlen NSA (8 packed sequences)
     w = workloads.nsa_varlen(device=dev)
     flops, hbm, gather, groups = nsa_work(w)
@@ -689,6 +747,12 @@ def run_case(args):
             sba.blocksparse_attn_fwd(w.q, w.k, w.v, m.q_positions, m.q_segment_ids, m.kv_positions,
                                      m.kv_segment_ids, lo, up, lof, upf, 128, 128, causal=True,
                                      window_left=1024, window_right=0)
+    elif args.case == "nsa_bwd":
+        w = workloads.nsa_prefill(device=dev)
+        out, lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts, w.block_size)
+        do = torch.randn_like(w.q)
+        fn = lambda: sba.nsa_select_bwd(w.q, w.k, w.v, out, lse, do, w.block_indices, w.block_counts,
+                                        w.block_size)
     elif args.case == "mask_sweep":
         m = workloads.mask(device=dev, B=64, T=131072)
         fn = lambda: sba.sparse_mask_bounds(m.q_positions, m.q_segment_ids, m.kv_positions,

@@ -92,3 +92,23 @@ def test_full_size_sampled(sba):
     rows = [(int(b), int(t)) for b, t in zip(rng.integers(0, 4, 48), rng.integers(0, 16384, 48))]
     rows += [(0, 0), (3, 16383), (1, 16083), (2, 16084)]
     assert_attention_close(*_run(sba, w, rows=rows), what="bsa full sampled")
+
+
+def test_first_item_of_every_cta(sba):
+    """128 work items (B=2, 8 query blocks, 8 KV heads, one head pair each) on at most
+    152 persistent CTAs: every CTA runs exactly one item, its first, so a hazard on a
+    CTA's first item (operands read before they land, stale shared or tensor memory)
+    shows in every row.  Every query block holds padding rows and a segment change.
+    Run twice: the results must also be identical."""
+    w = workloads.blocksparse(device=DEV, B=2, T=1024, Hq=16, Hkv=8, D=128, mean_doc=90,
+                              pad_tail=0, window=(300, 0), seed=808)
+    seg = w.mask.q_segment_ids.cpu().numpy().copy()
+    for qb in range(8):
+        seg[:, qb * 128 + 100:qb * 128 + 112] = -1  # padding inside every query block
+    t = torch.from_numpy(seg.astype(np.int32)).to(DEV)
+    w.mask.q_segment_ids = t
+    w.mask.kv_segment_ids = t.clone()
+    got, ref, gl, rl = _run(sba, w)
+    assert_attention_close(got, ref, gl, rl, what="first items")
+    got2, _, gl2, _ = _run(sba, w)
+    assert np.array_equal(got, got2) and np.array_equal(gl, gl2), "second launch differs"

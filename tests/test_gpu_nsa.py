@@ -258,3 +258,13 @@ def test_host_entry_in_stream_order(sba):
         ref_out, ref_lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts,
                                               w.block_size)
         assert torch.equal(out, ref_out.cpu()) and torch.equal(lse, ref_lse.cpu())
+
+
+def test_first_item_of_every_cta(sba):
+    """128 work items (1,024 tokens in groups of 8, one KV head) on at most 152
+    persistent CTAs: every CTA runs exactly one item, its first.  Run twice: identical."""
+    w = workloads.nsa_prefill(device=DEV, B=1, T=1024, Hq=16, Hkv=1, D=128, seed=909)
+    got, ref, gl, rl = _run(sba, w)
+    assert_attention_close(got, ref, gl, rl, what="nsa first items")
+    got2, _, gl2, _ = _run(sba, w)
+    assert np.array_equal(got, got2) and np.array_equal(gl, gl2), "second launch differs"
