@@ -510,8 +510,8 @@ def run_cuda(args, rank, world, local_rank):
         "e2e": {"value": round(flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "path": "sba_nsa_select_fwd_host: pinned host buffers, copies of batch-row "
-                        "chunks overlapped with the computation"},
+                "path": "sba_nsa_select_fwd_host: pinned host buffers, copies of (batch row, token range) "
+                        "chunks overlapped with the computation (K/V prefix copied once)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "rows": rows,

@@ -179,11 +179,15 @@ SBA_API size_t sba_nsa_select_host_workspace_size(int B, int T, int Hq, int Hkv,
  *                   lse_h != NULL) bytes, 256-byte aligned, owned by the caller; its
  *                   contents are scratch.
  *
- * The batch is split into up to four chunks of rows.  Each chunk's inputs are copied
- * to the device on a library stream, computed on `stream`, and its outputs copied
- * back on a second library stream, so that the copy of one chunk overlaps the
- * computation of its neighbours (the library keeps these two non-blocking streams
- * per device from the first call on).  Ordering: the call's work starts after the
+ * The work is split into up to eight chunks.  With bf16 inputs, T a multiple of 128 and
+ * T >= 256, a chunk is a (batch row, range of 128-token spans) piece, token ranges
+ * first: under causal masking a chunk copies only the K/V rows it adds to its row's
+ * prefix (the earlier chunks' rows are already on the device), otherwise the row's
+ * first chunk copies the row's K/V.  Else a chunk is a group of whole batch rows.  Each
+ * chunk's inputs are copied to the device on a library stream, computed on `stream`,
+ * and its outputs copied back on a second library stream, so that the copy of one
+ * chunk overlaps the computation of its neighbours (the library keeps these two
+ * non-blocking streams per device from the first call on).  Ordering: the call's work starts after the
  * work already enqueued on `stream`, and its end (the last copy to out_h / lse_h) is
  * enqueued on `stream`: synchronize `stream` before reading out_h or lse_h, and do not
  * reuse the workspace or the host buffers before that.

@@ -61,13 +61,14 @@ int num_sms() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-constexpr int kHostChunks = 4;  // batch-row chunks of the host-buffer entry point
+constexpr int kHostChunks = 8;  // chunks of the host-buffer entry point (16 measured no faster)
 
 // Two non-blocking streams per device for the host-buffer entry point: one carries the
 // host-to-device copies, the other the device-to-host copies.  Created on first use and
 // kept for the life of the process; calls that share a device share them.
+constexpr int kCopyStreams = 1;  // per direction (two measured slower: the copies share the link)
 struct CopyStreams {
-  cudaStream_t in = nullptr, out = nullptr;
+  cudaStream_t in[kCopyStreams] = {}, out[kCopyStreams] = {};
 };
 static std::mutex g_copy_mutex;
 static CopyStreams g_copy_streams[64];
@@ -79,14 +80,20 @@ static int copy_streams(CopyStreams** cs) {
   if (dev < 0 || dev >= 64) return set_error(SBA_ERR_UNSUPPORTED, "device ordinal must be < 64");
   std::lock_guard<std::mutex> lock(g_copy_mutex);
   CopyStreams& c = g_copy_streams[dev];
-  if (c.in == nullptr) {
-    if ((e = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking)) != cudaSuccess)
-      return cuda_error(e, "copy stream");
-    if ((e = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking)) != cudaSuccess) {
-      cudaStreamDestroy(c.in);
-      c.in = nullptr;
+  if (c.in[0] == nullptr) {
+    CopyStreams fresh;
+    for (int i = 0; i < kCopyStreams && e == cudaSuccess; ++i) {
+      e = cudaStreamCreateWithFlags(&fresh.in[i], cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&fresh.out[i], cudaStreamNonBlocking);
+    }
+    if (e != cudaSuccess) {
+      for (int i = 0; i < kCopyStreams; ++i) {
+        if (fresh.in[i]) cudaStreamDestroy(fresh.in[i]);
+        if (fresh.out[i]) cudaStreamDestroy(fresh.out[i]);
+      }
       return cuda_error(e, "copy stream");
     }
+    c = fresh;
   }
   *cs = &c;
   return SBA_OK;
@@ -268,65 +275,125 @@ int sba_nsa_select_fwd_host(const void* q_h, const void* k_h, const void* v_h,
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt(static_cast<float>(D));
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int nchunks = B < kHostChunks ? B : kHostChunks;
+  // Chunks: for bf16 with T a multiple of 128, (batch row, token range) pieces of whole
+  // 128-token spans, token-range major; a chunk's queries see keys up to its last token,
+  // so under causal masking it only needs the K/V rows it adds to what earlier chunks of
+  // its row copied (without causal masking the first chunk of a row copies the row's
+  // K/V).  Otherwise whole batch rows.
+  struct Chunk { int b0, rows; long long t0, t1, kv0, kv1; };
+  Chunk chunks[kHostChunks];
+  int nchunks = 0;
+  if (dtype == SBA_BF16 && T % 128 == 0 && T >= 256 && B < kHostChunks) {
+    const int per_row = std::max(1, std::min(kHostChunks / B, T / 128));
+    const long long span = (static_cast<long long>(T) / 128 + per_row - 1) / per_row * 128;
+    for (long long t0 = 0; t0 < T; t0 += span)
+      for (int b = 0; b < B; ++b) {
+        const long long t1 = std::min<long long>(t0 + span, T);
+        const long long kv0 = causal ? t0 : (t0 == 0 ? 0 : T);
+        const long long kv1 = causal ? t1 : T;
+        chunks[nchunks++] = Chunk{b, 1, t0, t1, kv0, std::max(kv0, kv1)};
+      }
+  } else {
+    const int n = B < kHostChunks ? B : kHostChunks;
+    for (int c = 0; c < n; ++c) {
+      const int r0 = static_cast<int>(static_cast<long long>(B) * c / n);
+      const int rows = static_cast<int>(static_cast<long long>(B) * (c + 1) / n) - r0;
+      chunks[nchunks++] = Chunk{r0, rows, 0, T, 0, T};
+    }
+  }
 
   // events: start, then per chunk "inputs copied" and "computed", then "outputs copied"
-  cudaEvent_t ev[2 + 2 * kHostChunks];
+  // events: start, per chunk "inputs copied" and "computed", per output stream "done"
+  cudaEvent_t ev[1 + 2 * kHostChunks + kCopyStreams];
   int nev = 0;
   auto cleanup = [&]() {
     for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);  // released once they complete
   };
-  for (; nev < 2 + 2 * nchunks; ++nev) {
+  for (; nev < 1 + 2 * nchunks + kCopyStreams; ++nev) {
     cudaError_t e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
     if (e != cudaSuccess) { cleanup(); return cuda_error(e, "event create"); }
   }
-  cudaEvent_t ev_start = ev[0], ev_done = ev[1];
+  cudaEvent_t ev_start = ev[0];
   cudaError_t e = cudaEventRecord(ev_start, st);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->in, ev_start, 0);
+  for (int i = 0; i < kCopyStreams && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(cs->in[i], ev_start, 0);
   if (e != cudaSuccess) { cleanup(); return cuda_error(e, "stream ordering"); }
+  cudaStream_t in_s = cs->in[0], out_s = cs->out[0];
 
-  auto h2d = [&](size_t off, const void* src, size_t row_bytes, int r0, int rows) {
-    if (row_bytes == 0) return cudaSuccess;
-    return cudaMemcpyAsync(ws + off + row_bytes * r0,
-                           static_cast<const uint8_t*>(src) + row_bytes * r0, row_bytes * rows,
-                           cudaMemcpyHostToDevice, cs->in);
+  // rows [r0, r0 + rows) x tokens [t0, t1) of an array with `tok_bytes` per token: one
+  // contiguous range when it covers one row or whole rows
+  auto span_bytes = [&](size_t tok_bytes, int r0, int rows, long long t0, long long t1,
+                        size_t& off, size_t& bytes) {
+    off = (static_cast<size_t>(r0) * T + static_cast<size_t>(t0)) * tok_bytes;
+    bytes = (rows == 1 ? static_cast<size_t>(t1 - t0) : static_cast<size_t>(rows) * T) * tok_bytes;
   };
-  auto d2h = [&](void* dst, size_t off, size_t row_bytes, int r0, int rows) {
-    if (row_bytes == 0) return cudaSuccess;
-    return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + row_bytes * r0, ws + off + row_bytes * r0,
-                           row_bytes * rows, cudaMemcpyDeviceToHost, cs->out);
+  auto h2d = [&](size_t base, const void* src, size_t row_bytes, int r0, int rows, long long t0,
+                 long long t1) {
+    if (row_bytes == 0 || t1 <= t0) return cudaSuccess;
+    size_t off, bytes;
+    span_bytes(row_bytes / T, r0, rows, t0, t1, off, bytes);
+    return cudaMemcpyAsync(ws + base + off, static_cast<const uint8_t*>(src) + off, bytes,
+                           cudaMemcpyHostToDevice, in_s);
   };
+  auto d2h = [&](void* dst, size_t base, size_t row_bytes, int r0, int rows, long long t0,
+                 long long t1) {
+    if (row_bytes == 0) return cudaSuccess;
+    size_t off, bytes;
+    span_bytes(row_bytes / T, r0, rows, t0, t1, off, bytes);
+    return cudaMemcpyAsync(static_cast<uint8_t*>(dst) + off, ws + base + off, bytes,
+                           cudaMemcpyDeviceToHost, out_s);
+  };
+  const bool split = nchunks > 0 && (chunks[0].t0 != 0 || chunks[0].t1 != T || nchunks > B);
   for (int c = 0; c < nchunks; ++c) {
-    const int r0 = static_cast<int>(static_cast<long long>(B) * c / nchunks);
-    const int rows = static_cast<int>(static_cast<long long>(B) * (c + 1) / nchunks) - r0;
-    cudaEvent_t ev_in = ev[2 + 2 * c], ev_k = ev[3 + 2 * c];
-    // rows r0 .. r0 + rows - 1: inputs in, selection forward, outputs out
-    e = h2d(L.q, q_h, L.q_row, r0, rows);
-    if (e == cudaSuccess) e = h2d(L.k, k_h, L.kv_row, r0, rows);
-    if (e == cudaSuccess) e = h2d(L.v, v_h, L.kv_row, r0, rows);
-    if (e == cudaSuccess) e = h2d(L.idx, block_indices_h, L.idx_row, r0, rows);
-    if (e == cudaSuccess && block_counts_h) e = h2d(L.cnt, block_counts_h, L.cnt_row, r0, rows);
-    if (e == cudaSuccess && g_slc_h) e = h2d(L.g, g_slc_h, L.g_row, r0, rows);
-    if (e == cudaSuccess) e = cudaEventRecord(ev_in, cs->in);
+    const Chunk& ch = chunks[c];
+    cudaEvent_t ev_in = ev[1 + 2 * c], ev_k = ev[2 + 2 * c];
+    // consecutive chunks alternate between the copy streams of each direction; the
+    // compute stream waits for every chunk's inputs in chunk order, so a chunk's K/V
+    // prefix (copied by earlier chunks on either stream) is complete when it runs
+    in_s = cs->in[c % kCopyStreams];
+    out_s = cs->out[c % kCopyStreams];
+    e = h2d(L.q, q_h, L.q_row, ch.b0, ch.rows, ch.t0, ch.t1);
+    if (e == cudaSuccess) e = h2d(L.k, k_h, L.kv_row, ch.b0, ch.rows, ch.kv0, ch.kv1);
+    if (e == cudaSuccess) e = h2d(L.v, v_h, L.kv_row, ch.b0, ch.rows, ch.kv0, ch.kv1);
+    if (e == cudaSuccess) e = h2d(L.idx, block_indices_h, L.idx_row, ch.b0, ch.rows, ch.t0, ch.t1);
+    if (e == cudaSuccess && block_counts_h)
+      e = h2d(L.cnt, block_counts_h, L.cnt_row, ch.b0, ch.rows, ch.t0, ch.t1);
+    if (e == cudaSuccess && g_slc_h) e = h2d(L.g, g_slc_h, L.g_row, ch.b0, ch.rows, ch.t0, ch.t1);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in, in_s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_in, 0);
     if (e != cudaSuccess) { cleanup(); return cuda_error(e, "host-to-device copy"); }
-    const int rc = launch_nsa_select(
-        ws + L.q + L.q_row * r0, ws + L.k + L.kv_row * r0, ws + L.v + L.kv_row * r0,
-        g_slc_h ? ws + L.g + L.g_row * r0 : nullptr,
-        reinterpret_cast<const int32_t*>(ws + L.idx + L.idx_row * r0),
-        block_counts_h ? reinterpret_cast<const int32_t*>(ws + L.cnt + L.cnt_row * r0) : nullptr,
-        block_count_scalar, S, nullptr, 0, rows, T, Hq, Hkv, D, block_size, causal ? 1 : 0, scale,
-        dtype, ws + L.out + L.q_row * r0,
-        lse_h ? reinterpret_cast<float*>(ws + L.lse + L.lse_row * r0) : nullptr, st);
+    int rc;
+    if (split) {
+      // the whole staged batch, restricted to this chunk's tokens
+      rc = launch_nsa_select(
+          ws + L.q, ws + L.k, ws + L.v, g_slc_h ? ws + L.g : nullptr,
+          reinterpret_cast<const int32_t*>(ws + L.idx),
+          block_counts_h ? reinterpret_cast<const int32_t*>(ws + L.cnt) : nullptr,
+          block_count_scalar, S, nullptr, 0, B, T, Hq, Hkv, D, block_size, causal ? 1 : 0, scale,
+          dtype, ws + L.out, lse_h ? reinterpret_cast<float*>(ws + L.lse) : nullptr, st,
+          static_cast<long long>(ch.b0) * T + ch.t0, static_cast<long long>(ch.b0) * T + ch.t1);
+    } else {
+      const int r0 = ch.b0, rows = ch.rows;
+      rc = launch_nsa_select(
+          ws + L.q + L.q_row * r0, ws + L.k + L.kv_row * r0, ws + L.v + L.kv_row * r0,
+          g_slc_h ? ws + L.g + L.g_row * r0 : nullptr,
+          reinterpret_cast<const int32_t*>(ws + L.idx + L.idx_row * r0),
+          block_counts_h ? reinterpret_cast<const int32_t*>(ws + L.cnt + L.cnt_row * r0) : nullptr,
+          block_count_scalar, S, nullptr, 0, rows, T, Hq, Hkv, D, block_size, causal ? 1 : 0, scale,
+          dtype, ws + L.out + L.q_row * r0,
+          lse_h ? reinterpret_cast<float*>(ws + L.lse + L.lse_row * r0) : nullptr, st);
+    }
     if (rc != SBA_OK) { cleanup(); return rc; }
     e = cudaEventRecord(ev_k, st);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs->out, ev_k, 0);
-    if (e == cudaSuccess) e = d2h(out_h, L.out, L.q_row, r0, rows);
-    if (e == cudaSuccess && lse_h) e = d2h(lse_h, L.lse, L.lse_row, r0, rows);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(out_s, ev_k, 0);
+    if (e == cudaSuccess) e = d2h(out_h, L.out, L.q_row, ch.b0, ch.rows, ch.t0, ch.t1);
+    if (e == cudaSuccess && lse_h) e = d2h(lse_h, L.lse, L.lse_row, ch.b0, ch.rows, ch.t0, ch.t1);
     if (e != cudaSuccess) { cleanup(); return cuda_error(e, "device-to-host copy"); }
   }
-  e = cudaEventRecord(ev_done, cs->out);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_done, 0);
+  for (int i = 0; i < kCopyStreams && e == cudaSuccess; ++i) {
+    cudaEvent_t ev_done = ev[1 + 2 * nchunks + i];
+    e = cudaEventRecord(ev_done, cs->out[i]);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ev_done, 0);
+  }
   cleanup();
   if (e != cudaSuccess) return cuda_error(e, "stream ordering");
   return SBA_OK;

@@ -44,7 +44,8 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const void* g
                       const int32_t* block_counts, int block_count_scalar, int S,
                       const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
                       int D, int block_size, int causal, float scale, int dtype, void* out,
-                      float* lse, cudaStream_t stream);
+                      float* lse, cudaStream_t stream, long long tok_begin = 0,
+                      long long tok_end = -1);
 int launch_sparse_mask_bounds(const int32_t* q_pos, const int32_t* q_seg, const int32_t* kv_pos,
                               const int32_t* kv_seg, int B, int Tq, int Tkv, int q_block,
                               int kv_block, int causal, int window_left, int window_right,

@@ -19,10 +19,11 @@
 //   4. dQ kernel (query-centric, tensor cores): a work item is NT = 128 / G consecutive
 //      tokens and one KV head, 128 query rows; the union of the tokens' selected blocks
 //      is walked in 64-key tiles gathered by TMA.  Per tile: S = Q K^T and dP = dO V^T
-//      (both operands in shared memory, fp32 in tensor memory), then four softmax warps
-//      (one row each) form dS in bf16 into tensor memory, and dQ += dS K accumulates in
-//      tensor memory (A = dS from TMEM).  S/dP and dS are double-buffered so the next
-//      tile's MMAs run while the softmax warps work;
+//      (both operands in shared memory, fp32 in tensor memory), then a softmax
+//      warpgroup (one row per thread) forms dS in bf16 into tensor memory, and
+//      dQ += dS K accumulates in tensor memory (A = dS from TMEM).  S/dP and dS are
+//      double-buffered and two softmax warpgroups take alternate tiles, so one tile's
+//      MMAs run while the other tile's softmax works;
 //   5. dK/dV kernel (key-centric, tensor cores): a work item is one key block of one KV
 //      head; the tokens that selected it are processed in chunks of NT tokens (their Q
 //      and dO rows gathered by TMA, one box of G heads per token).  Per chunk: S and dP
@@ -55,7 +56,8 @@ constexpr int kRows = 128;                  // MMA M: NT tokens x G query heads
 constexpr int kMaxNT = 16;
 constexpr int kMaxSel = 32;
 constexpr int kMaxUnion = kMaxNT * kMaxSel;
-constexpr int kThreads = 256;               // warps 0-3: loader, MMA, builder, spare; 4-7 softmax
+constexpr int kThreads = 256;               // dK/dV: warps 0-3 loader, MMA, spare; 4-7 softmax
+constexpr int kDqThreads = 384;             // dQ: warps 0-3 loader, MMA, builder, spare; 4-11 softmax
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleBuilder = 4 };
@@ -406,7 +408,7 @@ __device__ void build_dq_item(const Params& p, int g, int hkv, int lane, DqItem&
   __syncwarp();
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
 nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_do,
                   const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const Params p) {
@@ -438,15 +440,15 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   };
 
   if (threadIdx.x == 0) {
-    // an item slot is released by the loader, the MMA thread and the 4 softmax warps
-    for (int i = 0; i < C::kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 6); }
+    // an item slot is released by the loader, the MMA thread and the 8 softmax warps
+    for (int i = 0; i < C::kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 10); }
     mbar_init(qdo_full, 1); mbar_init(qdo_empty, 1);
     for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1); mbar_init(&sdp_empty[i], 4);
       mbar_init(&ds_full[i], 4); mbar_init(&ds_empty[i], 1);
     }
-    mbar_init(dq_full, 1); mbar_init(dq_empty, 4); mbar_init(mma_done, 1);
+    mbar_init(dq_full, 1); mbar_init(dq_empty, 8); mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -599,13 +601,17 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
+    // Two warpgroups: warpgroup w takes the tiles that land in S/dP and dS buffer w (the
+    // MMA thread alternates buffers tile by tile, across items), and in the epilogue
+    // head-dim columns 64 w .. 64 w + 63 of dQ.
+    const int w = (warp - 4) >> 2;
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;          // row of the item = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int ti = r / p.G, h = r - (r / p.G) * p.G;
     int islot = 0; uint32_t iphase = 0;
-    uint32_t sdp_ph[2] = {0u, 0u}, ds_ph[2] = {0u, 0u}, dqph = 0;
-    int buf = 0;
+    uint32_t sdp_ph = 0, ds_ph = 0, dqph = 0;
+    int tiles_before = 0;                  // tiles of earlier items of this CTA
     for (int item = blockIdx.x; item < p.n_items_dq; item += gridDim.x) {
       const int hkv = item % p.Hkv;
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
@@ -622,41 +628,41 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const bool live = tok >= 0 && lse2 != -INFINITY;
       const unsigned tbit = 1u << ti;
       bool ok = true;
-      for (int u = 0; u < nu; ++u) {
+      for (int u = ((tiles_before & 1) == w) ? 0 : 1; u < nu; u += 2) {
         const int x0 = it.ux[u];
         const bool sel = live && (it.ubits[u] & tbit) != 0u;
         const int nvalid = sel ? min(max(limit - x0 + 1, 0), kBS) : 0;
-        if (!warp_wait(&sdp_full[buf], sdp_ph[buf], ab, kRoleSoftmax, kBarSdpFull, item)) { ok = false; break; }
-        sdp_ph[buf] ^= 1;
+        if (!warp_wait(&sdp_full[w], sdp_ph, ab, kRoleSoftmax, kBarSdpFull, item)) { ok = false; break; }
+        sdp_ph ^= 1;
         tc_fence_after();
         float s[64], dp[64];
-        tmem_ld64(tmem + lane_off + C::kSCol + buf * kBS, s);
-        tmem_ld64(tmem + lane_off + C::kDpCol + buf * kBS, dp);
+        tmem_ld64(tmem + lane_off + C::kSCol + w * kBS, s);
+        tmem_ld64(tmem + lane_off + C::kDpCol + w * kBS, dp);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sdp_empty[buf]);
+        if (lane == 0) mbar_arrive(&sdp_empty[w]);
         uint32_t ds_pk[32];
         row_grads(s, dp, nvalid, p.scale_log2, lse2, delta, nullptr, ds_pk);
         // the dQ MMA that read this dS buffer two tiles ago must be done
-        if (!warp_wait(&ds_empty[buf], ds_ph[buf] ^ 1, ab, kRoleSoftmax, kBarDsEmpty, item)) { ok = false; break; }
-        ds_ph[buf] ^= 1;
+        if (!warp_wait(&ds_empty[w], ds_ph ^ 1, ab, kRoleSoftmax, kBarDsEmpty, item)) { ok = false; break; }
+        ds_ph ^= 1;
         tc_fence_after();
-        tmem_st_32x32b_x32_u(tmem + lane_off + C::kDsCol + buf * (kBS / 2), ds_pk);
+        tmem_st_32x32b_x32_u(tmem + lane_off + C::kDsCol + w * (kBS / 2), ds_pk);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ds_full[buf]);
-        buf ^= 1;
+        if (lane == 0) mbar_arrive(&ds_full[w]);
       }
       if (!ok) break;
-      __nv_bfloat16* drow = p.dq + hrow * kD;
+      tiles_before += nu;
+      __nv_bfloat16* drow = p.dq + hrow * kD + w * (kD / 2);
       if (nu > 0) {
         if (!warp_wait(dq_full, dqph, ab, kRoleSoftmax, kBarAccFull, item)) break;
         dqph ^= 1;
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < kD / 32; ++c) {
+        for (int c = 0; c < kD / 64; ++c) {
           float v[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + C::kDqCol + c * 32, v);
+          tmem_ld_32x32b_x32(tmem + lane_off + C::kDqCol + w * (kD / 2) + c * 32, v);
           if (tok >= 0) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
@@ -674,7 +680,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (lane == 0) mbar_arrive(dq_empty);
       } else if (tok >= 0) {
 #pragma unroll
-        for (int j = 0; j < kD; j += 8) *reinterpret_cast<uint4*>(drow + j) = make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < kD / 2; j += 8) *reinterpret_cast<uint4*>(drow + j) = make_uint4(0u, 0u, 0u, 0u);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[islot]);
@@ -714,11 +720,16 @@ struct KvCfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void kv_item(const Params& p, int item, int& b, int& hkv, int& sidx) {
+// Work items in (KV head, batch row, key block) order, so that the items running at once
+// gather Q / dO rows of one KV head's query heads in one batch row (a working set that
+// stays in L2).  The slot arrays are indexed (batch row, KV head, key block).
+__device__ __forceinline__ void kv_item(const Params& p, int item, int& b, int& hkv, int& sidx,
+                                        int& slot) {
   sidx = item % p.nbr;
   const int r = item / p.nbr;
-  hkv = r % p.Hkv;
-  b = r / p.Hkv;
+  b = r % p.B;
+  hkv = r / p.B;
+  slot = (b * p.Hkv + hkv) * p.nbr + sidx;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -780,10 +791,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     bool q_issued[2] = {false, false}; uint32_t q_last[2] = {0u, 0u};
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-      int b, hkv, sidx, row0 = 0, nkeys = 0;
-      kv_item(p, item, b, hkv, sidx);
+      int b, hkv, sidx, slot, row0 = 0, nkeys = 0;
+      kv_item(p, item, b, hkv, sidx, slot);
       if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
-      const int cnt = p.slot_cnt[item], off = p.slot_off[item];
+      const int cnt = p.slot_cnt[slot], off = p.slot_off[slot];
       if (cnt == 0) continue;
       if (!warp_wait(kv_empty, kvph ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) break;
       if (lane == 0) {
@@ -839,10 +850,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const uint64_t p_desc = make_sdesc(smem_base + C::kOffP, C::kPBytes, 1024, kLayoutSW128);
       const uint64_t ds_desc = make_sdesc(smem_base + C::kOffDs, C::kPBytes, 1024, kLayoutSW128);
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        int b, hkv, sidx, row0 = 0, nkeys = 0;
-        kv_item(p, item, b, hkv, sidx);
+        int b, hkv, sidx, slot, row0 = 0, nkeys = 0;
+        kv_item(p, item, b, hkv, sidx, slot);
         if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
-        const int cnt = p.slot_cnt[item];
+        const int cnt = p.slot_cnt[slot];
         if (cnt == 0) continue;
         if (!bounded_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
         kvph ^= 1;
@@ -918,10 +929,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint8_t* prow = smem + C::kOffP + r * 128;
     uint8_t* dsrow = smem + C::kOffDs + r * 128;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-      int b, hkv, sidx, row0 = 0, nkeys = 0;
-      kv_item(p, item, b, hkv, sidx);
+      int b, hkv, sidx, slot, row0 = 0, nkeys = 0;
+      kv_item(p, item, b, hkv, sidx, slot);
       if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
-      const int cnt = p.slot_cnt[item], off = p.slot_off[item];
+      const int cnt = p.slot_cnt[slot], off = p.slot_off[slot];
       if (cnt == 0) {
         // no token chose this block: its keys get zero gradients
         for (int i = r; i < nkeys * (kD / 8); i += kRows) {
@@ -1122,7 +1133,7 @@ int launch_nsa_select_bwd(const void* q, const void* k, const void* v, const voi
   nsa_bwd_prep_kernel<false><<<prep_blocks, 256, 0, stream>>>(p);
   nsa_bwd_scan_kernel<<<1, 1024, 0, stream>>>(p);
   nsa_bwd_prep_kernel<true><<<prep_blocks, 256, 0, stream>>>(p);
-  nsa_bwd_dq_kernel<<<std::min(p.n_items_dq, num_sms()), kThreads, DqCfg::kSmemBytes, stream>>>(
+  nsa_bwd_dq_kernel<<<std::min(p.n_items_dq, num_sms()), kDqThreads, DqCfg::kSmemBytes, stream>>>(
       tq_dq, tdo_dq, tk, tv, p);
   nsa_bwd_dkdv_kernel<<<std::min(p.n_slots, num_sms()), kThreads, KvCfg::kSmemBytes, stream>>>(
       tq_kv, tdo_kv, tk, tv, p);

@@ -82,6 +82,7 @@ struct Params {
   int ranked;    // items are formed from count-ranked windows (see build_item)
   float scale, scale_log2;
   int n_items, n_tok;
+  int item0;             // work items [item0, n_items) of this launch
   long long wait_limit;  // cycles a bounded wait may take
 };
 
@@ -398,7 +399,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ------------------------------------------------------------------ item builder
     int islot = 0; uint32_t iphase = 0;
     int cached_seq = 0;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    for (int item = p.item0 + blockIdx.x; item < p.n_items; item += gridDim.x) {
       const int g = item / p.Hkv, hkv = item - g * p.Hkv;
       if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, item)) break;
       build_item<BS>(p, g, hkv, lane, cached_seq, item_at(islot), keys);
@@ -415,7 +416,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int i = 0; i < 8; ++i) { issued[i] = false; last_parity[i] = 0; }
     const uint32_t q_box_bytes = static_cast<uint32_t>(C::kPanels * 128 * p.G * p.NT);
     bool ok = true;
-    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+    for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, item)) break;
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union, hkv = it.hkv;
@@ -492,7 +493,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bool ok = true;
       // descriptors of the shared-memory operands; a byte offset x adds x >> 4
       const uint64_t st_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
-      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+      for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
         mbar_arrive(&item_empty[islot]);
@@ -549,7 +550,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bool ok = true;
       const uint64_t v_desc0 =
           make_sdesc(smem_base + C::kOffStages + C::kKBytes, C::kPanelBytes, 1024, kLayoutSW128);
-      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+      for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
         mbar_arrive(&item_empty[islot]);
@@ -602,7 +603,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t sph = 0, pvph = 0, xph = 0;
     int par = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+    for (int item = p.item0 + blockIdx.x; item < p.n_items; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union;
@@ -808,7 +809,7 @@ nsa_select_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   const int tid = threadIdx.x, lane = tid & 31;
   float* out = static_cast<float*>(p.out);
   int cached_seq = 0;
-  for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
+  for (int item = p.item0 + blockIdx.x; item < p.n_items; item += gridDim.x) {
     int b, hkv, t;
     decode_item(p, item, b, hkv, t);
     const long long out_row0 = ((long long)b * p.T + t) * p.Hq + (long long)hkv * p.G;
@@ -945,7 +946,7 @@ int launch_bf16(const void* q, const void* k, const void* v, const Params& p, cu
     if (e != cudaSuccess) return cuda_error(e, "nsa_select: set smem attribute");
     attr_done = true;
   }
-  const int grid = std::min(p.n_items, num_sms());
+  const int grid = std::min(p.n_items - p.item0, num_sms());
   nsa_union_kernel<D, BS><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "nsa_select launch");
@@ -984,7 +985,7 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const void* g
                       const int32_t* block_counts, int block_count_scalar, int S,
                       const int32_t* cu_seqlens, int num_seqs, int B, int T, int Hq, int Hkv,
                       int D, int block_size, int causal, float scale, int dtype, void* out,
-                      float* lse, cudaStream_t stream) {
+                      float* lse, cudaStream_t stream, long long tok_begin, long long tok_end) {
   Params p;
   p.g_slc = g_slc;
   p.block_indices = block_indices;
@@ -1003,6 +1004,7 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const void* g
   p.NT = std::min(kMaxNT, kRows / p.G);
   p.rows = p.NT * p.G;
   p.ranked = 0;
+  p.item0 = 0;
   p.wait_limit = wait_timeout_cycles();
   if ((long long)B * T * Hkv >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "nsa_select: too many items");
   p.n_tok = B * T;
@@ -1013,6 +1015,15 @@ int launch_nsa_select(const void* q, const void* k, const void* v, const void* g
     const long long groups = p.ranked ? (p.n_tok + 8 * p.NT - 1) / (8 * p.NT) * 8
                                       : (p.n_tok + p.NT - 1) / p.NT;
     p.n_items = static_cast<int>(groups * Hkv);
+    if (tok_begin > 0 || (tok_end >= 0 && tok_end < p.n_tok)) {
+      // tokens [tok_begin, tok_end) only: the host keeps both ends multiples of 128 tokens
+      // (whole count-ranked windows and groups), so they map to a contiguous item range
+      const long long t1 = tok_end < 0 ? p.n_tok : tok_end;
+      if (tok_begin % 128 != 0 || (t1 % 128 != 0 && t1 != p.n_tok) || tok_begin >= t1)
+        return set_error(SBA_ERR_INVALID_ARG, "nsa_select: token range must be 128-aligned");
+      p.item0 = static_cast<int>(tok_begin / p.NT * Hkv);
+      p.n_items = static_cast<int>(std::min<long long>((t1 + p.NT - 1) / p.NT * Hkv, p.n_items));
+    }
     if (D == 128) return dispatch_bs<128>(block_size, q, k, v, p, stream);
     return dispatch_bs<64>(block_size, q, k, v, p, stream);
   }

@@ -268,3 +268,31 @@ def test_first_item_of_every_cta(sba):
     assert_attention_close(got, ref, gl, rl, what="nsa first items")
     got2, _, gl2, _ = _run(sba, w)
     assert np.array_equal(got, got2) and np.array_equal(gl, gl2), "second launch differs"
+
+
+@pytest.mark.parametrize("B,causal,gate", [(1, True, False), (2, True, True), (2, False, False)])
+def test_host_entry_split_along_tokens(sba, B, causal, gate):
+    """T = 1024 (a multiple of 128): the host entry stages (batch row, token range)
+    chunks, each computed once the K/V prefix it needs has arrived (without causal
+    masking, the whole row's K/V with the row's first chunk).  The chunks hold whole
+    item windows, so the result equals the device entry bit for bit; and the oracle."""
+    w = workloads.nsa_prefill(device=DEV, B=B, T=1024, Hq=32, Hkv=2, D=128, seed=450 + B)
+    g = None
+    if gate:
+        g = torch.sigmoid(workloads.randn(tuple(w.q.shape[:3]), torch.float32, DEV, seed=451)).to(w.q.dtype)
+    pin = lambda t: None if t is None else t.cpu().pin_memory()
+    out, lse = sba.nsa_select_fwd_host(pin(w.q), pin(w.k), pin(w.v), pin(w.block_indices),
+                                       pin(w.block_counts), w.block_size, causal=causal, g_slc=pin(g))
+    torch.cuda.synchronize()
+    sba.check_error()
+    ref_out, ref_lse = sba.nsa_select_fwd(w.q, w.k, w.v, w.block_indices, w.block_counts,
+                                          w.block_size, causal=causal, g_slc=g)
+    sba.check_error()
+    assert torch.equal(out, ref_out.cpu()) and torch.equal(lse, ref_lse.cpu())
+    rows = [(b, t) for b in range(B) for t in (0, 1, 255, 256, 511, 700, 1023)]
+    ref, rl = oracle.nsa_select_attention(
+        to_np(w.q), to_np(w.k), to_np(w.v), w.block_indices.cpu().numpy(),
+        w.block_counts.cpu().numpy(), w.block_size, causal=causal, rows=rows,
+        g_slc=None if g is None else to_np(g))
+    idx = tuple(np.array(rows).T)
+    assert_attention_close(to_np(out)[idx], ref[idx], to_np(lse)[idx], rl[idx], what="host split")
