@@ -56,7 +56,7 @@ constexpr int kRows = 128;                  // MMA M: NT tokens x G query heads
 constexpr int kMaxNT = 16;
 constexpr int kMaxSel = 32;
 constexpr int kMaxUnion = kMaxNT * kMaxSel;
-constexpr int kThreads = 256;               // dK/dV: warps 0-3 loader, MMA, spare; 4-7 softmax
+constexpr int kThreads = 256;               // dK/dV: warps 0-3 loader, 2 MMA, spare; 4-7 softmax
 constexpr int kDqThreads = 384;             // dQ: warps 0-3 loader, MMA, builder, spare; 4-11 softmax
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -301,7 +301,7 @@ struct DqCfg {
   static constexpr int kOffItems = kOffRing + kStages * 2 * kTileBytes;
   static constexpr int kOffSort = kOffItems + kItemSlots * kItemBytes;
   static constexpr int kOffBars = kOffSort + kMaxUnion * 8;
-  static constexpr int kNumBars = 2 * kItemSlots + 2 + 2 * kStages + 8 + 2 + 1;
+  static constexpr int kNumBars = 2 * kItemSlots + 2 + 2 * kStages + 8 + 2 + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // tensor memory: S[2], dP[2] (64 fp32 each), dS[2] (64 bf16 = 32 columns each), dQ (128)
@@ -430,7 +430,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   uint64_t* ds_empty = bb;   bb += 2;
   uint64_t* dq_full = bb;    bb += 1;
   uint64_t* dq_empty = bb;   bb += 1;
-  uint64_t* mma_done = bb;
+  uint64_t* mma_done = bb;   // [2]: per issuing thread
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Abort ab{abort_flag, &g_err_nsab, 3u, p.wait_limit};
@@ -440,15 +440,16 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   };
 
   if (threadIdx.x == 0) {
-    // an item slot is released by the loader, the MMA thread and the 8 softmax warps
-    for (int i = 0; i < C::kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 10); }
+    // an item slot is released by the loader, the two MMA threads and the 8 softmax warps
+    for (int i = 0; i < C::kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 11); }
     mbar_init(qdo_full, 1); mbar_init(qdo_empty, 1);
     for (int i = 0; i < C::kStages; ++i) { mbar_init(&kv_full[i], 1); mbar_init(&kv_empty[i], 1); }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1); mbar_init(&sdp_empty[i], 4);
       mbar_init(&ds_full[i], 4); mbar_init(&ds_empty[i], 1);
     }
-    mbar_init(dq_full, 1); mbar_init(dq_empty, 8); mbar_init(mma_done, 1);
+    mbar_init(dq_full, 1); mbar_init(dq_empty, 8);
+    mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -526,14 +527,19 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (issued[s]) drain_wait(&kv_full[s], last[s]);
       if (q_issued) drain_wait(qdo_full, q_last);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Two threads issue MMAs: warp 1 S = Q K^T and dP = dO V^T of each tile, warp 3
+    // dQ += dS K.  A thread's barrier wait then stalls only its own stream while the
+    // tensor core runs the other's MMAs.  A tile's K/V stage is released by the dQ
+    // thread: its dQ MMA follows the tile's softmax, which followed the S/dP MMAs.
+    const bool sdp_role = warp == 1;
     if (lane == 0) {
       int islot = 0; uint32_t iphase = 0;
       uint32_t qph = 0, dqph = 0;
       int stage = 0; uint32_t kph = 0;
       uint32_t sdp_ph[2] = {0u, 0u}, ds_ph[2] = {0u, 0u};
-      int sbuf = 0, dbuf = 0;  // next S/dP buffer to fill, next dS buffer to consume
+      int buf = 0;  // S/dP (sdp_role) or dS buffer of the next tile
       bool ok = true;
       const uint64_t q_desc = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
       const uint64_t do_desc = make_sdesc(smem_base + C::kOffDO, 16, 1024, kLayoutSW128);
@@ -545,58 +551,59 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         mbar_arrive(&item_empty[islot]);
         if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
         if (nu == 0) continue;
-        if (!bounded_wait(qdo_full, qph, ab, kRoleMma, kBarQdoFull, item)) break;
-        qph ^= 1;
-        int st_u = stage;  // stage of the tile whose dQ MMA is next
-        // S = Q K^T and dP = dO V^T of tile u into S/dP buffer sbuf
-        auto issue_sdp = [&](int u) -> bool {
-          if (!bounded_wait(&kv_full[stage], kph, ab, kRoleMma, kBarKvFull, item)) return false;
-          if (!bounded_wait(&sdp_empty[sbuf], sdp_ph[sbuf] ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) return false;
-          tc_fence_after();
-          const uint64_t kd = ring_k + static_cast<uint64_t>((stage * 2 * C::kTileBytes) >> 4);
-          const uint64_t vd = kd + static_cast<uint64_t>(C::kTileBytes >> 4);
+        if (sdp_role) {
+          if (!bounded_wait(qdo_full, qph, ab, kRoleMma, kBarQdoFull, item)) break;
+          qph ^= 1;
+          for (int u = 0; u < nu; ++u) {
+            if (!bounded_wait(&kv_full[stage], kph, ab, kRoleMma, kBarKvFull, item) ||
+                !bounded_wait(&sdp_empty[buf], sdp_ph[buf] ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t kd = ring_k + static_cast<uint64_t>((stage * 2 * C::kTileBytes) >> 4);
+            const uint64_t vd = kd + static_cast<uint64_t>(C::kTileBytes >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_f16_ss(tmem + C::kSCol + sbuf * kBS, q_desc + kmajor_step(kk, C::kQPanel),
-                       kd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_f16_ss(tmem + C::kSCol + buf * kBS, q_desc + kmajor_step(kk, C::kQPanel),
+                         kd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_f16_ss(tmem + C::kDpCol + sbuf * kBS, do_desc + kmajor_step(kk, C::kQPanel),
-                       vd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
-          mma_commit(&sdp_full[sbuf]);
-          if (u == nu - 1) mma_commit(qdo_empty);
-          sdp_ph[sbuf] ^= 1;
-          sbuf ^= 1;
-          if (++stage == C::kStages) { stage = 0; kph ^= 1; }
-          return true;
-        };
-        if (!issue_sdp(0)) break;
-        for (int u = 0; u < nu && ok; ++u) {
-          if (u + 1 < nu && !issue_sdp(u + 1)) { ok = false; break; }
-          // dQ += dS(u) K(u)
-          if (!bounded_wait(&ds_full[dbuf], ds_ph[dbuf], ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
-          ds_ph[dbuf] ^= 1;
-          if (u == 0) {
-            if (!bounded_wait(dq_empty, dqph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
-            dqph ^= 1;
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_f16_ss(tmem + C::kDpCol + buf * kBS, do_desc + kmajor_step(kk, C::kQPanel),
+                         vd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_commit(&sdp_full[buf]);
+            if (u == nu - 1) mma_commit(qdo_empty);
+            sdp_ph[buf] ^= 1;
+            buf ^= 1;
+            if (++stage == C::kStages) { stage = 0; kph ^= 1; }
           }
-          tc_fence_after();
-          const uint64_t kmn = ring_kmn + static_cast<uint64_t>((st_u * 2 * C::kTileBytes) >> 4);
+        } else {
+          for (int u = 0; u < nu; ++u) {
+            // dQ += dS(u) K(u)
+            if (!bounded_wait(&ds_full[buf], ds_ph[buf], ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+            ds_ph[buf] ^= 1;
+            if (u == 0) {
+              if (!bounded_wait(dq_empty, dqph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
+              dqph ^= 1;
+            }
+            tc_fence_after();
+            const uint64_t kmn = ring_kmn + static_cast<uint64_t>((stage * 2 * C::kTileBytes) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kBS / 16; ++kk)
-            mma_f16_ts(tmem + C::kDqCol, tmem + C::kDsCol + dbuf * (kBS / 2) + kk * 8,
-                       kmn + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::kIdescDq,
-                       (u == 0 && kk == 0) ? 0u : 1u);
-          mma_commit(&kv_empty[st_u]);
-          mma_commit(&ds_empty[dbuf]);
-          dbuf ^= 1;
-          if (++st_u == C::kStages) st_u = 0;
+            for (int kk = 0; kk < kBS / 16; ++kk)
+              mma_f16_ts(tmem + C::kDqCol, tmem + C::kDsCol + buf * (kBS / 2) + kk * 8,
+                         kmn + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::kIdescDq,
+                         (u == 0 && kk == 0) ? 0u : 1u);
+            mma_commit(&kv_empty[stage]);
+            mma_commit(&ds_empty[buf]);
+            buf ^= 1;
+            if (++stage == C::kStages) stage = 0;
+          }
+          if (ok) mma_commit(dq_full);
         }
-        if (!ok) break;
-        mma_commit(dq_full);
       }
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
+      // every tcgen05 op issued by this thread has finished once its mma_done fires
+      mma_commit(&mma_done[sdp_role ? 0 : 1]);
+      drain_wait(&mma_done[sdp_role ? 0 : 1], 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
@@ -709,7 +716,7 @@ struct KvCfg {
   static constexpr int kOffP = kOffQ + 4 * kQBytes;
   static constexpr int kOffDs = kOffP + kPBytes;
   static constexpr int kOffBars = kOffDs + kPBytes;
-  static constexpr int kNumBars = 2 + 4 + 2 + 2 + 2 + 1;
+  static constexpr int kNumBars = 2 + 4 + 2 + 2 + 2 + 2;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // tensor memory: S, dP (64 fp32 each), dV^T, dK^T (lanes = head dim, 64 key columns)
@@ -751,7 +758,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   uint64_t* pds_empty = bb;  bb += 1;
   uint64_t* acc_full = bb;   bb += 1;
   uint64_t* acc_empty = bb;  bb += 1;
-  uint64_t* mma_done = bb;
+  uint64_t* mma_done = bb;   // [2]: per issuing thread
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   const Abort ab{abort_flag, &g_err_nsab, 4u, p.wait_limit};
@@ -764,7 +771,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(sdp_full, 1); mbar_init(sdp_empty, 4);
     mbar_init(pds_full, 4); mbar_init(pds_empty, 1);
     mbar_init(acc_full, 1); mbar_init(acc_empty, 4);
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -836,8 +843,13 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       for (int i = 0; i < 2; ++i)
         if (q_issued[i]) drain_wait(&qdo_full[i], q_last[i]);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 1 issues S = Q K^T and dP = dO V^T of each chunk (running one chunk ahead of
+    // the softmax warps, which release S / dP as soon as they have loaded them); warp 2
+    // issues dV^T += dO^T P and dK^T += Q^T dS and releases the chunk's Q / dO buffer,
+    // and at the end of an item the K / V tile (its MMAs follow the item's last S / dP).
+    const bool sdp_role = warp == 1;
     if (lane == 0) {
       uint32_t kvph = 0, sdph = 0, pdph = 0, accph = 0;
       uint32_t qph[2] = {0u, 0u};
@@ -855,68 +867,65 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
         const int cnt = p.slot_cnt[slot];
         if (cnt == 0) continue;
-        if (!bounded_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
-        kvph ^= 1;
         const int nch = (cnt + p.NT - 1) / p.NT;
-        // S = Q K^T and dP = dO V^T of chunk c (Q / dO buffer c & 1 of this item's run)
-        int sq = qb;  // buffer of the next chunk to start
-        auto issue_sdp = [&]() -> bool {
-          if (!bounded_wait(&qdo_full[sq], qph[sq], ab, kRoleMma, kBarQdoFull, item) ||
-              !bounded_wait(sdp_empty, sdph ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) return false;
-          qph[sq] ^= 1;
-          sdph ^= 1;
-          tc_fence_after();
-          const uint64_t qo = static_cast<uint64_t>((sq * 2 * C::kQBytes) >> 4);
-          const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
+        if (sdp_role) {
+          if (!bounded_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
+          kvph ^= 1;
+          for (int c = 0; c < nch; ++c) {
+            if (!bounded_wait(&qdo_full[qb], qph[qb], ab, kRoleMma, kBarQdoFull, item) ||
+                !bounded_wait(sdp_empty, sdph ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) { ok = false; break; }
+            qph[qb] ^= 1;
+            sdph ^= 1;
+            tc_fence_after();
+            const uint64_t qo = static_cast<uint64_t>((qb * 2 * C::kQBytes) >> 4);
+            const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_f16_ss(tmem + C::kSCol, qk_desc + qo + kmajor_step(kk, C::kQPanel),
-                       k_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_f16_ss(tmem + C::kSCol, qk_desc + qo + kmajor_step(kk, C::kQPanel),
+                         k_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_f16_ss(tmem + C::kDpCol, qk_desc + doo + kmajor_step(kk, C::kQPanel),
-                       v_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
-          mma_commit(sdp_full);
-          sq ^= 1;
-          return true;
-        };
-        if (!issue_sdp()) break;
-        for (int c = 0; c < nch && ok; ++c) {
-          // the next chunk's S / dP run while the softmax warps work on this one (they
-          // release S / dP as soon as they have loaded them)
-          if (c + 1 < nch && !issue_sdp()) { ok = false; break; }
-          // dV^T += dO^T P and dK^T += Q^T dS over the chunk's 128 rows (K = rows)
-          if (!bounded_wait(pds_full, pdph, ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
-          pdph ^= 1;
-          if (c == 0) {
-            if (!bounded_wait(acc_empty, accph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
-            accph ^= 1;
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_f16_ss(tmem + C::kDpCol, qk_desc + doo + kmajor_step(kk, C::kQPanel),
+                         v_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
+            mma_commit(sdp_full);
+            qb ^= 1;
           }
-          tc_fence_after();
-          const uint64_t qo = static_cast<uint64_t>((qb * 2 * C::kQBytes) >> 4);
-          const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
+        } else {
+          for (int c = 0; c < nch; ++c) {
+            // dV^T += dO^T P and dK^T += Q^T dS over the chunk's 128 rows (K = rows)
+            if (!bounded_wait(pds_full, pdph, ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+            pdph ^= 1;
+            if (c == 0) {
+              if (!bounded_wait(acc_empty, accph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
+              accph ^= 1;
+            }
+            tc_fence_after();
+            const uint64_t qo = static_cast<uint64_t>((qb * 2 * C::kQBytes) >> 4);
+            const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk) {
-            const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-            mma_f16_ss(tmem + C::kDvCol, qmn_desc + doo + step, p_desc + step, C::kIdescAcc,
-                       (c == 0 && kk == 0) ? 0u : 1u);
-          }
+            for (int kk = 0; kk < kRows / 16; ++kk) {
+              const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+              mma_f16_ss(tmem + C::kDvCol, qmn_desc + doo + step, p_desc + step, C::kIdescAcc,
+                         (c == 0 && kk == 0) ? 0u : 1u);
+            }
 #pragma unroll
-          for (int kk = 0; kk < kRows / 16; ++kk) {
-            const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-            mma_f16_ss(tmem + C::kDkCol, qmn_desc + qo + step, ds_desc + step, C::kIdescAcc,
-                       (c == 0 && kk == 0) ? 0u : 1u);
+            for (int kk = 0; kk < kRows / 16; ++kk) {
+              const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+              mma_f16_ss(tmem + C::kDkCol, qmn_desc + qo + step, ds_desc + step, C::kIdescAcc,
+                         (c == 0 && kk == 0) ? 0u : 1u);
+            }
+            mma_commit(&qdo_empty[qb]);
+            mma_commit(pds_empty);
+            qb ^= 1;
           }
-          mma_commit(&qdo_empty[qb]);
-          mma_commit(pds_empty);
-          qb ^= 1;
+          if (!ok) break;
+          mma_commit(kv_empty);
+          mma_commit(acc_full);
         }
-        if (!ok) break;
-        mma_commit(kv_empty);
-        mma_commit(acc_full);
       }
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
+      // every tcgen05 op issued by this thread has finished once its mma_done fires
+      mma_commit(&mma_done[sdp_role ? 0 : 1]);
+      drain_wait(&mma_done[sdp_role ? 0 : 1], 0);
     }
     __syncwarp();
   } else if (warp >= 4) {
