@@ -319,7 +319,8 @@ SBA_API size_t sba_ragged_decode_workspace_size(int B, int Hq, int S, int D, int
  *             sba_ragged_decode_workspace_size(B, Hq, S, D, window_left) bytes,
  *             16-byte aligned, caller-owned; contents need no initialisation.
  * Supported: D == 128, 1 <= Hq / Hkv <= 16, num_sinks <= 16, sequence_end <= S, bf16.
- * Internally: split-KV partial kernel + combine kernel on `stream`.
+ * Internally, on `stream`: a memset of the workspace's split counters and one split-KV
+ * kernel whose last split of each row tile merges the partials.
  */
 SBA_API int sba_ragged_decode_fwd(const void* q, const void* k, const void* v,
                           const int32_t* seq_start, const int32_t* seq_end,
@@ -349,7 +350,8 @@ SBA_API int sba_ragged_decode_fwd(const void* q, const void* k, const void* v,
  *  - All calls on a device share the array: calls that may overlap on the GPU (different
  *    streams, no ordering between them) race and corrupt each other's results.  Calls on
  *    one stream are ordered and safe.  The array keeps the last call's partials; every
- *    slot a call reads was written by that call, so nothing needs clearing.
+ *    partial a call reads was written by that call, and the per-tile split counters it
+ *    needs zeroed are cleared by the call itself (cudaMemsetAsync on `stream`).
  *  - Neither the call nor its first-call set-up calls cudaMalloc, cudaFree or any
  *    allocating routine.  The 16 MiB are reserved when the library's device code is
  *    loaded onto the GPU; with lazy module loading (CUDA_MODULE_LOADING=LAZY, the
@@ -403,7 +405,8 @@ SBA_API size_t sba_ragged_flash_attention_workspace_size(int B, int Q, int Hq, i
  * D == 128, num_sinks <= 16, B * ceil(Q * Hq / Hkv / 16) <= 65535, Q <= 65535.
  * Internally, on `stream`: with Q >= 128, no soft cap and no sinks, one launch of the
  * tensor-memory block kernel (query blocks of 128 rows, key blocks of 128; the workspace
- * is not touched); otherwise a split-KV partial kernel + combine kernel.
+ * is not touched); otherwise a memset of the workspace's split counters and one split-KV
+ * kernel whose last split of each row tile merges the partials.
  */
 SBA_API int sba_ragged_flash_attention_fwd(const void* q, const void* k, const void* v,
                                            const int32_t* seq_start, const int32_t* seq_end,

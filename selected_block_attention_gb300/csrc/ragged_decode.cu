@@ -1,5 +1,5 @@
-// Ragged decode attention, one or several query tokens per batch row: split-KV partial
-// kernel + combine kernel.
+// Ragged decode attention, one or several query tokens per batch row: split-KV kernel
+// whose last split of each row tile combines the partials.
 //
 // Follows "ejkernel.kernels._xla.ragged_decode_attention._xla_impl_fwd" (API page):
 // ragged_decode_mqa_xla / inner_decode_xla (one query per row) and
@@ -23,9 +23,10 @@
 // inside every row's window skip the per-element mask; edge tiles mask each element
 // with its own row's window.  Sink keys outside [lo, hi) go through an extra sink tile
 // of split 0.  The four warps merge through shared memory and write one fp32 partial
-// (o * exp(-m), m, l) per (row, split, query, head); the combine kernel merges the
-// partials of a (query, head) with max / exp weights and writes the bf16 output and
-// the natural-log LSE.
+// (o * exp(-m), m, l) per (row, split, query, head).  The CTA that completes the last
+// split of a row tile (a counter per tile in the workspace, cleared before the launch)
+// merges the tile's partials with max / exp weights and writes the bf16 output and the
+// natural-log LSE, so one launch does the whole call.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -114,6 +115,9 @@ struct MqParams {
   const float* sink_bias;
   float* o_part;   // [B][max_splits][Q][Hq][D]
   float* ml_part;  // [B][max_splits][Q][Hq][2]
+  int* tile_count; // [B][Hkv][row_tiles]: splits of a row tile done (zero between calls)
+  __nv_bfloat16* out;
+  float* lse;
   int B, Qn, Hq, Hkv, S, G, max_splits, row_tiles;
   float scale, cap;
   int window_left, window_right, num_sinks, sink_per_head;
@@ -127,8 +131,8 @@ struct MqRange {
   int n_split;
 };
 
-// Key range of row tile rt of batch row b.  Shared by the split and the combine kernel so
-// that both agree on the number of splits.
+// Key range of row tile rt of batch row b: every CTA of the tile derives the same number
+// of splits from it (the last one to finish combines).
 __device__ __forceinline__ MqRange mq_tile_range(const MqParams& p, int b, int rt) {
   MqRange R;
   R.start = max(p.seq_start[b], 0);
@@ -169,7 +173,20 @@ ragged_mq_split_kernel(const MqParams p) {
   const int g = lane >> 2, c = lane & 3;
 
   const MqRange R = mq_tile_range(p, b, rt);
-  if (s >= R.n_split) return;  // the combine kernel writes 0 / -inf for empty rows
+  if (R.n_split == 0) {
+    // no attendable key for any row of the tile: output 0 and LSE -inf, once
+    if (s == 0) {
+      const int nr = p.Qn * p.G, tile_rows = min(16, nr - rt * 16);
+      for (int r = 0; r < tile_rows; ++r) {
+        const int rr = rt * 16 + r;
+        const long long orow = ((long long)b * p.Qn + rr / p.G) * p.Hq + h * p.G + rr % p.G;
+        p.out[orow * kD + threadIdx.x] = __float2bfloat16_rn(0.f);
+        if (p.lse != nullptr && threadIdx.x == 0) p.lse[orow] = -INFINITY;
+      }
+    }
+    return;
+  }
+  if (s >= R.n_split) return;
   const bool do_sinks = (s == 0) && (warp == 0) && R.sink_tile;
   const int key_lo = R.lo + s * kKeysPerCta + warp * kKeysPerWarp;
   const int key_hi = min(key_lo + kKeysPerWarp, R.hi);
@@ -472,31 +489,92 @@ ragged_mq_split_kernel(const MqParams p) {
       p.ml_part[slot * 2 + 1] = L;
     }
   }
-}
-
-__global__ void __launch_bounds__(kD)
-ragged_mq_combine_kernel(const MqParams p, __nv_bfloat16* __restrict__ out,
-                         float* __restrict__ lse) {
-  const int hq = blockIdx.x, qi = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
-  const int rr = qi * p.G + hq % p.G;
-  const MqRange R = mq_tile_range(p, b, rr / 16);
-  const long long base = ((long long)b * p.max_splits * p.Qn + qi) * p.Hq + hq;
-  const long long split_stride = (long long)p.Qn * p.Hq;
-  float M = -INFINITY;
-  for (int s = 0; s < R.n_split; ++s) M = fmaxf(M, p.ml_part[(base + s * split_stride) * 2]);
-  float L = 0.f, O = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < R.n_split; ++s) {
-      const long long slot = base + s * split_stride;
-      const float ms = p.ml_part[slot * 2];
-      const float f = ms == -INFINITY ? 0.f : ptx::ex2((ms - M) * kLog2e);
-      L += f * p.ml_part[slot * 2 + 1];
-      O += f * p.o_part[slot * kD + d];
-    }
+  // Combine: the CTA that finishes a row tile's last split merges the tile's partials
+  // (max / exp weights over the splits) and writes the bf16 output and the LSE.  Each
+  // thread's partial stores are made visible before the count (fence, barrier, atomic);
+  // the last CTA fences again before it reads the others' partials.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int* cnt = p.tile_count + ((long long)b * p.Hkv + h) * p.row_tiles + rt;
+    const int done = atomicAdd(cnt, 1) + 1;
+    s_last = done == R.n_split;
+    if (s_last) *cnt = 0;  // every split has counted: ready for the next call
   }
-  const long long orow = ((long long)b * p.Qn + qi) * p.Hq + hq;
-  out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
-  if (lse != nullptr && d == 0) lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // weights of each (row, split): (m, l) of all splits into shared memory, then one
+  // thread per row; then every thread sums its head-dim column over rows and splits
+  const long long split_stride = (long long)p.Qn * p.Hq;
+  // shared memory after the merge buffers holds 16 rows x kComboSplits splits of weights
+  constexpr int kComboFloats = (kSmemBytes / 4) - (kWarps * 16 * kD + kWarps * 16 * 2 + 16 * kWarps + 32);
+  constexpr int kComboSplits = (kComboFloats - 32) / (16 * 3);
+  if (R.n_split > kComboSplits) {
+    // very long rows: one (row, split) at a time
+    for (int r = 0; r < tile_rows; ++r) {
+      const int rr = rt * 16 + r;
+      const int qi = rr / p.G, hq = h * p.G + rr % p.G;
+      const long long base = ((long long)b * p.max_splits * p.Qn + qi) * p.Hq + hq;
+      float M = -INFINITY;
+      for (int sp = 0; sp < R.n_split; ++sp) M = fmaxf(M, __ldcg(&p.ml_part[(base + sp * split_stride) * 2]));
+      float L = 0.f, O = 0.f;
+      if (M != -INFINITY) {
+        for (int sp = 0; sp < R.n_split; ++sp) {
+          const long long slot = base + sp * split_stride;
+          const float ms = __ldcg(&p.ml_part[slot * 2]);
+          const float f = ms == -INFINITY ? 0.f : ptx::ex2((ms - M) * kLog2e);
+          L += f * __ldcg(&p.ml_part[slot * 2 + 1]);
+          O += f * __ldcg(&p.o_part[slot * kD + d]);
+        }
+      }
+      const long long orow = ((long long)b * p.Qn + qi) * p.Hq + hq;
+      p.out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+      if (p.lse != nullptr && d == 0) p.lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
+    }
+    return;
+  }
+  float* c_ml = s_l + 16;                       // [16][kComboSplits][2]
+  float* c_w = c_ml + 16 * kComboSplits * 2;    // [16][kComboSplits] weights
+  float* c_ml_row = c_w + 16 * kComboSplits;    // [16][2] merged max and sum
+  for (int i = threadIdx.x; i < tile_rows * R.n_split; i += blockDim.x) {
+    const int r = i / R.n_split, sp = i - r * R.n_split;
+    const int rr = rt * 16 + r;
+    const long long slot = ((long long)b * p.max_splits * p.Qn + rr / p.G) * p.Hq + h * p.G + rr % p.G +
+                           sp * split_stride;
+    c_ml[(r * kComboSplits + sp) * 2] = __ldcg(&p.ml_part[slot * 2]);
+    c_ml[(r * kComboSplits + sp) * 2 + 1] = __ldcg(&p.ml_part[slot * 2 + 1]);
+  }
+  __syncthreads();
+  if (threadIdx.x < tile_rows) {
+    const int r = threadIdx.x;
+    float M = -INFINITY;
+    for (int sp = 0; sp < R.n_split; ++sp) M = fmaxf(M, c_ml[(r * kComboSplits + sp) * 2]);
+    float L = 0.f;
+    for (int sp = 0; sp < R.n_split; ++sp) {
+      const float ms = c_ml[(r * kComboSplits + sp) * 2];
+      const float f = (M == -INFINITY || ms == -INFINITY) ? 0.f : ptx::ex2((ms - M) * kLog2e);
+      c_w[r * kComboSplits + sp] = f;
+      L += f * c_ml[(r * kComboSplits + sp) * 2 + 1];
+    }
+    c_ml_row[r * 2] = M;
+    c_ml_row[r * 2 + 1] = L;
+  }
+  __syncthreads();
+#pragma unroll 4
+  for (int r = 0; r < tile_rows; ++r) {
+    const int rr = rt * 16 + r;
+    const int qi = rr / p.G, hq = h * p.G + rr % p.G;
+    const long long base = ((long long)b * p.max_splits * p.Qn + qi) * p.Hq + hq;
+    float O = 0.f;
+    for (int sp = 0; sp < R.n_split; ++sp)
+      O = fmaf(c_w[r * kComboSplits + sp], __ldcg(&p.o_part[(base + sp * split_stride) * kD + d]), O);
+    const float M = c_ml_row[r * 2], L = c_ml_row[r * 2 + 1];
+    const long long orow = ((long long)b * p.Qn + qi) * p.Hq + hq;
+    p.out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? O / L : 0.f);
+    if (p.lse != nullptr && d == 0) p.lse[orow] = L > 0.f ? M + logf(L) : -INFINITY;
+  }
 }
 
 }  // namespace
@@ -521,10 +599,20 @@ static int mq_max_splits(int Qn, int S, int window_left, int window_right) {
   return static_cast<int>(std::max<long long>(1, (win + kKeysPerCta - 1) / kKeysPerCta));
 }
 
+// Workspace: fp32 partials o [B][splits][Q][Hq][D] and (m, l) [..][2], then the row
+// tiles' split counters [B][Hkv][row_tiles], cleared on the stream before each launch.
+static size_t mq_partials_bytes(int B, int Qn, int Hq, int S, int window_left, int window_right) {
+  const size_t splits = mq_max_splits(Qn, S, window_left, window_right);
+  return ((size_t)B * splits * Qn * Hq * (kD + 2) * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+static size_t mq_counter_bytes(int B, int Qn, int Hq) {
+  // Hkv * ceil(Q * G / 16) <= Q * Hq / 16 + Hkv <= ceil(Q * Hq / 16) + Hq
+  return (size_t)B * (((size_t)Qn * Hq + 15) / 16 + Hq) * sizeof(int);
+}
+
 size_t ragged_mq_workspace_bytes(int B, int Qn, int Hq, int S, int window_left,
                                  int window_right) {
-  const size_t splits = mq_max_splits(Qn, S, window_left, window_right);
-  return (size_t)B * splits * Qn * Hq * (kD + 2) * sizeof(float);
+  return mq_partials_bytes(B, Qn, Hq, S, window_left, window_right) + mq_counter_bytes(B, Qn, Hq);
 }
 
 int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t* seq_start,
@@ -552,6 +640,10 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
                      "ragged attention: B * ceil(Q * Hq / Hkv / 16), Hkv and Q must be <= 65535");
   p.o_part = static_cast<float*>(workspace);
   p.ml_part = p.o_part + (size_t)B * p.max_splits * Qn * Hq * kD;
+  p.tile_count = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) +
+                                        mq_partials_bytes(B, Qn, Hq, S, window_left, window_right));
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
   p.scale = scale;
   p.cap = cap > 0.f ? cap : 0.f;
   p.window_left = window_left;
@@ -568,17 +660,15 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
     if (e != cudaSuccess) return cuda_error(e, "ragged attention: set smem attribute");
     attr_done = true;
   }
+  cudaError_t e = cudaMemsetAsync(p.tile_count, 0, (size_t)B * Hkv * p.row_tiles * sizeof(int), stream);
+  if (e != cudaSuccess) return cuda_error(e, "ragged attention: clear split counters");
   dim3 grid(p.max_splits, Hkv, B * p.row_tiles);
   const bool hi_rows = Qn * p.G > 8, capped = p.cap > 0.f;
   auto kernel = hi_rows ? (capped ? ragged_mq_split_kernel<true, true> : ragged_mq_split_kernel<true, false>)
                         : (capped ? ragged_mq_split_kernel<false, true> : ragged_mq_split_kernel<false, false>);
   kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "ragged attention split launch");
-  ragged_mq_combine_kernel<<<dim3(Hq, Qn, B), kD, 0, stream>>>(
-      p, static_cast<__nv_bfloat16*>(out), lse);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_error(e, "ragged attention combine launch");
+  if (e != cudaSuccess) return cuda_error(e, "ragged attention split launch");
   return SBA_OK;
 }
 
@@ -664,8 +754,9 @@ extern "C" SBA_API int sba_ragged_decode_fwd_noalloc(
   void* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);
   if (rc != SBA_OK) return rc;
-  // The partials need no initialisation: every slot the combine kernel reads is written
-  // by the split kernel of the same call.
+  // The partials need no initialisation: every slot the combining CTA reads is written
+  // by the same call, and the call clears the split counters itself (a memset on the
+  // stream, no allocation).
   return sba_ragged_decode_fwd(q, k, v, seq_start, seq_end, B, Hq, Hkv, S, D, softmax_scale,
                                window_left, window_right, logits_soft_cap, sink_bias, num_sinks,
                                sink_bias_per_head, out, lse, scratch, kNoAllocScratchBytes, stream);

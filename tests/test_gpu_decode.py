@@ -85,3 +85,13 @@ def test_workspace_contract(sba):
     small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
     with pytest.raises(sba.SBAError):
         sba.ragged_decode_fwd(w.q, w.k, w.v, w.sequence_start, w.sequence_end, workspace=small)
+
+
+def test_long_rows_beyond_the_parallel_combine(sba):
+    """No window over a 200,000-key cache: 196 splits of 1,024 keys per row, more than
+    the combining CTA stages in shared memory, so it merges them one at a time; a short
+    row in the same launch uses the staged path."""
+    ends = [200_000, 3_000]
+    w = workloads.decode(device=DEV, B=2, Hq=8, Hkv=2, S=200_000, window=(-1, -1), cap=0.0,
+                         num_sinks=2, ends=ends, seed=403)
+    assert_attention_close(*_run(sba, w), what="decode long rows")
