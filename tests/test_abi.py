@@ -149,7 +149,8 @@ def test_workspace_size_grows_with_window():
 
 
 def test_multi_query_workspace_arithmetic():
-    """Split count of the multi-query workspace (1024 keys per split): a 16-row tile
+    """Split count of the multi-query workspace (1024 keys per split) and its split
+    counters: a 16-row tile
     spans queries i_lo..i_hi (at most 16), so its key range is at most
     left + min(Q, right + 16) keys with both window bounds, left + Q with only a left
     bound, S without one; Q = 1 gives the decode workspace."""
@@ -160,18 +161,24 @@ def test_multi_query_workspace_arithmetic():
     except RuntimeError:
         pytest.skip("library not built")
     ws = lib.sba_ragged_flash_attention_workspace_size
-    row = 4 * 32 * (128 + 2) * 4      # Q * Hq * (D + 2) fp32 per row and split
-    assert ws(64, 4, 32, 32768, 128, 4096, 0) == 64 * 5 * row     # 4100 keys
-    assert ws(64, 4, 32, 32768, 128, 4096, -1) == 64 * 5 * row
-    assert ws(64, 4, 32, 32768, 128, -1, 0) == 64 * 32 * row
-    assert ws(64, 4, 32, 32768, 128, 1020, 0) == 64 * 1 * row     # 1024 keys
-    assert ws(64, 4, 32, 32768, 128, 1021, 0) == 64 * 2 * row     # 1025 keys
-    row64 = 64 * 32 * (128 + 2) * 4
-    assert ws(2, 64, 32, 32768, 128, 1000, 8) == 2 * 1 * row64  # 1000 + 24 keys
-    assert ws(2, 64, 32, 32768, 128, 1000, -1) == 2 * 2 * row64  # 1000 + 64 keys
-    assert ws(2, 64, 32, 32768, 128, 1000, 40) == 2 * 2 * row64  # 1000 + 56 keys
-    assert ws(2, 64, 32, 32768, 128, 1000, 60) == 2 * 2 * row64  # 1000 + 64 keys
-    assert ws(2, 64, 32, 1000, 128, -1, 60) == 2 * 1 * row64     # S = 1000
+
+    def expect(B, Q, Hq, splits):
+        # fp32 partials (D + 2 per row, split, query, head) rounded up to 256 bytes, then
+        # one int counter per (batch row, KV head, 16-row tile): at most
+        # ceil(Q * Hq / 16) + Hq per batch row whatever Hkv is
+        partials = B * splits * Q * Hq * (128 + 2) * 4
+        return (partials + 255) // 256 * 256 + B * ((Q * Hq + 15) // 16 + Hq) * 4
+
+    assert ws(64, 4, 32, 32768, 128, 4096, 0) == expect(64, 4, 32, 5)     # 4100 keys
+    assert ws(64, 4, 32, 32768, 128, 4096, -1) == expect(64, 4, 32, 5)
+    assert ws(64, 4, 32, 32768, 128, -1, 0) == expect(64, 4, 32, 32)
+    assert ws(64, 4, 32, 32768, 128, 1020, 0) == expect(64, 4, 32, 1)     # 1024 keys
+    assert ws(64, 4, 32, 32768, 128, 1021, 0) == expect(64, 4, 32, 2)     # 1025 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 8) == expect(2, 64, 32, 1)     # 1000 + 24 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, -1) == expect(2, 64, 32, 2)    # 1000 + 64 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 40) == expect(2, 64, 32, 2)    # 1000 + 56 keys
+    assert ws(2, 64, 32, 32768, 128, 1000, 60) == expect(2, 64, 32, 2)    # 1000 + 64 keys
+    assert ws(2, 64, 32, 1000, 128, -1, 60) == expect(2, 64, 32, 1)       # S = 1000
     for wl in (-1, 0, 4096, 5000):
         assert ws(64, 1, 32, 32768, 128, wl, 7) == lib.sba_ragged_decode_workspace_size(64, 32, 32768, 128, wl)
 
