@@ -21,6 +21,10 @@ taken over exactly those keys.  Readings of points the page leaves open:
 * default ``softmax_scale`` is ``1 / sqrt(D)``;
 * the log-sum-exp is natural-log; a row with no admissible key has output 0 and
   LSE ``-inf``.
+
+The optional ``g_slc`` gate is a reading, parity unpinned: the page lists the
+argument in the operation's signature but never states its effect, so nothing on
+the pages can check the per-row multiplier used here (its test only restates it).
 """
 
 from __future__ import annotations

@@ -214,8 +214,10 @@ def test_gqa_equals_repeated_heads():
 
 
 def test_selection_gate_scales_rows_and_leaves_lse():
-    """g_slc gates each (token, query head) output row of the selection branch; rows
-    with no admissible key stay 0 and the LSE is the ungated attention's."""
+    """The g_slc reading (parity unpinned: the pages give the gate's signature, not its
+    effect): each (token, query head) output row is multiplied by its gate; rows with
+    no admissible key stay 0 and the LSE is the ungated attention's.  This restates the
+    reading; it does not pin it against the pages."""
     rng = np.random.default_rng(12)
     B, T, Hq, Hkv, D, bs = 1, 40, 4, 2, 8, 8
     q = rng.standard_normal((B, T, Hq, D))
