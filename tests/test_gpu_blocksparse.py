@@ -112,3 +112,26 @@ def test_first_item_of_every_cta(sba):
     assert_attention_close(got, ref, gl, rl, what="first items")
     got2, _, gl2, _ = _run(sba, w)
     assert np.array_equal(got, got2) and np.array_equal(gl, gl2), "second launch differs"
+
+
+@pytest.mark.parametrize("kv_block", [128, 64])
+def test_unsorted_segments_and_positions(sba, kv_block):
+    """Key blocks whose positions are not consecutive or whose segment ids are not
+    sorted take the per-key mask test; the others the per-row column interval.  Mixed
+    here: random segment ids in half the rows' span, positions swapped inside a few
+    blocks, padding tokens scattered."""
+    w = workloads.blocksparse(device=DEV, B=2, T=1024, Hq=4, Hkv=2, D=128, mean_doc=400,
+                              pad_tail=20, window=(-1, -1), seed=880 + kv_block)
+    rng = np.random.default_rng(kv_block)
+    seg = w.mask.q_segment_ids.cpu().numpy().copy()
+    pos = w.mask.q_positions.cpu().numpy().copy()
+    seg[:, 512:] = rng.integers(0, 3, size=(2, 512))
+    seg[rng.random(seg.shape) < 0.03] = -1
+    for blk in (1, 3, 6):
+        a, b = blk * 128 + 5, blk * 128 + 70
+        pos[:, [a, b]] = pos[:, [b, a]]
+    to = lambda a: torch.from_numpy(a.astype(np.int32)).to(DEV)
+    w.mask.q_segment_ids, w.mask.kv_segment_ids = to(seg), to(seg)
+    w.mask.q_positions, w.mask.kv_positions = to(pos), to(pos)
+    w.mask.causal = True
+    assert_attention_close(*_run(sba, w, kv_block=kv_block), what=f"unsorted kb={kv_block}")
