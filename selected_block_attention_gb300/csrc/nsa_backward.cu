@@ -85,6 +85,7 @@ struct Params {
   int* slot_off;
   int* slot_cur;
   int* slot_tok;
+  int* kv_next;                 // next dK/dV work item (zeroed by the scan kernel)
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -239,6 +240,7 @@ __global__ void __launch_bounds__(1024) nsa_bwd_scan_kernel(const Params p) {
       p.slot_off[i] = before;
       p.slot_cur[i] = 0;
     }
+    if (c0 == 0 && tid == 0) *p.kv_next = 0;
     __syncthreads();
     if (tid == 0) carry += warp_sums[31];
     __syncthreads();
@@ -716,7 +718,7 @@ struct KvCfg {
   static constexpr int kOffP = kOffQ + 4 * kQBytes;
   static constexpr int kOffDs = kOffP + kPBytes;
   static constexpr int kOffBars = kOffDs + kPBytes;
-  static constexpr int kNumBars = 2 + 4 + 2 + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 + 4 + 2 + 2 + 2 + 2 + 4;
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   // tensor memory: S, dP (64 fp32 each), dV^T, dK^T (lanes = head dim, 64 key columns)
@@ -758,12 +760,33 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   uint64_t* pds_empty = bb;  bb += 1;
   uint64_t* acc_full = bb;   bb += 1;
   uint64_t* acc_empty = bb;  bb += 1;
-  uint64_t* mma_done = bb;   // [2]: per issuing thread
+  uint64_t* mma_done = bb;   bb += 2;   // per issuing thread
+  uint64_t* item_full = bb;  bb += 2;   // work item published in slot i
+  uint64_t* item_empty = bb;            // [2]: slot i read by every consumer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  volatile int* slot_item = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);  // [2]
   const Abort ab{abort_flag, &g_err_nsab, 4u, p.wait_limit};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = p.n_slots;
+  // Work items are handed out dynamically (a global counter, in item order): the CTAs
+  // then work on neighbouring items, i.e. on one (KV head, batch row) group at a time,
+  // whose Q / dO rows stay in L2 across the groups' token lists.  The loader fetches an
+  // item and publishes it in a two-slot ring that the MMA threads and the softmax warps
+  // read (-1: no more items).
+  auto take_item = [&](int& islot, uint32_t& iph, unsigned role) -> int {
+    const bool ok = role == kRoleSoftmax ? warp_wait(&item_full[islot], iph, ab, role, kBarItemFull, -1)
+                                         : bounded_wait(&item_full[islot], iph, ab, role, kBarItemFull, -1);
+    int item = ok ? slot_item[islot] : -1;
+    if (role == kRoleSoftmax) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
+    } else {
+      mbar_arrive(&item_empty[islot]);
+    }
+    if (++islot == 2) { islot = 0; iph ^= 1; }
+    return item;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1); mbar_init(kv_empty, 1);
@@ -772,6 +795,8 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(pds_full, 4); mbar_init(pds_empty, 1);
     mbar_init(acc_full, 1); mbar_init(acc_empty, 4);
     mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1);
+    // an item slot is read by the two MMA threads and the four softmax warps
+    for (int i = 0; i < 2; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 6); }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -791,13 +816,26 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 
   if (warp == 0) {
     // ------------------------------------------------------------------ loader
+    int pslot = 0; uint32_t pph = 0;
     uint32_t kvph = 0;
     uint32_t qph[2] = {0u, 0u};
     int qb = 0;
     bool kv_issued = false; uint32_t kv_last = 0;
     bool q_issued[2] = {false, false}; uint32_t q_last[2] = {0u, 0u};
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    while (ok) {
+      // fetch the next item and publish it
+      if (!warp_wait(&item_empty[pslot], pph ^ 1, ab, kRoleLoader, kBarItemEmpty, -1)) break;
+      int item = 0;
+      if (lane == 0) {
+        item = atomicAdd(p.kv_next, 1);
+        if (item >= n_items) item = -1;
+        slot_item[pslot] = item;
+        mbar_arrive(&item_full[pslot]);
+      }
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (++pslot == 2) { pslot = 0; pph ^= 1; }
+      if (item < 0) break;
       int b, hkv, sidx, slot, row0 = 0, nkeys = 0;
       kv_item(p, item, b, hkv, sidx, slot);
       if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
@@ -861,7 +899,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       const uint64_t qmn_desc = make_sdesc(smem_base + C::kOffQ, C::kQPanel, 1024, kLayoutSW128);
       const uint64_t p_desc = make_sdesc(smem_base + C::kOffP, C::kPBytes, 1024, kLayoutSW128);
       const uint64_t ds_desc = make_sdesc(smem_base + C::kOffDs, C::kPBytes, 1024, kLayoutSW128);
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      int islot = 0; uint32_t iph = 0;
+      while (ok) {
+        const int item = take_item(islot, iph, kRoleMma);
+        if (item < 0) break;
         int b, hkv, sidx, slot, row0 = 0, nkeys = 0;
         kv_item(p, item, b, hkv, sidx, slot);
         if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
@@ -937,7 +978,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint32_t sdph = 0, pdph = 0, accph = 0;
     uint8_t* prow = smem + C::kOffP + r * 128;
     uint8_t* dsrow = smem + C::kOffDs + r * 128;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    int islot = 0; uint32_t iph = 0;
+    while (true) {
+      const int item = take_item(islot, iph, kRoleSoftmax);
+      if (item < 0) break;
       int b, hkv, sidx, slot, row0 = 0, nkeys = 0;
       kv_item(p, item, b, hkv, sidx, slot);
       if (!decode_slot(p, b, sidx, row0, nkeys)) continue;
@@ -1022,7 +1066,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }
 
 struct BwdLayout {
-  size_t delta, cnt, off, cur, tok, total;
+  size_t delta, cnt, off, cur, tok, next, total;
 };
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 BwdLayout bwd_layout(int B, int T, int Hq, int Hkv, int S, int num_seqs) {
@@ -1035,6 +1079,7 @@ BwdLayout bwd_layout(int B, int T, int Hq, int Hkv, int S, int num_seqs) {
   L.off = o;   o += round256(n_slots * 4);
   L.cur = o;   o += round256(n_slots * 4);
   L.tok = o;   o += round256(static_cast<size_t>(B) * T * Hkv * std::min(S, kMaxSel) * 4);
+  L.next = o;  o += 256;
   L.total = o;
   return L;
 }
@@ -1092,6 +1137,7 @@ int launch_nsa_select_bwd(const void* q, const void* k, const void* v, const voi
   p.slot_off = reinterpret_cast<int*>(ws + L.off);
   p.slot_cur = reinterpret_cast<int*>(ws + L.cur);
   p.slot_tok = reinterpret_cast<int*>(ws + L.tok);
+  p.kv_next = reinterpret_cast<int*>(ws + L.next);
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
