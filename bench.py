@@ -2,8 +2,8 @@
 
 Headline (``value``): NSA selection forward TFLOP/s on the B=2, T=8192, Hq=64,
 Hkv=4, D=128, block 64 causal prefill (bf16), inputs resident in HBM, L2 flushed
-between steps (a 256 MB buffer is rewritten before each timed step, outside the
-step's events).  FLOPs are algorithmic: 4 * D * (number of admissible keys) per
+between steps (a 256 MB buffer is rewritten and another 256 MB read before each
+timed step, outside the step's events, so the step starts with a clean L2).  FLOPs are algorithmic: 4 * D * (number of admissible keys) per
 (token, query head), i.e. the work the selection defines, not padded tiles.
 
 The same JSON line carries ``roofline`` (dominant kernel vs the measured peak),
@@ -270,17 +270,40 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(sel)}
 
 
-def timed_steps(fn, steps, warmup, flush_buf, stream):
+HOLD_CYCLES = 400_000  # ~0.2 ms of GPU spin ahead of each timed step
+
+
+class L2Flush:
+    """Between timed steps: rewrite a buffer larger than L2 (evicts every input line),
+    then read a second one, so the rewritten lines are written back to HBM before the
+    step starts: the step begins with a clean L2 that holds none of its inputs (no
+    write-back of someone else's dirty lines inside the timed region)."""
+
+    def __init__(self, dev):
+        self.w = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.add_(1)
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
+def timed_steps(fn, steps, warmup, flush, stream):
     """Per-step device time (ms) with CUDA events on ``stream``; the L2 flush runs
-    before every step, outside its events."""
+    before every step, outside its events.  A short GPU spin ahead of the flush keeps
+    the device busy while the host enqueues the step, so the events bracket the step's
+    own GPU work and not the host's argument marshalling (host cost is what the
+    end-to-end figure measures)."""
     for _ in range(warmup):
-        flush_buf.add_(1)
+        flush()
         fn()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     for i in range(steps):
-        flush_buf.add_(1)
+        torch.cuda._sleep(HOLD_CYCLES)
+        flush()
         starts[i].record(stream)
         fn()
         ends[i].record(stream)
@@ -388,7 +411,7 @@ def run_cuda(args, rank, world, local_rank):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     peaks, peak_src = load_peaks()
-    flush = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     w = workloads.nsa_prefill(device=dev)
     flops, hbm_bytes, gather_bytes, groups = nsa_work(w)
@@ -470,7 +493,7 @@ def run_cuda(args, rank, world, local_rank):
             "workload": "nsa_select_prefill B=2 T=8192 Hq=64 Hkv=4 D=128 block_size=64 causal, "
                         "counts U{1..16} clipped, own block + distinct uniform earlier blocks",
             "tokens": w.q.shape[0] * w.q.shape[1], "token_groups": groups,
-            "flop_per_step": flops, "l2": "256 MB buffer rewritten before every timed step",
+            "flop_per_step": flops, "l2": "flushed before every timed step: a 256 MB buffer rewritten, then another 256 MB read (clean L2, no input resident)",
             "parallelism": f"replicas x{world}"},
         "roofline": {
             "bound": "tensor",
@@ -577,7 +600,7 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
         "frac_tensor": round(bflops / ms / 1e9 / peaks["bf16_tflops"], 4),
         "executed_mma_tflops": round(exec_fl / ms / 1e9, 1),
         "executed_mma_frac": round(exec_fl / ms / 1e9 / peaks["bf16_tflops"], 4),
-        "hbm_bytes": int(bhbm), "kernels_per_call": 5,
+        "hbm_bytes": int(bhbm), "kernels_per_call": 5, "memsets_per_call": 1,
         "flop_per_call": bflops, "token_list_chunks": sel["chunks"]}
     del w, out, lse, do, dq, dk, dv, bws
     torch.cuda.empty_cache()
@@ -684,7 +707,7 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
     rows["ragged_decode"] = {
         "workload": w.name, "us": round(ms * 1e3, 2), "tok/s": round(w.q.shape[0] / (ms * 1e-3), 1),
         "GB/s": round(nbytes / ms / 1e6, 1), "frac_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
-        "kernels_per_call": 2}
+        "kernels_per_call": 1, "memsets_per_call": 1}
     del w
     torch.cuda.empty_cache()
 
@@ -712,7 +735,7 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
             "frac_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
             "TFLOP/s": round(mfl / ms / 1e9, 2),
             "frac_tensor": round(mfl / ms / 1e9 / peaks["bf16_tflops"], 4),
-            "kernels_per_call": 2}
+            "kernels_per_call": 1, "memsets_per_call": 1 if w.q.shape[1] < 128 else 0}
         del w, ws, out
         torch.cuda.empty_cache()
     sba.check_error(dev)

@@ -55,6 +55,7 @@ constexpr int kBS = 64;                     // selection block = key tile
 constexpr int kRows = 128;                  // MMA M: NT tokens x G query heads
 constexpr int kMaxNT = 16;
 constexpr int kMaxSel = 32;
+constexpr int kMaxG = 16;                   // query heads per KV head
 constexpr int kMaxUnion = kMaxNT * kMaxSel;
 constexpr int kThreads = 256;               // dK/dV: warps 0-3 loader, 2 MMA, spare; 4-7 softmax
 constexpr int kDqThreads = 384;             // dQ: warps 0-3 loader, MMA, builder, spare; 4-11 softmax
@@ -158,23 +159,41 @@ __global__ void __launch_bounds__(256) nsa_bwd_prep_kernel(const Params p) {
        w += warps) {
     const int tok = static_cast<int>(w / p.Hkv), hkv = static_cast<int>(w - (long long)tok * p.Hkv);
     if (!kFill) {
-      // Delta[tok, hq] = <dO, O> in fp32, one head per iteration, 4 elements per lane
-      for (int h = 0; h < p.G; ++h) {
-        const long long base = ((long long)tok * p.Hq + hkv * p.G + h) * kD + lane * 4;
-        const uint2 ov = *reinterpret_cast<const uint2*>(p.out + base);
-        const uint2 dv = *reinterpret_cast<const uint2*>(p.dout + base);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-        float acc = 0.f;
+      // Delta[tok, hq] = <dO, O> in fp32.  The G heads of one KV head are contiguous
+      // (G x 128 bf16): each lane loads 16 B per step, so one step covers two heads
+      // (lanes 0-15 head 2i, lanes 16-31 head 2i+1); all loads are issued before the
+      // half-warp reductions.
+      const long long base = ((long long)tok * p.Hq + hkv * p.G) * kD;
+      const uint4* o4 = reinterpret_cast<const uint4*>(p.out + base) + lane;
+      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + base) + lane;
+      const int steps = p.G >> 1;
+      uint4 ov[kMaxG / 2], dv[kMaxG / 2];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const float2 a = __bfloat1622float2(o2[u]), c = __bfloat1622float2(d2[u]);
-          acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
+      for (int i = 0; i < kMaxG / 2; ++i) {
+        if (i < steps) {
+          ov[i] = o4[i * 32];
+          dv[i] = d4[i * 32];
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) p.delta[(long long)tok * p.Hq + hkv * p.G + h] = acc;
       }
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxG / 2; ++i) {
+        if (i < steps) {
+          const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov[i]);
+          const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv[i]);
+          float acc = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 a = __bfloat1622float2(o2[u]), c = __bfloat1622float2(d2[u]);
+            acc = fmaf(a.x, c.x, fmaf(a.y, c.y, acc));
+          }
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+          if ((lane & 15) == i) mine = acc;
+        }
+      }
+      if ((lane & 15) < steps)
+        p.delta[(long long)tok * p.Hq + hkv * p.G + 2 * (lane & 15) + (lane >> 4)] = mine;
     }
     const int b = p.cu_seqlens ? 0 : tok / p.T;
     const int t = p.cu_seqlens ? tok : tok - b * p.T;
