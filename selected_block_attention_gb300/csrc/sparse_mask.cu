@@ -9,10 +9,12 @@
 //   1. every block of the row is summarised exactly once (min/max of positions and of
 //      remapped segment ids, coalesced 16-byte loads, several blocks in flight per
 //      warp, warp min/max reductions): CTA r of the cluster takes the r-th slice of the
-//      inner blocks and of the outer blocks;
-//   2. after a cluster barrier each CTA copies the whole row of inner summaries out of
-//      its peers' shared memory (distributed shared memory) and builds prefix maxima /
-//      suffix minima of the summary fields the attend test compares;
+//      inner blocks, arrives on the cluster barrier, then takes the r-th slice of the
+//      outer blocks (so waiting for the slowest peer overlaps its own reads);
+//   2. after the cluster barrier each CTA copies the whole row of inner summaries out of
+//      its peers' shared memory (distributed shared memory) and, in the same pass,
+//      builds prefix maxima / suffix minima of the summary fields the attend test
+//      compares;
 //   3. per outer block (one lane each, so the searches of 32 outer blocks run side by
 //      side) those monotone arrays give, by binary search, a candidate range of inner
 //      blocks outside of which the attend test provably fails (e.g. under causal
@@ -293,66 +295,98 @@ __device__ __forceinline__ void summarize_slice(const int* pos, const int* seg, 
   }
 }
 
-// The six monotone arrays of one row from its inner summaries `v`, in one pass over the
-// CTA: out[0..2] = prefix maxima of pos_min, pos_max, seg_max (out[f][i] = max over
-// v[0..i]) and out[3..5] = suffix minima of pos_min, pos_max, seg_min (out[f][i] = min
-// over v[i..n-1]).  Thread t owns a contiguous chunk (from the left for the prefix
-// arrays, from the right for the suffix arrays); chunk totals are combined with warp
-// shuffles and one exchange of warp totals through `tmp` (6 * kCWarps ints), then each
-// thread rescans its chunk with that offset and writes it.  Ends with the CTA
+// Gathers the row's inner summaries out of the cluster's shared memory and builds the
+// six monotone arrays of the row in the same pass: out[0..2] = prefix maxima of
+// pos_min, pos_max, seg_max (out[f][i] = max over v[0..i]) and out[3..5] = suffix minima
+// of pos_min, pos_max, seg_min (out[f][i] = min over v[i..n-1]).  Thread t owns the
+// contiguous chunk [t c, t c + c): it copies the chunk from its owners (block i lives
+// in CTA i / islice at own_inner[i % islice]) into `all`, folds it, and the chunk totals
+// are combined with warp shuffles (prefix: in thread order; suffix: in reverse thread
+// order) and one exchange of warp totals through `tmp` (6 * kCWarps ints); then each
+// thread rescans its chunk with its offset and writes it.  Ends with the CTA
 // synchronised.
-__device__ void cta_scans(const int4* v, int n, int* const (&out)[6], int* tmp) {
+__device__ void gather_scans(cg::cluster_group& cluster, int4* own_inner, int islice, int4* all,
+                             int n, int* const (&out)[6], int* tmp) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = (n + kCThreads - 1) / kCThreads;
-  const int plo = min(tid * chunk, n), phi = min(plo + chunk, n);       // prefix chunk
-  const int shi = max(n - tid * chunk, 0), slo = max(shi - chunk, 0);   // suffix chunk
+  const int lo = min(tid * chunk, n), hi = min(lo + chunk, n);
   int run[6] = {INT_MIN, INT_MIN, INT_MIN, INT_MAX, INT_MAX, INT_MAX};
-  for (int i = plo; i < phi; ++i) {
-    const int4 x = v[i];
-    run[0] = max(run[0], x.x); run[1] = max(run[1], x.y); run[2] = max(run[2], x.w);
+  for (int i0 = lo; i0 < hi; i0 += 4) {
+    int4 x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // remote loads first, so they are in flight together
+      if (i0 + u < hi) {
+        const int i = i0 + u;
+        x[u] = *cluster.map_shared_rank(own_inner + i % islice, i / islice);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (i0 + u < hi) {
+        all[i0 + u] = x[u];
+        run[0] = max(run[0], x[u].x); run[1] = max(run[1], x[u].y); run[2] = max(run[2], x[u].w);
+        run[3] = min(run[3], x[u].x); run[4] = min(run[4], x[u].y); run[5] = min(run[5], x[u].z);
+      }
+    }
   }
-  for (int i = slo; i < shi; ++i) {
-    const int4 x = v[i];
-    run[3] = min(run[3], x.x); run[4] = min(run[4], x.y); run[5] = min(run[5], x.z);
-  }
-  // inclusive scan of the chunk totals in thread order, within the warp
+  // inclusive scans of the chunk totals within the warp: prefix arrays towards higher
+  // lanes, suffix arrays towards lower lanes
   int incl[6];
 #pragma unroll
   for (int f = 0; f < 6; ++f) incl[f] = run[f];
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
 #pragma unroll
-    for (int f = 0; f < 6; ++f) {
+    for (int f = 0; f < 3; ++f) {
       const int o = __shfl_up_sync(0xffffffffu, incl[f], d);
-      if (lane >= d) incl[f] = f < 3 ? max(incl[f], o) : min(incl[f], o);
+      if (lane >= d) incl[f] = max(incl[f], o);
+    }
+#pragma unroll
+    for (int f = 3; f < 6; ++f) {
+      const int o = __shfl_down_sync(0xffffffffu, incl[f], d);
+      if (lane + d < 32) incl[f] = min(incl[f], o);
     }
   }
   if (lane == 31) {
 #pragma unroll
-    for (int f = 0; f < 6; ++f) tmp[f * kCWarps + warp] = incl[f];
+    for (int f = 0; f < 3; ++f) tmp[f * kCWarps + warp] = incl[f];
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int f = 3; f < 6; ++f) tmp[f * kCWarps + warp] = incl[f];
   }
   __syncthreads();
-  // exclusive offset of this thread: earlier warps' totals, then earlier lanes'
+  // exclusive offset of this thread: for the prefix arrays the totals of earlier warps
+  // and earlier lanes, for the suffix arrays those of later warps and later lanes
   int ex[6];
 #pragma unroll
   for (int f = 0; f < 6; ++f) {
-    int wt = lane < warp ? tmp[f * kCWarps + lane] : (f < 3 ? INT_MIN : INT_MAX);
+    const bool pre = f < 3;
+    int wt = pre ? (lane < warp ? tmp[f * kCWarps + lane] : INT_MIN)
+                 : (lane > warp && lane < kCWarps ? tmp[f * kCWarps + lane] : INT_MAX);
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) {
       const int o = __shfl_xor_sync(0xffffffffu, wt, d);
-      wt = f < 3 ? max(wt, o) : min(wt, o);
+      wt = pre ? max(wt, o) : min(wt, o);
     }
-    int e = __shfl_up_sync(0xffffffffu, incl[f], 1);
-    if (lane == 0) e = f < 3 ? INT_MIN : INT_MAX;
-    ex[f] = f < 3 ? max(e, wt) : min(e, wt);
+    int e;
+    if (pre) {
+      e = __shfl_up_sync(0xffffffffu, incl[f], 1);
+      if (lane == 0) e = INT_MIN;
+      ex[f] = max(e, wt);
+    } else {
+      e = __shfl_down_sync(0xffffffffu, incl[f], 1);
+      if (lane == 31) e = INT_MAX;
+      ex[f] = min(e, wt);
+    }
   }
-  for (int i = plo; i < phi; ++i) {
-    const int4 x = v[i];
+  for (int i = lo; i < hi; ++i) {
+    const int4 x = all[i];
     ex[0] = max(ex[0], x.x); ex[1] = max(ex[1], x.y); ex[2] = max(ex[2], x.w);
     out[0][i] = ex[0]; out[1][i] = ex[1]; out[2][i] = ex[2];
   }
-  for (int i = shi - 1; i >= slo; --i) {
-    const int4 x = v[i];
+  for (int i = hi - 1; i >= lo; --i) {
+    const int4 x = all[i];
     ex[3] = min(ex[3], x.x); ex[4] = min(ex[4], x.y); ex[5] = min(ex[5], x.z);
     out[3][i] = ex[3]; out[4][i] = ex[4]; out[5][i] = ex[5];
   }
@@ -396,28 +430,25 @@ sparse_mask_cluster_kernel(Side outer, Side inner, int causal, int window_left, 
   int* smn_pmax = smn_pmin + nbi;                               // suffix min of pos_max
   int* smn_smin = smn_pmax + nbi;                               // suffix min of seg_min
 
-  // 1. this CTA's slices of the row, each block summarised once
+  // 1. this CTA's slices of the row, each block summarised once: the inner slice, then
+  // (while the cluster's other CTAs finish theirs) the outer slice
   const int i0 = r * islice, ni = max(0, min(islice, nbi - i0));
   const int o0 = r * oslice, no = max(0, min(oslice, nbo - o0));
   summarize_slice(inner.pos + (long long)b * inner.T, inner.seg + (long long)b * inner.T, inner,
                   i0, ni, vec_inner != 0, pad_id, pad_remap, own_inner);
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   summarize_slice(outer.pos + (long long)b * outer.T, outer.seg + (long long)b * outer.T, outer,
                   o0, no, vec_outer != 0, pad_id, pad_remap, own_outer);
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 
-  // 2. the whole row of inner summaries from the cluster's shared memory
-  cluster.sync();
-  for (int i = threadIdx.x; i < nbi; i += kCThreads) {
-    const int4* peer = cluster.map_shared_rank(own_inner, i / islice);
-    all_inner[i] = peer[i % islice];
-  }
-  // This CTA's slice must stay in place until every peer has copied it: arrive now,
-  // wait at the very end of the kernel (the barrier's latency hides behind the work).
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  __syncthreads();
+  // 2. the whole row of inner summaries from the cluster's shared memory, scanned on the
+  // way in.  This CTA's slice must stay in place until every peer has copied it: arrive
+  // once the copies are done, wait at the very end of the kernel.
   {
     int* const arrays[6] = {pmx_pmin, pmx_pmax, pmx_smax, smn_pmin, smn_pmax, smn_smin};
-    cta_scans(all_inner, nbi, arrays, scan_tmp);
+    gather_scans(cluster, own_inner, islice, all_inner, nbi, arrays, scan_tmp);
   }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
   // 3. candidate ranges with one lane per outer block (the binary searches run in
   // parallel across lanes), then per outer block the exact predicates on its candidates
