@@ -450,91 +450,105 @@ sparse_mask_cluster_kernel(Side outer, Side inner, int causal, int window_left, 
   }
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 
-  // 3. candidate ranges with one lane per outer block (the binary searches run in
-  // parallel across lanes), then per outer block the exact predicates on its candidates
-  // with one inner block per lane.  Outer block jl goes to warp jl % kCWarps, lane
-  // (jl / kCWarps) % 32, so every warp gets work.
-  for (int g0 = 0; g0 < no; g0 += kCWarps * 32) {
-    const int jl = g0 + lane * kCWarps + warp;
+  // 3. candidate ranges with one lane pair per outer block (the binary searches run in
+  // parallel across lanes: the even lane finds the lower end, the odd lane the upper
+  // end), then per outer block the exact predicates on its candidates, split between
+  // the pair.  Outer block jl goes to warp jl % kCWarps, pair (jl / kCWarps) % 16, so
+  // every warp gets work.
+  const int pair = lane >> 1, half = lane & 1;
+  // the page's predicates on the candidates i_begin, i_begin + i_step, ... of one outer
+  // block, folded into the four bounds
+  auto eval_range = [&](const int4& ob, int i_begin, int i_end, int i_step, int& lo, int& up,
+                        int& lo_full, int& up_full) {
+    const long long o_min = ob.x, o_max = ob.y;
+    for (int i = i_begin; i < i_end; i += i_step) {
+      const int4 in = all_inner[i];
+      const bool attend_seg = (in.z <= ob.w) && (ob.z <= in.w);
+      const bool full_seg = (ob.z == ob.w) && (in.z == in.w);
+      bool attend_pos, full_pos;
+      position_tests<kQueryOuter>(causal != 0, window_left, window_right, o_min, o_max, in.x,
+                                  in.y, attend_pos, full_pos);
+      const bool attend = attend_pos && attend_seg && !(in.z == pad_remap);
+      const bool full = full_seg && full_pos && attend;
+      if (attend) { up = max(up, i + 1); lo = min(lo, i); }
+      if (full) { up_full = max(up_full, i + 1); lo_full = min(lo_full, i); }
+    }
+  };
+  // clipped as the fix-up does; `which` 0 stores lower / upper, 1 lower_full /
+  // upper_full, 2 all four
+  auto store = [&](long long out, bool all_pad, int lo, int up, int lo_full, int up_full, int which) {
+    if (all_pad) {  // query / key block made only of padding
+      lo = up = lo_full = up_full = 0;
+    } else {
+      lo = min(max(lo, 0), nbi);
+      up = min(max(up, 0), nbi);
+      lo = min(lo, up);
+      lo_full = max(min(max(lo_full, 0), nbi), lo);
+      up_full = min(max(min(max(up_full, 0), nbi), lo_full), up);
+    }
+    if (which != 1) { lower[out] = lo; upper[out] = up; }
+    if (which != 0) { lower_full[out] = lo_full; upper_full[out] = up_full; }
+  };
+  for (int g0 = 0; g0 < no; g0 += kCWarps * 16) {
+    const int jl = g0 + pair * kCWarps + warp;
+    const bool mine = jl < no;
     int4 o = make_int4(0, 0, 0, 0);
-    int clo = 0, cup = 0;
-    if (jl < no) {
+    int bound = 0;
+    if (mine) {
       o = own_outer[jl];
-      const long long o_min = o.x, o_max = o.y;
+      const long long o_max = o.y;
       // lower end: the first block from which every necessary "inner >= threshold"
       // condition can hold (prefix maxima: each condition, and so their conjunction, is
       // false then true along the row); upper end: the first block from which some
       // necessary "inner <= threshold" condition fails for it and every later block
       // (suffix minima: the disjunction is false then true as well)
       const bool wl_on = window_left >= 0, wr_on = window_right >= 0, causal_on = causal != 0;
-      const long long thr_l = o_min - window_left, thr_r = o_max + window_right;
+      const long long thr_l = (long long)o.x - window_left, thr_r = o_max + window_right;
       if (kQueryOuter) {
-        clo = first_true(nbi, [&](int i) {
-          return pmx_smax[i] >= o.z && (!wl_on || (long long)pmx_pmin[i] >= thr_l);
-        });
-        cup = first_true(nbi, [&](int i) {
-          return smn_smin[i] > o.w || (causal_on && (long long)smn_pmin[i] > o_max) ||
-                 (wr_on && (long long)smn_pmax[i] > thr_r);
-        });
+        if (half == 0)
+          bound = first_true(nbi, [&](int i) {
+            return pmx_smax[i] >= o.z && (!wl_on || (long long)pmx_pmin[i] >= thr_l);
+          });
+        else
+          bound = first_true(nbi, [&](int i) {
+            return smn_smin[i] > o.w || (causal_on && (long long)smn_pmin[i] > o_max) ||
+                   (wr_on && (long long)smn_pmax[i] > thr_r);
+          });
       } else {
-        clo = first_true(nbi, [&](int i) {
-          return pmx_smax[i] >= o.z && (!causal_on || (long long)pmx_pmax[i] >= o_min) &&
-                 (!wl_on || (long long)pmx_pmax[i] >= thr_l);
-        });
-        cup = first_true(nbi, [&](int i) {
-          return smn_smin[i] > o.w || (wr_on && (long long)smn_pmin[i] > thr_r);
-        });
+        if (half == 0)
+          bound = first_true(nbi, [&](int i) {
+            return pmx_smax[i] >= o.z && (!causal_on || (long long)pmx_pmax[i] >= o.x) &&
+                   (!wl_on || (long long)pmx_pmax[i] >= thr_l);
+          });
+        else
+          bound = first_true(nbi, [&](int i) {
+            return smn_smin[i] > o.w || (wr_on && (long long)smn_pmin[i] > thr_r);
+          });
       }
     }
-    // the page's predicates on the candidates of one outer block, folded into the
-    // four bounds (clipped as the fix-up does) and stored
-    auto eval_range = [&](const int4& ob, int i_begin, int i_end, int i_step, int& lo, int& up,
-                          int& lo_full, int& up_full) {
-      const long long o_min = ob.x, o_max = ob.y;
-      for (int i = i_begin; i < i_end; i += i_step) {
-        const int4 in = all_inner[i];
-        const bool attend_seg = (in.z <= ob.w) && (ob.z <= in.w);
-        const bool full_seg = (ob.z == ob.w) && (in.z == in.w);
-        bool attend_pos, full_pos;
-        position_tests<kQueryOuter>(causal != 0, window_left, window_right, o_min, o_max, in.x,
-                                    in.y, attend_pos, full_pos);
-        const bool attend = attend_pos && attend_seg && !(in.z == pad_remap);
-        const bool full = full_seg && full_pos && attend;
-        if (attend) { up = max(up, i + 1); lo = min(lo, i); }
-        if (full) { up_full = max(up_full, i + 1); lo_full = min(lo_full, i); }
-      }
-    };
-    auto store = [&](long long out, bool all_pad, int lo, int up, int lo_full, int up_full) {
-      if (all_pad) {  // query / key block made only of padding
-        lower[out] = 0; upper[out] = 0; lower_full[out] = 0; upper_full[out] = 0;
-        return;
-      }
-      lo = min(max(lo, 0), nbi);
-      up = min(max(up, 0), nbi);
-      lo = min(lo, up);
-      lo_full = max(min(max(lo_full, 0), nbi), lo);
-      up_full = min(max(min(max(up_full, 0), nbi), lo_full), up);
-      lower[out] = lo; upper[out] = up; lower_full[out] = lo_full; upper_full[out] = up_full;
-    };
-    const bool mine = jl < no;
+    const int other = __shfl_xor_sync(0xffffffffu, bound, 1);
+    const int clo = half ? other : bound, cup = half ? bound : other;
     const bool pad_blk = mine && (o.z == o.w) && (o.z == pad_remap);
     const int ncand = mine && !pad_blk ? max(cup - clo, 0) : 0;
     if (__reduce_max_sync(0xffffffffu, ncand) <= 64) {
-      // short ranges: each lane evaluates its own outer block
-      if (mine) {
-        int up = 0, lo = nbi, up_full = 0, lo_full = nbi;
-        if (!pad_blk) eval_range(o, clo, cup, 1, lo, up, lo_full, up_full);
-        store((long long)b * nbo + o0 + jl, pad_blk, lo, up, lo_full, up_full);
-      }
+      // short ranges: the pair evaluates its own outer block, alternate candidates each
+      int up = 0, lo = nbi, up_full = 0, lo_full = nbi;
+      if (mine && !pad_blk) eval_range(o, clo + half, cup, 2, lo, up, lo_full, up_full);
+      up = max(up, __shfl_xor_sync(0xffffffffu, up, 1));
+      lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, 1));
+      up_full = max(up_full, __shfl_xor_sync(0xffffffffu, up_full, 1));
+      lo_full = min(lo_full, __shfl_xor_sync(0xffffffffu, lo_full, 1));
+      if (mine) store((long long)b * nbo + o0 + jl, pad_blk, lo, up, lo_full, up_full, half);
       continue;
     }
     // long ranges: the warp evaluates one outer block at a time, one inner block per lane
-    for (int k = 0; k < 32; ++k) {
+    for (int k = 0; k < 16; ++k) {
       const int jk = g0 + k * kCWarps + warp;
       if (jk >= no) break;  // warp-uniform
-      const int4 ok4 = make_int4(__shfl_sync(0xffffffffu, o.x, k), __shfl_sync(0xffffffffu, o.y, k),
-                                 __shfl_sync(0xffffffffu, o.z, k), __shfl_sync(0xffffffffu, o.w, k));
-      const int klo = __shfl_sync(0xffffffffu, clo, k), kup = __shfl_sync(0xffffffffu, cup, k);
+      const int src = 2 * k;
+      const int4 ok4 = make_int4(__shfl_sync(0xffffffffu, o.x, src), __shfl_sync(0xffffffffu, o.y, src),
+                                 __shfl_sync(0xffffffffu, o.z, src), __shfl_sync(0xffffffffu, o.w, src));
+      const int klo = __shfl_sync(0xffffffffu, clo, src), kup = __shfl_sync(0xffffffffu, cup, src);
       const bool kpad = (ok4.z == ok4.w) && (ok4.z == pad_remap);
       int up = 0, lo = nbi, up_full = 0, lo_full = nbi;
       if (!kpad) eval_range(ok4, klo + lane, kup, 32, lo, up, lo_full, up_full);
@@ -542,7 +556,7 @@ sparse_mask_cluster_kernel(Side outer, Side inner, int causal, int window_left, 
       lo = __reduce_min_sync(0xffffffffu, lo);
       up_full = __reduce_max_sync(0xffffffffu, up_full);
       lo_full = __reduce_min_sync(0xffffffffu, lo_full);
-      if (lane == 0) store((long long)b * nbo + o0 + jk, kpad, lo, up, lo_full, up_full);
+      if (lane == 0) store((long long)b * nbo + o0 + jk, kpad, lo, up, lo_full, up_full, 2);
     }
   }
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
