@@ -510,14 +510,15 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             }
           }
         }
-        // row maximum: eight chains of three-input max (two new scores per instruction)
+        // row maximum: eight chains of three-input max (two new scores per instruction);
+        // chain u takes the scores u, u + 8, u + 16, ... of the row
         float mx[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) mx[j] = x[j];
+        for (int u = 0; u < 8; ++u) mx[u] = fmaxf(x[u], x[u + 8]);
 #pragma unroll
-        for (int j = 8; j < KB; j += 16) {
+        for (int j = 16; j < KB; j += 16) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) mx[u] = fmax3f(mx[u], x[j + 2 * u], x[j + 2 * u + 1]);
+          for (int u = 0; u < 8; ++u) mx[u] = fmax3f(mx[u], x[j + u], x[j + 8 + u]);
         }
         const float tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
                                   fmaxf(mx[6], mx[7])) * p.scale_log2;
