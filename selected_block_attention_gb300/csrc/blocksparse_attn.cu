@@ -7,25 +7,28 @@
 // causal and inclusive window on positions) is applied to every other block.
 //
 // Work item = (batch row, query block of 128 tokens, KV head, pair of its query heads):
-// two 128-row problems that read the same key/value blocks and share the token mask.
-// A persistent CTA per SM runs a warp-specialised pipeline:
-//   warp 0      loader: publishes the item (bounds of its query block), then TMA loads
-//               Q of each head into its own buffer and, per key block, K into a K ring
-//               and V plus the block's key positions / segment ids into a V ring;
-//   warp 1      MMA issuer (one thread): S_w = Q_w K^T (both operands in shared
-//               memory, N = one key block) and O_w += P_w V (P_w read from tensor
-//               memory), in the order S0(j) S1(j) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
-//               so that the tensor core runs one head's MMAs while the other head's
-//               softmax works;
+// two 128-row problems that read the same keys / values and share the token mask.  Keys
+// are walked in tiles of 64 (a key block of 128 is two tiles).  A persistent CTA per SM
+// runs a warp-specialised pipeline:
+//   warp 0      loader: publishes the item (its tile range and full-tile range), then TMA
+//               loads Q of each head into its own buffer and, per key tile, K into a K
+//               ring and V plus the tile's key positions / segment ids into a V ring;
+//   warps 1, 2  one MMA-issuing thread per head slot w: S_w = Q_w K^T (both operands in
+//               shared memory, N = 64 keys) into one of two S buffers of the head, and
+//               O_w += P_w V (P_w read from tensor memory over the S buffer it replaced),
+//               in the order S(0) S(1) | PV(t) S(t + 2) | ...; so the scores of tile t + 1
+//               are ready while the softmax still works on tile t, and each thread's
+//               barrier waits overlap the other head's MMAs;
 //   warps 4..7  softmax of head slot 0, warps 8..11 of head slot 1: one thread per query
-//               row; the row's scores of S_w come out of tensor memory in one pass (four
-//               loads under one wait) into registers, are masked outside the full block
-//               range, and P_w (bf16) is written in place over the S_w columns; lazy
-//               online softmax (O_w rescaled only when the row maximum grows by > 2^8);
-//               epilogue O_w / l.
-// Tensor memory: S0, S1 (one key block of fp32 columns each, P aliased in place), O0,
-// O1 (D columns each).  A commit after S_w(j + 1) also covers PV_w(j), so a softmax
-// warpgroup that sees S_w(j + 1) may rescale O_w without a further wait.
+//               row; the row's 64 scores of a tile come out of tensor memory in one pass
+//               into registers, are masked outside the full tile range, and P (bf16) is
+//               written in place over the tile's S buffer; lazy online softmax (O_w
+//               rescaled only when the row maximum grows by > 2^8, after the previous
+//               tile's PV has landed); epilogue: O_w leaves tensor memory at once (the
+//               next item's PV may start), O / l in bf16 is staged in shared memory and
+//               written by TMA stores.
+// Tensor memory: S_w,0 S_w,1 (64 fp32 columns each, P aliased in place) for w = 0, 1,
+// then O_0, O_1 (D columns each): 512 columns at D = 128.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -43,15 +46,12 @@ namespace {
 
 using namespace ptx;
 
-// Warpgroup 0: warp 0 loader, warp 1 MMA issuer (warps 2, 3 idle), 72 registers each;
-// warpgroups 1 and 2: softmax, 192 registers each (a row's 128 scores stay in
-// registers).  The pool at launch is 384 threads x 168 registers = 64512 >=
-// 128 x 72 + 256 x 192 = 58368.
+// Warp 0 loader, warps 1 and 2 MMA issuers (warp 3 idle), warps 4-11 two softmax
+// warpgroups.  No register split: a row of 64 scores fits the 168 registers a thread
+// of a 384-thread CTA gets.
 constexpr int kThreads = 384;
-constexpr int kRegsLow = 72;
-constexpr int kRegsHigh = 192;
-static_assert(128 * kRegsLow + 256 * kRegsHigh <= 384 * 168, "register split exceeds the pool");
 constexpr int kM = 128;         // query rows per head slot
+constexpr int kKT = 64;         // keys per tile (N of S = Q K^T, K of O += P V)
 constexpr int kItemSlots = 3;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -59,8 +59,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct Item {
   int b, hkv, qblk, h0, nh;  // heads h0 .. h0 + nh - 1 (nh = 1 or 2)
-  int lo, up, lof, upf;      // kv blocks [lo, up); [lof, upf) need no token mask
-  int n_tiles;               // = up - lo (one key block per tile)
+  int tlo, tup, tlof, tupf;  // key tiles [tlo, tup); [tlof, tupf) need no token mask
+  int n_tiles;               // = tup - tlo
   int start, end;            // ragged mode: the row's key range
 };
 
@@ -79,6 +79,7 @@ struct Params {
   float* lse;
   int B, T, Hq, Hkv, G, nbq, causal, window_left, window_right, pad_id;
   int q_rows, kv_rows;   // query / key rows per batch row (T and T; ragged: Q and S)
+  int kv_block;          // key block of the bounds (64 or 128; ragged: 128)
   float scale_log2;
   int n_pairs, n_items;
   long long wait_limit;  // cycles a bounded wait may take
@@ -87,38 +88,40 @@ struct Params {
 enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 enum BarId : unsigned {
   kBarItemFull = 1, kBarItemEmpty, kBarQFull, kBarQEmpty, kBarKFull, kBarKEmpty, kBarVFull,
-  kBarVEmpty, kBarSFull, kBarPFull, kBarPvDone, kBarOEmpty
+  kBarVEmpty, kBarSFull, kBarPFull, kBarPvTile, kBarPvLast, kBarOEmpty
 };
 
-template <int D, int KB>
+template <int D>
 struct Cfg {
   static constexpr int kPanels = D / 64;                   // 64-element (128-byte) panels
   static constexpr int kQPanelBytes = kM * 128;
   static constexpr int kQBytes = kPanels * kQPanelBytes;   // Q of one head slot
-  static constexpr int kKPanelBytes = KB * 128;
-  static constexpr int kKBytes = kPanels * kKPanelBytes;   // K (or V) of one key block
-  static constexpr int kPosSegBytes = 2 * KB * 4;
-  static constexpr int kVStageBytes = (kKBytes + kPosSegBytes + 1023) & ~1023;
+  static constexpr int kTPanelBytes = kKT * 128;
+  static constexpr int kTBytes = kPanels * kTPanelBytes;   // K (or V) of one key tile
+  static constexpr int kPosSegBytes = 2 * kKT * 4;
+  static constexpr int kVStageBytes = (kTBytes + kPosSegBytes + 1023) & ~1023;
   static constexpr int kItemBytes = (static_cast<int>(sizeof(Item)) + 15) & ~15;
-  static constexpr int kFixed = 2 * kQBytes + kItemSlots * kItemBytes + 1024 + 1024;
-  static constexpr int kRingFit = (232448 - kFixed) / (kKBytes + kVStageBytes);
-  static constexpr int kStages = kRingFit > 4 ? 4 : kRingFit;   // K and V rings
+  static constexpr int kStages = 3;                        // K and V rings
+  // output staging: per softmax warp 16 rows x D bf16 (one 128-byte swizzled panel per
+  // 64 columns), stored to global memory by TMA
+  static constexpr int kStgPanelBytes = 16 * 128;
+  static constexpr int kStgWarpBytes = kPanels * kStgPanelBytes;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kKBytes;
-  static constexpr int kOffItems = kOffV + kStages * kVStageBytes;
+  static constexpr int kOffV = kOffK + kStages * kTBytes;
+  static constexpr int kOffStage = kOffV + kStages * kVStageBytes;
+  static constexpr int kOffItems = kOffStage + 8 * kStgWarpBytes;
   static constexpr int kOffBars = (kOffItems + kItemSlots * kItemBytes + 7) & ~7;
-  static constexpr int kNumBars = 2 * kItemSlots + 4 + 4 * kStages + 8;
+  static constexpr int kNumBars = 2 * kItemSlots + 4 + 4 * kStages + 4 + 4 + 2 + 2 + 2 + 2;
   static constexpr int kOffMisc = ((kOffBars + kNumBars * 8) + 15) & ~15;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
-  // tensor memory columns: S_w (P_w aliased) and O_w per head slot
-  static constexpr int kSCol = 0;                          // S_w at w * KB
-  static constexpr int kOCol = 2 * KB;                     // O_w at kOCol + w * D
-  static constexpr int kTmemNeed = 2 * KB + 2 * D;
+  // tensor memory columns: S_w,buf at (2 w + buf) * kKT (P aliased), O_w at kOCol + w * D
+  static constexpr int kOCol = 4 * kKT;
+  static constexpr int kTmemNeed = 4 * kKT + 2 * D;
   static constexpr int kTmemCols = kTmemNeed <= 256 ? 256 : 512;
-  static constexpr uint32_t kIdescQK = make_idesc(128, KB, 1u, false, false);
+  static constexpr uint32_t kIdescQK = make_idesc(128, kKT, 1u, false, false);
   static constexpr uint32_t kIdescPV = make_idesc(128, D, 1u, false, true);
-  static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kOffStage % 1024 == 0, "staging panels must start on 1024-byte swizzle atoms");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kTmemNeed <= 512, "tensor memory budget");
 };
@@ -138,13 +141,14 @@ __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, i
 
 // kRagged: the ragged multi-query form of the same computation (queries are the last Q
 // tokens of [start, end) of a KV cache, each with its own inclusive window); the key
-// range and the full blocks of a query block follow from start, end and the window, and
+// range and the full tiles of a query block follow from start, end and the window, and
 // the per-row key range replaces the position / segment test.
-template <int D, int KB, bool kRagged>
+template <int D, bool kRagged>
 __global__ void __launch_bounds__(kThreads, 1)
 blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const Params p) {
-  using C = Cfg<D, KB>;
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                        const Params p) {
+  using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -157,13 +161,14 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   uint64_t* k_empty = bb;     bb += C::kStages;
   uint64_t* v_full = bb;      bb += C::kStages;
   uint64_t* v_empty = bb;     bb += C::kStages;
-  uint64_t* s_full = bb;      bb += 2;   // S_w(j) written (and PV_w(j - 1) done)
-  uint64_t* p_full = bb;      bb += 2;   // P_w(j) stored, O_w rescaled
-  uint64_t* pv_done = bb;     bb += 2;   // last PV_w of an item done
+  uint64_t* s_full = bb;      bb += 4;   // [2 w + buf]: S_w of the buffer written
+  uint64_t* p_full = bb;      bb += 4;   // [2 w + buf]: P_w stored, O_w rescaled
+  uint64_t* pv_tile = bb;     bb += 2;   // each PV_w done
+  uint64_t* pv_last = bb;     bb += 2;   // last PV_w of an item done
   uint64_t* o_empty = bb;     bb += 2;   // epilogue has read O_w
+  uint64_t* mma_done = bb;    bb += 2;   // teardown: every MMA of issuer w finished
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
-  uint64_t* mma_done = reinterpret_cast<uint64_t*>(smem + C::kOffMisc + 8);
   const Abort ab{abort_flag, &g_err_bsa, 2u, p.wait_limit};
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto item_at = [&](int slot) -> Item& {
@@ -171,23 +176,25 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   };
 
   if (threadIdx.x == 0) {
-    // an item slot is read by the MMA thread and the eight softmax warps
-    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 9); }
+    // an item slot is read by the two MMA threads and the eight softmax warps; a K / V
+    // stage is released by both MMA threads
+    for (int i = 0; i < kItemSlots; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 10); }
     for (int w = 0; w < 2; ++w) {
       mbar_init(&q_full[w], 1); mbar_init(&q_empty[w], 1);
-      mbar_init(&s_full[w], 1); mbar_init(&p_full[w], 4);
-      mbar_init(&pv_done[w], 1); mbar_init(&o_empty[w], 4);
+      mbar_init(&pv_tile[w], 1); mbar_init(&pv_last[w], 1);
+      mbar_init(&o_empty[w], 4); mbar_init(&mma_done[w], 1);
     }
+    for (int i = 0; i < 4; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); }
     for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 1);
-      mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 1);
+      mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 2);
+      mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 2);
     }
-    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   if (warp == 1) {
     tmem_alloc(tmem_holder, C::kTmemCols);
@@ -198,10 +205,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t smem_base = smem_u32(smem);
-  const int nbkv = (p.kv_rows + KB - 1) / KB;
+  const int nbkv = (p.kv_rows + p.kv_block - 1) / p.kv_block;
 
-  if (warp < 4) {
-    setmaxnreg_dec<kRegsLow>();
   if (warp == 0) {
     // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
@@ -218,7 +223,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       int b, hkv, qblk, h0, nh;
       decode_item(p, item, b, hkv, qblk, h0, nh);
-      int lo = 0, up = 0, lof = 0, upf = 0, start = 0, end = 0;
+      int tlo = 0, tup = 0, tlof = 0, tupf = 0, start = 0, end = 0;
       if constexpr (kRagged) {
         // rows i0 .. i1 of this query block sit at end - Q + i; their windows' union is
         // [kmin(i0), kmax(i1)] and the keys every row sees are [kmin(i1), kmax(i0)]
@@ -235,25 +240,30 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         };
         const long long klo = kmin(i0), khi = kmax(i1);
         if (end > start && khi >= klo) {
-          lo = static_cast<int>(klo / KB);
-          up = static_cast<int>(khi / KB) + 1;
+          tlo = static_cast<int>(klo / kKT);
+          tup = static_cast<int>(khi / kKT) + 1;
           const long long flo = kmin(i1), fhi = kmax(i0);
-          lof = static_cast<int>((flo + KB - 1) / KB);
-          upf = fhi >= flo ? static_cast<int>((fhi + 1) / KB) : lof;
+          tlof = static_cast<int>((flo + kKT - 1) / kKT);
+          tupf = fhi >= flo ? static_cast<int>((fhi + 1) / kKT) : tlof;
         }
       } else {
+        // block bounds in tiles: a key block of kv_block keys is kv_block / kKT tiles
+        const int tpb = p.kv_block / kKT;
         const long long brow = (long long)b * p.nbq + qblk;
-        lo = max(p.lower[brow], 0);
-        up = min(p.upper[brow], nbkv);
-        lof = p.lower_full[brow];
-        upf = p.upper_full[brow];
+        const int lo = max(p.lower[brow], 0), up = min(p.upper[brow], nbkv);
+        if (up > lo) {
+          tlo = lo * tpb;
+          tup = up * tpb;
+          tlof = p.lower_full[brow] * tpb;
+          tupf = p.upper_full[brow] * tpb;
+        }
       }
-      const int nt = up > lo ? up - lo : 0;
+      const int nt = tup > tlo ? tup - tlo : 0;
       if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleLoader, kBarItemEmpty, item)) break;
       if (lane == 0) {
         Item& it = item_at(islot);
         it.b = b; it.hkv = hkv; it.qblk = qblk; it.h0 = h0; it.nh = nh;
-        it.lo = lo; it.up = up; it.lof = lof; it.upf = upf;
+        it.tlo = tlo; it.tup = tup; it.tlof = tlof; it.tupf = tupf;
         it.n_tiles = nt;
         it.start = start; it.end = end;
         mbar_arrive(&item_full[islot]);
@@ -276,13 +286,13 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       }
       if (!ok) break;
       for (int t = 0; t < nt; ++t) {
-        const int tok0 = b * p.kv_rows + (lo + t) * KB;
+        const int tok0 = b * p.kv_rows + (tlo + t) * kKT;
         if (!warp_wait(&k_empty[ks], kphase ^ 1, ab, kRoleLoader, kBarKEmpty, item)) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&k_full[ks], C::kKBytes);
+          mbar_arrive_expect_tx(&k_full[ks], C::kTBytes);
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(smem + C::kOffK + ks * C::kKBytes + pn * C::kKPanelBytes, &tm_k, &k_full[ks],
+            tma_load_3d(smem + C::kOffK + ks * C::kTBytes + pn * C::kTPanelBytes, &tm_k, &k_full[ks],
                         pn * 64, hkv, tok0);
         }
         k_issued[ks] = true;
@@ -291,13 +301,13 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (!warp_wait(&v_empty[vs], vphase ^ 1, ab, kRoleLoader, kBarVEmpty, item)) { ok = false; break; }
         if (lane == 0) {
           uint8_t* vdst = smem + C::kOffV + vs * C::kVStageBytes;
-          mbar_arrive_expect_tx(&v_full[vs], C::kKBytes + (kRagged ? 0 : C::kPosSegBytes));
+          mbar_arrive_expect_tx(&v_full[vs], C::kTBytes + (kRagged ? 0 : C::kPosSegBytes));
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_load_3d(vdst + pn * C::kKPanelBytes, &tm_v, &v_full[vs], pn * 64, hkv, tok0);
+            tma_load_3d(vdst + pn * C::kTPanelBytes, &tm_v, &v_full[vs], pn * 64, hkv, tok0);
           if (!kRagged) {
-            bulk_load(vdst + C::kKBytes, p.kv_pos + tok0, KB * 4, &v_full[vs]);
-            bulk_load(vdst + C::kKBytes + KB * 4, p.kv_seg + tok0, KB * 4, &v_full[vs]);
+            bulk_load(vdst + C::kTBytes, p.kv_pos + tok0, kKT * 4, &v_full[vs]);
+            bulk_load(vdst + C::kTBytes + kKT * 4, p.kv_seg + tok0, kKT * 4, &v_full[vs]);
           }
         }
         v_issued[vs] = true;
@@ -314,39 +324,39 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       for (int w = 0; w < 2; ++w)
         if (q_issued[w]) drain_wait(&q_full[w], q_last[w]);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuer of head slot w
     if (lane == 0) {
+      const int w = warp - 1;
       int islot = 0; uint32_t iphase = 0;
-      uint32_t qph[2] = {0u, 0u}, pph[2] = {0u, 0u}, oph[2] = {0u, 0u};
-      int ks = 0; uint32_t kphase = 0;
-      int vs = 0; uint32_t vphase = 0;
+      uint32_t qph = 0u, oph = 0u, pph[2] = {0u, 0u};
+      int ks = 0; uint32_t kphase = 0;   // next K tile to consume (for an S)
+      int vs = 0; uint32_t vphase = 0;   // next V tile to consume (for a PV)
       bool ok = true;
       // descriptors of the shared-memory operands; a byte offset x adds x >> 4
-      const uint64_t q_desc0 = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
+      const uint64_t q_desc = make_sdesc(smem_base + C::kOffQ + w * C::kQBytes, 16, 1024, kLayoutSW128);
       const uint64_t k_desc0 = make_sdesc(smem_base + C::kOffK, 16, 1024, kLayoutSW128);
-      const uint64_t v_desc0 = make_sdesc(smem_base + C::kOffV, C::kKPanelBytes, 1024, kLayoutSW128);
+      const uint64_t v_desc0 = make_sdesc(smem_base + C::kOffV, C::kTPanelBytes, 1024, kLayoutSW128);
+      const uint32_t o_tmem = tmem + C::kOCol + w * D;
+      auto s_tmem = [&](int buf) { return tmem + (2 * w + buf) * kKT; };
       auto kstep = [](int kk, int panel_bytes) -> uint64_t {
         return static_cast<uint64_t>(((kk / 4) * panel_bytes + (kk % 4) * 32) >> 4);
       };
-      // S_w = Q_w K^T of the K stage `stage`
-      auto issue_s = [&](int w, int stage) {
-        const uint64_t qd = q_desc0 + static_cast<uint64_t>((w * C::kQBytes) >> 4);
-        const uint64_t kd = k_desc0 + static_cast<uint64_t>((stage * C::kKBytes) >> 4);
+      auto next_k = [&]() { if (++ks == C::kStages) { ks = 0; kphase ^= 1; } };
+      auto next_v = [&]() { if (++vs == C::kStages) { vs = 0; vphase ^= 1; } };
+      // S_w,buf = Q_w K^T of the next K tile, then release the K stage
+      auto issue_s = [&](int buf, int item) -> bool {
+        if (!bounded_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) return false;
+        tc_fence_after();
+        const uint64_t kd = k_desc0 + static_cast<uint64_t>((ks * C::kTBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16_ss(tmem + C::kSCol + w * KB, qd + kstep(kk, C::kQPanelBytes),
-                     kd + kstep(kk, C::kKPanelBytes), C::kIdescQK, kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[w]);
-      };
-      // O_w (+)= P_w V of the V stage `stage` (P_w: bf16 pairs over the S_w columns)
-      auto issue_pv = [&](int w, int stage, bool first) {
-        const uint64_t vd = v_desc0 + static_cast<uint64_t>((stage * C::kVStageBytes) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < KB / 16; ++kk)
-          mma_f16_ts(tmem + C::kOCol + w * D, tmem + C::kSCol + w * KB + kk * 8,
-                     vd + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::kIdescPV,
-                     (first && kk == 0) ? 0u : 1u);
+          mma_f16_ss(s_tmem(buf), q_desc + kstep(kk, C::kQPanelBytes), kd + kstep(kk, C::kTPanelBytes),
+                     C::kIdescQK, kk > 0 ? 1u : 0u);
+        mma_commit(&s_full[2 * w + buf]);
+        mma_commit(&k_empty[ks]);
+        next_k();
+        return true;
       };
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
         if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
@@ -354,75 +364,71 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         if (nt == 0) continue;
-        for (int w = 0; w < nh && ok; ++w) {
-          if (!bounded_wait(&q_full[w], qph[w], ab, kRoleMma, kBarQFull, item)) ok = false;
-          qph[w] ^= 1;
+        if (w >= nh) {
+          // no head in this slot: release each K / V stage once it has been loaded, so
+          // the rings stay in step with the loader and the other MMA thread
+          for (int t = 0; t < nt && ok; ++t) {
+            if (!bounded_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) { ok = false; break; }
+            mbar_arrive(&k_empty[ks]);
+            next_k();
+            if (!bounded_wait(&v_full[vs], vphase, ab, kRoleMma, kBarVFull, item)) { ok = false; break; }
+            mbar_arrive(&v_empty[vs]);
+            next_v();
+          }
+          continue;
         }
-        if (!ok) break;
-        // S of tile 0 for every head slot
-        if (!bounded_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) break;
-        tc_fence_after();
-        for (int w = 0; w < nh; ++w) {
-          issue_s(w, ks);
-          if (nt == 1) mma_commit(&q_empty[w]);
+        if (!bounded_wait(&q_full[w], qph, ab, kRoleMma, kBarQFull, item)) break;
+        qph ^= 1;
+        // S of tiles 0 and 1 into the two buffers
+        for (int t = 0; t < 2 && t < nt && ok; ++t) {
+          if (!issue_s(t, item)) { ok = false; break; }
+          if (t == nt - 1) mma_commit(&q_empty[w]);
         }
-        mma_commit(&k_empty[ks]);
-        int ks_next = ks + 1 == C::kStages ? 0 : ks + 1;
-        uint32_t kphase_next = ks + 1 == C::kStages ? kphase ^ 1 : kphase;
         for (int t = 0; t < nt && ok; ++t) {
-          const bool more = t + 1 < nt;
+          const int buf = t & 1;
           if (!bounded_wait(&v_full[vs], vphase, ab, kRoleMma, kBarVFull, item)) { ok = false; break; }
-          for (int w = 0; w < nh; ++w) {
-            if (t == 0) {
-              if (!bounded_wait(&o_empty[w], oph[w] ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
-              oph[w] ^= 1;
-            }
-            if (!bounded_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
-            pph[w] ^= 1;
-            tc_fence_after();
-            issue_pv(w, vs, t == 0);
-            if (!more) mma_commit(&pv_done[w]);
-            if (w == nh - 1) mma_commit(&v_empty[vs]);
-            if (more) {
-              if (w == 0) {
-                if (!bounded_wait(&k_full[ks_next], kphase_next, ab, kRoleMma, kBarKFull, item)) { ok = false; break; }
-                tc_fence_after();
-              }
-              issue_s(w, ks_next);   // also covers PV_w(t) for the softmax warpgroup
-              if (t + 1 == nt - 1) mma_commit(&q_empty[w]);
-              if (w == nh - 1) mma_commit(&k_empty[ks_next]);
-            }
+          if (t == 0) {
+            if (!bounded_wait(&o_empty[w], oph ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
+            oph ^= 1;
           }
-          if (!ok) break;
-          if (++vs == C::kStages) { vs = 0; vphase ^= 1; }
-          if (more) {
-            ks = ks_next; kphase = kphase_next;
-            ks_next = ks + 1 == C::kStages ? 0 : ks + 1;
-            kphase_next = ks + 1 == C::kStages ? kphase ^ 1 : kphase;
+          if (!bounded_wait(&p_full[2 * w + buf], pph[buf], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+          pph[buf] ^= 1;
+          tc_fence_after();
+          // O_w (+)= P_w V of this tile (P_w: bf16 pairs over the S_w,buf columns)
+          const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * C::kVStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kKT / 16; ++kk)
+            mma_f16_ts(o_tmem, s_tmem(buf) + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                       C::kIdescPV, (t == 0 && kk == 0) ? 0u : 1u);
+          mma_commit(&pv_tile[w]);
+          if (t == nt - 1) mma_commit(&pv_last[w]);
+          mma_commit(&v_empty[vs]);
+          next_v();
+          // S of tile t + 2 into the buffer PV(t) has just read (issued after it, so it
+          // overwrites P only once the PV has consumed it)
+          if (t + 2 < nt) {
+            if (!issue_s(buf, item)) { ok = false; break; }
+            if (t + 2 == nt - 1) mma_commit(&q_empty[w]);
           }
         }
-        if (!ok) break;
-        // the last K stage of this item was consumed; move past it
-        ks = ks_next; kphase = kphase_next;
       }
       // every tcgen05 op issued by this thread has finished once mma_done fires
-      mma_commit(mma_done);
-      drain_wait(mma_done, 0);
+      mma_commit(&mma_done[w]);
+      drain_wait(&mma_done[w], 0);
     }
     __syncwarp();
-  }
-  } else {
-    setmaxnreg_inc<kRegsHigh>();
+  } else if (warp >= 4) {
     // ------------------------------------------------------------------ softmax / epilogue
     const int w = (warp - 4) >> 2;   // head slot of this warpgroup
     const int q4 = warp & 3;         // TMEM lane quadrant of this warp
     const int r = q4 * 32 + lane;    // query row of the item = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t s_col = tmem + lane_off + C::kSCol + w * KB;
     const uint32_t o_col = tmem + lane_off + C::kOCol + w * D;
     int islot = 0; uint32_t iphase = 0;
     int vs = 0; uint32_t vphase = 0;
-    uint32_t sph = 0, pvph = 0;
+    uint32_t sph[2] = {0u, 0u};
+    uint32_t pvt_ph = 0u;  // parity of the next pv_tile completion not yet passed
+    uint32_t pvl_ph = 0u;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
       const Item it = item_at(islot);
@@ -439,7 +445,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           for (int j = 0; j < D; j += 8) *reinterpret_cast<uint4*>(orow + j) = make_uint4(0u, 0u, 0u, 0u);
           if (p.lse != nullptr) p.lse[tok * p.Hq + hq] = -INFINITY;
         }
-        // keep the V ring position in step with the loader and the MMA thread
+        // keep the V ring position in step with the loader
         for (int t = 0; t < nt; ++t)
           if (++vs == C::kStages) { vs = 0; vphase ^= 1; }
         __syncwarp();
@@ -472,35 +478,37 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const bool none = klo > khi;
       float m = -INFINITY, l = 0.f;  // log2 units, lazily moved reference max
       for (int t = 0; t < nt; ++t) {
-        const int blk = it.lo + t;
-        const bool full = blk >= it.lof && blk < it.upf;
-        if (!warp_wait(&s_full[w], sph, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
-        sph ^= 1;
+        const int buf = t & 1;
+        const int ti = it.tlo + t;
+        const bool full = ti >= it.tlof && ti < it.tupf;
+        const uint32_t s_col = tmem + lane_off + (2 * w + buf) * kKT;
+        if (!warp_wait(&s_full[2 * w + buf], sph[buf], ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        sph[buf] ^= 1;
         const int* ps = nullptr;
         if (!full && !kRagged) {
-          // the block's key positions / segment ids arrived with its V
+          // the tile's key positions / segment ids arrived with its V
           if (!warp_wait(&v_full[vs], vphase, ab, kRoleSoftmax, kBarVFull, item)) { ok = false; break; }
-          ps = reinterpret_cast<const int*>(smem + C::kOffV + vs * C::kVStageBytes + C::kKBytes);
+          ps = reinterpret_cast<const int*>(smem + C::kOffV + vs * C::kVStageBytes + C::kTBytes);
         }
         if (++vs == C::kStages) { vs = 0; vphase ^= 1; }
-        // the row's KB raw scores: four loads in flight, one wait
-        float x[KB];
+        // the row's 64 raw scores: two loads in flight, one wait
+        float x[kKT];
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < KB / 32; ++c) tmem_ld_32x32b_x32_nw(s_col + c * 32, x + c * 32);
+        for (int c = 0; c < kKT / 32; ++c) tmem_ld_32x32b_x32_nw(s_col + c * 32, x + c * 32);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < KB; ++j) tmem_ld_ready(x[j]);
+        for (int j = 0; j < kKT; ++j) tmem_ld_ready(x[j]);
         if (!full && kRagged) {
-          const int key0 = blk * KB;  // key index of column 0
+          const int key0 = ti * kKT;  // key index of column 0
 #pragma unroll
-          for (int j = 0; j < KB; ++j)
+          for (int j = 0; j < kKT; ++j)
             if (!(!none && key0 + j >= kmin && key0 + j <= kmax)) x[j] = -INFINITY;
         } else if (!full) {
 #pragma unroll
-          for (int j = 0; j < KB; j += 4) {
+          for (int j = 0; j < kKT; j += 4) {
             const int4 kp4 = *reinterpret_cast<const int4*>(ps + j);
-            const int4 ks4 = *reinterpret_cast<const int4*>(ps + KB + j);
+            const int4 ks4 = *reinterpret_cast<const int4*>(ps + kKT + j);
             const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
             const int ksg[4] = {ks4.x, ks4.y, ks4.z, ks4.w};
 #pragma unroll
@@ -510,13 +518,13 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             }
           }
         }
-        // row maximum: eight chains of three-input max (two new scores per instruction);
-        // chain u takes the scores u, u + 8, u + 16, ... of the row
+        // row maximum: eight chains of three-input max; chain u takes the scores u,
+        // u + 8, u + 16, ... of the tile
         float mx[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) mx[u] = fmaxf(x[u], x[u + 8]);
 #pragma unroll
-        for (int j = 16; j < KB; j += 16) {
+        for (int j = 16; j < kKT; j += 16) {
 #pragma unroll
           for (int u = 0; u < 8; ++u) mx[u] = fmax3f(mx[u], x[j + u], x[j + 8 + u]);
         }
@@ -526,7 +534,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         float m_new = m;
         if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
         const float alpha = (m == -INFINITY || m_new == m) ? (m_new == m ? 1.f : 0.f) : ex2(m - m_new);
-        // exponentials; P (bf16 pairs) over the S_w columns, 32 keys at a time.  The
+        // exponentials; P (bf16 pairs) over the S_w,buf columns, 32 keys at a time.  The
         // argument x * scale - m and the row sum run two lanes per instruction.
         float psum = 0.f;
         {
@@ -534,7 +542,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
           const uint64_t negm2 = pack_f32x2(-m_new, -m_new);
 #pragma unroll
-          for (int c = 0; c < KB / 32; ++c) {
+          for (int c = 0; c < kKT / 32; ++c) {
             uint32_t pk[16];
             if (m_new == -INFINITY) {
 #pragma unroll
@@ -546,14 +554,9 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
                 float a0, a1;
                 unpack_f32x2(a2, a0, a1);
                 const float e0 = ex2(a0), e1 = ex2(a1);
-                x[c * 32 + j] = e0;
-                x[c * 32 + j + 1] = e1;
                 ps2[(j >> 1) & 3] = add_f32x2(ps2[(j >> 1) & 3], pack_f32x2(e0, e1));
-              }
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(x[c * 32 + 2 * j], x[c * 32 + 2 * j + 1]);
-                pk[j] = *reinterpret_cast<uint32_t*>(&h2);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                pk[j >> 1] = *reinterpret_cast<uint32_t*>(&h2);
               }
             }
             tmem_st_32x32b_x16_u_nw(s_col + c * 16, pk);
@@ -565,10 +568,13 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           psum = lo + hi;
         }
         if (t > 0) {
-          // S_w(t) implies PV_w(t - 1) is done: O_w may be rescaled.  TMEM loads/stores
-          // are warp-collective, so the whole warp rescales when any of its rows moved.
+          // O_w holds PV(0 .. t - 2) for sure (S(t) was issued after PV(t - 2)); a rescale
+          // also waits for PV(t - 1).  TMEM loads/stores are warp-collective, so the whole
+          // warp rescales when any of its rows moved.
           const bool my_rescale = m_new != m && m != -INFINITY;
           if (__any_sync(0xffffffffu, my_rescale)) {
+            if (!warp_wait(&pv_tile[w], pvt_ph, ab, kRoleSoftmax, kBarPvTile, item)) { ok = false; break; }
+            tc_fence_after();
             const float f = my_rescale ? alpha : 1.f;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -579,44 +585,72 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               tmem_st_32x32b_x32(o_col + c * 32, ov);
             }
           }
+          pvt_ph ^= 1u;  // PV(t - 1) passed
         }
         l = l * alpha + psum;
         m = m_new;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[w]);
+        if (lane == 0) mbar_arrive(&p_full[2 * w + buf]);
       }
       if (!ok) break;
-      if (!warp_wait(&pv_done[w], pvph, ab, kRoleSoftmax, kBarPvDone, item)) break;
-      pvph ^= 1;
+      if (!warp_wait(&pv_last[w], pvl_ph, ab, kRoleSoftmax, kBarPvLast, item)) break;
+      pvl_ph ^= 1u;
+      pvt_ph ^= 1u;  // PV(nt - 1) passed
       tc_fence_after();
+      float ov[D];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld_32x32b_x32_nw(o_col + c * 32, ov + c * 32);
+      tmem_wait_ld();
+#pragma unroll
+      for (int j = 0; j < D; ++j) tmem_ld_ready(ov[j]);
+      // O_w is in registers: the next item's first PV may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_empty[w]);
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.out + (tok * p.Hq + hq) * D;
+      uint32_t wv[D / 2];
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        float ov[32];
-        tmem_ld_32x32b_x32(o_col + c * 32, ov);
-        if (!row_ok) continue;  // warp-collective load above, no store for a padded row
+      for (int j = 0; j < D / 2; ++j) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[2 * j] * inv, ov[2 * j + 1] * inv);
+        wv[j] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      // rows of this warp in two halves of 16: staged in the 128-byte swizzle the tensor
+      // map expects (16-byte chunk c of row i at c ^ (i % 8)), then one TMA store per
+      // 64-column panel; rows past the query range are clipped by the map
+      uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kStgWarpBytes;
 #pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint32_t wv[4];
+      for (int half = 0; half < 2; ++half) {
+        if (lane == 0) bulk_wait_group_read<0>();  // the staging rows are free again
+        __syncwarp();
+        if ((lane >> 4) == half) {
+          const int rr = lane & 15;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[j + 2 * u] * inv, ov[j + 2 * u + 1] * inv);
-            wv[u] = *reinterpret_cast<uint32_t*>(&h2);
+          for (int pn = 0; pn < C::kPanels; ++pn) {
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+              const uint32_t* src = wv + pn * 32 + c8 * 4;
+              *reinterpret_cast<uint4*>(stg + pn * C::kStgPanelBytes + rr * 128 + ((c8 ^ (rr & 7)) * 16)) =
+                  make_uint4(src[0], src[1], src[2], src[3]);
+            }
           }
-          *reinterpret_cast<uint4*>(orow + c * 32 + j) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int pn = 0; pn < C::kPanels; ++pn)
+            tma_store_4d(&tm_o, stg + pn * C::kStgPanelBytes, pn * 64, hq, it.qblk * kM + q4 * 32 + half * 16,
+                         it.b);
+          bulk_commit_group();
         }
       }
       if (p.lse != nullptr && row_ok) p.lse[tok * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&o_empty[w]);
-        mbar_arrive(&item_empty[islot]);
-      }
+      if (lane == 0) mbar_arrive(&item_empty[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
     }
+    if (lane == 0) bulk_wait_group<0>();  // this warp's output stores have completed
   }
 
   tc_fence_before();
@@ -627,9 +661,9 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   }
 }
 
-template <int D, int KB, bool kRagged>
+template <int D, bool kRagged>
 int launch_impl(const void* q, const void* k, const void* v, const Params& p, cudaStream_t stream) {
-  using C = Cfg<D, KB>;
+  using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.B * p.q_rows};
@@ -642,22 +676,31 @@ int launch_impl(const void* q, const void* k, const void* v, const Params& p, cu
   {
     cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.kv_rows};
     cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)KB};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)kKT};
     if (encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(k), dims,
                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
         encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(v), dims,
                           strides, box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
       return set_error(SBA_ERR_CUDA, "blocksparse_attn: tensor map (k/v) failed");
   }
+  CUtensorMap to;
+  {
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)p.Hq, (cuuint64_t)p.q_rows, (cuuint64_t)p.B};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hq * D * 2, (cuuint64_t)p.q_rows * p.Hq * D * 2};
+    cuuint32_t box[4] = {64, 1, 16, 1};
+    if (encode_tensor_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, p.out, dims, strides, box,
+                          CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+      return set_error(SBA_ERR_CUDA, "blocksparse_attn: tensor map (out) failed");
+  }
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(blocksparse_attn_kernel<D, KB, kRagged>,
+    cudaError_t e = cudaFuncSetAttribute(blocksparse_attn_kernel<D, kRagged>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return cuda_error(e, "blocksparse_attn: set smem attribute");
     attr_done = true;
   }
   const int grid = std::min(p.n_items, num_sms());
-  blocksparse_attn_kernel<D, KB, kRagged><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, p);
+  blocksparse_attn_kernel<D, kRagged><<<grid, kThreads, C::kSmemBytes, stream>>>(tq, tk, tv, to, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "blocksparse_attn launch");
   return SBA_OK;
@@ -696,6 +739,7 @@ int launch_blocksparse_attn(const void* q, const void* k, const void* v, const i
   p.B = B; p.T = T; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
   p.q_rows = T;
   p.kv_rows = T;
+  p.kv_block = kv_block;
   p.seq_start = nullptr;
   p.seq_end = nullptr;
   p.nbq = T / kM;
@@ -709,10 +753,8 @@ int launch_blocksparse_attn(const void* q, const void* k, const void* v, const i
   const long long n_items = (long long)B * Hkv * p.nbq * p.n_pairs;
   if (n_items >= (1LL << 31)) return set_error(SBA_ERR_UNSUPPORTED, "blocksparse_attn: too many items");
   p.n_items = static_cast<int>(n_items);
-  if (D == 128 && kv_block == 128) return launch_impl<128, 128, false>(q, k, v, p, stream);
-  if (D == 128 && kv_block == 64) return launch_impl<128, 64, false>(q, k, v, p, stream);
-  if (D == 64 && kv_block == 128) return launch_impl<64, 128, false>(q, k, v, p, stream);
-  return launch_impl<64, 64, false>(q, k, v, p, stream);
+  if (D == 128) return launch_impl<128, false>(q, k, v, p, stream);
+  return launch_impl<64, false>(q, k, v, p, stream);
 }
 
 // Ragged multi-query attention on the block pipeline (no soft cap, no sinks): queries
@@ -729,6 +771,7 @@ int launch_ragged_chunk(const void* q, const void* k, const void* v, const int32
   p.B = B; p.T = 0; p.Hq = Hq; p.Hkv = Hkv; p.G = Hq / Hkv;
   p.q_rows = Qn;
   p.kv_rows = S;
+  p.kv_block = 128;
   p.nbq = (Qn + kM - 1) / kM;
   p.causal = 0;  // causality comes from window_right = 0
   p.window_left = window_left;
@@ -741,7 +784,7 @@ int launch_ragged_chunk(const void* q, const void* k, const void* v, const int32
   if (n_items >= (1LL << 31) || (long long)B * S >= (1LL << 31) || (long long)B * Qn >= (1LL << 31))
     return set_error(SBA_ERR_UNSUPPORTED, "ragged attention: too many rows");
   p.n_items = static_cast<int>(n_items);
-  return launch_impl<128, 128, true>(q, k, v, p, stream);
+  return launch_impl<128, true>(q, k, v, p, stream);
 }
 
 }  // namespace sba
