@@ -326,8 +326,11 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA issuer of head slot w
-    if (lane == 0) {
+    // The whole warp runs the loop (converged); one elected lane issues the MMAs and
+    // commits, lane 0 the plain arrivals.
+    {
       const int w = warp - 1;
+      const uint32_t leader = elect_one();
       int islot = 0; uint32_t iphase = 0;
       uint32_t qph = 0u, oph = 0u, pph[2] = {0u, 0u};
       int ks = 0; uint32_t kphase = 0;   // next K tile to consume (for an S)
@@ -346,74 +349,74 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       auto next_v = [&]() { if (++vs == C::kStages) { vs = 0; vphase ^= 1; } };
       // S_w,buf = Q_w K^T of the next K tile, then release the K stage
       auto issue_s = [&](int buf, int item) -> bool {
-        if (!bounded_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) return false;
+        if (!warp_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) return false;
         tc_fence_after();
         const uint64_t kd = k_desc0 + static_cast<uint64_t>((ks * C::kTBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_f16_ss(s_tmem(buf), q_desc + kstep(kk, C::kQPanelBytes), kd + kstep(kk, C::kTPanelBytes),
+          mma_f16_ss_by(leader, s_tmem(buf), q_desc + kstep(kk, C::kQPanelBytes), kd + kstep(kk, C::kTPanelBytes),
                      C::kIdescQK, kk > 0 ? 1u : 0u);
-        mma_commit(&s_full[2 * w + buf]);
-        mma_commit(&k_empty[ks]);
+        mma_commit_by(leader, &s_full[2 * w + buf]);
+        mma_commit_by(leader, &k_empty[ks]);
         next_k();
         return true;
       };
       for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles, nh = item_at(islot).nh;
-        mbar_arrive(&item_empty[islot]);
+        if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         if (nt == 0) continue;
         if (w >= nh) {
           // no head in this slot: release each K / V stage once it has been loaded, so
           // the rings stay in step with the loader and the other MMA thread
           for (int t = 0; t < nt && ok; ++t) {
-            if (!bounded_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) { ok = false; break; }
-            mbar_arrive(&k_empty[ks]);
+            if (!warp_wait(&k_full[ks], kphase, ab, kRoleMma, kBarKFull, item)) { ok = false; break; }
+            if (lane == 0) mbar_arrive(&k_empty[ks]);
             next_k();
-            if (!bounded_wait(&v_full[vs], vphase, ab, kRoleMma, kBarVFull, item)) { ok = false; break; }
-            mbar_arrive(&v_empty[vs]);
+            if (!warp_wait(&v_full[vs], vphase, ab, kRoleMma, kBarVFull, item)) { ok = false; break; }
+            if (lane == 0) mbar_arrive(&v_empty[vs]);
             next_v();
           }
           continue;
         }
-        if (!bounded_wait(&q_full[w], qph, ab, kRoleMma, kBarQFull, item)) break;
+        if (!warp_wait(&q_full[w], qph, ab, kRoleMma, kBarQFull, item)) break;
         qph ^= 1;
         // S of tiles 0 and 1 into the two buffers
         for (int t = 0; t < 2 && t < nt && ok; ++t) {
           if (!issue_s(t, item)) { ok = false; break; }
-          if (t == nt - 1) mma_commit(&q_empty[w]);
+          if (t == nt - 1) mma_commit_by(leader, &q_empty[w]);
         }
         for (int t = 0; t < nt && ok; ++t) {
           const int buf = t & 1;
-          if (!bounded_wait(&v_full[vs], vphase, ab, kRoleMma, kBarVFull, item)) { ok = false; break; }
+          if (!warp_wait(&v_full[vs], vphase, ab, kRoleMma, kBarVFull, item)) { ok = false; break; }
           if (t == 0) {
-            if (!bounded_wait(&o_empty[w], oph ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
+            if (!warp_wait(&o_empty[w], oph ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
             oph ^= 1;
           }
-          if (!bounded_wait(&p_full[2 * w + buf], pph[buf], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+          if (!warp_wait(&p_full[2 * w + buf], pph[buf], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
           pph[buf] ^= 1;
           tc_fence_after();
           // O_w (+)= P_w V of this tile (P_w: bf16 pairs over the S_w,buf columns)
           const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * C::kVStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kKT / 16; ++kk)
-            mma_f16_ts(o_tmem, s_tmem(buf) + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+            mma_f16_ts_by(leader, o_tmem, s_tmem(buf) + kk * 8, vd + static_cast<uint64_t>((kk * 16 * 128) >> 4),
                        C::kIdescPV, (t == 0 && kk == 0) ? 0u : 1u);
-          mma_commit(&pv_tile[w]);
-          if (t == nt - 1) mma_commit(&pv_last[w]);
-          mma_commit(&v_empty[vs]);
+          mma_commit_by(leader, &pv_tile[w]);
+          if (t == nt - 1) mma_commit_by(leader, &pv_last[w]);
+          mma_commit_by(leader, &v_empty[vs]);
           next_v();
           // S of tile t + 2 into the buffer PV(t) has just read (issued after it, so it
           // overwrites P only once the PV has consumed it)
           if (t + 2 < nt) {
             if (!issue_s(buf, item)) { ok = false; break; }
-            if (t + 2 == nt - 1) mma_commit(&q_empty[w]);
+            if (t + 2 == nt - 1) mma_commit_by(leader, &q_empty[w]);
           }
         }
       }
       // every tcgen05 op issued by this thread has finished once mma_done fires
-      mma_commit(&mma_done[w]);
+      mma_commit_by(leader, &mma_done[w]);
       drain_wait(&mma_done[w], 0);
     }
     __syncwarp();

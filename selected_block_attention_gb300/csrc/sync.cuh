@@ -26,14 +26,23 @@ struct Abort {
   long long limit;  // SM cycles a wait may take before the CTA gives up
 };
 
+// Below this limit (SM cycles) the probes never suspend the thread: a converged warp's
+// try_wait sleeps until the phase completes (or a system-dependent time passes), so a
+// short limit would otherwise never be looked at.
+constexpr long long kShortWaitLimit = 1LL << 20;
+
 // Bounded wait of one thread on an mbarrier phase.
 __device__ __forceinline__ bool bounded_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
                                              unsigned role, unsigned bar_id, int item) {
   const uint32_t a = ptx::smem_u32(bar);
-  if (ptx::mbar_try_wait(a, parity)) return true;
+  const bool short_limit = ab.limit < kShortWaitLimit;
+  auto probe = [&]() {
+    return short_limit ? ptx::mbar_test_wait(a, parity) : ptx::mbar_try_wait(a, parity);
+  };
+  if (probe()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (ptx::mbar_try_wait(a, parity)) return true;
+    if (probe()) return true;
     if (*ab.flag) return false;
     if (clock64() - t0 > ab.limit) {
       atomicOr(&ab.err->flags, kDevErrTimeout);
