@@ -483,9 +483,12 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (issued[s]) drain_wait(&st_full[s], last_parity[s]);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ QK issuer
-    // Two threads issue the MMAs (QK here, PV in warp 3): a thread's wait on a barrier
-    // stalls only its own stream while the tensor core runs the other's MMAs.
-    if (lane == 0) {
+    // Two warps issue the MMAs (QK here, PV in warp 3): a warp's wait on a barrier stalls
+    // only its own stream while the tensor core runs the other's MMAs.  Each runs its
+    // loop converged; one elected lane issues the tcgen05 operations, lane 0 the plain
+    // arrivals.
+    {
+      const uint32_t leader = elect_one();
       int islot = 0; uint32_t iphase = 0;
       uint32_t quphase = 0, sphase = 0;
       bool q_in_use = false;  // a QK of an earlier item may still read the TMEM copy of Q
@@ -494,16 +497,16 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       // descriptors of the shared-memory operands; a byte offset x adds x >> 4
       const uint64_t st_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
       for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
-        mbar_arrive(&item_empty[islot]);
+        if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         const int np = (nt + 1) / 2;
         if (np == 0) continue;
         // Q of this item (its first ring stage) -> TMEM, once the previous item's QKs are done
-        if (!bounded_wait(&st_full[stage], phase, ab, kRoleMma, kBarQFull, item)) break;
+        if (!warp_wait(&st_full[stage], phase, ab, kRoleMma, kBarQFull, item)) break;
         if (q_in_use) {
-          if (!bounded_wait(q_used, quphase, ab, kRoleMma, kBarQEmpty, item)) break;
+          if (!warp_wait(q_used, quphase, ab, kRoleMma, kBarQEmpty, item)) break;
           quphase ^= 1;
         }
         tc_fence_after();
@@ -511,38 +514,39 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const uint64_t qd = st_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            tmem_cp_128x256b(tmem + C::kQCol + kk * 8,
+            tmem_cp_128x256b_by(leader, tmem + C::kQCol + kk * 8,
                              qd + static_cast<uint64_t>(((kk / 4) * C::kQPanelBytes + (kk % 4) * 32) >> 4));
         }
-        mma_commit(&st_empty[stage]);
+        mma_commit_by(leader, &st_empty[stage]);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         for (int pp = 0; pp < np; ++pp) {
-          if (!bounded_wait(&st_full[stage], phase, ab, kRoleMma, kBarKvFull, item) ||
-              !bounded_wait(s_empty, sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
+          if (!warp_wait(&st_full[stage], phase, ab, kRoleMma, kBarKvFull, item) ||
+              !warp_wait(s_empty, sphase ^ 1, ab, kRoleMma, kBarSEmpty, item)) { ok = false; break; }
           sphase ^= 1;
           tc_fence_after();
           const uint64_t kd = st_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
-            mma_f16_ts(tmem + C::kSCol, tmem + C::kQCol + kk * 8,
+            mma_f16_ts_by(leader, tmem + C::kSCol, tmem + C::kQCol + kk * 8,
                        kd + static_cast<uint64_t>(((kk / 4) * C::kPanelBytes + (kk % 4) * 32) >> 4),
                        C::kIdescQK, kk > 0);
-          mma_commit(s_full);
+          mma_commit_by(leader, s_full);
           if (pp == np - 1) {
-            mma_commit(q_used);
+            mma_commit_by(leader, q_used);
             q_in_use = true;
           }
           if (++stage == C::kStages) { stage = 0; phase ^= 1; }
         }
       }
       // every tcgen05 op issued by this thread has finished once mma_done fires
-      mma_commit(&mma_done[0]);
+      mma_commit_by(leader, &mma_done[0]);
       drain_wait(&mma_done[0], 0);
     }
     __syncwarp();
   } else if (warp == 3) {
     // ------------------------------------------------------------------ PV issuer
-    if (lane == 0) {
+    {
+      const uint32_t leader = elect_one();
       int islot = 0; uint32_t iphase = 0;
       int stage = 0;
       uint32_t pph[2] = {0u, 0u};
@@ -551,9 +555,9 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const uint64_t v_desc0 =
           make_sdesc(smem_base + C::kOffStages + C::kKBytes, C::kPanelBytes, 1024, kLayoutSW128);
       for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nt = item_at(islot).n_tiles;
-        mbar_arrive(&item_empty[islot]);
+        if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         const int np = (nt + 1) / 2;
         if (np == 0) continue;
@@ -565,26 +569,26 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           const uint64_t vd = v_desc0 + static_cast<uint64_t>((stage * C::kStageBytes) >> 4);
 #pragma unroll
           for (int w = 0; w < 2; ++w) {
-            if (!bounded_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+            if (!warp_wait(&p_full[w], pph[w], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
             pph[w] ^= 1;
             if (pp == 0 && w == 0) {
-              if (!bounded_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
+              if (!warp_wait(o_empty, ophase ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
               ophase ^= 1;
             }
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < kTileKeys / 16; ++k)
-              mma_f16_ts(tmem + C::kOCol + w * D, tmem + C::kPCol + w * (kTileKeys / 2) + k * 8,
+              mma_f16_ts_by(leader, tmem + C::kOCol + w * D, tmem + C::kPCol + w * (kTileKeys / 2) + k * 8,
                          vd + static_cast<uint64_t>(((w * kTileKeys + k * 16) * 128) >> 4), C::kIdescPV,
                          (pp == 0 && k == 0) ? 0u : 1u);
-            mma_commit(&pv_done[w]);
+            mma_commit_by(leader, &pv_done[w]);
           }
           if (!ok) break;
-          mma_commit(&st_empty[stage]);
+          mma_commit_by(leader, &st_empty[stage]);
           if (++stage == C::kStages) stage = 0;
         }
       }
-      mma_commit(&mma_done[1]);
+      mma_commit_by(leader, &mma_done[1]);
       drain_wait(&mma_done[1], 0);
     }
     __syncwarp();

@@ -184,6 +184,14 @@ __device__ __forceinline__ uint32_t elect_one() {
 __device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
   asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
 }
+// tmem_cp_128x256b issued by the lane whose `leader` is nonzero (converged warp).
+__device__ __forceinline__ void tmem_cp_128x256b_by(uint32_t leader, uint32_t taddr, uint64_t s_desc) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t"
+      "@q tcgen05.cp.cta_group::1.128x256b [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(s_desc), "r"(leader)
+      : "memory");
+}
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(
