@@ -551,11 +551,13 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------------ MMA issuers
     // Two threads issue MMAs: warp 1 S = Q K^T and dP = dO V^T of each tile, warp 3
-    // dQ += dS K.  A thread's barrier wait then stalls only its own stream while the
-    // tensor core runs the other's MMAs.  A tile's K/V stage is released by the dQ
+    // dQ += dS K.  A warp's barrier wait then stalls only its own stream while the
+    // tensor core runs the other's MMAs.  Each warp runs its loop converged; one elected
+    // lane issues the tcgen05 operations, lane 0 the plain arrivals.  A tile's K/V stage is released by the dQ
     // thread: its dQ MMA follows the tile's softmax, which followed the S/dP MMAs.
     const bool sdp_role = warp == 1;
-    if (lane == 0) {
+    {
+      const uint32_t leader = elect_one();
       int islot = 0; uint32_t iphase = 0;
       uint32_t qph = 0, dqph = 0;
       int stage = 0; uint32_t kph = 0;
@@ -567,17 +569,17 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint64_t ring_k = make_sdesc(smem_base + C::kOffRing, 16, 1024, kLayoutSW128);
       const uint64_t ring_kmn = make_sdesc(smem_base + C::kOffRing, C::kTilePanel, 1024, kLayoutSW128);
       for (int item = blockIdx.x; item < p.n_items_dq && ok; item += gridDim.x) {
-        if (!bounded_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
         const int nu = item_at(islot).n_union;
-        mbar_arrive(&item_empty[islot]);
+        if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
         if (nu == 0) continue;
         if (sdp_role) {
-          if (!bounded_wait(qdo_full, qph, ab, kRoleMma, kBarQdoFull, item)) break;
+          if (!warp_wait(qdo_full, qph, ab, kRoleMma, kBarQdoFull, item)) break;
           qph ^= 1;
           for (int u = 0; u < nu; ++u) {
-            if (!bounded_wait(&kv_full[stage], kph, ab, kRoleMma, kBarKvFull, item) ||
-                !bounded_wait(&sdp_empty[buf], sdp_ph[buf] ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) {
+            if (!warp_wait(&kv_full[stage], kph, ab, kRoleMma, kBarKvFull, item) ||
+                !warp_wait(&sdp_empty[buf], sdp_ph[buf] ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) {
               ok = false;
               break;
             }
@@ -586,14 +588,14 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             const uint64_t vd = kd + static_cast<uint64_t>(C::kTileBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_f16_ss(tmem + C::kSCol + buf * kBS, q_desc + kmajor_step(kk, C::kQPanel),
+              mma_f16_ss_by(leader, tmem + C::kSCol + buf * kBS, q_desc + kmajor_step(kk, C::kQPanel),
                          kd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_f16_ss(tmem + C::kDpCol + buf * kBS, do_desc + kmajor_step(kk, C::kQPanel),
+              mma_f16_ss_by(leader, tmem + C::kDpCol + buf * kBS, do_desc + kmajor_step(kk, C::kQPanel),
                          vd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
-            mma_commit(&sdp_full[buf]);
-            if (u == nu - 1) mma_commit(qdo_empty);
+            mma_commit_by(leader, &sdp_full[buf]);
+            if (u == nu - 1) mma_commit_by(leader, qdo_empty);
             sdp_ph[buf] ^= 1;
             buf ^= 1;
             if (++stage == C::kStages) { stage = 0; kph ^= 1; }
@@ -601,29 +603,29 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         } else {
           for (int u = 0; u < nu; ++u) {
             // dQ += dS(u) K(u)
-            if (!bounded_wait(&ds_full[buf], ds_ph[buf], ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+            if (!warp_wait(&ds_full[buf], ds_ph[buf], ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
             ds_ph[buf] ^= 1;
             if (u == 0) {
-              if (!bounded_wait(dq_empty, dqph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
+              if (!warp_wait(dq_empty, dqph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
               dqph ^= 1;
             }
             tc_fence_after();
             const uint64_t kmn = ring_kmn + static_cast<uint64_t>((stage * 2 * C::kTileBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBS / 16; ++kk)
-              mma_f16_ts(tmem + C::kDqCol, tmem + C::kDsCol + buf * (kBS / 2) + kk * 8,
+              mma_f16_ts_by(leader, tmem + C::kDqCol, tmem + C::kDsCol + buf * (kBS / 2) + kk * 8,
                          kmn + static_cast<uint64_t>((kk * 16 * 128) >> 4), C::kIdescDq,
                          (u == 0 && kk == 0) ? 0u : 1u);
-            mma_commit(&kv_empty[stage]);
-            mma_commit(&ds_empty[buf]);
+            mma_commit_by(leader, &kv_empty[stage]);
+            mma_commit_by(leader, &ds_empty[buf]);
             buf ^= 1;
             if (++stage == C::kStages) stage = 0;
           }
-          if (ok) mma_commit(dq_full);
+          if (ok) mma_commit_by(leader, dq_full);
         }
       }
       // every tcgen05 op issued by this thread has finished once its mma_done fires
-      mma_commit(&mma_done[sdp_role ? 0 : 1]);
+      mma_commit_by(leader, &mma_done[sdp_role ? 0 : 1]);
       drain_wait(&mma_done[sdp_role ? 0 : 1], 0);
     }
     __syncwarp();
@@ -793,16 +795,12 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
   // whose Q / dO rows stay in L2 across the groups' token lists.  The loader fetches an
   // item and publishes it in a two-slot ring that the MMA threads and the softmax warps
   // read (-1: no more items).
+  // (called by whole warps: the MMA warps and the softmax warps)
   auto take_item = [&](int& islot, uint32_t& iph, unsigned role) -> int {
-    const bool ok = role == kRoleSoftmax ? warp_wait(&item_full[islot], iph, ab, role, kBarItemFull, -1)
-                                         : bounded_wait(&item_full[islot], iph, ab, role, kBarItemFull, -1);
+    const bool ok = warp_wait(&item_full[islot], iph, ab, role, kBarItemFull, -1);
     int item = ok ? slot_item[islot] : -1;
-    if (role == kRoleSoftmax) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&item_empty[islot]);
-    } else {
-      mbar_arrive(&item_empty[islot]);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_empty[islot]);
     if (++islot == 2) { islot = 0; iph ^= 1; }
     return item;
   };
@@ -814,7 +812,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     mbar_init(pds_full, 4); mbar_init(pds_empty, 1);
     mbar_init(acc_full, 1); mbar_init(acc_empty, 4);
     mbar_init(&mma_done[0], 1); mbar_init(&mma_done[1], 1);
-    // an item slot is read by the two MMA threads and the four softmax warps
+    // an item slot is read by the two MMA warps and the four softmax warps
     for (int i = 0; i < 2; ++i) { mbar_init(&item_full[i], 1); mbar_init(&item_empty[i], 6); }
     *abort_flag = 0;
     fence_mbar_init();
@@ -906,8 +904,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // the softmax warps, which release S / dP as soon as they have loaded them); warp 2
     // issues dV^T += dO^T P and dK^T += Q^T dS and releases the chunk's Q / dO buffer,
     // and at the end of an item the K / V tile (its MMAs follow the item's last S / dP).
+    // Each warp runs its loop converged; one elected lane issues the tcgen05 operations.
     const bool sdp_role = warp == 1;
-    if (lane == 0) {
+    {
+      const uint32_t leader = elect_one();
       uint32_t kvph = 0, sdph = 0, pdph = 0, accph = 0;
       uint32_t qph[2] = {0u, 0u};
       int qb = 0;
@@ -929,11 +929,11 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (cnt == 0) continue;
         const int nch = (cnt + p.NT - 1) / p.NT;
         if (sdp_role) {
-          if (!bounded_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
+          if (!warp_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
           kvph ^= 1;
           for (int c = 0; c < nch; ++c) {
-            if (!bounded_wait(&qdo_full[qb], qph[qb], ab, kRoleMma, kBarQdoFull, item) ||
-                !bounded_wait(sdp_empty, sdph ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) { ok = false; break; }
+            if (!warp_wait(&qdo_full[qb], qph[qb], ab, kRoleMma, kBarQdoFull, item) ||
+                !warp_wait(sdp_empty, sdph ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) { ok = false; break; }
             qph[qb] ^= 1;
             sdph ^= 1;
             tc_fence_after();
@@ -941,22 +941,22 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             const uint64_t doo = qo + static_cast<uint64_t>(C::kQBytes >> 4);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_f16_ss(tmem + C::kSCol, qk_desc + qo + kmajor_step(kk, C::kQPanel),
+              mma_f16_ss_by(leader, tmem + C::kSCol, qk_desc + qo + kmajor_step(kk, C::kQPanel),
                          k_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
-              mma_f16_ss(tmem + C::kDpCol, qk_desc + doo + kmajor_step(kk, C::kQPanel),
+              mma_f16_ss_by(leader, tmem + C::kDpCol, qk_desc + doo + kmajor_step(kk, C::kQPanel),
                          v_desc + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
-            mma_commit(sdp_full);
+            mma_commit_by(leader, sdp_full);
             qb ^= 1;
           }
         } else {
           for (int c = 0; c < nch; ++c) {
             // dV^T += dO^T P and dK^T += Q^T dS over the chunk's 128 rows (K = rows)
-            if (!bounded_wait(pds_full, pdph, ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+            if (!warp_wait(pds_full, pdph, ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
             pdph ^= 1;
             if (c == 0) {
-              if (!bounded_wait(acc_empty, accph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
+              if (!warp_wait(acc_empty, accph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
               accph ^= 1;
             }
             tc_fence_after();
@@ -965,26 +965,26 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk) {
               const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-              mma_f16_ss(tmem + C::kDvCol, qmn_desc + doo + step, p_desc + step, C::kIdescAcc,
+              mma_f16_ss_by(leader, tmem + C::kDvCol, qmn_desc + doo + step, p_desc + step, C::kIdescAcc,
                          (c == 0 && kk == 0) ? 0u : 1u);
             }
 #pragma unroll
             for (int kk = 0; kk < kRows / 16; ++kk) {
               const uint64_t step = static_cast<uint64_t>((kk * 16 * 128) >> 4);
-              mma_f16_ss(tmem + C::kDkCol, qmn_desc + qo + step, ds_desc + step, C::kIdescAcc,
+              mma_f16_ss_by(leader, tmem + C::kDkCol, qmn_desc + qo + step, ds_desc + step, C::kIdescAcc,
                          (c == 0 && kk == 0) ? 0u : 1u);
             }
-            mma_commit(&qdo_empty[qb]);
-            mma_commit(pds_empty);
+            mma_commit_by(leader, &qdo_empty[qb]);
+            mma_commit_by(leader, pds_empty);
             qb ^= 1;
           }
           if (!ok) break;
-          mma_commit(kv_empty);
-          mma_commit(acc_full);
+          mma_commit_by(leader, kv_empty);
+          mma_commit_by(leader, acc_full);
         }
       }
       // every tcgen05 op issued by this thread has finished once its mma_done fires
-      mma_commit(&mma_done[sdp_role ? 0 : 1]);
+      mma_commit_by(leader, &mma_done[sdp_role ? 0 : 1]);
       drain_wait(&mma_done[sdp_role ? 0 : 1], 0);
     }
     __syncwarp();
