@@ -641,17 +641,21 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         sph ^= 1;
         float x[kTileKeys];
         if (any) {
+          // both loads in flight, one wait
           tc_fence_after();
-          tmem_ld_32x32b_x32(s_col, x);
-          tmem_ld_32x32b_x32(s_col + 32, x + 32);
+          tmem_ld_32x32b_x32_nw(s_col, x);
+          tmem_ld_32x32b_x32_nw(s_col + 32, x + 32);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < kTileKeys; ++j) tmem_ld_ready(x[j]);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_empty);
         float m_new = m, alpha = 1.f, psum = 0.f;
+        uint32_t pk[kTileKeys / 2];
         if (any) {
-          // masked raw scores; maximum with four independent chains
-          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          // masked raw scores (keys of a segment past its valid count)
 #pragma unroll
           for (int e = 0; e < C::kSegs; ++e) {
             if (nv[e] < C::kSegLen) {
@@ -659,43 +663,54 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
               for (int jj = 0; jj < C::kSegLen; ++jj)
                 if (jj >= nv[e]) x[e * C::kSegLen + jj] = -INFINITY;
             }
-#pragma unroll
-            for (int jj = 0; jj < C::kSegLen; ++jj) {
-              const int j = e * C::kSegLen + jj;
-              mx[j & 3] = fmaxf(mx[j & 3], x[j]);
-            }
           }
-          const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.scale_log2;
+          // maximum: eight chains of three-input max; chain u takes the keys u, u + 8, ...
+          float mx[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) mx[u] = fmaxf(x[u], x[u + 8]);
+#pragma unroll
+          for (int j = 16; j < kTileKeys; j += 16) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) mx[u] = fmax3f(mx[u], x[j + u], x[j + 8 + u]);
+          }
+          const float tmax = fmax3f(fmax3f(mx[0], mx[1], mx[2]), fmax3f(mx[3], mx[4], mx[5]),
+                                    fmaxf(mx[6], mx[7])) * p.scale_log2;
           // lazy online softmax: move the reference max only when it grows by > 2^8
           if (tmax > m + kRescaleThreshold || (m == -INFINITY && tmax != -INFINITY)) m_new = tmax;
           alpha = (m == -INFINITY || m_new == m) ? (m_new == m ? 1.f : 0.f) : ex2(m - m_new);
-          float ps[4] = {0.f, 0.f, 0.f, 0.f};
+          // exponentials, P as bf16 pairs and the row sum; the argument x * scale - m and
+          // the sum run two lanes per instruction
+          const uint64_t scale2 = pack_f32x2(p.scale_log2, p.scale_log2);
+          const uint64_t negm2 = pack_f32x2(-m_new, -m_new);
+          uint64_t ps2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
           for (int e = 0; e < C::kSegs; ++e) {
             if (nv[e] > 0) {
 #pragma unroll
-              for (int jj = 0; jj < C::kSegLen; ++jj) {
+              for (int jj = 0; jj < C::kSegLen; jj += 2) {
                 const int j = e * C::kSegLen + jj;
-                x[j] = ex2(fmaf(x[j], p.scale_log2, -m_new));
-                ps[j & 3] += x[j];
+                const uint64_t a2 = fma_f32x2(pack_f32x2(x[j], x[j + 1]), scale2, negm2);
+                float a0, a1;
+                unpack_f32x2(a2, a0, a1);
+                const float e0 = ex2(a0), e1 = ex2(a1);
+                ps2[(j >> 1) & 3] = add_f32x2(ps2[(j >> 1) & 3], pack_f32x2(e0, e1));
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+                pk[j >> 1] = *reinterpret_cast<uint32_t*>(&h2);
               }
             } else {
 #pragma unroll
-              for (int jj = 0; jj < C::kSegLen; ++jj) x[e * C::kSegLen + jj] = 0.f;
+              for (int jj = 0; jj < C::kSegLen; jj += 2) pk[(e * C::kSegLen + jj) >> 1] = 0u;
             }
           }
-          psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          const uint64_t s01 = add_f32x2(ps2[0], ps2[1]), s23 = add_f32x2(ps2[2], ps2[3]);
+          float lo, hi;
+          unpack_f32x2(add_f32x2(s01, s23), lo, hi);
+          psum = lo + hi;
         } else {
 #pragma unroll
-          for (int j = 0; j < kTileKeys; ++j) x[j] = 0.f;
+          for (int j = 0; j < kTileKeys / 2; ++j) pk[j] = 0u;
         }
         l = l * alpha + psum;
-        uint32_t pk[kTileKeys / 2];
-#pragma unroll
-        for (int j = 0; j < kTileKeys / 2; ++j) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(x[2 * j], x[2 * j + 1]);
-          pk[j] = *reinterpret_cast<uint32_t*>(&h2);
-        }
         // this warpgroup's previous PV must be done before its P is replaced and its O
         // rescaled
         if (pp > 0) {
