@@ -272,13 +272,18 @@ __device__ __forceinline__ uint64_t kmajor_step(int kk, int panel_bytes) {
   return static_cast<uint64_t>(((kk / 4) * panel_bytes + (kk % 4) * 32) >> 4);
 }
 
-// 64 fp32 columns of one TMEM lane row (two loads, one wait)
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* x) {
-  tmem_ld_32x32b_x32_nw(taddr, x);
-  tmem_ld_32x32b_x32_nw(taddr + 32, x + 32);
+// 64 columns at each of two TMEM addresses of the lane row (four loads, one wait)
+__device__ __forceinline__ void tmem_ld64x2(uint32_t ta, float* x, uint32_t tb, float* y) {
+  tmem_ld_32x32b_x32_nw(ta, x);
+  tmem_ld_32x32b_x32_nw(ta + 32, x + 32);
+  tmem_ld_32x32b_x32_nw(tb, y);
+  tmem_ld_32x32b_x32_nw(tb + 32, y + 32);
   tmem_wait_ld();
 #pragma unroll
-  for (int j = 0; j < 64; ++j) tmem_ld_ready(x[j]);
+  for (int j = 0; j < 64; ++j) {
+    tmem_ld_ready(x[j]);
+    tmem_ld_ready(y[j]);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
@@ -287,14 +292,22 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // P and dS of one row from its S and dP columns: the first nvalid keys are admissible.
+// P = 2^(s scale log2(e) - lse log2(e)), dS = P (dP - Delta); two keys per instruction.
 __device__ __forceinline__ void row_grads(const float* s, const float* dp, int nvalid, float scale_log2,
                                           float lse2, float delta, uint32_t* p_pk, uint32_t* ds_pk) {
+  const uint64_t scale2 = pack_f32x2(scale_log2, scale_log2);
+  const uint64_t neglse2 = pack_f32x2(-lse2, -lse2);
+  const uint64_t negdelta2 = pack_f32x2(-delta, -delta);
 #pragma unroll
   for (int j = 0; j < 64; j += 2) {
-    const float p0 = j < nvalid ? ex2(fmaf(s[j], scale_log2, -lse2)) : 0.f;
-    const float p1 = j + 1 < nvalid ? ex2(fmaf(s[j + 1], scale_log2, -lse2)) : 0.f;
+    float a0, a1;
+    unpack_f32x2(fma_f32x2(pack_f32x2(s[j], s[j + 1]), scale2, neglse2), a0, a1);
+    const float p0 = j < nvalid ? ex2(a0) : 0.f;
+    const float p1 = j + 1 < nvalid ? ex2(a1) : 0.f;
     if (p_pk != nullptr) p_pk[j >> 1] = pack_bf16(p0, p1);
-    ds_pk[j >> 1] = pack_bf16(p0 * (dp[j] - delta), p1 * (dp[j + 1] - delta));
+    float d0, d1;
+    unpack_f32x2(mul_f32x2(add_f32x2(pack_f32x2(dp[j], dp[j + 1]), negdelta2), pack_f32x2(p0, p1)), d0, d1);
+    ds_pk[j >> 1] = pack_bf16(d0, d1);
   }
 }
 
@@ -666,8 +679,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         sdp_ph ^= 1;
         tc_fence_after();
         float s[64], dp[64];
-        tmem_ld64(tmem + lane_off + C::kSCol + w * kBS, s);
-        tmem_ld64(tmem + lane_off + C::kDpCol + w * kBS, dp);
+        tmem_ld64x2(tmem + lane_off + C::kSCol + w * kBS, s, tmem + lane_off + C::kDpCol + w * kBS, dp);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sdp_empty[w]);
@@ -1032,8 +1044,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         sdph ^= 1;
         tc_fence_after();
         float s[64], dp[64];
-        tmem_ld64(tmem + lane_off + C::kSCol, s);
-        tmem_ld64(tmem + lane_off + C::kDpCol, dp);
+        tmem_ld64x2(tmem + lane_off + C::kSCol, s, tmem + lane_off + C::kDpCol, dp);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(sdp_empty);
@@ -1060,8 +1071,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       accph ^= 1;
       tc_fence_after();
       float av[64], ak[64];
-      tmem_ld64(tmem + lane_off + C::kDvCol, av);
-      tmem_ld64(tmem + lane_off + C::kDkCol, ak);
+      tmem_ld64x2(tmem + lane_off + C::kDvCol, av, tmem + lane_off + C::kDkCol, ak);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty);
