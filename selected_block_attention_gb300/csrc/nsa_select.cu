@@ -218,12 +218,15 @@ __device__ __forceinline__ void build_item(const Params& p, int g, int hkv, int 
       key[j] = (cnt << 8) | li;
     }
     int rank[kPer] = {0, 0, 0, 0};
+    const int npl = (wn + 31) / 32;     // tokens per lane of this window (2 to 4)
     for (int src = 0; src < 32; ++src) {
 #pragma unroll
       for (int jj = 0; jj < kPer; ++jj) {
+        if (jj >= npl) break;           // warp-uniform
         const int other = __shfl_sync(kFull, key[jj], src);
 #pragma unroll
-        for (int j = 0; j < kPer; ++j) rank[j] += other < key[j];
+        for (int j = 0; j < kPer; ++j)
+          if (j < npl) rank[j] += other < key[j];
       }
     }
 #pragma unroll
@@ -262,7 +265,24 @@ __device__ __forceinline__ void build_item(const Params& p, int g, int hkv, int 
     const int trow = __shfl_sync(kFull, tok, i);
     if (idx < total && trow >= 0) ev[c] = p.block_indices[((long long)trow * p.Hkv + hkv) * p.S + j];
   }
-  int n = 0;
+  // When every token of the item lies in one sequence and that sequence's blocks fit the
+  // sort buffer as one 32-bit token mask per block, the union is read off a per-block
+  // mask (blocks come out in row order); otherwise the (row, token bit) keys are sorted.
+  const unsigned tv_bal = __ballot_sync(kFull, tv);
+  bool use_map = false;
+  int map_seq0 = 0, map_nb = 0;
+  if (tv_bal != 0u) {
+    const int src = __ffs(tv_bal) - 1;
+    map_seq0 = __shfl_sync(kFull, seq0, src);
+    map_nb = (__shfl_sync(kFull, slen, src) + BS - 1) / BS;
+    use_map = __all_sync(kFull, !tv || seq0 == map_seq0) && map_nb <= 2 * kMaxUnion;
+  }
+  uint32_t* bmap = reinterpret_cast<uint32_t*>(keys);
+  if (use_map) {
+    for (int idx = lane; idx < map_nb; idx += 32) bmap[idx] = 0u;
+    __syncwarp();
+  }
+  int n = 0, emax = -1;
 #pragma unroll
   for (int c = 0; c < kChunks; ++c) {
     if (c * 32 >= total) break;
@@ -276,57 +296,80 @@ __device__ __forceinline__ void build_item(const Params& p, int g, int hkv, int 
     const int e = ev[c];
     const int nb = (slen_i + BS - 1) / BS;
     const bool valid = idx < total && j < cnt_i && e >= 0 && e < nb && (!p.causal || e * BS <= trel_i);
-    const unsigned bal = __ballot_sync(kFull, valid);
-    if (valid)
-      keys[n + __popc(bal & lt_mask)] =
-          (static_cast<uint64_t>(static_cast<uint32_t>(seq0_i + e * BS)) << 16) | (1u << i);
-    n += __popc(bal);
-  }
-  int N = 32;
-  while (N < n) N <<= 1;
-  for (int idx = n + lane; idx < N; idx += 32) keys[idx] = ~0ull;
-  __syncwarp();
-  for (int k = 2; k <= N; k <<= 1) {
-    for (int jj = k >> 1; jj > 0; jj >>= 1) {
-      for (int idx = lane; idx < N; idx += 32) {
-        const int ixj = idx ^ jj;
-        if (ixj > idx) {
-          const uint64_t a = keys[idx], b = keys[ixj];
-          if ((a > b) == ((idx & k) == 0)) {
-            keys[idx] = b;
-            keys[ixj] = a;
-          }
-        }
+    if (use_map) {
+      if (valid) {
+        atomicOr(&bmap[e], 1u << i);
+        emax = max(emax, e);
       }
-      __syncwarp();
+    } else {
+      const unsigned bal = __ballot_sync(kFull, valid);
+      if (valid)
+        keys[n + __popc(bal & lt_mask)] =
+            (static_cast<uint64_t>(static_cast<uint32_t>(seq0_i + e * BS)) << 16) | (1u << i);
+      n += __popc(bal);
     }
   }
   int nu = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int idx = base + lane;
-    bool head = false;
-    uint32_t x = 0;
-    unsigned bits = 0;
-    if (idx < n) {
-      const uint64_t key = keys[idx];
-      x = static_cast<uint32_t>(key >> 16);
-      head = idx == 0 || static_cast<uint32_t>(keys[idx - 1] >> 16) != x;
-      if (head) {
-        bits = static_cast<unsigned>(key & 0xFFFFu);
-        for (int u = idx + 1; u < n; ++u) {
-          const uint64_t k2 = keys[u];
-          if (static_cast<uint32_t>(k2 >> 16) != x) break;
-          bits |= static_cast<unsigned>(k2 & 0xFFFFu);
+  if (use_map) {
+    __syncwarp();
+    const int nscan = __reduce_max_sync(kFull, emax) + 1;
+    for (int base = 0; base < nscan; base += 32) {
+      const int idx = base + lane;
+      const uint32_t bits = idx < nscan ? bmap[idx] : 0u;
+      const unsigned bal = __ballot_sync(kFull, bits != 0u);
+      if (bits != 0u) {
+        const int pos = nu + __popc(bal & lt_mask);
+        it.ux[pos] = map_seq0 + idx * BS;
+        it.ubits[pos] = static_cast<unsigned short>(bits);
+      }
+      nu += __popc(bal);
+    }
+  } else {
+    int N = 32;
+    while (N < n) N <<= 1;
+    for (int idx = n + lane; idx < N; idx += 32) keys[idx] = ~0ull;
+    __syncwarp();
+    for (int k = 2; k <= N; k <<= 1) {
+      for (int jj = k >> 1; jj > 0; jj >>= 1) {
+        for (int idx = lane; idx < N; idx += 32) {
+          const int ixj = idx ^ jj;
+          if (ixj > idx) {
+            const uint64_t a = keys[idx], b = keys[ixj];
+            if ((a > b) == ((idx & k) == 0)) {
+              keys[idx] = b;
+              keys[ixj] = a;
+            }
+          }
         }
+        __syncwarp();
       }
     }
-    const unsigned bal = __ballot_sync(kFull, head);
-    if (head) {
-      const int pos = nu + __popc(bal & lt_mask);
-      it.ux[pos] = static_cast<int>(x);
-      it.ubits[pos] = static_cast<unsigned short>(bits);
+    for (int base = 0; base < n; base += 32) {
+      const int idx = base + lane;
+      bool head = false;
+      uint32_t x = 0;
+      unsigned bits = 0;
+      if (idx < n) {
+        const uint64_t key = keys[idx];
+        x = static_cast<uint32_t>(key >> 16);
+        head = idx == 0 || static_cast<uint32_t>(keys[idx - 1] >> 16) != x;
+        if (head) {
+          bits = static_cast<unsigned>(key & 0xFFFFu);
+          for (int u = idx + 1; u < n; ++u) {
+            const uint64_t k2 = keys[u];
+            if (static_cast<uint32_t>(k2 >> 16) != x) break;
+            bits |= static_cast<unsigned>(k2 & 0xFFFFu);
+          }
+        }
+      }
+      const unsigned bal = __ballot_sync(kFull, head);
+      if (head) {
+        const int pos = nu + __popc(bal & lt_mask);
+        it.ux[pos] = static_cast<int>(x);
+        it.ubits[pos] = static_cast<unsigned short>(bits);
+      }
+      nu += __popc(bal);
     }
-    nu += __popc(bal);
   }
   if (lane < kMaxNT) it.limit[lane] = limit;
   const unsigned tv_bits = __ballot_sync(kFull, tv);
