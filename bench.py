@@ -614,12 +614,22 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
     ms = sum(t) / len(t)
     log(f"varlen nsa {ms:.4f} ms")
     terms, t_roof = t_roof_terms(flops, hbm, peaks, gather, bw_l2)
+    # the union walk's own floor: its executed MMA work at the tensor peak, or the K/V of
+    # its union tiles at the L2 read bandwidth (as for the headline)
+    vt = union_tiles(w)
+    v_exec = 4.0 * 128 * 64 * w.q.shape[3] * vt
+    v_floor_us = max(v_exec / (peaks["bf16_tflops"] * 1e12),
+                     vt * 64.0 * w.q.shape[3] * 2 * 2 / (bw_l2 * 1e9)) * 1e6
     rows["nsa_select_varlen"] = {
         "workload": w.name, "ms": round(ms, 4), "TFLOP/s": round(flops / ms / 1e9, 2),
         "frac_tensor": round(flops / ms / 1e9 / peaks["bf16_tflops"], 4),
+        "union_tiles": vt, "executed_mma_frac": round(v_exec / ms / 1e9 / peaks["bf16_tflops"], 4),
+        "exec_floor_us": round(v_floor_us, 2), "frac_exec_floor": round(v_floor_us / (ms * 1e3), 4),
         "hbm_GB/s": round(hbm / ms / 1e6, 1), "gather_GB/s": round(gather / ms / 1e6, 1),
         "terms_us": terms, "t_roof_us": round(t_roof, 2),
-        "frac_t_roof": round(t_roof / (ms * 1e3), 4)}
+        "frac_t_roof": round(t_roof / (ms * 1e3), 4),
+        "t_roof_note": "l2_gather term = per-token gather of every selected block, which the "
+                       "union walk does not pay; frac_exec_floor is the kernel's own floor"}
     del w
     torch.cuda.empty_cache()
 
