@@ -508,16 +508,36 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           for (int j = 0; j < kKT; ++j)
             if (!(!none && key0 + j >= kmin && key0 + j <= kmax)) x[j] = -INFINITY;
         } else if (!full) {
+          // A tile whose keys have consecutive positions p0, p0 + 1, ... and one segment
+          // s0 (the causal diagonal, a window edge inside a document) admits for this row
+          // exactly the key indices j in [kmin - p0, kmax - p0] when s0 is the row's
+          // segment: an interval test per key, no per-key loads.  Other tiles test every
+          // key's position and segment.
+          const int p0 = ps[0], s0 = ps[kKT];
+          const bool shape = (long long)ps[lane] == (long long)p0 + lane &&
+                             (long long)ps[32 + lane] == (long long)p0 + 32 + lane &&
+                             ps[kKT + lane] == s0 && ps[kKT + 32 + lane] == s0;
+          if (__all_sync(0xffffffffu, shape)) {
+            int jlo = 0, jhi = -1;  // empty unless the row attends some of the tile
+            if (!none && s0 == qs) {
+              jlo = static_cast<int>(min(max((long long)kmin - p0, 0LL), (long long)kKT));
+              jhi = static_cast<int>(max(min((long long)kmax - p0, (long long)kKT - 1), -1LL));
+            }
 #pragma unroll
-          for (int j = 0; j < kKT; j += 4) {
-            const int4 kp4 = *reinterpret_cast<const int4*>(ps + j);
-            const int4 ks4 = *reinterpret_cast<const int4*>(ps + kKT + j);
-            const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
-            const int ksg[4] = {ks4.x, ks4.y, ks4.z, ks4.w};
+            for (int j = 0; j < kKT; ++j)
+              if (j < jlo || j > jhi) x[j] = -INFINITY;
+          } else {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const bool ok_k = !none && ksg[u] == qs && kp[u] >= kmin && kp[u] <= kmax;
-              if (!ok_k) x[j + u] = -INFINITY;
+            for (int j = 0; j < kKT; j += 4) {
+              const int4 kp4 = *reinterpret_cast<const int4*>(ps + j);
+              const int4 ks4 = *reinterpret_cast<const int4*>(ps + kKT + j);
+              const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
+              const int ksg[4] = {ks4.x, ks4.y, ks4.z, ks4.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const bool ok_k = !none && ksg[u] == qs && kp[u] >= kmin && kp[u] <= kmax;
+                if (!ok_k) x[j + u] = -INFINITY;
+              }
             }
           }
         }
