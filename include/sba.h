@@ -277,6 +277,8 @@ SBA_API int sba_sparse_mask_dkdv_bounds(const int32_t* q_pos, const int32_t* q_s
  *  lower, upper, lower_full, upper_full [B, 1, T / q_block] int32 (as produced by
  *  sba_sparse_mask_bounds with the same block sizes)
  *  out [B, T, Hq, D] bf16 (written); lse [B, T, Hq] float32 (written) or NULL.
+ * q, k, v, out, q_pos, q_seg, kv_pos and kv_seg must be 16-byte aligned (the kernel
+ * copies them with TMA / bulk copies); SBA_ERR_INVALID_ARG otherwise.
  * Supported: q_block == 128, kv_block in {64, 128}, T % 128 == 0, D in {64, 128},
  * 1 <= Hq / Hkv, bf16 only.
  */

@@ -454,8 +454,8 @@ int sba_blocksparse_attn_fwd(const void* q, const void* k, const void* v, const 
   SBA_REQUIRE(B >= 1 && T >= 1 && Hq >= 1 && Hkv >= 1 && Hq % Hkv == 0, "bad head/size arguments");
   SBA_REQUIRE(window_left >= -1 && window_right >= -1, "windows must be >= -1");
   SBA_REQUIRE(aligned16(q) && aligned16(k) && aligned16(v) && aligned16(out) &&
-                  aligned16(kv_pos) && aligned16(kv_seg),
-              "q, k, v, out, kv_pos and kv_seg must be 16-byte aligned");
+                  aligned16(q_pos) && aligned16(q_seg) && aligned16(kv_pos) && aligned16(kv_seg),
+              "q, k, v, out, q_pos, q_seg, kv_pos and kv_seg must be 16-byte aligned");
   SBA_REQUIRE(std::isfinite(softmax_scale), "softmax_scale must be finite");
   SBA_SUPPORT(q_block == 128, "q_block must be 128");
   SBA_SUPPORT(kv_block == 64 || kv_block == 128, "kv_block must be 64 or 128");

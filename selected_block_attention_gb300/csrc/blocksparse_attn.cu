@@ -58,6 +58,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct Item {
+  int qpos[kM];              // positions / segment ids of the query block's rows (copied in
+  int qseg[kM];              // by the loader with the item; SparseMask mode)
   int b, hkv, qblk, h0, nh;  // heads h0 .. h0 + nh - 1 (nh = 1 or 2)
   int tlo, tup, tlof, tupf;  // key tiles [tlo, tup); [tlof, tupf) need no token mask
   int n_tiles;               // = tup - tlo
@@ -266,7 +268,15 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         it.tlo = tlo; it.tup = tup; it.tlof = tlof; it.tupf = tupf;
         it.n_tiles = nt;
         it.start = start; it.end = end;
-        mbar_arrive(&item_full[islot]);
+        if (!kRagged && nt > 0) {
+          // the rows' positions and segment ids ride on the item barrier
+          const long long row0 = (long long)b * p.q_rows + qblk * kM;
+          bulk_load(it.qpos, p.q_pos + row0, kM * 4, &item_full[islot]);
+          bulk_load(it.qseg, p.q_seg + row0, kM * 4, &item_full[islot]);
+          mbar_arrive_expect_tx(&item_full[islot], 2 * kM * 4);
+        } else {
+          mbar_arrive(&item_full[islot]);
+        }
       }
       __syncwarp();
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
@@ -434,7 +444,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     uint32_t pvl_ph = 0u;
     for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
       if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
-      const Item it = item_at(islot);
+      const Item& it = item_at(islot);  // valid until this warp releases the slot
       const int nt = it.n_tiles;
       const bool mine = w < it.nh;
       const long long tok = (long long)it.b * p.q_rows + it.qblk * kM + r;
@@ -467,8 +477,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (p.window_right >= 0) khi = min(khi, qpos + p.window_right);
         if (!row_ok) { klo = 1; khi = 0; }
       } else {
-        const int qp = p.q_pos[tok];
-        qs = p.q_seg[tok];
+        const int qp = it.qpos[r];
+        qs = it.qseg[r];
         // key positions this row may attend (causal and inclusive window, exact in 64
         // bits, then clamped to the int32 range of the positions); padding sees none
         if (p.causal) khi = min(khi, (long long)qp);
