@@ -89,16 +89,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Issue the cp.async copies of one 16-key K/V tile of KV head h (keys clamped into
-// the cache so no copy leaves the tensor; clamped rows are masked later).
+// Issue the cp.async copies of one 16-key K/V tile of KV head h.  Keys are clamped into
+// the row's own range [start, end) (end > start), so no copy reads a cache slot the row
+// does not own (never written, possibly NaN: its V row would reach P V, where 0 * NaN is
+// NaN); the clamped duplicates are masked later.
 __device__ __forceinline__ void load_tile(const __nv_bfloat16* k, const __nv_bfloat16* v, int S,
-                                          int Hkv, int b, int h, int key0, uint32_t k_dst,
-                                          uint32_t v_dst, int lane) {
+                                          int Hkv, int b, int h, int key0, int start, int end,
+                                          uint32_t k_dst, uint32_t v_dst, int lane) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int u = lane + 32 * i;  // 256 chunks of 16 bytes per tensor
     const int key = u >> 4, part = u & 15;
-    const int kk = min(max(key0 + key, 0), S - 1);
+    const int kk = min(max(key0 + key, start), end - 1);
     const long long row = ((long long)b * S + kk) * Hkv + h;
     const uint32_t off = key * kRowBytes + part * 16;
     cp_async16(k_dst + off, k + row * kD + part * 8);
@@ -248,12 +250,13 @@ ragged_mq_split_kernel(const MqParams p) {
   auto v_stage = [&](int st) { return wbase + st * 2 * kTileBytes + kTileBytes; };
   auto tile_key0 = [&](int t) { return t < 0 ? 0 : key_lo + t * kTileKeys; };
   // Copies of one tile: lane copies 16-byte part (lane & 15) of keys 2 i + (lane >> 4).
-  // Tiles inside the cache step one pointer; the rare edge tile clamps key by key.
+  // Tiles inside the row's range [start, end) step one pointer; the rare edge tile clamps
+  // key by key into that range.
   const long long key_stride = (long long)p.Hkv * kD;
   const long long lane_off = ((long long)b * p.S * p.Hkv + h) * kD + (lane & 15) * 8;
   const uint32_t lane_dst = (lane >> 4) * kRowBytes + (lane & 15) * 16;
   auto issue_tile = [&](int key0, uint32_t k_dst, uint32_t v_dst) {
-    if (key0 >= 0 && key0 + kTileKeys <= p.S) {
+    if (key0 >= R.start && key0 + kTileKeys <= R.end) {
       const long long off = lane_off + (long long)(key0 + (lane >> 4)) * key_stride;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -261,7 +264,7 @@ ragged_mq_split_kernel(const MqParams p) {
         cp_async16(v_dst + lane_dst + 2 * i * kRowBytes, p.v + off + 2 * i * key_stride);
       }
     } else {
-      load_tile(p.k, p.v, p.S, p.Hkv, b, h, key0, k_dst, v_dst, lane);
+      load_tile(p.k, p.v, p.S, p.Hkv, b, h, key0, R.start, R.end, k_dst, v_dst, lane);
     }
   };
   // Logits in log2 units: s * scale * log2(e), or with the cap

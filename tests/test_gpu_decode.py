@@ -95,3 +95,23 @@ def test_long_rows_beyond_the_parallel_combine(sba):
     w = workloads.decode(device=DEV, B=2, Hq=8, Hkv=2, S=200_000, window=(-1, -1), cap=0.0,
                          num_sinks=2, ends=ends, seed=403)
     assert_attention_close(*_run(sba, w), what="decode long rows")
+
+
+@pytest.mark.parametrize("cap,sinks", [(0.0, 0), (50.0, 4)])
+def test_unowned_cache_slots_do_not_leak(sba, cap, sinks):
+    """Cache slots outside a row's [start, end) belong to nobody (never written, here
+    NaN).  Keys there are masked out of the softmax, and their values must not reach the
+    output either: rows shorter than one 64-key stage, ranges that start mid-cache, ends
+    just past a stage boundary, and a cache of fewer than 64 slots per row."""
+    for S, ends, starts in [(700, [1, 5, 63, 64, 65, 129, 700, 300], [0, 3, 0, 10, 60, 100, 650, 0]),
+                            (40, [1, 17, 40, 39], [0, 2, 30, 0])]:
+        w = workloads.decode(device=DEV, B=len(ends), Hq=8, Hkv=2, S=S, window=(100, 0),
+                             cap=cap, num_sinks=sinks, ends=ends, seed=404)
+        w.sequence_start = torch.as_tensor(starts, dtype=torch.int32, device=DEV)
+        for b, (st, en) in enumerate(zip(starts, ends)):
+            for t in (w.k, w.v):
+                t[b, :st] = float("nan")
+                t[b, en:] = float("nan")
+        got, ref, gl, rl = _run(sba, w)
+        assert np.isfinite(got).all(), f"S={S}: NaN from unowned cache slots"
+        assert_attention_close(got, ref, gl, rl, what=f"unowned slots S={S} cap={cap} sinks={sinks}")
