@@ -717,7 +717,7 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
     rows["ragged_decode"] = {
         "workload": w.name, "us": round(ms * 1e3, 2), "tok/s": round(w.q.shape[0] / (ms * 1e-3), 1),
         "GB/s": round(nbytes / ms / 1e6, 1), "frac_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
-        "kernels_per_call": 1, "memsets_per_call": 1}
+        "kernels_per_call": 2, "memsets_per_call": 0}
     del w
     torch.cuda.empty_cache()
 
@@ -745,7 +745,7 @@ def measure_rows(sba, dev, stream, flush, peaks, args, bw_l2):
             "frac_hbm": round(nbytes / ms / 1e6 / peaks["hbm_gbs"], 4),
             "TFLOP/s": round(mfl / ms / 1e9, 2),
             "frac_tensor": round(mfl / ms / 1e9 / peaks["bf16_tflops"], 4),
-            "kernels_per_call": 1, "memsets_per_call": 1 if w.q.shape[1] < 128 else 0}
+            "kernels_per_call": 2 if w.q.shape[1] < 128 else 1, "memsets_per_call": 0}
         del w, ws, out
         torch.cuda.empty_cache()
     sba.check_error(dev)

@@ -24,9 +24,10 @@
 // with its own row's window.  Sink keys outside [lo, hi) go through an extra sink tile
 // of split 0.  The four warps merge through shared memory and write one fp32 partial
 // (o * exp(-m), m, l) per (row, split, query, head).  The CTA that completes the last
-// split of a row tile (a counter per tile in the workspace, cleared before the launch)
-// merges the tile's partials with max / exp weights and writes the bf16 output and the
-// natural-log LSE, so one launch does the whole call.
+// split of a row tile (a counter per tile in the workspace, cleared by a small kernel
+// launched just before, which the split kernel overlaps and waits for only at its first
+// counter use) merges the tile's partials with max / exp weights and writes the bf16
+// output and the natural-log LSE.
 #include <cuda_bf16.h>
 
 #include <climits>
@@ -501,6 +502,9 @@ ragged_mq_split_kernel(const MqParams p) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int* cnt = p.tile_count + ((long long)b * p.Hkv + h) * p.row_tiles + rt;
+    // the counters were cleared by the launch before this one, which may still be running
+    // (programmatic dependent launch): wait for it to finish before the first use
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int done = atomicAdd(cnt, 1) + 1;
     s_last = done == R.n_split;
     if (s_last) *cnt = 0;  // every split has counted: ready for the next call
@@ -582,6 +586,15 @@ ragged_mq_split_kernel(const MqParams p) {
 
 }  // namespace
 
+// Clears the split counters of a call.  It lets the split kernel launch at once
+// (programmatic dependent launch): that kernel waits for this one only where it first
+// touches a counter, after its loads and arithmetic.
+__global__ void clear_counters_kernel(int* cnt, long long n) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (long long i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
+    cnt[i] = 0;
+}
+
 unsigned read_and_clear_error_decode(cudaStream_t, std::string*) {
   unsigned w = 0, zero = 0;
   cudaMemcpyFromSymbol(&w, g_err_decode, sizeof(w));
@@ -603,7 +616,7 @@ static int mq_max_splits(int Qn, int S, int window_left, int window_right) {
 }
 
 // Workspace: fp32 partials o [B][splits][Q][Hq][D] and (m, l) [..][2], then the row
-// tiles' split counters [B][Hkv][row_tiles], cleared on the stream before each launch.
+// tiles' split counters [B][Hkv][row_tiles], cleared on the stream by each call.
 static size_t mq_partials_bytes(int B, int Qn, int Hq, int S, int window_left, int window_right) {
   const size_t splits = mq_max_splits(Qn, S, window_left, window_right);
   return ((size_t)B * splits * Qn * Hq * (kD + 2) * sizeof(float) + 255) & ~static_cast<size_t>(255);
@@ -663,14 +676,26 @@ int launch_ragged_mq(const void* q, const void* k, const void* v, const int32_t*
     if (e != cudaSuccess) return cuda_error(e, "ragged attention: set smem attribute");
     attr_done = true;
   }
-  cudaError_t e = cudaMemsetAsync(p.tile_count, 0, (size_t)B * Hkv * p.row_tiles * sizeof(int), stream);
+  const long long n_cnt = (long long)B * Hkv * p.row_tiles;
+  clear_counters_kernel<<<(int)std::min<long long>((n_cnt + 255) / 256, 64), 256, 0, stream>>>(p.tile_count, n_cnt);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "ragged attention: clear split counters");
   dim3 grid(p.max_splits, Hkv, B * p.row_tiles);
   const bool hi_rows = Qn * p.G > 8, capped = p.cap > 0.f;
   auto kernel = hi_rows ? (capped ? ragged_mq_split_kernel<true, true> : ragged_mq_split_kernel<true, false>)
                         : (capped ? ragged_mq_split_kernel<false, true> : ragged_mq_split_kernel<false, false>);
-  kernel<<<grid, kWarps * 32, kSmemBytes, stream>>>(p);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_error(e, "ragged attention split launch");
   return SBA_OK;
 }
@@ -758,7 +783,7 @@ extern "C" SBA_API int sba_ragged_decode_fwd_noalloc(
   const int rc = scratch_for_current_device(&scratch);
   if (rc != SBA_OK) return rc;
   // The partials need no initialisation: every slot the combining CTA reads is written
-  // by the same call, and the call clears the split counters itself (a memset on the
+  // by the same call, and the call clears the split counters itself (a kernel on the
   // stream, no allocation).
   return sba_ragged_decode_fwd(q, k, v, seq_start, seq_end, B, Hq, Hkv, S, D, softmax_scale,
                                window_left, window_right, logits_soft_cap, sink_bias, num_sinks,
