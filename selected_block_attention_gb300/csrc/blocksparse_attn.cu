@@ -13,15 +13,18 @@
 //   warp 0      loader: publishes the item (its tile range and full-tile range), then TMA
 //               loads Q of each head into its own buffer and, per key tile, K into a K
 //               ring and V plus the tile's key positions / segment ids into a V ring;
-//   warps 1, 2  one MMA-issuing thread per head slot w: S_w = Q_w K^T (both operands in
-//               shared memory, N = 64 keys) into one of two S buffers of the head, and
-//               O_w += P_w V (P_w read from tensor memory over the S buffer it replaced),
-//               in the order S(0) S(1) | PV(t) S(t + 2) | ...; so the scores of tile t + 1
-//               are ready while the softmax still works on tile t, and each thread's
-//               barrier waits overlap the other head's MMAs;
+//   warps 1, 2  one MMA-issuing warp per head slot w (converged; an elected lane
+//               issues): S_w = Q_w K^T (both operands in shared memory, N = 64 keys) into
+//               one of two S buffers of the head, and O_w += P_w V (P_w read from tensor
+//               memory over the S buffer it replaced), in the order S(0) S(1) | PV(t)
+//               S(t + 2) | ...; so the scores of tile t + 1 are ready while the softmax
+//               still works on tile t, and each warp's barrier waits overlap the other
+//               head's MMAs;
 //   warps 4..7  softmax of head slot 0, warps 8..11 of head slot 1: one thread per query
 //               row; the row's 64 scores of a tile come out of tensor memory in one pass
-//               into registers, are masked outside the full tile range, and P (bf16) is
+//               into registers, are masked outside the full tile range (an exact per-row
+//               key interval when the tile's keys are consecutive positions of one
+//               segment, else a test per key), and P (bf16) is
 //               written in place over the tile's S buffer; lazy online softmax (O_w
 //               rescaled only when the row maximum grows by > 2^8, after the previous
 //               tile's PV has landed); epilogue: O_w leaves tensor memory at once (the
