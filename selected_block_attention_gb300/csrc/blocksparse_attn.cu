@@ -144,6 +144,21 @@ __device__ __forceinline__ void decode_item(const Params& p, int item, int& b, i
   nh = min(2, p.G - 2 * pair);
 }
 
+// Scores of a tile outside the column interval [jlo, jhi] set to -inf, the interval held
+// as keep bits in two 32-bit words: per score one bit test against a constant and one
+// select (a compare of the column against both ends per score costs several times more).
+__device__ __forceinline__ void mask_interval(float (&x)[kKT], int jlo, int jhi) {
+  static_assert(kKT == 64, "two 32-bit keep words");
+  const uint32_t w0 = (jlo <= 31 && jhi >= 0)
+      ? ((jhi >= 31 ? 0xffffffffu : ((2u << jhi) - 1u)) & (0xffffffffu << min(max(jlo, 0), 31))) : 0u;
+  const uint32_t w1 = (jhi >= 32 && jlo <= 63)
+      ? ((jhi >= 63 ? 0xffffffffu : ((2u << (jhi - 32)) - 1u)) & (0xffffffffu << max(jlo - 32, 0))) : 0u;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[j] = (w0 & (1u << j)) ? x[j] : -INFINITY;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) x[32 + j] = (w1 & (1u << j)) ? x[32 + j] : -INFINITY;
+}
+
 // kRagged: the ragged multi-query form of the same computation (queries are the last Q
 // tokens of [start, end) of a KV cache, each with its own inclusive window); the key
 // range and the full tiles of a query block follow from start, end and the window, and
@@ -516,10 +531,15 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 #pragma unroll
         for (int j = 0; j < kKT; ++j) tmem_ld_ready(x[j]);
         if (!full && kRagged) {
-          const int key0 = ti * kKT;  // key index of column 0
-#pragma unroll
-          for (int j = 0; j < kKT; ++j)
-            if (!(!none && key0 + j >= kmin && key0 + j <= kmax)) x[j] = -INFINITY;
+          // the row's keys [kmin, kmax] as columns of this tile (key index of column 0:
+          // ti * 64)
+          const long long key0 = (long long)ti * kKT;
+          int jlo = 0, jhi = -1;
+          if (!none) {
+            jlo = static_cast<int>(min(max((long long)kmin - key0, 0LL), (long long)kKT));
+            jhi = static_cast<int>(max(min((long long)kmax - key0, (long long)kKT - 1), -1LL));
+          }
+          mask_interval(x, jlo, jhi);
         } else if (!full) {
           // A tile whose keys have consecutive positions p0, p0 + 1, ... and one segment
           // s0 (the causal diagonal, a window edge inside a document) admits for this row
@@ -536,9 +556,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
               jlo = static_cast<int>(min(max((long long)kmin - p0, 0LL), (long long)kKT));
               jhi = static_cast<int>(max(min((long long)kmax - p0, (long long)kKT - 1), -1LL));
             }
-#pragma unroll
-            for (int j = 0; j < kKT; ++j)
-              if (j < jlo || j > jhi) x[j] = -INFINITY;
+            mask_interval(x, jlo, jhi);
           } else {
 #pragma unroll
             for (int j = 0; j < kKT; j += 4) {
