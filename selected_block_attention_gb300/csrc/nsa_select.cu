@@ -698,14 +698,22 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         float m_new = m, alpha = 1.f, psum = 0.f;
         uint32_t pk[kTileKeys / 2];
         if (any) {
-          // masked raw scores (keys of a segment past its valid count)
+          // masked raw scores (keys of a segment past its valid count), the valid keys as
+          // keep bits in two 32-bit words: one bit test and one select per score
+          static_assert(kTileKeys == 64 && (C::kSegLen == 32 || C::kSegLen == 64), "keep words");
+          uint32_t kw[2];
+          if constexpr (C::kSegLen == 64) {
+            kw[0] = nv[0] >= 32 ? 0xffffffffu : (1u << nv[0]) - 1u;
+            kw[1] = nv[0] >= 64 ? 0xffffffffu : (nv[0] > 32 ? (1u << (nv[0] - 32)) - 1u : 0u);
+          } else {
 #pragma unroll
-          for (int e = 0; e < C::kSegs; ++e) {
-            if (nv[e] < C::kSegLen) {
+            for (int e = 0; e < 2; ++e) kw[e] = nv[e] >= 32 ? 0xffffffffu : (1u << nv[e]) - 1u;
+          }
+          if (!__all_sync(0xffffffffu, (kw[0] & kw[1]) == 0xffffffffu)) {
 #pragma unroll
-              for (int jj = 0; jj < C::kSegLen; ++jj)
-                if (jj >= nv[e]) x[e * C::kSegLen + jj] = -INFINITY;
-            }
+            for (int j = 0; j < 32; ++j) x[j] = (kw[0] & (1u << j)) ? x[j] : -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[32 + j] = (kw[1] & (1u << j)) ? x[32 + j] : -INFINITY;
           }
           // maximum: eight chains of three-input max; chain u takes the keys u, u + 8, ...
           float mx[8];
