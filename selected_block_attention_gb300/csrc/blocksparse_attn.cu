@@ -106,18 +106,21 @@ struct Cfg {
   static constexpr int kPosSegBytes = 2 * kKT * 4;
   static constexpr int kVStageBytes = (kTBytes + kPosSegBytes + 1023) & ~1023;
   static constexpr int kItemBytes = (static_cast<int>(sizeof(Item)) + 15) & ~15;
-  static constexpr int kStages = 3;                        // K and V rings
-  // output staging: per softmax warp 16 rows x D bf16 (one 128-byte swizzled panel per
-  // 64 columns), stored to global memory by TMA
+  static constexpr int kStages = 3;                        // V ring (V + key positions / segments)
+  static constexpr int kStagesK = 2;                       // K ring (a K stage is free once both S MMAs read it)
+  // output staging: per softmax warp two halves of 16 rows x D bf16 (one 128-byte
+  // swizzled panel per 64 columns each), stored to global memory by TMA; the second half
+  // does not wait for the first half's store to leave shared memory
   static constexpr int kStgPanelBytes = 16 * 128;
-  static constexpr int kStgWarpBytes = kPanels * kStgPanelBytes;
+  static constexpr int kStgHalfBytes = kPanels * kStgPanelBytes;
+  static constexpr int kStgWarpBytes = 2 * kStgHalfBytes;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = 2 * kQBytes;
-  static constexpr int kOffV = kOffK + kStages * kTBytes;
+  static constexpr int kOffV = kOffK + kStagesK * kTBytes;
   static constexpr int kOffStage = kOffV + kStages * kVStageBytes;
   static constexpr int kOffItems = kOffStage + 8 * kStgWarpBytes;
   static constexpr int kOffBars = (kOffItems + kItemSlots * kItemBytes + 7) & ~7;
-  static constexpr int kNumBars = 2 * kItemSlots + 4 + 4 * kStages + 4 + 4 + 2 + 2 + 2 + 2;
+  static constexpr int kNumBars = 2 * kItemSlots + 4 + 2 * kStagesK + 2 * kStages + 4 + 4 + 2 + 2 + 2 + 2;
   static constexpr int kOffMisc = ((kOffBars + kNumBars * 8) + 15) & ~15;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   // tensor memory columns: S_w,buf at (2 w + buf) * kKT (P aliased), O_w at kOCol + w * D
@@ -177,8 +180,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   uint64_t* item_empty = bb;  bb += kItemSlots;
   uint64_t* q_full = bb;      bb += 2;   // per head slot
   uint64_t* q_empty = bb;     bb += 2;
-  uint64_t* k_full = bb;      bb += C::kStages;
-  uint64_t* k_empty = bb;     bb += C::kStages;
+  uint64_t* k_full = bb;      bb += C::kStagesK;
+  uint64_t* k_empty = bb;     bb += C::kStagesK;
   uint64_t* v_full = bb;      bb += C::kStages;
   uint64_t* v_empty = bb;     bb += C::kStages;
   uint64_t* s_full = bb;      bb += 4;   // [2 w + buf]: S_w of the buffer written
@@ -205,10 +208,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       mbar_init(&o_empty[w], 4); mbar_init(&mma_done[w], 1);
     }
     for (int i = 0; i < 4; ++i) { mbar_init(&s_full[i], 1); mbar_init(&p_full[i], 4); }
-    for (int i = 0; i < C::kStages; ++i) {
-      mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 2);
-      mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 2);
-    }
+    for (int i = 0; i < C::kStagesK; ++i) { mbar_init(&k_full[i], 1); mbar_init(&k_empty[i], 2); }
+    for (int i = 0; i < C::kStages; ++i) { mbar_init(&v_full[i], 1); mbar_init(&v_empty[i], 2); }
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -235,10 +236,11 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     uint32_t q_last[2] = {0u, 0u};
     int ks = 0; uint32_t kphase = 0;
     int vs = 0; uint32_t vphase = 0;
-    bool k_issued[C::kStages], v_issued[C::kStages];
-    uint32_t k_last[C::kStages], v_last[C::kStages];
+    bool k_issued[C::kStagesK], v_issued[C::kStages];
+    uint32_t k_last[C::kStagesK], v_last[C::kStages];
 #pragma unroll
-    for (int i = 0; i < C::kStages; ++i) { k_issued[i] = v_issued[i] = false; k_last[i] = v_last[i] = 0; }
+    for (int i = 0; i < C::kStagesK; ++i) { k_issued[i] = false; k_last[i] = 0; }
+    for (int i = 0; i < C::kStages; ++i) { v_issued[i] = false; v_last[i] = 0; }
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       int b, hkv, qblk, h0, nh;
@@ -325,7 +327,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         }
         k_issued[ks] = true;
         k_last[ks] = kphase;
-        if (++ks == C::kStages) { ks = 0; kphase ^= 1; }
+        if (++ks == C::kStagesK) { ks = 0; kphase ^= 1; }
         if (!warp_wait(&v_empty[vs], vphase ^ 1, ab, kRoleLoader, kBarVEmpty, item)) { ok = false; break; }
         if (lane == 0) {
           uint8_t* vdst = smem + C::kOffV + vs * C::kVStageBytes;
@@ -345,10 +347,10 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     }
     // Drain: wait (bounded) for every copy this warp issued before the CTA exits.
     if (lane == 0) {
-      for (int s = 0; s < C::kStages; ++s) {
+      for (int s = 0; s < C::kStagesK; ++s)
         if (k_issued[s]) drain_wait(&k_full[s], k_last[s]);
+      for (int s = 0; s < C::kStages; ++s)
         if (v_issued[s]) drain_wait(&v_full[s], v_last[s]);
-      }
       for (int w = 0; w < 2; ++w)
         if (q_issued[w]) drain_wait(&q_full[w], q_last[w]);
     }
@@ -373,7 +375,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       auto kstep = [](int kk, int panel_bytes) -> uint64_t {
         return static_cast<uint64_t>(((kk / 4) * panel_bytes + (kk % 4) * 32) >> 4);
       };
-      auto next_k = [&]() { if (++ks == C::kStages) { ks = 0; kphase ^= 1; } };
+      auto next_k = [&]() { if (++ks == C::kStagesK) { ks = 0; kphase ^= 1; } };
       auto next_v = [&]() { if (++vs == C::kStages) { vs = 0; vphase ^= 1; } };
       // S_w,buf = Q_w K^T of the next K tile, then release the K stage
       auto issue_s = [&](int buf, int item) -> bool {
@@ -675,7 +677,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kStgWarpBytes;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        if (lane == 0) bulk_wait_group_read<0>();  // the staging rows are free again
+        // both halves' staging rows are free once the previous item's stores have read them
+        if (half == 0 && lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
         if ((lane >> 4) == half) {
           const int rr = lane & 15;
@@ -684,7 +687,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
               const uint32_t* src = wv + pn * 32 + c8 * 4;
-              *reinterpret_cast<uint4*>(stg + pn * C::kStgPanelBytes + rr * 128 + ((c8 ^ (rr & 7)) * 16)) =
+              *reinterpret_cast<uint4*>(stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes + rr * 128 +
+                                        ((c8 ^ (rr & 7)) * 16)) =
                   make_uint4(src[0], src[1], src[2], src[3]);
             }
           }
@@ -694,7 +698,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         if (lane == 0) {
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_store_4d(&tm_o, stg + pn * C::kStgPanelBytes, pn * 64, hq, it.qblk * kM + q4 * 32 + half * 16,
+            tma_store_4d(&tm_o, stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes, pn * 64, hq, it.qblk * kM + q4 * 32 + half * 16,
                          it.b);
           bulk_commit_group();
         }
