@@ -36,6 +36,7 @@
 
 #include <climits>
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -44,6 +45,11 @@
 namespace sba {
 
 static __device__ DevError g_err_bsa = {0u, 0u, 0};
+// Item counters of the launches: [next item, CTAs done] per slot; launches take the slots
+// in turn, so up to kSchedSlots launches (on any streams) may run at once.  Each launch
+// finds its slot zero and leaves it zero.
+constexpr int kSchedSlots = 64;
+static __device__ int g_bsa_sched[2 * kSchedSlots];
 
 namespace {
 
@@ -65,8 +71,9 @@ struct Item {
   int qseg[kM];              // by the loader with the item; SparseMask mode)
   int b, hkv, qblk, h0, nh;  // heads h0 .. h0 + nh - 1 (nh = 1 or 2)
   int tlo, tup, tlof, tupf;  // key tiles [tlo, tup); [tlof, tupf) need no token mask
-  int n_tiles;               // = tup - tlo
+  int n_tiles;               // = tup - tlo; -1: no more items (the loader's last publication)
   int start, end;            // ragged mode: the row's key range
+  int idx;                   // item index (for error reports)
 };
 
 struct Params {
@@ -88,6 +95,7 @@ struct Params {
   float scale_log2;
   int n_pairs, n_items;
   long long wait_limit;  // cycles a bounded wait may take
+  int* sched;            // [next item, CTAs done] of this launch (zero at launch, left zero)
 };
 
 enum Role : unsigned { kRoleLoader = 1, kRoleMma = 2, kRoleSoftmax = 3 };
@@ -242,7 +250,23 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     for (int i = 0; i < C::kStagesK; ++i) { k_issued[i] = false; k_last[i] = 0; }
     for (int i = 0; i < C::kStages; ++i) { v_issued[i] = false; v_last[i] = 0; }
     bool ok = true;
-    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+    // Items are handed out one at a time from the launch's counter (in index order), so a
+    // CTA that drew short items takes more: the kernel ends near the average CTA load
+    // instead of the heaviest fixed share.
+    while (ok) {
+      int item = 0;
+      if (lane == 0) item = atomicAdd(&p.sched[0], 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= p.n_items) {
+        // no more items: publish the end marker
+        if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleLoader, kBarItemEmpty, item)) break;
+        if (lane == 0) {
+          item_at(islot).n_tiles = -1;
+          mbar_arrive(&item_full[islot]);
+        }
+        __syncwarp();
+        break;
+      }
       int b, hkv, qblk, h0, nh;
       decode_item(p, item, b, hkv, qblk, h0, nh);
       int tlo = 0, tup = 0, tlof = 0, tupf = 0, start = 0, end = 0;
@@ -288,6 +312,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         it.tlo = tlo; it.tup = tup; it.tlof = tlof; it.tupf = tupf;
         it.n_tiles = nt;
         it.start = start; it.end = end;
+        it.idx = item;
         if (!kRagged && nt > 0) {
           // the rows' positions and segment ids ride on the item barrier
           const long long row0 = (long long)b * p.q_rows + qblk * kM;
@@ -391,9 +416,10 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         next_k();
         return true;
       };
-      for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
-        const int nt = item_at(islot).n_tiles, nh = item_at(islot).nh;
+      while (ok) {
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, -1)) break;
+        const int nt = item_at(islot).n_tiles, nh = item_at(islot).nh, item = item_at(islot).idx;
+        if (nt < 0) break;  // no more items
         if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         if (nt == 0) continue;
@@ -462,10 +488,11 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     uint32_t sph[2] = {0u, 0u};
     uint32_t pvt_ph = 0u;  // parity of the next pv_tile completion not yet passed
     uint32_t pvl_ph = 0u;
-    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x) {
-      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
+    while (true) {
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, -1)) break;
       const Item& it = item_at(islot);  // valid until this warp releases the slot
-      const int nt = it.n_tiles;
+      const int nt = it.n_tiles, item = it.idx;
+      if (nt < 0) break;  // no more items
       const bool mine = w < it.nh;
       const long long tok = (long long)it.b * p.q_rows + it.qblk * kM + r;
       const int hq = it.h0 + w;
@@ -717,10 +744,39 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // every loader of the launch has stopped drawing items once all CTAs counted
+  // themselves here: the last one leaves the counter zero for the next launch
+  if (threadIdx.x == 0 && atomicAdd(&p.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+    p.sched[0] = 0;
+    p.sched[1] = 0;
+    __threadfence();
+  }
+}
+
+// Device address of this launch's item counters (the slot after the previous launch's).
+int sched_slot(int** out) {
+  static std::mutex mu;
+  static int* base[64] = {};
+  static unsigned next = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "blocksparse_attn: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(SBA_ERR_UNSUPPORTED, "blocksparse_attn: device ordinal >= 64");
+  std::lock_guard<std::mutex> lock(mu);
+  if (base[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_bsa_sched);
+    if (e != cudaSuccess || ptr == nullptr) return cuda_error(e, "blocksparse_attn: item counters");
+    base[dev] = static_cast<int*>(ptr);
+  }
+  *out = base[dev] + 2 * (next++ % kSchedSlots);
+  return SBA_OK;
 }
 
 template <int D, bool kRagged>
-int launch_impl(const void* q, const void* k, const void* v, const Params& p, cudaStream_t stream) {
+int launch_impl(const void* q, const void* k, const void* v, const Params& p_in, cudaStream_t stream) {
+  Params p = p_in;
+  if (int rc = sched_slot(&p.sched)) return rc;
   using C = Cfg<D>;
   CUtensorMap tq, tk, tv;
   {
