@@ -38,6 +38,7 @@
 #include <cuda_bf16.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 #include "ptx.cuh"
@@ -46,6 +47,11 @@
 namespace sba {
 
 static __device__ DevError g_err_nsa = {0u, 0u, 0};
+// Item counters of the union kernel's launches: [next item, CTAs done] per slot; launches
+// take the slots in turn, so up to kSchedSlots launches (on any streams) may run at once.
+// Each launch finds its slot zero and leaves it zero.
+constexpr int kSchedSlots = 64;
+static __device__ int g_nsa_sched[2 * kSchedSlots];
 
 namespace {
 
@@ -84,11 +90,12 @@ struct Params {
   int n_items, n_tok;
   int item0;             // work items [item0, n_items) of this launch
   long long wait_limit;  // cycles a bounded wait may take
+  int* sched;            // union kernel: [next item, CTAs done] of this launch (zero at launch, left zero)
 };
 
 // One union-walk item as the builder hands it to the other roles.
 struct Item {
-  int g, hkv, n_union, n_tiles;
+  int g, hkv, n_union, n_tiles;    // n_tiles = -1: no more items (the builder's last publication)
   unsigned tok_valid;              // bit i: token slot i holds a token
   int tok[kMaxNT];                 // token of slot i (-1: none)
   int limit[kMaxNT];               // last key row (absolute) token i may see; -1 if none
@@ -442,9 +449,24 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ------------------------------------------------------------------ item builder
     int islot = 0; uint32_t iphase = 0;
     int cached_seq = 0;
-    for (int item = p.item0 + blockIdx.x; item < p.n_items; item += gridDim.x) {
+    // Items are handed out one at a time from the launch's counter once a slot is free,
+    // so a CTA that drew small unions takes more: the kernel ends near the average CTA
+    // load instead of the heaviest fixed share.
+    while (true) {
+      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, -1)) break;
+      int item = 0;
+      if (lane == 0) item = p.item0 + atomicAdd(&p.sched[0], 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= p.n_items) {
+        // no more items: publish the end marker
+        if (lane == 0) {
+          item_at(islot).n_tiles = -1;
+          mbar_arrive(&item_full[islot]);
+        }
+        __syncwarp();
+        break;
+      }
       const int g = item / p.Hkv, hkv = item - g * p.Hkv;
-      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, item)) break;
       build_item<BS>(p, g, hkv, lane, cached_seq, item_at(islot), keys);
       if (lane == 0) mbar_arrive(&item_full[islot]);
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
@@ -459,10 +481,12 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     for (int i = 0; i < 8; ++i) { issued[i] = false; last_parity[i] = 0; }
     const uint32_t q_box_bytes = static_cast<uint32_t>(C::kPanels * 128 * p.G * p.NT);
     bool ok = true;
-    for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-      if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, item)) break;
+    while (ok) {
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, -1)) break;
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union, hkv = it.hkv;
+      if (nt < 0) break;  // no more items
+      const int item = it.g * p.Hkv + hkv;
       const int np = (nt + 1) / 2;
       for (int pp = np > 0 ? -1 : 0; pp < np; ++pp) {  // pp = -1: the item's Q
         if (!warp_wait(&st_empty[stage], phase ^ 1, ab, kRoleLoader, kBarKvEmpty, item)) { ok = false; break; }
@@ -539,9 +563,11 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bool ok = true;
       // descriptors of the shared-memory operands; a byte offset x adds x >> 4
       const uint64_t st_desc0 = make_sdesc(smem_base + C::kOffStages, 16, 1024, kLayoutSW128);
-      for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+      while (ok) {
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, -1)) break;
         const int nt = item_at(islot).n_tiles;
+        if (nt < 0) break;  // no more items
+        const int item = item_at(islot).g * p.Hkv + item_at(islot).hkv;
         if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         const int np = (nt + 1) / 2;
@@ -597,9 +623,11 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       bool ok = true;
       const uint64_t v_desc0 =
           make_sdesc(smem_base + C::kOffStages + C::kKBytes, C::kPanelBytes, 1024, kLayoutSW128);
-      for (int item = p.item0 + blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+      while (ok) {
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, -1)) break;
         const int nt = item_at(islot).n_tiles;
+        if (nt < 0) break;  // no more items
+        const int item = item_at(islot).g * p.Hkv + item_at(islot).hkv;
         if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
         const int np = (nt + 1) / 2;
@@ -650,10 +678,12 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     uint32_t sph = 0, pvph = 0, xph = 0;
     int par = 0;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-    for (int item = p.item0 + blockIdx.x; item < p.n_items; item += gridDim.x) {
-      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
+    while (true) {
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, -1)) break;
       const Item& it = item_at(islot);
       const int nt = it.n_tiles, nu = it.n_union;
+      if (nt < 0) break;  // no more items
+      const int item = it.g * p.Hkv + it.hkv;
       const int np = (nt + 1) / 2;
       const bool row_ok = r < p.rows && ((it.tok_valid >> ti) & 1u);
       const int limit = r < p.rows ? it.limit[ti] : -1;
@@ -860,6 +890,13 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  // every builder of the launch has stopped drawing items once all CTAs counted
+  // themselves here: the last one leaves the counter zero for the next launch
+  if (threadIdx.x == 0 && atomicAdd(&p.sched[1], 1) == static_cast<int>(gridDim.x) - 1) {
+    p.sched[0] = 0;
+    p.sched[1] = 0;
+    __threadfence();
+  }
 }
 
 
@@ -984,9 +1021,31 @@ nsa_select_f32_kernel(const float* __restrict__ q, const float* __restrict__ k,
   }
 }
 
+// Device address of this launch's item counters (the slot after the previous launch's).
+int sched_slot(int** out) {
+  static std::mutex mu;
+  static int* base[64] = {};
+  static unsigned next = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error(e, "nsa_select: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return set_error(SBA_ERR_UNSUPPORTED, "nsa_select: device ordinal >= 64");
+  std::lock_guard<std::mutex> lock(mu);
+  if (base[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_nsa_sched);
+    if (e != cudaSuccess || ptr == nullptr) return cuda_error(e, "nsa_select: item counters");
+    base[dev] = static_cast<int*>(ptr);
+  }
+  *out = base[dev] + 2 * (next++ % kSchedSlots);
+  return SBA_OK;
+}
+
 template <int D, int BS>
-int launch_bf16(const void* q, const void* k, const void* v, const Params& p, cudaStream_t stream) {
+int launch_bf16(const void* q, const void* k, const void* v, const Params& p_in, cudaStream_t stream) {
   using C = Cfg<D, BS>;
+  Params p = p_in;
+  if (int rc = sched_slot(&p.sched)) return rc;
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   CUtensorMap tq, tk, tv;
   {
