@@ -87,6 +87,7 @@ struct Params {
   int* slot_cur;
   int* slot_tok;
   int* kv_next;                 // next dK/dV work item (zeroed by the scan kernel)
+  int* dq_next;                 // next dQ work item (zeroed by the scan kernel)
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
@@ -259,7 +260,10 @@ __global__ void __launch_bounds__(1024) nsa_bwd_scan_kernel(const Params p) {
       p.slot_off[i] = before;
       p.slot_cur[i] = 0;
     }
-    if (c0 == 0 && tid == 0) *p.kv_next = 0;
+    if (c0 == 0 && tid == 0) {
+      *p.kv_next = 0;
+      *p.dq_next = 0;
+    }
     __syncthreads();
     if (tid == 0) carry += warp_sums[31];
     __syncthreads();
@@ -313,7 +317,8 @@ __device__ __forceinline__ void row_grads(const float* s, const float* dp, int n
 
 // ------------------------------------------------------------------ 4. dQ kernel
 struct DqItem {
-  int n_union;
+  int n_union;                      // -1: no more items (the builder's last publication)
+  int item;                         // item index: g * Hkv + hkv
   unsigned tok_valid;
   int tok[kMaxNT];                  // token of slot i (-1: none)
   int limit[kMaxNT];                // last key row (absolute) token i may see; -1 if none
@@ -504,11 +509,28 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
   if (warp == 2) {
     // ------------------------------------------------------------------ item builder
     int islot = 0; uint32_t iphase = 0;
-    for (int item = blockIdx.x; item < p.n_items_dq; item += gridDim.x) {
+    // items are handed out one at a time from a counter once a slot is free, so a CTA
+    // that drew small unions takes more
+    while (true) {
+      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, -1)) break;
+      int item = 0;
+      if (lane == 0) item = atomicAdd(p.dq_next, 1);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= p.n_items_dq) {
+        // no more items: publish the end marker
+        if (lane == 0) {
+          item_at(islot).n_union = -1;
+          mbar_arrive(&item_full[islot]);
+        }
+        __syncwarp();
+        break;
+      }
       const int g = item / p.Hkv, hkv = item - g * p.Hkv;
-      if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, item)) break;
       build_dq_item(p, g, hkv, lane, item_at(islot), keys);
-      if (lane == 0) mbar_arrive(&item_full[islot]);
+      if (lane == 0) {
+        item_at(islot).item = item;
+        mbar_arrive(&item_full[islot]);
+      }
       if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
     }
   } else if (warp == 0) {
@@ -520,11 +542,13 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint32_t last[C::kStages] = {0u, 0u, 0u};
     bool q_issued = false; uint32_t q_last = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < p.n_items_dq && ok; item += gridDim.x) {
-      const int g = item / p.Hkv, hkv = item - g * p.Hkv;
-      if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, item)) break;
+    while (ok) {
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleLoader, kBarItemFull, -1)) break;
       const DqItem& it = item_at(islot);
       const int nu = it.n_union;
+      if (nu < 0) break;  // no more items
+      const int item = it.item;
+      const int g = item / p.Hkv, hkv = item - g * p.Hkv;
       if (nu > 0) {
         if (!warp_wait(qdo_empty, qph ^ 1, ab, kRoleLoader, kBarQdoEmpty, item)) break;
         if (lane == 0) {
@@ -581,9 +605,11 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       const uint64_t do_desc = make_sdesc(smem_base + C::kOffDO, 16, 1024, kLayoutSW128);
       const uint64_t ring_k = make_sdesc(smem_base + C::kOffRing, 16, 1024, kLayoutSW128);
       const uint64_t ring_kmn = make_sdesc(smem_base + C::kOffRing, C::kTilePanel, 1024, kLayoutSW128);
-      for (int item = blockIdx.x; item < p.n_items_dq && ok; item += gridDim.x) {
-        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, item)) break;
+      while (ok) {
+        if (!warp_wait(&item_full[islot], iphase, ab, kRoleMma, kBarItemFull, -1)) break;
         const int nu = item_at(islot).n_union;
+        if (nu < 0) break;  // no more items
+        const int item = item_at(islot).item;
         if (lane == 0) mbar_arrive(&item_empty[islot]);
         if (++islot == C::kItemSlots) { islot = 0; iphase ^= 1; }
         if (nu == 0) continue;
@@ -655,11 +681,13 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     int islot = 0; uint32_t iphase = 0;
     uint32_t sdp_ph = 0, ds_ph = 0, dqph = 0;
     int tiles_before = 0;                  // tiles of earlier items of this CTA
-    for (int item = blockIdx.x; item < p.n_items_dq; item += gridDim.x) {
-      const int hkv = item % p.Hkv;
-      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, item)) break;
+    while (true) {
+      if (!warp_wait(&item_full[islot], iphase, ab, kRoleSoftmax, kBarItemFull, -1)) break;
       const DqItem& it = item_at(islot);
       const int nu = it.n_union;
+      if (nu < 0) break;  // no more items
+      const int item = it.item;
+      const int hkv = item % p.Hkv;
       const int tok = ti < p.NT ? it.tok[ti] : -1;
       const int limit = ti < p.NT ? it.limit[ti] : -1;
       const long long hrow = (long long)(tok >= 0 ? tok : 0) * p.Hq + hkv * p.G + h;
@@ -1167,6 +1195,7 @@ int launch_nsa_select_bwd(const void* q, const void* k, const void* v, const voi
   p.slot_cur = reinterpret_cast<int*>(ws + L.cur);
   p.slot_tok = reinterpret_cast<int*>(ws + L.tok);
   p.kv_next = reinterpret_cast<int*>(ws + L.next);
+  p.dq_next = p.kv_next + 1;
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
