@@ -451,13 +451,15 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     int cached_seq = 0;
     // Items are handed out one at a time from the launch's counter once a slot is free,
     // so a CTA that drew small unions takes more: the kernel ends near the average CTA
-    // load instead of the heaviest fixed share.
+    // load instead of the heaviest fixed share.  They go out from the last token group to
+    // the first: under causal masking later tokens see more blocks, so the large unions
+    // are taken first and the small ones fill the end.
     while (true) {
       if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, -1)) break;
       int item = 0;
-      if (lane == 0) item = p.item0 + atomicAdd(&p.sched[0], 1);
+      if (lane == 0) item = p.n_items - 1 - atomicAdd(&p.sched[0], 1);
       item = __shfl_sync(0xffffffffu, item, 0);
-      if (item >= p.n_items) {
+      if (item < p.item0) {
         // no more items: publish the end marker
         if (lane == 0) {
           item_at(islot).n_tiles = -1;
