@@ -239,16 +239,12 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
   if (warp == 0) {
     // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
-    uint32_t qphase[2] = {0u, 0u};
-    bool q_issued[2] = {false, false};
-    uint32_t q_last[2] = {0u, 0u};
+    // Per-slot / per-stage flags and phases are bit sets (bit i: slot or stage i): indexed
+    // at run time, small arrays would live in local memory.
+    uint32_t qphase = 0u, q_issued = 0u, q_last = 0u;
     int ks = 0; uint32_t kphase = 0;
     int vs = 0; uint32_t vphase = 0;
-    bool k_issued[C::kStagesK], v_issued[C::kStages];
-    uint32_t k_last[C::kStagesK], v_last[C::kStages];
-#pragma unroll
-    for (int i = 0; i < C::kStagesK; ++i) { k_issued[i] = false; k_last[i] = 0; }
-    for (int i = 0; i < C::kStages; ++i) { v_issued[i] = false; v_last[i] = 0; }
+    uint32_t k_issued = 0u, k_last = 0u, v_issued = 0u, v_last = 0u;
     bool ok = true;
     // Items are handed out one at a time from the launch's counter (in index order), so a
     // CTA that drew short items takes more: the kernel ends near the average CTA load
@@ -327,7 +323,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       if (++islot == kItemSlots) { islot = 0; iphase ^= 1; }
       if (nt == 0) continue;
       for (int w = 0; w < nh; ++w) {
-        if (!warp_wait(&q_empty[w], qphase[w] ^ 1, ab, kRoleLoader, kBarQEmpty, item)) { ok = false; break; }
+        if (!warp_wait(&q_empty[w], ((qphase >> w) & 1u) ^ 1u, ab, kRoleLoader, kBarQEmpty, item)) { ok = false; break; }
         if (lane == 0) {
           mbar_arrive_expect_tx(&q_full[w], C::kQBytes);
 #pragma unroll
@@ -335,9 +331,9 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tma_load_3d(smem + C::kOffQ + w * C::kQBytes + pn * C::kQPanelBytes, &tm_q, &q_full[w],
                         pn * 64, h0 + w, b * p.q_rows + qblk * kM);
         }
-        q_issued[w] = true;
-        q_last[w] = qphase[w];
-        qphase[w] ^= 1;
+        q_issued |= 1u << w;
+        q_last = (q_last & ~(1u << w)) | (qphase & (1u << w));
+        qphase ^= 1u << w;
       }
       if (!ok) break;
       for (int t = 0; t < nt; ++t) {
@@ -350,8 +346,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             tma_load_3d(smem + C::kOffK + ks * C::kTBytes + pn * C::kTPanelBytes, &tm_k, &k_full[ks],
                         pn * 64, hkv, tok0);
         }
-        k_issued[ks] = true;
-        k_last[ks] = kphase;
+        k_issued |= 1u << ks;
+        k_last = (k_last & ~(1u << ks)) | (kphase << ks);
         if (++ks == C::kStagesK) { ks = 0; kphase ^= 1; }
         if (!warp_wait(&v_empty[vs], vphase ^ 1, ab, kRoleLoader, kBarVEmpty, item)) { ok = false; break; }
         if (lane == 0) {
@@ -365,19 +361,19 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             bulk_load(vdst + C::kTBytes + kKT * 4, p.kv_seg + tok0, kKT * 4, &v_full[vs]);
           }
         }
-        v_issued[vs] = true;
-        v_last[vs] = vphase;
+        v_issued |= 1u << vs;
+        v_last = (v_last & ~(1u << vs)) | (vphase << vs);
         if (++vs == C::kStages) { vs = 0; vphase ^= 1; }
       }
     }
     // Drain: wait (bounded) for every copy this warp issued before the CTA exits.
     if (lane == 0) {
       for (int s = 0; s < C::kStagesK; ++s)
-        if (k_issued[s]) drain_wait(&k_full[s], k_last[s]);
+        if ((k_issued >> s) & 1u) drain_wait(&k_full[s], (k_last >> s) & 1u);
       for (int s = 0; s < C::kStages; ++s)
-        if (v_issued[s]) drain_wait(&v_full[s], v_last[s]);
+        if ((v_issued >> s) & 1u) drain_wait(&v_full[s], (v_last >> s) & 1u);
       for (int w = 0; w < 2; ++w)
-        if (q_issued[w]) drain_wait(&q_full[w], q_last[w]);
+        if ((q_issued >> w) & 1u) drain_wait(&q_full[w], (q_last >> w) & 1u);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA issuer of head slot w
@@ -387,7 +383,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       const int w = warp - 1;
       const uint32_t leader = elect_one();
       int islot = 0; uint32_t iphase = 0;
-      uint32_t qph = 0u, oph = 0u, pph[2] = {0u, 0u};
+      uint32_t qph = 0u, oph = 0u, pph = 0u;  // pph: P-full phase of S buffer i in bit i
       int ks = 0; uint32_t kphase = 0;   // next K tile to consume (for an S)
       int vs = 0; uint32_t vphase = 0;   // next V tile to consume (for a PV)
       bool ok = true;
@@ -450,8 +446,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             if (!warp_wait(&o_empty[w], oph ^ 1, ab, kRoleMma, kBarOEmpty, item)) { ok = false; break; }
             oph ^= 1;
           }
-          if (!warp_wait(&p_full[2 * w + buf], pph[buf], ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
-          pph[buf] ^= 1;
+          if (!warp_wait(&p_full[2 * w + buf], (pph >> buf) & 1u, ab, kRoleMma, kBarPFull, item)) { ok = false; break; }
+          pph ^= 1u << buf;
           tc_fence_after();
           // O_w (+)= P_w V of this tile (P_w: bf16 pairs over the S_w,buf columns)
           const uint64_t vd = v_desc0 + static_cast<uint64_t>((vs * C::kVStageBytes) >> 4);
@@ -485,7 +481,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     const uint32_t o_col = tmem + lane_off + C::kOCol + w * D;
     int islot = 0; uint32_t iphase = 0;
     int vs = 0; uint32_t vphase = 0;
-    uint32_t sph[2] = {0u, 0u};
+    uint32_t sph = 0u;  // S-full phase of buffer i in bit i (a bit set: no local memory)
     uint32_t pvt_ph = 0u;  // parity of the next pv_tile completion not yet passed
     uint32_t pvl_ph = 0u;
     while (true) {
@@ -542,8 +538,8 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
         const int ti = it.tlo + t;
         const bool full = ti >= it.tlof && ti < it.tupf;
         const uint32_t s_col = tmem + lane_off + (2 * w + buf) * kKT;
-        if (!warp_wait(&s_full[2 * w + buf], sph[buf], ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
-        sph[buf] ^= 1;
+        if (!warp_wait(&s_full[2 * w + buf], (sph >> buf) & 1u, ab, kRoleSoftmax, kBarSFull, item)) { ok = false; break; }
+        sph ^= 1u << buf;
         const int* ps = nullptr;
         if (!full && !kRagged) {
           // the tile's key positions / segment ids arrived with its V

@@ -598,7 +598,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
       int islot = 0; uint32_t iphase = 0;
       uint32_t qph = 0, dqph = 0;
       int stage = 0; uint32_t kph = 0;
-      uint32_t sdp_ph[2] = {0u, 0u}, ds_ph[2] = {0u, 0u};
+      uint32_t sdp_ph = 0u, ds_ph = 0u;  // phase of buffer i in bit i (bit sets: no local memory)
       int buf = 0;  // S/dP (sdp_role) or dS buffer of the next tile
       bool ok = true;
       const uint64_t q_desc = make_sdesc(smem_base + C::kOffQ, 16, 1024, kLayoutSW128);
@@ -618,7 +618,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
           qph ^= 1;
           for (int u = 0; u < nu; ++u) {
             if (!warp_wait(&kv_full[stage], kph, ab, kRoleMma, kBarKvFull, item) ||
-                !warp_wait(&sdp_empty[buf], sdp_ph[buf] ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) {
+                !warp_wait(&sdp_empty[buf], ((sdp_ph >> buf) & 1u) ^ 1u, ab, kRoleMma, kBarSdpEmpty, item)) {
               ok = false;
               break;
             }
@@ -635,15 +635,15 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                          vd + kmajor_step(kk, C::kTilePanel), C::kIdescS, kk > 0 ? 1u : 0u);
             mma_commit_by(leader, &sdp_full[buf]);
             if (u == nu - 1) mma_commit_by(leader, qdo_empty);
-            sdp_ph[buf] ^= 1;
+            sdp_ph ^= 1u << buf;
             buf ^= 1;
             if (++stage == C::kStages) { stage = 0; kph ^= 1; }
           }
         } else {
           for (int u = 0; u < nu; ++u) {
             // dQ += dS(u) K(u)
-            if (!warp_wait(&ds_full[buf], ds_ph[buf], ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
-            ds_ph[buf] ^= 1;
+            if (!warp_wait(&ds_full[buf], (ds_ph >> buf) & 1u, ab, kRoleMma, kBarDsFull, item)) { ok = false; break; }
+            ds_ph ^= 1u << buf;
             if (u == 0) {
               if (!warp_wait(dq_empty, dqph ^ 1, ab, kRoleMma, kBarAccEmpty, item)) { ok = false; break; }
               dqph ^= 1;
@@ -875,10 +875,10 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // ------------------------------------------------------------------ loader
     int pslot = 0; uint32_t pph = 0;
     uint32_t kvph = 0;
-    uint32_t qph[2] = {0u, 0u};
+    uint32_t qph = 0u;  // phase of Q / dO buffer i in bit i (bit sets: no local memory)
     int qb = 0;
     bool kv_issued = false; uint32_t kv_last = 0;
-    bool q_issued[2] = {false, false}; uint32_t q_last[2] = {0u, 0u};
+    uint32_t q_issued = 0u, q_last = 0u;
     bool ok = true;
     while (ok) {
       // fetch the next item and publish it
@@ -910,7 +910,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       kv_issued = true; kv_last = kvph; kvph ^= 1;
       const int nch = (cnt + p.NT - 1) / p.NT;
       for (int c = 0; c < nch; ++c) {
-        if (!warp_wait(&qdo_empty[qb], qph[qb] ^ 1, ab, kRoleLoader, kBarQdoEmpty, item)) { ok = false; break; }
+        if (!warp_wait(&qdo_empty[qb], ((qph >> qb) & 1u) ^ 1u, ab, kRoleLoader, kBarQdoEmpty, item)) { ok = false; break; }
         // lane i < NT: token of slot i of this chunk (past the list: a row past the end,
         // which the TMA fills with zeros)
         const int k = c * p.NT + lane;
@@ -929,14 +929,14 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
           }
         }
-        q_issued[qb] = true; q_last[qb] = qph[qb]; qph[qb] ^= 1;
+        q_issued |= 1u << qb; q_last = (q_last & ~(1u << qb)) | (qph & (1u << qb)); qph ^= 1u << qb;
         qb ^= 1;
       }
     }
     if (lane == 0) {
       if (kv_issued) drain_wait(kv_full, kv_last);
       for (int i = 0; i < 2; ++i)
-        if (q_issued[i]) drain_wait(&qdo_full[i], q_last[i]);
+        if ((q_issued >> i) & 1u) drain_wait(&qdo_full[i], (q_last >> i) & 1u);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA issuers
@@ -949,7 +949,7 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     {
       const uint32_t leader = elect_one();
       uint32_t kvph = 0, sdph = 0, pdph = 0, accph = 0;
-      uint32_t qph[2] = {0u, 0u};
+      uint32_t qph = 0u;  // phase of Q / dO buffer i in bit i
       int qb = 0;
       bool ok = true;
       const uint64_t k_desc = make_sdesc(smem_base + C::kOffK, 16, 1024, kLayoutSW128);
@@ -972,9 +972,9 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
           if (!warp_wait(kv_full, kvph, ab, kRoleMma, kBarKvFull, item)) break;
           kvph ^= 1;
           for (int c = 0; c < nch; ++c) {
-            if (!warp_wait(&qdo_full[qb], qph[qb], ab, kRoleMma, kBarQdoFull, item) ||
+            if (!warp_wait(&qdo_full[qb], (qph >> qb) & 1u, ab, kRoleMma, kBarQdoFull, item) ||
                 !warp_wait(sdp_empty, sdph ^ 1, ab, kRoleMma, kBarSdpEmpty, item)) { ok = false; break; }
-            qph[qb] ^= 1;
+            qph ^= 1u << qb;
             sdph ^= 1;
             tc_fence_after();
             const uint64_t qo = static_cast<uint64_t>((qb * 2 * C::kQBytes) >> 4);
