@@ -688,43 +688,47 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&o_empty[w]);
       const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint64_t inv2 = pack_f32x2(inv, inv);
       uint32_t wv[D / 2];
 #pragma unroll
       for (int j = 0; j < D / 2; ++j) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(ov[2 * j] * inv, ov[2 * j + 1] * inv);
+        float a, c;
+        unpack_f32x2(mul_f32x2(pack_f32x2(ov[2 * j], ov[2 * j + 1]), inv2), a, c);
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(a, c);
         wv[j] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      // rows of this warp in two halves of 16: staged in the 128-byte swizzle the tensor
-      // map expects (16-byte chunk c of row i at c ^ (i % 8)), then one TMA store per
-      // 64-column panel; rows past the query range are clipped by the map
+      // rows of this warp in two halves of 16, each in its own buffer (lanes 0-15 the
+      // first, 16-31 the second, written at once): staged in the 128-byte swizzle the
+      // tensor map expects (16-byte chunk c of row i at c ^ (i % 8)), then one TMA store per
+      // half and 64-column panel; rows past the query range are clipped by the map
       uint8_t* stg = smem + C::kOffStage + (warp - 4) * C::kStgWarpBytes;
+      // the staging rows are free once the previous item's stores have read them
+      if (lane == 0) bulk_wait_group_read<0>();
+      __syncwarp();
+      {
+        const int half = lane >> 4, rr = lane & 15;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        // both halves' staging rows are free once the previous item's stores have read them
-        if (half == 0 && lane == 0) bulk_wait_group_read<0>();
-        __syncwarp();
-        if ((lane >> 4) == half) {
-          const int rr = lane & 15;
+        for (int pn = 0; pn < C::kPanels; ++pn) {
 #pragma unroll
-          for (int pn = 0; pn < C::kPanels; ++pn) {
-#pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-              const uint32_t* src = wv + pn * 32 + c8 * 4;
-              *reinterpret_cast<uint4*>(stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes + rr * 128 +
-                                        ((c8 ^ (rr & 7)) * 16)) =
-                  make_uint4(src[0], src[1], src[2], src[3]);
-            }
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint32_t* src = wv + pn * 32 + c8 * 4;
+            *reinterpret_cast<uint4*>(stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes + rr * 128 +
+                                      ((c8 ^ (rr & 7)) * 16)) =
+                make_uint4(src[0], src[1], src[2], src[3]);
           }
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_store_4d(&tm_o, stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes, pn * 64, hq, it.qblk * kM + q4 * 32 + half * 16,
-                         it.b);
-          bulk_commit_group();
+            tma_store_4d(&tm_o, stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes, pn * 64, hq,
+                         it.qblk * kM + q4 * 32 + half * 16, it.b);
         }
+        bulk_commit_group();
       }
       if (p.lse != nullptr && row_ok) p.lse[tok * p.Hq + hq] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
       __syncwarp();
