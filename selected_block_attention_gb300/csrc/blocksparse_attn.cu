@@ -584,16 +584,10 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
             mask_interval(x, jlo, jhi);
           } else {
 #pragma unroll
-            for (int j = 0; j < kKT; j += 4) {
-              const int4 kp4 = *reinterpret_cast<const int4*>(ps + j);
-              const int4 ks4 = *reinterpret_cast<const int4*>(ps + kKT + j);
-              const int kp[4] = {kp4.x, kp4.y, kp4.z, kp4.w};
-              const int ksg[4] = {ks4.x, ks4.y, ks4.z, ks4.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const bool ok_k = !none && ksg[u] == qs && kp[u] >= kmin && kp[u] <= kmax;
-                if (!ok_k) x[j + u] = -INFINITY;
-              }
+            for (int j = 0; j < kKT; ++j) {
+              const int kp = ps[j], ksg = ps[kKT + j];
+              const bool ok_k = !none && ksg == qs && kp >= kmin && kp <= kmax;
+              if (!ok_k) x[j] = -INFINITY;
             }
           }
         }
@@ -677,26 +671,6 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       pvl_ph ^= 1u;
       pvt_ph ^= 1u;  // PV(nt - 1) passed
       tc_fence_after();
-      float ov[D];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld_32x32b_x32_nw(o_col + c * 32, ov + c * 32);
-      tmem_wait_ld();
-#pragma unroll
-      for (int j = 0; j < D; ++j) tmem_ld_ready(ov[j]);
-      // O_w is in registers: the next item's first PV may overwrite it
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&o_empty[w]);
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const uint64_t inv2 = pack_f32x2(inv, inv);
-      uint32_t wv[D / 2];
-#pragma unroll
-      for (int j = 0; j < D / 2; ++j) {
-        float a, c;
-        unpack_f32x2(mul_f32x2(pack_f32x2(ov[2 * j], ov[2 * j + 1]), inv2), a, c);
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(a, c);
-        wv[j] = *reinterpret_cast<uint32_t*>(&h2);
-      }
       // rows of this warp in two halves of 16, each in its own buffer (lanes 0-15 the
       // first, 16-31 the second, written at once): staged in the 128-byte swizzle the
       // tensor map expects (16-byte chunk c of row i at c ^ (i % 8)), then one TMA store per
@@ -705,28 +679,47 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       // the staging rows are free once the previous item's stores have read them
       if (lane == 0) bulk_wait_group_read<0>();
       __syncwarp();
-      {
-        const int half = lane >> 4, rr = lane & 15;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint64_t inv2 = pack_f32x2(inv, inv);
+      const int half = lane >> 4, rr = lane & 15;
+      // O_w leaves tensor memory one 64-column panel at a time (fewer live registers); the
+      // next item's first PV may overwrite it once the last panel is in registers
 #pragma unroll
-        for (int pn = 0; pn < C::kPanels; ++pn) {
+      for (int pn = 0; pn < C::kPanels; ++pn) {
+        float ov[64];
+        tmem_ld_32x32b_x32_nw(o_col + pn * 64, ov);
+        tmem_ld_32x32b_x32_nw(o_col + pn * 64 + 32, ov + 32);
+        tmem_wait_ld();
 #pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint32_t* src = wv + pn * 32 + c8 * 4;
-            *reinterpret_cast<uint4*>(stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes + rr * 128 +
-                                      ((c8 ^ (rr & 7)) * 16)) =
-                make_uint4(src[0], src[1], src[2], src[3]);
-          }
+        for (int j = 0; j < 64; ++j) tmem_ld_ready(ov[j]);
+        if (pn == C::kPanels - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_empty[w]);
         }
+        uint32_t wv[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          float a, c;
+          unpack_f32x2(mul_f32x2(pack_f32x2(ov[2 * j], ov[2 * j + 1]), inv2), a, c);
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(a, c);
+          wv[j] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8)
+          *reinterpret_cast<uint4*>(stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes + rr * 128 +
+                                    ((c8 ^ (rr & 7)) * 16)) =
+              make_uint4(wv[c8 * 4], wv[c8 * 4 + 1], wv[c8 * 4 + 2], wv[c8 * 4 + 3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int hh = 0; hh < 2; ++hh) {
 #pragma unroll
           for (int pn = 0; pn < C::kPanels; ++pn)
-            tma_store_4d(&tm_o, stg + half * C::kStgHalfBytes + pn * C::kStgPanelBytes, pn * 64, hq,
-                         it.qblk * kM + q4 * 32 + half * 16, it.b);
+            tma_store_4d(&tm_o, stg + hh * C::kStgHalfBytes + pn * C::kStgPanelBytes, pn * 64, hq,
+                         it.qblk * kM + q4 * 32 + hh * 16, it.b);
         }
         bulk_commit_group();
       }
