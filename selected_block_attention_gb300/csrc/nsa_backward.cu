@@ -538,8 +538,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     int islot = 0; uint32_t iphase = 0;
     uint32_t qph = 0;
     int stage = 0; uint32_t kph = 0;
-    bool issued[C::kStages] = {false, false, false};
-    uint32_t last[C::kStages] = {0u, 0u, 0u};
+    uint32_t issued = 0u, last = 0u;  // stage i issued / parity of its last load in bit i
     bool q_issued = false; uint32_t q_last = 0;
     bool ok = true;
     while (ok) {
@@ -572,7 +571,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                           it.ux[u]);
             }
           }
-          issued[stage] = true; last[stage] = kph;
+          issued |= 1u << stage; last = (last & ~(1u << stage)) | (kph << stage);
           if (++stage == C::kStages) { stage = 0; kph ^= 1; }
         }
       }
@@ -582,7 +581,7 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     }
     if (lane == 0) {
       for (int s = 0; s < C::kStages; ++s)
-        if (issued[s]) drain_wait(&kv_full[s], last[s]);
+        if ((issued >> s) & 1u) drain_wait(&kv_full[s], (last >> s) & 1u);
       if (q_issued) drain_wait(qdo_full, q_last);
     }
   } else if (warp == 1 || warp == 3) {

@@ -477,10 +477,9 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // ------------------------------------------------------------------ loader
     int islot = 0; uint32_t iphase = 0;
     int stage = 0; uint32_t phase = 0;
-    bool issued[8];
-    uint32_t last_parity[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) { issued[i] = false; last_parity[i] = 0; }
+    // stage i issued / parity of its last load in bit i (bit sets: indexed at run time, an
+    // array would live in local memory)
+    uint32_t issued = 0u, last_parity = 0u;
     const uint32_t q_box_bytes = static_cast<uint32_t>(C::kPanels * 128 * p.G * p.NT);
     bool ok = true;
     while (ok) {
@@ -538,8 +537,8 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
           }
         }
-        issued[stage] = true;
-        last_parity[stage] = phase;
+        issued |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == C::kStages) { stage = 0; phase ^= 1; }
       }
       __syncwarp();
@@ -549,7 +548,7 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // Drain: wait (bounded) for every copy this warp issued before the CTA exits.
     if (lane == 0)
       for (int s = 0; s < C::kStages; ++s)
-        if (issued[s]) drain_wait(&st_full[s], last_parity[s]);
+        if ((issued >> s) & 1u) drain_wait(&st_full[s], (last_parity >> s) & 1u);
   } else if (warp == 1) {
     // ------------------------------------------------------------------ QK issuer
     // Two warps issue the MMAs (QK here, PV in warp 3): a warp's wait on a barrier stalls
