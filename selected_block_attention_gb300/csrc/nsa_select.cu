@@ -847,6 +847,9 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
       const float inv = L > 0.f ? gate / L : 0.f;
       if (np > 0) {
         tc_fence_after();
+        // O = (O_0 a0 + O_1 a1) * gate / L, with the factor folded into both weights: two
+        // columns per packed multiply and multiply-add
+        const uint64_t a0i = pack_f32x2(a0 * inv, a0 * inv), a1i = pack_f32x2(a1 * inv, a1 * inv);
 #pragma unroll
         for (int c = 0; c < kOutHalf / 32; ++c) {
           const int col = w * kOutHalf + c * 32;
@@ -860,9 +863,11 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int j0 = j + 2 * u;
-                const float v0 = o0[j0] * a0 + o1[j0] * a1;
-                const float v1 = o0[j0 + 1] * a0 + o1[j0 + 1] * a1;
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(v0 * inv, v1 * inv);
+                float v0, v1;
+                unpack_f32x2(fma_f32x2(pack_f32x2(o1[j0], o1[j0 + 1]), a1i,
+                                       mul_f32x2(pack_f32x2(o0[j0], o0[j0 + 1]), a0i)),
+                             v0, v1);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(v0, v1);
                 wv[u] = *reinterpret_cast<uint32_t*>(&h2);
               }
               *reinterpret_cast<uint4*>(out + orow * D + col + j) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
