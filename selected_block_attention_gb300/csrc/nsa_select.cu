@@ -856,6 +856,12 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
           float o0[32], o1[32];
           tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + col, o0);
           tmem_ld_32x32b_x32(tmem + lane_off + C::kOCol + D + col, o1);
+          if (c == kOutHalf / 32 - 1) {
+            // O_0 and O_1 are read: the next item's first PV may overwrite them
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_empty);
+          }
           if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 32; j += 8) {
@@ -874,9 +880,6 @@ nsa_union_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(o_empty);
       } else if (row_ok) {
 #pragma unroll
         for (int j = 0; j < kOutHalf; j += 8)
