@@ -246,14 +246,35 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     int vs = 0; uint32_t vphase = 0;
     uint32_t k_issued = 0u, k_last = 0u, v_issued = 0u, v_last = 0u;
     bool ok = true;
-    // Items are handed out one at a time from the launch's counter (in index order), so a
-    // CTA that drew short items takes more: the kernel ends near the average CTA load
-    // instead of the heaviest fixed share.
+    // Items are handed out one at a time from the launch's counter, so a CTA that drew
+    // short items takes more: the kernel ends near the average CTA load instead of the
+    // heaviest fixed share.  The ragged form with at most 32 rows hands the rows out
+    // longest first (all items of a row before the next row's; rank by clamped length,
+    // ties by index), so the largest items start first and the short ones fill the end of
+    // the launch; otherwise items go in index order.
+    const bool by_length = kRagged && p.B <= 32;
+    int row_of_rank = lane;  // lane r: the row of rank r
+    if (by_length) {
+      int len = -1;
+      if (lane < p.B)
+        len = max(min(max(p.seq_end[lane], 0), p.kv_rows) - min(max(p.seq_start[lane], 0), p.kv_rows), 0);
+      int rank = 0;
+      for (int j = 0; j < p.B; ++j) {
+        const int lj = __shfl_sync(0xffffffffu, len, j);
+        rank += (lj > len || (lj == len && j < lane)) ? 1 : 0;
+      }
+      for (int j = 0; j < p.B; ++j)
+        if (__shfl_sync(0xffffffffu, rank, j) == lane) row_of_rank = j;
+    }
+    const int per_row = p.Hkv * p.nbq * p.n_pairs;
     while (ok) {
-      int item = 0;
-      if (lane == 0) item = atomicAdd(&p.sched[0], 1);
-      item = __shfl_sync(0xffffffffu, item, 0);
-      if (item >= p.n_items) {
+      int k = 0;
+      if (lane == 0) k = atomicAdd(&p.sched[0], 1);
+      k = __shfl_sync(0xffffffffu, k, 0);
+      int item = k;
+      if (by_length && k < p.n_items)
+        item = __shfl_sync(0xffffffffu, row_of_rank, k / per_row) * per_row + k % per_row;
+      if (k >= p.n_items) {
         // no more items: publish the end marker
         if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleLoader, kBarItemEmpty, item)) break;
         if (lane == 0) {
