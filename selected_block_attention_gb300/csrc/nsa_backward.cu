@@ -1055,15 +1055,32 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       const int nch = (cnt + p.NT - 1) / p.NT;
       bool ok = true;
-      for (int c = 0; c < nch; ++c) {
+      // This row's token of a chunk (-1: none), and its LSE (log2 units) and Delta.  The
+      // loads run ahead of their use: a chunk's token two chunks early, its LSE / Delta
+      // one chunk early, so neither global latency sits between two chunks.
+      auto chunk_tok = [&](int c) -> int {
         const int k = c * p.NT + ti;
-        const int tok = k < cnt ? p.slot_tok[off + k] : -1;
-        float lse2 = -INFINITY, delta = 0.f;
-        if (tok >= 0) {
-          const long long hrow = (long long)tok * p.Hq + hkv * p.G + h;
-          lse2 = p.lse[hrow] * kLog2e;
-          delta = p.delta[hrow];
+        return (c < nch && k < cnt) ? p.slot_tok[off + k] : -1;
+      };
+      auto tok_lse = [&](int tk, float& l2, float& dl) {
+        l2 = -INFINITY;
+        dl = 0.f;
+        if (tk >= 0) {
+          const long long hrow = (long long)tk * p.Hq + hkv * p.G + h;
+          l2 = p.lse[hrow] * kLog2e;
+          dl = p.delta[hrow];
         }
+      };
+      int tok_n = chunk_tok(0);      // chunk c + 1 at the top of chunk c
+      float lse2_n, delta_n;
+      tok_lse(tok_n, lse2_n, delta_n);
+      int tok_nn = chunk_tok(1);     // chunk c + 2
+      for (int c = 0; c < nch; ++c) {
+        const int tok = tok_n;
+        const float lse2 = lse2_n, delta = delta_n;
+        tok_n = tok_nn;
+        tok_lse(tok_n, lse2_n, delta_n);
+        tok_nn = chunk_tok(c + 2);
         // keys of the block this row may see: causal limit of its token, the block's end
         int nvalid = 0;
         if (tok >= 0 && lse2 != -INFINITY) nvalid = p.causal ? min(max(tok - row0 + 1, 0), nkeys) : nkeys;
