@@ -695,18 +695,20 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         lse2 = p.lse[hrow] * kLog2e;
         delta = p.delta[hrow];
       }
-      const bool live = tok >= 0 && lse2 != -INFINITY;
+      // the LSE / Delta loads above are first used after the first tile's wait and score
+      // loads, so their latency overlaps that wait
       const unsigned tbit = 1u << ti;
       bool ok = true;
       for (int u = ((tiles_before & 1) == w) ? 0 : 1; u < nu; u += 2) {
         const int x0 = it.ux[u];
-        const bool sel = live && (it.ubits[u] & tbit) != 0u;
-        const int nvalid = sel ? min(max(limit - x0 + 1, 0), kBS) : 0;
+        const bool sel = tok >= 0 && (it.ubits[u] & tbit) != 0u;
+        int nvalid = sel ? min(max(limit - x0 + 1, 0), kBS) : 0;
         if (!warp_wait(&sdp_full[w], sdp_ph, ab, kRoleSoftmax, kBarSdpFull, item)) { ok = false; break; }
         sdp_ph ^= 1;
         tc_fence_after();
         float s[64], dp[64];
         tmem_ld64x2(tmem + lane_off + C::kSCol + w * kBS, s, tmem + lane_off + C::kDpCol + w * kBS, dp);
+        if (lse2 == -INFINITY) nvalid = 0;  // a row with no attended key: P = dS = 0
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sdp_empty[w]);
@@ -908,12 +910,17 @@ nsa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
       }
       kv_issued = true; kv_last = kvph; kvph ^= 1;
       const int nch = (cnt + p.NT - 1) / p.NT;
-      for (int c = 0; c < nch; ++c) {
-        if (!warp_wait(&qdo_empty[qb], ((qph >> qb) & 1u) ^ 1u, ab, kRoleLoader, kBarQdoEmpty, item)) { ok = false; break; }
-        // lane i < NT: token of slot i of this chunk (past the list: a row past the end,
-        // which the TMA fills with zeros)
+      // lane i < NT: token of slot i of a chunk (past the list: a row past the end, which
+      // the TMA fills with zeros); loaded one chunk ahead of its TMA loads
+      auto chunk_tok = [&](int c) -> int {
         const int k = c * p.NT + lane;
-        const int tk = (lane < p.NT && k < cnt) ? p.slot_tok[off + k] : p.n_tok;
+        return (c < nch && lane < p.NT && k < cnt) ? p.slot_tok[off + k] : p.n_tok;
+      };
+      int tk_n = chunk_tok(0);
+      for (int c = 0; c < nch; ++c) {
+        const int tk = tk_n;
+        tk_n = chunk_tok(c + 1);
+        if (!warp_wait(&qdo_empty[qb], ((qph >> qb) & 1u) ^ 1u, ab, kRoleLoader, kBarQdoEmpty, item)) { ok = false; break; }
         if (lane == 0) mbar_arrive_expect_tx(&qdo_full[qb], 2 * C::kQBytes);
         __syncwarp();
         uint8_t* qdst = smem + C::kOffQ + qb * 2 * C::kQBytes;
