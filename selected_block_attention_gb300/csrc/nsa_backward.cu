@@ -510,13 +510,14 @@ nsa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     // ------------------------------------------------------------------ item builder
     int islot = 0; uint32_t iphase = 0;
     // items are handed out one at a time from a counter once a slot is free, so a CTA
-    // that drew small unions takes more
+    // that drew small unions takes more; from the last token group down, since under
+    // causal masking later tokens choose among more blocks and have the larger unions
     while (true) {
       if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleBuilder, kBarItemEmpty, -1)) break;
       int item = 0;
-      if (lane == 0) item = atomicAdd(p.dq_next, 1);
+      if (lane == 0) item = p.n_items_dq - 1 - atomicAdd(p.dq_next, 1);
       item = __shfl_sync(0xffffffffu, item, 0);
-      if (item >= p.n_items_dq) {
+      if (item < 0) {
         // no more items: publish the end marker
         if (lane == 0) {
           item_at(islot).n_union = -1;
