@@ -89,6 +89,17 @@ def test_small_all_elements(sba, Hq, Hkv):
     assert_grad_close(to_np(dv), rv, "dv")
 
 
+def test_group_windows_with_a_short_last_window(sba):
+    """B=3, Hkv=2: six (batch row, KV head) groups, so the dK/dV items' windows of four
+    groups end with a window of two; every element against the oracle."""
+    w = workloads.nsa_prefill(device=DEV, B=3, T=384, Hq=16, Hkv=2, D=128, seed=1050)
+    do, dq, dk, dv = _run(sba, w, seed=2)
+    rq, rk, rv = _oracle(w, do)
+    assert_grad_close(to_np(dq), rq, "dq")
+    assert_grad_close(to_np(dk), rk, "dk")
+    assert_grad_close(to_np(dv), rv, "dv")
+
+
 @pytest.mark.parametrize("causal", [True, False])
 def test_messy_indices_ragged_tail(sba, causal):
     """-1, out of range, future blocks, duplicates, counts beyond S; T not a multiple of

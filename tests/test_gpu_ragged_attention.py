@@ -173,3 +173,17 @@ def test_long_chunks_on_the_block_pipeline(sba, Q, Hq, Hkv, S, window):
     _compare(sba, w, what=f"mq block pipeline Q={Q} Hq={Hq} Hkv={Hkv} S={S} {window}")
     _, lse = _gpu(sba, w)
     assert torch.isneginf(lse[3]).all()
+
+
+
+@pytest.mark.parametrize("B,equal", [(5, True), (40, False)])
+def test_block_pipeline_row_order(sba, B, equal):
+    """The block pipeline hands rows out longest first when there are at most 32 of them
+    (ties by index) and in index order otherwise: rows of equal lengths, and more than 32
+    rows of mixed lengths, against the oracle."""
+    Q, S = 128, 512
+    rng = np.random.default_rng(530 + B)
+    ends = [S] * B if equal else [int(x) for x in rng.integers(Q, S + 1, size=B)]
+    w = workloads.ragged_attention(device=DEV, B=B, Q=Q, Hq=4, Hkv=2, S=S, window=(-1, 0),
+                                   cap=0.0, num_sinks=0, ends=ends, seed=530 + B)
+    _compare(sba, w, what=f"mq block pipeline row order B={B} equal={equal}")
