@@ -23,8 +23,8 @@
 //   warps 4..7  softmax of head slot 0, warps 8..11 of head slot 1: one thread per query
 //               row; the row's 64 scores of a tile come out of tensor memory in one pass
 //               into registers, are masked outside the full tile range (an exact per-row
-//               key interval when the tile's keys are consecutive positions of one
-//               segment, else a test per key), and P (bf16) is
+//               key interval when the tile's keys are consecutive positions of at most
+//               two segments, else a test per key), and P (bf16) is
 //               written in place over the tile's S buffer; lazy online softmax (O_w
 //               rescaled only when the row maximum grows by > 2^8, after the previous
 //               tile's PV has landed); epilogue: O_w leaves tensor memory at once (the
@@ -592,15 +592,26 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
           // exactly the key indices j in [kmin - p0, kmax - p0] when s0 is the row's
           // segment: an interval test per key, no per-key loads.  Other tiles test every
           // key's position and segment.
-          const int p0 = ps[0], s0 = ps[kKT];
-          const bool shape = (long long)ps[lane] == (long long)p0 + lane &&
-                             (long long)ps[32 + lane] == (long long)p0 + 32 + lane &&
-                             ps[kKT + lane] == s0 && ps[kKT + 32 + lane] == s0;
-          if (__all_sync(0xffffffffu, shape)) {
+          // Consecutive positions split into two runs of one segment each (a document
+          // boundary or the start of padding inside the tile: keys [0, j0) of segment s0,
+          // [j0, 64) of s1) still give every row one interval, inside its own segment's run.
+          const int p0 = ps[0], s0 = ps[kKT], s1 = ps[kKT + kKT - 1];
+          const int sg0 = ps[kKT + lane], sg1 = ps[kKT + 32 + lane];
+          const bool consec = (long long)ps[lane] == (long long)p0 + lane &&
+                              (long long)ps[32 + lane] == (long long)p0 + 32 + lane;
+          const unsigned b0 = __ballot_sync(0xffffffffu, sg0 == s0);
+          const unsigned b1 = __ballot_sync(0xffffffffu, sg1 == s0);
+          const int j0 = __popc(b0) + __popc(b1);  // keys of segment s0, a prefix if contiguous
+          const bool runs = (sg0 == s0 || sg0 == s1) && (sg1 == s0 || sg1 == s1) &&
+                            b0 == (j0 >= 32 ? 0xffffffffu : (1u << j0) - 1u) &&
+                            b1 == (j0 <= 32 ? 0u : (j0 >= 64 ? 0xffffffffu : (1u << (j0 - 32)) - 1u));
+          if (__all_sync(0xffffffffu, consec && runs)) {
             int jlo = 0, jhi = -1;  // empty unless the row attends some of the tile
-            if (!none && s0 == qs) {
-              jlo = static_cast<int>(min(max((long long)kmin - p0, 0LL), (long long)kKT));
-              jhi = static_cast<int>(max(min((long long)kmax - p0, (long long)kKT - 1), -1LL));
+            if (!none && (s0 == qs || s1 == qs)) {
+              const bool first = s0 == qs;  // the row's run: [0, j0) or [j0, 64)
+              const long long rlo = first ? 0 : j0, rhi = first ? j0 - 1 : kKT - 1;
+              jlo = static_cast<int>(min(max((long long)kmin - p0, rlo), (long long)kKT));
+              jhi = static_cast<int>(max(min((long long)kmax - p0, rhi), -1LL));
             }
             mask_interval(x, jlo, jhi);
           } else {
