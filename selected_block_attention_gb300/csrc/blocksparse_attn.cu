@@ -170,6 +170,33 @@ __device__ __forceinline__ void mask_interval(float (&x)[kKT], int jlo, int jhi)
   for (int j = 0; j < 32; ++j) x[32 + j] = (w1 & (1u << j)) ? x[32 + j] : -INFINITY;
 }
 
+// Ragged form: key tiles [tlo, tup) of query block qblk of row b and the full ones
+// [tlof, tupf): rows i0 .. i1 of the block sit at end - Q + i; their windows' union is
+// [kmin(i0), kmax(i1)] and the keys every row sees are [kmin(i1), kmax(i0)].
+__device__ __forceinline__ void ragged_tiles(const Params& p, int b, int qblk, int& start, int& end,
+                                             int& tlo, int& tup, int& tlof, int& tupf) {
+  start = min(max(p.seq_start[b], 0), p.kv_rows);
+  end = min(max(p.seq_end[b], 0), p.kv_rows);
+  tlo = tup = tlof = tupf = 0;
+  const int i0 = qblk * kM, i1 = min(i0 + kM, p.q_rows) - 1;
+  auto kmin = [&](int i) -> long long {
+    const long long pos = (long long)end - p.q_rows + i;
+    return p.window_left >= 0 ? max((long long)start, pos - p.window_left) : (long long)start;
+  };
+  auto kmax = [&](int i) -> long long {
+    const long long pos = (long long)end - p.q_rows + i;
+    return p.window_right >= 0 ? min((long long)end - 1, pos + p.window_right) : (long long)end - 1;
+  };
+  const long long klo = kmin(i0), khi = kmax(i1);
+  if (end > start && khi >= klo) {
+    tlo = static_cast<int>(klo / kKT);
+    tup = static_cast<int>(khi / kKT) + 1;
+    const long long flo = kmin(i1), fhi = kmax(i0);
+    tlof = static_cast<int>((flo + kKT - 1) / kKT);
+    tupf = fhi >= flo ? static_cast<int>((fhi + 1) / kKT) : tlof;
+  }
+}
+
 // kRagged: the ragged multi-query form of the same computation (queries are the last Q
 // tokens of [start, end) of a KV cache, each with its own inclusive window); the key
 // range and the full tiles of a query block follow from start, end and the window, and
@@ -248,32 +275,48 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
     bool ok = true;
     // Items are handed out one at a time from the launch's counter, so a CTA that drew
     // short items takes more: the kernel ends near the average CTA load instead of the
-    // heaviest fixed share.  The ragged form with at most 32 rows hands the rows out
-    // longest first (all items of a row before the next row's; rank by clamped length,
-    // ties by index), so the largest items start first and the short ones fill the end of
-    // the launch; otherwise items go in index order.
-    const bool by_length = kRagged && p.B <= 32;
-    int row_of_rank = lane;  // lane r: the row of rank r
-    if (by_length) {
-      int len = -1;
-      if (lane < p.B)
-        len = max(min(max(p.seq_end[lane], 0), p.kv_rows) - min(max(p.seq_start[lane], 0), p.kv_rows), 0);
-      int rank = 0;
-      for (int j = 0; j < p.B; ++j) {
-        const int lj = __shfl_sync(0xffffffffu, len, j);
-        rank += (lj > len || (lj == len && j < lane)) ? 1 : 0;
+    // heaviest fixed share.  The ragged form hands the largest items out first: with at
+    // most 32 (row, query block) groups each lane ranks one group by its tile count (ties
+    // by index) and the groups go out in rank order (all KV heads and head pairs of a
+    // group together); with at most 32 rows, the rows by clamped length; otherwise items
+    // go in index order.  Each CTA's loader ranks once, at the start.
+    const int ng = p.B * p.nbq;
+    const int by_group = kRagged && ng <= 32 ? 1 : (kRagged && p.B <= 32 ? 2 : 0);
+    int of_rank = lane;  // lane r: the group (1) or row (2) of rank r
+    if (by_group != 0) {
+      const int n = by_group == 1 ? ng : p.B;
+      int size = -1;
+      if (lane < n) {
+        if (by_group == 1) {
+          int st, en, t0, t1, f0, f1;
+          ragged_tiles(p, lane / p.nbq, lane % p.nbq, st, en, t0, t1, f0, f1);
+          size = t1 - t0;
+        } else {
+          size = max(min(max(p.seq_end[lane], 0), p.kv_rows) - min(max(p.seq_start[lane], 0), p.kv_rows), 0);
+        }
       }
-      for (int j = 0; j < p.B; ++j)
-        if (__shfl_sync(0xffffffffu, rank, j) == lane) row_of_rank = j;
+      int rank = 0;
+      for (int j = 0; j < n; ++j) {
+        const int sj = __shfl_sync(0xffffffffu, size, j);
+        rank += (sj > size || (sj == size && j < lane)) ? 1 : 0;
+      }
+      for (int j = 0; j < n; ++j)
+        if (__shfl_sync(0xffffffffu, rank, j) == lane) of_rank = j;
     }
-    const int per_row = p.Hkv * p.nbq * p.n_pairs;
+    const int per_row = p.Hkv * p.nbq * p.n_pairs, per_group = p.Hkv * p.n_pairs;
     while (ok) {
       int k = 0;
       if (lane == 0) k = atomicAdd(&p.sched[0], 1);
       k = __shfl_sync(0xffffffffu, k, 0);
       int item = k;
-      if (by_length && k < p.n_items)
-        item = __shfl_sync(0xffffffffu, row_of_rank, k / per_row) * per_row + k % per_row;
+      if (by_group == 1 && k < p.n_items) {
+        // group (b, qblk) of rank k / per_group; its (hkv, pair) from the remainder
+        const int g = __shfl_sync(0xffffffffu, of_rank, k / per_group), rem = k % per_group;
+        const int gb = g / p.nbq, gq = g % p.nbq, hkv = rem / p.n_pairs, pair = rem % p.n_pairs;
+        item = ((gb * p.Hkv + hkv) * p.nbq + gq) * p.n_pairs + pair;
+      } else if (by_group == 2 && k < p.n_items) {
+        item = __shfl_sync(0xffffffffu, of_rank, k / per_row) * per_row + k % per_row;
+      }
       if (k >= p.n_items) {
         // no more items: publish the end marker
         if (!warp_wait(&item_empty[islot], iphase ^ 1, ab, kRoleLoader, kBarItemEmpty, item)) break;
@@ -288,27 +331,7 @@ blocksparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_c
       decode_item(p, item, b, hkv, qblk, h0, nh);
       int tlo = 0, tup = 0, tlof = 0, tupf = 0, start = 0, end = 0;
       if constexpr (kRagged) {
-        // rows i0 .. i1 of this query block sit at end - Q + i; their windows' union is
-        // [kmin(i0), kmax(i1)] and the keys every row sees are [kmin(i1), kmax(i0)]
-        start = min(max(p.seq_start[b], 0), p.kv_rows);
-        end = min(max(p.seq_end[b], 0), p.kv_rows);
-        const int i0 = qblk * kM, i1 = min(i0 + kM, p.q_rows) - 1;
-        auto kmin = [&](int i) -> long long {
-          const long long pos = (long long)end - p.q_rows + i;
-          return p.window_left >= 0 ? max((long long)start, pos - p.window_left) : (long long)start;
-        };
-        auto kmax = [&](int i) -> long long {
-          const long long pos = (long long)end - p.q_rows + i;
-          return p.window_right >= 0 ? min((long long)end - 1, pos + p.window_right) : (long long)end - 1;
-        };
-        const long long klo = kmin(i0), khi = kmax(i1);
-        if (end > start && khi >= klo) {
-          tlo = static_cast<int>(klo / kKT);
-          tup = static_cast<int>(khi / kKT) + 1;
-          const long long flo = kmin(i1), fhi = kmax(i0);
-          tlof = static_cast<int>((flo + kKT - 1) / kKT);
-          tupf = fhi >= flo ? static_cast<int>((fhi + 1) / kKT) : tlof;
-        }
+        ragged_tiles(p, b, qblk, start, end, tlo, tup, tlof, tupf);
       } else {
         // block bounds in tiles: a key block of kv_block keys is kv_block / kKT tiles
         const int tpb = p.kv_block / kKT;
